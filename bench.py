@@ -1,0 +1,385 @@
+"""Benchmark of the quantized sparse-MoE SwitchGLU layer forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode] [--impl reference]
+
+Default workload (the headline): batch-1 decode, H 4096, I 11008, E 64,
+top-4, 4-bit affine group 64, 256 single-token layer calls per step.  One
+step = all 256 calls, each a full layer forward (router + top-k, permute,
+fused gate_up + SiLU*up, down, combine), captured once in a CUDA graph and
+replayed.  Metric: MoE-layer tokens/s over all ranks.  Inputs (4.9 GB of
+expert weights, 304 MB active per call) are larger than L2.
+
+Also reported: the dominant kernel's achieved HBM GB/s over its algorithmic
+bytes (CUDA events around its launches), the end-to-end rate through the
+public API with pinned host buffers, the SM clocks seen during the timed
+region, and the CPU oracle on a bounded sample of the same workload.
+
+N > 1 (torchrun): every rank runs its own 256 calls on its own tokens
+against replicated weights -- independent replicas, weak scaling, no
+collective on the data path.  --impl reference runs the CPU oracle as the
+reference arm on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+GEMV_SRC = os.path.join(ROOT, "sparse_moe_expert_gb300", "csrc", "gemv.cu")
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--config", default="decode", choices=sorted(workloads.CONFIGS))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample", type=int, default=0, help="oracle sample size (calls/tokens)")
+    return p.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def shard_calls(n_calls: int, rank: int, world: int):
+    """Token stream offsets of this rank's calls: every rank runs n_calls
+    independent calls on its own tokens (weak scaling)."""
+    return [(rank * n_calls + c) for c in range(n_calls)]
+
+
+def load_peaks():
+    try:
+        with open(MEASURED_PEAKS) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def file_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def active_bytes_per_expert(cfg, which):
+    """Packed codes + fp16 scale + fp16 bias of one expert's matrix."""
+    if which == "gate_up":
+        rows, cols = 2 * cfg.I, cfg.H
+    else:
+        rows, cols = cfg.H, cfg.I
+    return rows * (cols * cfg.bits // 8 + (cols // 64) * 4)
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.tmp = None
+
+    def __enter__(self):
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.tmp.close()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.tmp.name) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 8 and parts[0].replace(".", "").isdigit():
+                        rows.append(parts)
+        finally:
+            os.unlink(self.tmp.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm = [float(r[0]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][1]),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+                if any(r[2].replace(".", "").isdigit() for r in rows) else None}
+
+
+# ------------------------------------------------------------- cpu oracle
+
+def oracle_sample(cfg, layer_np, x_bits, n, batch=0):
+    """Time the oracle (as it stands) on n tokens/calls of the workload."""
+    import oracle
+    t0, c0 = time.perf_counter(), time.process_time()
+    if cfg.calls > 1:
+        for c in range(n):
+            oracle.moe_forward(x_bits[c:c + 1], layer_np, keep_intermediates=False)
+        tokens = n
+    else:
+        toks = np.arange(n)
+        oracle.moe_forward(x_bits, layer_np, inv_temperature=cfg.inv_temperature(batch),
+                           tokens=toks, keep_intermediates=False)
+        tokens = n
+    wall = time.perf_counter() - t0
+    cpu = time.process_time() - c0
+    return tokens, wall, cpu
+
+
+def default_sample(cfg):
+    return {"decode": 2, "batched": 16, "prefill": 64, "entropy": 32, "tiny": 16}.get(cfg.name, 8)
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    cfg = workloads.CONFIGS[args.config]
+    layer_np = workloads.make_layer(cfg)
+    x_bits = workloads.make_tokens(cfg)
+    n = args.cpu_sample or (1 if cfg.calls > 1 else min(cfg.T, default_sample(cfg)))
+    for _ in range(args.warmup):
+        oracle_sample(cfg, layer_np, x_bits, n)
+    tok = wall = cpu = 0.0
+    for _ in range(args.steps):
+        t, w, c = oracle_sample(cfg, layer_np, x_bits, n)
+        tok += t
+        wall += w
+        cpu += c
+    value = tok / wall
+    cores = round(cpu / wall, 1) if wall > 0 else 1.0
+    line = {
+        "impl": "reference", "metric": metric_name(), "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * wall / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(cfg),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} {'calls' if cfg.calls > 1 else 'tokens'} per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def metric_name():
+    return "MoE-layer tokens/s; achieved HBM GB/s (decode) / tensor TFLOPS (prefill)"
+
+
+def workload_config(cfg):
+    desc = {
+        "decode": "batch-1 decode: H4096 I11008 E64 top-4, 4-bit affine g64, 256 calls x 1 token",
+        "batched": "batched decode: H4096 I1536 E64 top-4 T64, 4-bit, Zipf(1.1) log-prior",
+        "prefill": "prefill: H2048 I768 E128 top-8 T4096, 4-bit",
+        "entropy": "entropy-adaptive: H4096 I1536 E32 T512, 8-bit, k from batch entropy",
+        "tiny": "tiny: H256 I512 E8 top-2 T16, 4-bit",
+    }[cfg.name]
+    return {"workload": desc, "H": cfg.H, "I": cfg.I, "E": cfg.E, "k": cfg.k or "adaptive",
+            "tokens_per_call": cfg.T, "calls_per_step": cfg.calls, "bits": cfg.bits,
+            "l2": "inputs larger than L2 (expert weights stream from HBM every call)"}
+
+
+# ----------------------------------------------------------------- ours
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import sparse_moe_expert_gb300 as moe
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = workloads.CONFIGS[args.config]
+    layer_np = workloads.make_layer(cfg)
+    layer = moe.MoELayer.from_workload(layer_np, dev, free_sources=True)
+    calls = cfg.calls
+    T = cfg.T
+    starts = shard_calls(calls, rank, world)
+    x_bits = workloads.normal_bf16(0, workloads.STREAM_X, (calls * T, cfg.H), cfg.x_std,
+                                   start=starts[0] * T * cfg.H)
+    x_dev = moe.bf16_from_bits(x_bits, dev)
+    out_dev = torch.empty((calls * T, cfg.H), dtype=torch.bfloat16, device=dev)
+
+    def step(events=None):
+        for c in range(calls):
+            layer.forward(x_dev[c * T:(c + 1) * T], out=out_dev[c * T:(c + 1) * T],
+                          events=events)
+
+    # eager warm-up (sets kernel attributes), then capture one step in a graph
+    step()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+    gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    gpu_id = str(gpu_id) if gpu_id is not None else str(local)
+    if gpu_id and not gpu_id.startswith("GPU-") and "-" in gpu_id:
+        gpu_id = "GPU-" + gpu_id
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_id) as clk:
+        e0.record()
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+    barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens_per_step = calls * T
+    value = tokens_per_step * world / (ms / 1000.0)
+    clocks = clk.summary()
+
+    # per-kernel durations: the same calls launched eagerly with CUDA events
+    # around the two products (the graph above is not instrumented)
+    ksteps = max(1, min(args.steps, 20))
+    events = {}
+    torch.cuda.synchronize()
+    for _ in range(ksteps):
+        step(events)
+    torch.cuda.synchronize()
+    kt = {k: statistics.mean(a.elapsed_time(b) for a, b in v) for k, v in events.items()}
+    n_active = int((layer.buffers(T)["counts"] > 0).sum().item())
+    peaks, peak_src = load_peaks()
+    gu_bytes = active_bytes_per_expert(cfg, "gate_up") * n_active + T * cfg.H * 2
+    dn_bytes = active_bytes_per_expert(cfg, "down") * n_active
+    gu_gbs = gu_bytes / (kt["gate_up"] * 1e-3) / 1e9
+    dn_gbs = dn_bytes / (kt["down"] * 1e-3) / 1e9
+    traffic = None
+    try:
+        with open(TRAFFIC_FILE) as f:
+            tr = json.load(f)
+        if tr.get("gemv_sha") == file_sha(GEMV_SRC) and tr.get("config") == cfg.name:
+            traffic = tr.get("gate_up_dram_bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+
+    # end to end through the public API with pinned host buffers
+    x_host = torch.from_numpy(x_bits).view(torch.bfloat16).pin_memory()
+    o_host = torch.empty((calls * T, cfg.H), dtype=torch.bfloat16).pin_memory()
+    esteps = max(1, min(args.steps, 20))
+
+    def e2e_step():
+        for c in range(calls):
+            layer.forward_host(x_host[c * T:(c + 1) * T], o_host[c * T:(c + 1) * T])
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(esteps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / esteps
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = {"value": tokens_per_step * world / e2e_s, "unit": "tokens/s",
+           "h2d_bytes_per_step": tokens_per_step * cfg.H * 2,
+           "d2h_bytes_per_step": tokens_per_step * cfg.H * 2,
+           "how": "MoELayer.forward_host per call, eager launches, pinned host buffers"}
+
+    line = {
+        "metric": metric_name(), "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": workload_config(cfg),
+        "roofline": {"bound": "hbm", "achieved": gu_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gu_gbs / peaks["hbm_gbs"], "traffic": traffic,
+                     "kernel": "gemv_qmm_kernel (gate_up, SiLU*up epilogue)",
+                     "algorithmic_bytes_per_launch": gu_bytes, "peak_source": peak_src},
+        "kernels": {"gate_up_us": kt["gate_up"] * 1e3, "gate_up_gbs": gu_gbs,
+                    "down_us": kt["down"] * 1e3, "down_gbs": dn_gbs,
+                    "layer_us_per_call": ms * 1e3 / calls,
+                    "layer_gbs": (gu_bytes + dn_bytes) / (ms * 1e-3 / calls) / 1e9,
+                    "active_experts_last_call": n_active},
+        "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
+                   "reasons": clocks["reasons"], "samples": clocks["samples"]},
+        "e2e": e2e,
+        "gpu_launches": 5 * calls * args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = args.cpu_sample or default_sample(cfg)
+        tok, wall, cpu = oracle_sample(cfg, layer_np, x_bits, n)
+        line["cpu_baseline"] = {"value": tok / wall, "unit": "tokens/s",
+                                "cores": round(cpu / wall, 1), "kind": "oracle",
+                                "sample": f"{n} {'calls' if calls > 1 else 'tokens'} of the same "
+                                          f"workload ({wall:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -177,19 +177,30 @@ def permute(ids: np.ndarray, k: int, E: int) -> Permutation:
 def unpack_codes(q_words: np.ndarray, bits: int, cols: int) -> np.ndarray:
     """uint32 words -> codes [..., cols]; element i in word i/(32/bits) at bit
     offset bits*(i mod 32/bits)."""
-    per = 32 // bits
-    shifts = np.arange(per, dtype=np.uint32) * np.uint32(bits)
-    codes = (np.asarray(q_words, dtype=np.uint32)[..., None] >> shifts) & np.uint32((1 << bits) - 1)
-    return codes.reshape(*q_words.shape[:-1], cols).astype(np.uint8)
+    # Little-endian words: byte j of a word holds elements 2j (low nibble) and
+    # 2j+1 (high nibble) for 4-bit codes, element j for 8-bit codes.
+    q = np.asarray(q_words)
+    by = np.ascontiguousarray(q, dtype="<u4").view(np.uint8)
+    if bits == 8:
+        codes = by
+    elif bits == 4:
+        codes = np.empty(by.shape[:-1] + (2 * by.shape[-1],), dtype=np.uint8)
+        codes[..., 0::2] = by & 0x0F
+        codes[..., 1::2] = by >> 4
+    else:
+        raise ValueError("bits must be 4 or 8")
+    return codes.reshape(*q.shape[:-1], cols)
 
 
 def dequant(q_words, scales, biases, bits: int, cols: int, group: int = 64) -> np.ndarray:
     """w = scale * code + bias, scale and bias shared by `group` consecutive
     elements along the row (the contraction axis).  float64, exact."""
     codes = unpack_codes(q_words, bits, cols).astype(np.float64)
-    s = np.repeat(np.asarray(scales).astype(np.float64), group, axis=-1)
-    b = np.repeat(np.asarray(biases).astype(np.float64), group, axis=-1)
-    return s * codes + b
+    lead = codes.shape[:-1]
+    w = codes.reshape(lead + (cols // group, group))
+    w *= np.asarray(scales).astype(np.float64)[..., None]
+    w += np.asarray(biases).astype(np.float64)[..., None]
+    return w.reshape(lead + (cols,))
 
 
 @dataclasses.dataclass(frozen=True)
@@ -272,8 +283,6 @@ def moe_forward(x_bits, layer, k_fixed=None, kmax=None, inv_temperature=None, re
     k = routing.k
     perm = permute(routing.ids, k, E)
     want = np.ones(T, dtype=bool) if tokens is None else np.isin(np.arange(T), tokens)
-    gu_q, gu_s, gu_b = pack_gate_up(layer.gate.q, layer.gate.s, layer.gate.b,
-                                    layer.up.q, layer.up.s, layer.up.b)
     A = len(perm.sorted_assign)
     h_all = np.full((A, I), np.nan) if keep_intermediates else None
     y_all = np.full((A, H), np.nan)
@@ -285,7 +294,10 @@ def moe_forward(x_bits, layer, k_fixed=None, kmax=None, inv_temperature=None, re
         if len(rows) == 0:
             continue
         toks = perm.sorted_assign[rows] // kmax
-        gu = qmm_raw(xf[toks], gu_q[e], gu_s[e], gu_b[e], bits, H)      # [m, 2I]
+        gu_q, gu_s, gu_b = pack_gate_up(layer.gate.q[e:e + 1], layer.gate.s[e:e + 1],
+                                        layer.gate.b[e:e + 1], layer.up.q[e:e + 1],
+                                        layer.up.s[e:e + 1], layer.up.b[e:e + 1])
+        gu = qmm_raw(xf[toks], gu_q[0], gu_s[0], gu_b[0], bits, H)      # [m, 2I]
         h = swiglu(gu[:, :I], gu[:, I:])                                 # [m, I]
         y = qmm_raw(h, layer.down.q[e], layer.down.s[e], layer.down.b[e], bits, I)  # [m, H]
         if h_all is not None:

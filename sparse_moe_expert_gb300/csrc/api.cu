@@ -1,0 +1,176 @@
+// C-ABI entry points of libmoe_gb300 that are not defined next to their
+// kernels: status strings, the two quantized products (path selection and
+// argument checks) and the device error word.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace moe {
+moe_status_t gemv_qmm(const void* act, int act_kind, const int32_t* sorted,
+                      const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
+                      bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
+                      int bits, void* out, int out_dtype, cudaStream_t st);
+moe_status_t tc_qmm(const void* act, int act_kind, const int32_t* sorted,
+                    const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
+                    bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
+                    int bits, void* out, int out_dtype, cudaStream_t st);
+bool tc_available();
+}  // namespace moe
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Per-device error word.  Kernels receive its address; it lives for the
+// lifetime of the loaded module.
+__device__ unsigned int g_moe_device_error;
+
+struct DeviceCache {
+  int sm = 0;
+  unsigned int* err = nullptr;
+};
+DeviceCache g_cache[kMaxDevices];
+std::mutex g_cache_mu;
+
+DeviceCache& cache_for_current() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+  return g_cache[dev];
+}
+
+// Average tokens per expert above which the tensor-core path wins.
+constexpr int kTcMinTokensPerExpert = 24;
+
+}  // namespace
+
+namespace moe_host {
+
+int sm_count() {
+  DeviceCache& c = cache_for_current();
+  if (c.sm == 0) {
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      n = 1;
+    c.sm = n;
+  }
+  return c.sm;
+}
+
+unsigned int* device_error_word() {
+  DeviceCache& c = cache_for_current();
+  if (c.err == nullptr) {
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_moe_device_error) == cudaSuccess)
+      c.err = static_cast<unsigned int*>(p);
+  }
+  return c.err;
+}
+
+}  // namespace moe_host
+
+extern "C" const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported";
+    case MOE_ERR_INCOMPATIBLE: return "gate and up cannot be fused";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE: return "device-side check failed";
+  }
+  return "unknown status";
+}
+
+extern "C" int moe_abi_version(void) { return 1; }
+
+static int pick_path(int path, int T, int kmax, int E) {
+  if (path != MOE_PATH_AUTO) return path;
+  const int64_t per_expert = (int64_t)T * kmax / E;
+  return (per_expert >= kTcMinTokensPerExpert && moe::tc_available()) ? MOE_PATH_TC
+                                                                      : MOE_PATH_GEMV;
+}
+
+static bool common_shape_ok(int T, int kmax, int E) {
+  return T >= 0 && kmax >= 1 && kmax <= 16 && E >= 1 && E <= 1024 &&
+         (int64_t)T * kmax <= (1 << 24);
+}
+
+extern "C" moe_status_t moe_gate_up_qmm(const uint16_t* x, const int32_t* sorted_assign,
+                                        const int32_t* expert_offsets, const int32_t* k_dev,
+                                        int T, int kmax, int E, int H, int n_rows,
+                                        const uint32_t* w_q, const uint16_t* w_s,
+                                        const uint16_t* w_b, int bits, int epilogue,
+                                        int out_dtype, void* out, int path,
+                                        moe_stream_t stream) {
+  using namespace moe_host;
+  if (!common_shape_ok(T, kmax, E)) return MOE_ERR_INVALID_ARG;
+  if (H <= 0 || H % 64 != 0 || n_rows <= 0) return MOE_ERR_INVALID_ARG;
+  if (bits != 4 && bits != 8) return MOE_ERR_UNSUPPORTED;
+  if (epilogue != MOE_EPILOGUE_RAW && epilogue != MOE_EPILOGUE_SWIGLU) return MOE_ERR_INVALID_ARG;
+  if (out_dtype != MOE_DTYPE_F32 && out_dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
+  if (epilogue == MOE_EPILOGUE_RAW && out_dtype != MOE_DTYPE_F32) return MOE_ERR_UNSUPPORTED;
+  if (epilogue == MOE_EPILOGUE_SWIGLU && n_rows % 2 != 0) return MOE_ERR_INVALID_ARG;
+  if (path < MOE_PATH_AUTO || path > MOE_PATH_TC) return MOE_ERR_INVALID_ARG;
+  if (H > 49152) return MOE_ERR_UNSUPPORTED;
+  if (!expert_offsets || !k_dev) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  const void* ptrs[] = {x, sorted_assign, w_q, w_s, w_b, out};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  const bool swiglu = epilogue == MOE_EPILOGUE_SWIGLU;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int p = pick_path(path, T, kmax, E);
+  if (p == MOE_PATH_TC) {
+    if (!moe::tc_available()) return MOE_ERR_UNSUPPORTED;
+    return moe::tc_qmm(x, 0, sorted_assign, expert_offsets, T, kmax, E, H, n_rows, swiglu, w_q,
+                       w_s, w_b, bits, out, out_dtype, st);
+  }
+  return moe::gemv_qmm(x, 0, sorted_assign, expert_offsets, T, kmax, E, H, n_rows, swiglu, w_q,
+                       w_s, w_b, bits, out, out_dtype, st);
+}
+
+extern "C" moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* expert_offsets,
+                                     const int32_t* k_dev, int T, int kmax, int E, int I, int H,
+                                     const uint32_t* w_q, const uint16_t* w_s,
+                                     const uint16_t* w_b, int bits, float* y, int path,
+                                     moe_stream_t stream) {
+  using namespace moe_host;
+  if (!common_shape_ok(T, kmax, E)) return MOE_ERR_INVALID_ARG;
+  if (I <= 0 || I % 64 != 0 || H <= 0 || H % 64 != 0) return MOE_ERR_INVALID_ARG;
+  if (bits != 4 && bits != 8) return MOE_ERR_UNSUPPORTED;
+  if (h_dtype != MOE_DTYPE_F32 && h_dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
+  if (path < MOE_PATH_AUTO || path > MOE_PATH_TC) return MOE_ERR_INVALID_ARG;
+  if (I > 49152) return MOE_ERR_UNSUPPORTED;
+  if (!expert_offsets || !k_dev) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  const void* ptrs[] = {h, w_q, w_s, w_b, y};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  const int act_kind = h_dtype == MOE_DTYPE_F32 ? 1 : 2;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int p = pick_path(path, T, kmax, E);
+  if (p == MOE_PATH_TC) {
+    if (!moe::tc_available()) return MOE_ERR_UNSUPPORTED;
+    return moe::tc_qmm(h, act_kind, nullptr, expert_offsets, T, kmax, E, I, H, false, w_q, w_s,
+                       w_b, bits, y, MOE_DTYPE_F32, st);
+  }
+  return moe::gemv_qmm(h, act_kind, nullptr, expert_offsets, T, kmax, E, I, H, false, w_q, w_s,
+                       w_b, bits, y, MOE_DTYPE_F32, st);
+}
+
+extern "C" moe_status_t moe_get_device_error(uint32_t* flags, int clear, moe_stream_t stream) {
+  if (!flags) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  unsigned int* word = moe_host::device_error_word();
+  if (!word) return MOE_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpyAsync(&v, word, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (clear && cudaMemsetAsync(word, 0, sizeof v, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  *flags = v;
+  return MOE_OK;
+}

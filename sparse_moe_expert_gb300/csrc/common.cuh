@@ -1,0 +1,94 @@
+// Shared device helpers of libmoe_gb300 (sm_103a).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_gb300.h"
+
+namespace moe {
+
+constexpr int kGroup = 64;  // elements per scale/bias group
+
+// Kernels report data problems (MOE_DEVERR_* bits) into the per-device error
+// word whose address the launcher passes in; moe_get_device_error reads it.
+__device__ __forceinline__ void raise_device_error(unsigned int* err, unsigned int bit) {
+  if (err) atomicOr(err, bit);
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t v16) {
+  return __uint_as_float(v16 << 16);
+}
+
+// Two bf16 packed in one word -> two floats (low half first).
+__device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// fp32 -> bf16, round to nearest even (finite inputs; NaN kept quiet).
+__device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((u >> 16) | 0x40u);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+__device__ __forceinline__ float f16_bits_to_f32(uint16_t h) {
+  return __half2float(__ushort_as_half(h));
+}
+
+// SiLU(gate) * up, the SwitchGLU activation, in fp32.  Every path that
+// produces h (fused epilogues and the separate swiglu kernel) calls this one
+// function, so the fused and unfused results agree bit for bit.
+__device__ __forceinline__ float swiglu_f32(float g, float u) {
+  float sig_den = __fadd_rn(1.0f, expf(-g));
+  return __fmul_rn(__fdiv_rn(g, sig_den), u);
+}
+
+// Packed fp32x2 fused multiply-add (Blackwell FFMA2): d = a * b + c, lane-wise.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  unsigned long long ra, rb, rc, rd;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1,%2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1,%2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  float2 d;
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+  return d;
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint16_t ldg_u16(const uint16_t* p) { return __ldg(p); }
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+}  // namespace moe
+
+// Host-side helpers shared by the launchers.
+namespace moe_host {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Streaming multiprocessor count of the current device (cached per device).
+int sm_count();
+
+// Device address of the current device's error word (nullptr on failure).
+unsigned int* device_error_word();
+
+inline moe_status_t launch_status() {
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe_host

@@ -1,0 +1,172 @@
+// Permute: stable counting sort of the (token, slot) assignments by expert.
+//
+// Page "oMLX MoE gate/up 融合优化：qwen35_moe_gate_up 实现剖析", section
+// 如何验证正确性 (the sorted branch that groups token indices by expert before
+// the gathered product); page "Qwen3.5-MoE与Qwen3-MoE架构差异深度解析",
+// section 4.2 (per-expert activation counts).
+//
+// One CTA of 1024 threads.  Counts come from shared-memory atomics (integer,
+// so order-independent), the offsets from a block scan.  The scatter walks
+// the assignments in chunks of 1024 in ascending order; inside a chunk an
+// assignment's rank among equal experts is its rank within its warp
+// (__match_any_sync) plus the counts of the same expert in lower warps of the
+// chunk (a per-expert column scan over the 32 warp histograms) plus the
+// number already placed by earlier chunks.  The result is unique: for each
+// expert, its assignments in ascending a = t*kmax + j.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kPermuteThreads = 1024;
+constexpr int kPermuteWarps = kPermuteThreads / 32;
+
+struct PermuteParams {
+  const int32_t* ids;
+  const int32_t* k_dev;
+  int T, kmax, E;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted;
+  int32_t* inv_pos;
+  unsigned int* err;
+};
+
+__global__ void __launch_bounds__(kPermuteThreads) permute_kernel(PermuteParams p) {
+  extern __shared__ int smem_i[];
+  const int E = p.E;
+  int* cnt = smem_i;              // [E]
+  int* off = cnt + E;             // [E]
+  int* run = off + E;             // [E] placed so far
+  int* tot = run + E;             // [E] this chunk's count
+  int* wcnt = tot + E;            // [32][E] per-warp histograms / prefixes
+  __shared__ int warp_sums[kPermuteWarps];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k = *p.k_dev;
+  const int64_t slots = (int64_t)p.T * p.kmax;
+
+  for (int i = tid; i < E; i += kPermuteThreads) { cnt[i] = 0; run[i] = 0; }
+  for (int i = tid; i < kPermuteWarps * E; i += kPermuteThreads) wcnt[i] = 0;
+  __syncthreads();
+
+  // counts
+  for (int64_t a = tid; a < slots; a += kPermuteThreads) {
+    int j = (int)(a % p.kmax);
+    if (j < k) {
+      int e = p.ids[a];
+      if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+      else raise_device_error(p.err, MOE_DEVERR_BAD_EXPERT);
+    }
+  }
+  __syncthreads();
+
+  // exclusive scan of cnt -> off (E <= 1024 = blockDim)
+  {
+    int v = tid < E ? cnt[tid] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int ws = warp_sums[lane];
+      int wincl = ws;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(0xFFFFFFFFu, wincl, o);
+        if (lane >= o) wincl += n;
+      }
+      warp_sums[lane] = wincl - ws;  // exclusive prefix of warp totals
+    }
+    __syncthreads();
+    if (tid < E) {
+      int excl = incl - v + warp_sums[warp];
+      off[tid] = excl;
+      p.counts[tid] = v;
+      p.offsets[tid] = excl;
+      if (tid == E - 1) p.offsets[E] = excl + v;
+    }
+  }
+  __syncthreads();
+
+  // stable scatter, chunk by chunk
+  for (int64_t base = 0; base < slots; base += kPermuteThreads) {
+    const int64_t a = base + tid;
+    int e = -1;
+    if (a < slots) {
+      int j = (int)(a % p.kmax);
+      if (j < k) {
+        int v = p.ids[a];
+        if (v >= 0 && v < E) e = v;
+        else p.inv_pos[a] = -1;
+      } else {
+        p.inv_pos[a] = -1;
+      }
+    }
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+    const int rank_in_warp = __popc(peers & lanemask_lt());
+    const bool leader = (peers & lanemask_lt()) == 0u;
+    if (e >= 0 && leader) wcnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    for (int x = tid; x < E; x += kPermuteThreads) {
+      int running = 0;
+      for (int w = 0; w < kPermuteWarps; ++w) {
+        int c = wcnt[w * E + x];
+        wcnt[w * E + x] = running;
+        running += c;
+      }
+      tot[x] = running;
+    }
+    __syncthreads();
+    if (e >= 0) {
+      int pos = off[e] + run[e] + wcnt[warp * E + e] + rank_in_warp;
+      p.sorted[pos] = (int32_t)a;
+      p.inv_pos[a] = pos;
+    }
+    __syncthreads();
+    for (int x = tid; x < E; x += kPermuteThreads) {
+      run[x] += tot[x];
+      for (int w = 0; w < kPermuteWarps; ++w) wcnt[w * E + x] = 0;
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status_t moe_permute(const int32_t* topk_ids, const int32_t* k_dev, int T,
+                                    int kmax, int E, int32_t* expert_counts,
+                                    int32_t* expert_offsets, int32_t* sorted_assign,
+                                    int32_t* inv_pos, moe_stream_t stream) {
+  using namespace moe_host;
+  if (T < 0 || E < 1 || E > 1024 || kmax < 1 || kmax > 16) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)T * kmax > (1 << 24)) return MOE_ERR_INVALID_ARG;
+  if (!k_dev || !expert_counts || !expert_offsets) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_ids || !sorted_assign || !inv_pos)) return MOE_ERR_INVALID_ARG;
+  PermuteParams p;
+  p.ids = topk_ids;
+  p.k_dev = k_dev;
+  p.T = T;
+  p.kmax = kmax;
+  p.E = E;
+  p.counts = expert_counts;
+  p.offsets = expert_offsets;
+  p.sorted = sorted_assign;
+  p.inv_pos = inv_pos;
+  p.err = device_error_word();
+  size_t smem = (size_t)(4 + kPermuteWarps) * E * sizeof(int);
+  if (smem > 48 * 1024) {
+    if (cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  permute_kernel<<<1, kPermuteThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  return launch_status();
+}

@@ -1,0 +1,206 @@
+"""MoELayer: the six C-ABI calls composed into one quantized SwitchGLU MoE layer.
+
+Pages: "Qwen3.5 Block在llama.cpp中的映射与优化原理" section 4 (router, then
+only the chosen experts' FFN, then the weighted sum); "oMLX MoE gate/up 融合
+优化：qwen35_moe_gate_up 实现剖析" (gate and up fused once at load, one
+gate_up product per layer; the environment switch turns fusion off).
+"""
+from __future__ import annotations
+
+import dataclasses
+import os
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import binding as B
+from ._lib import EPILOGUE_RAW, EPILOGUE_SWIGLU, PATH_AUTO, PATH_GEMV, PATH_TC, MoEError
+
+FUSE_ENV = "MOE_GB300_FUSE_GATE_UP"
+TC_MIN_TOKENS_PER_EXPERT = 24  # mirrors the library's automatic path choice
+
+
+@dataclasses.dataclass
+class QTensor:
+    """Affine-quantized weights of E experts on the device."""
+    q: torch.Tensor  # uint32 [E, rows, cols*bits/32]
+    s: torch.Tensor  # float16 [E, rows, cols/64]
+    b: torch.Tensor  # float16 [E, rows, cols/64]
+    bits: int
+
+    @property
+    def rows(self) -> int:
+        return self.q.shape[1]
+
+    @property
+    def cols(self) -> int:
+        return self.q.shape[2] * 32 // self.bits
+
+
+def qtensor_from_numpy(m, device) -> QTensor:
+    """Upload a workloads.QuantMatrix (numpy) to the device."""
+    q = torch.from_numpy(np.ascontiguousarray(m.q)).to(device)
+    s = torch.from_numpy(np.ascontiguousarray(m.s)).to(device)
+    b = torch.from_numpy(np.ascontiguousarray(m.b)).to(device)
+    return QTensor(q, s, b, m.bits)
+
+
+def bf16_from_bits(x_bits: np.ndarray, device=None, pin: bool = False) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(x_bits, dtype=np.uint16)).view(torch.bfloat16)
+    if pin:
+        t = t.pin_memory()
+    return t.to(device) if device is not None else t
+
+
+class MoELayer:
+    """Forward of one quantized sparse-MoE SwitchGLU layer on one GPU.
+
+    k_fixed > 0 routes every token to k experts; k_fixed = 0 applies the
+    batch-entropy rule (k in {1, 2, 3}, kmax = 3).  ``fuse_gate_up`` (default:
+    the environment variable MOE_GB300_FUSE_GATE_UP, on unless "0") packs
+    gate and up once here; unfused layers run two RAW products plus the
+    separate activation.  ``path`` forces a kernel family for the products.
+    """
+
+    def __init__(self, router_w: torch.Tensor, logit_bias: Optional[torch.Tensor], gate: QTensor,
+                 up: QTensor, down: QTensor, k_fixed: int, kmax: Optional[int] = None,
+                 inv_temperature: float = 1.0, renormalize: bool = True,
+                 thresholds=(1.2, 2.5), fuse_gate_up: Optional[bool] = None,
+                 path: int = PATH_AUTO, free_sources: bool = False):
+        self.device = router_w.device
+        self.router_w = router_w.contiguous()
+        self.logit_bias = None if logit_bias is None else logit_bias.contiguous()
+        self.E, self.H = router_w.shape
+        self.I = gate.rows
+        self.bits = gate.bits
+        self.k_fixed = k_fixed
+        self.kmax = kmax if kmax is not None else (k_fixed if k_fixed > 0 else 3)
+        self.inv_temperature = float(inv_temperature)
+        self.renormalize = renormalize
+        self.thr = tuple(float(t) for t in thresholds)
+        self.path = path
+        self.down = down
+        if fuse_gate_up is None:
+            fuse_gate_up = os.environ.get(FUSE_ENV, "1") != "0"
+        self.fused = False
+        self.gate, self.up, self.gate_up = gate, up, None
+        if fuse_gate_up:
+            gd = B.qdesc(gate.rows, gate.cols, gate.bits)
+            ud = B.qdesc(up.rows, up.cols, up.bits)
+            try:
+                q, s, b = B.moe_pack_gate_up(gd, ud, gate.q, gate.s, gate.b, up.q, up.s, up.b)
+                self.gate_up = QTensor(q, s, b, gate.bits)
+                self.fused = True
+                if free_sources:
+                    self.gate = self.up = None
+            except MoEError as err:
+                if err.status != 3:  # MOE_ERR_INCOMPATIBLE keeps the unfused path
+                    raise
+        self._bufs = {}
+
+    @classmethod
+    def from_workload(cls, layer_inputs, device, batch: int = 0, **kw) -> "MoELayer":
+        cfg = layer_inputs.cfg
+        rw = torch.from_numpy(layer_inputs.router_w).to(device)
+        lb = None if layer_inputs.logit_bias is None else torch.from_numpy(layer_inputs.logit_bias).to(device)
+        kw.setdefault("inv_temperature", cfg.inv_temperature(batch))
+        return cls(rw, lb, qtensor_from_numpy(layer_inputs.gate, device),
+                   qtensor_from_numpy(layer_inputs.up, device),
+                   qtensor_from_numpy(layer_inputs.down, device), k_fixed=cfg.k,
+                   kmax=cfg.slots, **kw)
+
+    def resolved_path(self, T: int) -> int:
+        if self.path != PATH_AUTO:
+            return self.path
+        return PATH_TC if (T * self.kmax) // self.E >= TC_MIN_TOKENS_PER_EXPERT else PATH_GEMV
+
+    def buffers(self, T: int) -> dict:
+        key = T
+        if key not in self._bufs:
+            dev, A = self.device, max(T * self.kmax, 1)
+            h_dtype = torch.bfloat16 if self.resolved_path(T) == PATH_TC else torch.float32
+            bufs = dict(
+                topk_ids=torch.empty((T, self.kmax), dtype=torch.int32, device=dev),
+                topk_w=torch.empty((T, self.kmax), dtype=torch.float32, device=dev),
+                k_dev=torch.empty(1, dtype=torch.int32, device=dev),
+                mean_entropy=torch.empty(1, dtype=torch.float32, device=dev),
+                ws=torch.empty(B.moe_router_workspace_size(T), dtype=torch.uint8, device=dev),
+                counts=torch.empty(self.E, dtype=torch.int32, device=dev),
+                offsets=torch.empty(self.E + 1, dtype=torch.int32, device=dev),
+                sorted=torch.empty(A, dtype=torch.int32, device=dev),
+                inv_pos=torch.empty(A, dtype=torch.int32, device=dev),
+                h=torch.empty((A, self.I), dtype=h_dtype, device=dev),
+                y=torch.empty((A, self.H), dtype=torch.float32, device=dev),
+                out=torch.empty((T, self.H), dtype=torch.bfloat16, device=dev),
+            )
+            if not self.fused:
+                bufs["g_raw"] = torch.empty((A, self.I), dtype=torch.float32, device=dev)
+                bufs["u_raw"] = torch.empty((A, self.I), dtype=torch.float32, device=dev)
+            self._bufs[key] = bufs
+        return self._bufs[key]
+
+    def forward(self, x: torch.Tensor, out: Optional[torch.Tensor] = None,
+                inv_temperature: Optional[float] = None, events: Optional[dict] = None
+                ) -> torch.Tensor:
+        """x: bf16 [T, H] on the device.  Returns bf16 [T, H] (a reused buffer
+        unless ``out`` is given).  ``events``, if given, maps "gate_up" and
+        "down" to lists that receive (start, end) CUDA events around those
+        launches."""
+        T = x.shape[0]
+        b = self.buffers(T)
+        path = self.resolved_path(T)
+        it = self.inv_temperature if inv_temperature is None else float(inv_temperature)
+        B.moe_router_topk(x, self.router_w, self.logit_bias, it, self.k_fixed, self.kmax,
+                          self.thr[0], self.thr[1], self.renormalize, b["topk_ids"], b["topk_w"],
+                          b["k_dev"], b["mean_entropy"], b["ws"])
+        B.moe_permute(b["topk_ids"], b["k_dev"], self.E, b["counts"], b["offsets"], b["sorted"],
+                      b["inv_pos"])
+        ev = _Timer(events, "gate_up")
+        if self.fused:
+            g = self.gate_up
+            B.moe_gate_up_qmm(x, b["sorted"], b["offsets"], b["k_dev"], self.kmax, g.q, g.s, g.b,
+                              self.bits, EPILOGUE_SWIGLU, b["h"].dtype, b["h"], path)
+        else:
+            for m, dst in ((self.gate, b["g_raw"]), (self.up, b["u_raw"])):
+                B.moe_gate_up_qmm(x, b["sorted"], b["offsets"], b["k_dev"], self.kmax, m.q, m.s,
+                                  m.b, self.bits, EPILOGUE_RAW, torch.float32, dst, path)
+            B.moe_swiglu(b["g_raw"], b["u_raw"], b["k_dev"], T, self.kmax, b["h"].dtype, b["h"])
+        ev.stop()
+        d = self.down
+        ev = _Timer(events, "down")
+        B.moe_down_qmm(b["h"], b["offsets"], b["k_dev"], T, self.kmax, d.q, d.s, d.b, self.bits,
+                       b["y"], path)
+        ev.stop()
+        res = out if out is not None else b["out"]
+        B.moe_combine(b["y"], b["inv_pos"], b["topk_w"], b["k_dev"], T, self.kmax, res)
+        return res
+
+    __call__ = forward
+
+    def forward_host(self, x_host: torch.Tensor, out_host: torch.Tensor) -> torch.Tensor:
+        """End-to-end call with host buffers: copies x (pinned host, bf16
+        [T, H]) to the device, runs the layer and copies the result back into
+        out_host, all enqueued on the current stream (no synchronization)."""
+        T = x_host.shape[0]
+        b = self.buffers(T)
+        if "x_dev" not in b:
+            b["x_dev"] = torch.empty((T, self.H), dtype=torch.bfloat16, device=self.device)
+        b["x_dev"].copy_(x_host, non_blocking=True)
+        res = self.forward(b["x_dev"])
+        out_host.copy_(res, non_blocking=True)
+        return out_host
+
+
+class _Timer:
+    def __init__(self, events: Optional[dict], name: str):
+        self.events, self.name = events, name
+        if events is not None:
+            self.start = torch.cuda.Event(enable_timing=True)
+            self.start.record()
+
+    def stop(self):
+        if self.events is not None:
+            end = torch.cuda.Event(enable_timing=True)
+            end.record()
+            self.events.setdefault(self.name, []).append((self.start, end))

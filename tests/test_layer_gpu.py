@@ -1,0 +1,170 @@
+"""Quantized products and the whole layer on the GPU vs the CPU oracle."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from _parity import assert_layer_close, dev, rel_l2, to_np
+from test_parity_gpu import CFG, SMALL
+
+pytestmark = pytest.mark.gpu
+
+PATHS = ["gemv"]
+
+
+def path_id(moe, name):
+    return {"gemv": moe.PATH_GEMV, "tc": moe.PATH_TC}[name]
+
+
+def run_layer(moe, layer_np, x_bits, path, batch=0, **kw):
+    layer = moe.MoELayer.from_workload(layer_np, dev(), batch=batch, path=path, **kw)
+    out = layer(moe.bf16_from_bits(x_bits, dev()))
+    torch.cuda.synchronize()
+    return layer, to_np(out)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("name", list(SMALL))
+def test_layer_small_configs(cuda_lib, name, path):
+    cfg = SMALL[name]
+    layer_np = workloads.make_layer(cfg)
+    for b in range(cfg.batches):
+        x_bits = workloads.make_tokens(cfg, 0, b)
+        ref = oracle.moe_forward(x_bits, layer_np, inv_temperature=cfg.inv_temperature(b))
+        layer, out = run_layer(cuda_lib, layer_np, x_bits, path_id(cuda_lib, path), batch=b)
+        bufs = layer.buffers(x_bits.shape[0])
+        assert np.array_equal(to_np(bufs["topk_ids"]), ref.routing.ids)
+        A = len(ref.perm.sorted_assign)
+        h = to_np(bufs["h"])[:A]
+        y = to_np(bufs["y"])[:A]
+        h_tol = 1e-4 if bufs["h"].dtype == torch.float32 else 4e-3
+        assert rel_l2(h, ref.h) <= h_tol, f"h {rel_l2(h, ref.h):.2e}"
+        assert rel_l2(y, ref.y) <= 2 * h_tol, f"y {rel_l2(y, ref.y):.2e}"
+        assert_layer_close(out, ref.out, f"{name} batch {b}")
+        assert cuda_lib.moe_get_device_error() == 0
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("T,k,E", [(1, 4, 16), (40, 2, 8)])
+def test_fused_gate_up_bit_identical_to_two_products(cuda_lib, path, bits, T, k, E):
+    cfg = CFG["tiny"].scaled(H=512, I=384, E=E, k=k, T=T, bits=bits)
+    layer_np = workloads.make_layer(cfg)
+    x_bits = workloads.make_tokens(cfg)
+    d = dev()
+    moe = cuda_lib
+    p = path_id(moe, path)
+    layer = moe.MoELayer.from_workload(layer_np, d, path=p)
+    assert layer.fused
+    x = moe.bf16_from_bits(x_bits, d)
+    layer(x)
+    b = layer.buffers(T)
+    gu = layer.gate_up
+    raw_f = moe.moe_gate_up_qmm(x, b["sorted"], b["offsets"], b["k_dev"], cfg.slots, gu.q, gu.s,
+                                gu.b, bits, moe.EPILOGUE_RAW, path=p)
+    raw_g = moe.moe_gate_up_qmm(x, b["sorted"], b["offsets"], b["k_dev"], cfg.slots, layer.gate.q,
+                                layer.gate.s, layer.gate.b, bits, moe.EPILOGUE_RAW, path=p)
+    raw_u = moe.moe_gate_up_qmm(x, b["sorted"], b["offsets"], b["k_dev"], cfg.slots, layer.up.q,
+                                layer.up.s, layer.up.b, bits, moe.EPILOGUE_RAW, path=p)
+    A = T * k
+    I = cfg.I
+    assert torch.equal(raw_f[:A, :I].view(torch.int32), raw_g[:A].view(torch.int32))
+    assert torch.equal(raw_f[:A, I:].view(torch.int32), raw_u[:A].view(torch.int32))
+    for dt in (torch.float32, torch.bfloat16):
+        fused = moe.moe_gate_up_qmm(x, b["sorted"], b["offsets"], b["k_dev"], cfg.slots, gu.q,
+                                    gu.s, gu.b, bits, moe.EPILOGUE_SWIGLU, out_dtype=dt, path=p)
+        sep = moe.moe_swiglu(raw_g, raw_u, b["k_dev"], T, cfg.slots, out_dtype=dt)
+        isz = torch.int32 if dt == torch.float32 else torch.int16
+        assert torch.equal(fused[:A].view(isz), sep[:A].view(isz)), dt
+    # and the RAW product itself matches the oracle
+    ref = oracle.moe_forward(x_bits, layer_np)
+    gq, gs, gb = oracle.pack_gate_up(layer_np.gate.q, layer_np.gate.s, layer_np.gate.b,
+                                     layer_np.up.q, layer_np.up.s, layer_np.up.b)
+    srt = ref.perm.sorted_assign
+    xf = oracle.bf16_to_f64(x_bits)
+    got = to_np(raw_f)[:A]
+    for e in range(E):
+        lo, hi = ref.perm.offsets[e], ref.perm.offsets[e + 1]
+        if hi > lo:
+            want = oracle.qmm_raw(xf[srt[lo:hi] // cfg.slots], gq[e], gs[e], gb[e], bits, cfg.H)
+            assert rel_l2(got[lo:hi], want) <= 1e-5
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_unfused_switch_matches_fused_bitwise(cuda_lib, path):
+    cfg = SMALL["batched_s"]
+    layer_np = workloads.make_layer(cfg)
+    x_bits = workloads.make_tokens(cfg)
+    p = path_id(cuda_lib, path)
+    _, fused = run_layer(cuda_lib, layer_np, x_bits, p)
+    old = os.environ.get("MOE_GB300_FUSE_GATE_UP")
+    os.environ["MOE_GB300_FUSE_GATE_UP"] = "0"
+    try:
+        layer, unfused = run_layer(cuda_lib, layer_np, x_bits, p)
+        assert not layer.fused
+    finally:
+        if old is None:
+            del os.environ["MOE_GB300_FUSE_GATE_UP"]
+        else:
+            os.environ["MOE_GB300_FUSE_GATE_UP"] = old
+    assert np.array_equal(fused, unfused)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_repeated_runs_are_bitwise_identical(cuda_lib, path):
+    cfg = SMALL["prefill_s"]
+    layer_np = workloads.make_layer(cfg)
+    x_bits = workloads.make_tokens(cfg)
+    layer = cuda_lib.MoELayer.from_workload(layer_np, dev(), path=path_id(cuda_lib, path))
+    x = cuda_lib.bf16_from_bits(x_bits, dev())
+    outs = [layer(x).clone() for _ in range(3)]
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
+# ------------------------------------------------- full sizes, sampled tokens
+
+FULL_SAMPLES = {"decode": None, "batched": None, "prefill": 48, "entropy": 24}
+
+
+@pytest.fixture(scope="module")
+def full_layers():
+    cache = {}
+
+    def get(name):
+        if name not in cache:
+            cache.clear()
+            cache[name] = workloads.make_layer(CFG[name])
+        return cache[name]
+    return get
+
+
+@pytest.mark.parametrize("name", ["decode", "batched", "prefill", "entropy"])
+def test_full_size_sampled(cuda_lib, full_layers, name):
+    cfg = CFG[name]
+    layer_np = full_layers(name)
+    d = dev()
+    rng = np.random.default_rng(7)
+    for b in range(cfg.batches):
+        x_all = workloads.make_tokens(cfg, 0, b)
+        layer = cuda_lib.MoELayer.from_workload(layer_np, d, batch=b)
+        if cfg.calls > 1:
+            # batch-1 decode: each call routes one token; check three calls
+            for c in (0, 100, 255):
+                x_bits = x_all[c:c + 1]
+                out = to_np(layer(cuda_lib.bf16_from_bits(x_bits, d)))
+                ref = oracle.moe_forward(x_bits, layer_np)
+                assert_layer_close(out, ref.out, f"decode call {c}")
+            continue
+        out = to_np(layer(cuda_lib.bf16_from_bits(x_all, d)))
+        n = FULL_SAMPLES[name]
+        toks = np.arange(cfg.T) if n is None else np.sort(rng.choice(cfg.T, n, replace=False))
+        ref = oracle.moe_forward(x_all, layer_np, inv_temperature=cfg.inv_temperature(b),
+                                 tokens=toks, keep_intermediates=False)
+        assert np.array_equal(to_np(layer.buffers(cfg.T)["topk_ids"]), ref.routing.ids)
+        assert_layer_close(out[toks], ref.out[toks], f"{name} batch {b}")
+        del layer
+        torch.cuda.empty_cache()

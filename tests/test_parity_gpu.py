@@ -1,0 +1,132 @@
+"""GPU path vs the CPU oracle, element by element, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from _parity import assert_layer_close, dev, rel_l2, route_gpu, to_np
+
+pytestmark = pytest.mark.gpu
+
+CFG = workloads.CONFIGS
+
+
+def shrunk(name, **kw):
+    return CFG[name].scaled(**kw)
+
+
+# Sizes the oracle finishes in seconds that still span several GEMV items and
+# 128-row tensor tiles with a ragged tail (I, H not multiples of 128).
+SMALL = {
+    "tiny": CFG["tiny"],
+    "decode_s": shrunk("decode", H=1088, I=1344, E=16, T=3, calls=1),
+    "batched_s": shrunk("batched", H=1024, I=576, E=24, T=48),
+    "prefill_s": shrunk("prefill", H=576, I=320, E=16, k=4, T=600),
+    "entropy_s": shrunk("entropy", H=1024, I=448, E=12, T=96,
+                        inv_temperatures=(12.0, 3.0, 0.5)),
+}
+
+
+# ------------------------------------------------------------------ router
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "batched", "prefill", "entropy"])
+def test_router_full_size_bit_exact(cuda_lib, name):
+    cfg = CFG[name]
+    layer = workloads.make_layer(cfg)
+    for b in range(cfg.batches):
+        x_bits = workloads.make_tokens(cfg, 0, b)
+        if cfg.calls > 1:
+            x_bits = x_bits[:64]   # decode: routing of 64 single-token calls, batched as T=64
+        it = cfg.inv_temperature(b)
+        ref = oracle.route(x_bits, layer.router_w, layer.logit_bias, it, cfg.k, cfg.slots)
+        _, ids, tw, kd, me = route_gpu(cuda_lib, x_bits, layer, cfg.k, cfg.slots, it)
+        assert int(kd.item()) == ref.k
+        assert np.array_equal(to_np(ids), ref.ids)
+        w = to_np(tw)
+        assert np.allclose(w, ref.weights, rtol=1e-6, atol=1e-7)
+        assert abs(float(me.item()) - float(ref.mean_entropy)) < 1e-4
+        if cfg.k == 0:
+            assert ref.k == b + 1   # the three entropy batches hit k = 1, 2, 3
+
+
+def test_router_single_token_calls(cuda_lib):
+    cfg = CFG["decode"]
+    rw = workloads.normal_f32(0, workloads.STREAM_ROUTER, (cfg.E, cfg.H), cfg.router_std)
+    L = type("L", (), {"router_w": rw, "logit_bias": None})
+    x_all = workloads.make_tokens(cfg)
+    for c in (0, 1, 255):
+        x_bits = x_all[c:c + 1]
+        ref = oracle.route(x_bits, rw, None, 1.0, cfg.k, cfg.k)
+        _, ids, tw, kd, me = route_gpu(cuda_lib, x_bits, L, cfg.k, cfg.k)
+        assert np.array_equal(to_np(ids), ref.ids)
+        assert np.allclose(to_np(tw), ref.weights, rtol=1e-6)
+
+
+@pytest.mark.parametrize("E,k,kmax,T,renorm,bias,it", [
+    (5, 2, 4, 7, True, False, 1.0),
+    (37, 3, 3, 33, False, True, 0.7),
+    (64, 1, 1, 17, True, True, 2.0),
+    (130, 8, 16, 40, True, False, 1.3),
+    (1024, 4, 4, 9, True, True, 1.0),
+    (8, 0, 5, 21, True, False, 3.0),    # adaptive with kmax > 3
+    (8, 0, 3, 21, False, True, 0.2),
+])
+def test_router_edge_shapes(cuda_lib, E, k, kmax, T, renorm, bias, it):
+    rng = np.random.default_rng(E * 100 + T)
+    H = 192
+    rw = rng.normal(0, 0.05, (E, H)).astype(np.float32)
+    if E > 6:
+        rw[6] = rw[2]      # exact ties between experts 2 and 6
+    lb = rng.normal(0, 0.5, E).astype(np.float32) if bias else None
+    L = type("L", (), {"router_w": rw, "logit_bias": lb})
+    x_bits = workloads.normal_bf16(1, 9, (T, H), 1.0)
+    ref = oracle.route(x_bits, rw, lb, it, k, kmax, renorm)
+    _, ids, tw, kd, me = route_gpu(cuda_lib, x_bits, L, k, kmax, it, renorm)
+    assert int(kd.item()) == ref.k
+    assert np.array_equal(to_np(ids), ref.ids)
+    assert np.allclose(to_np(tw), ref.weights, rtol=1e-6, atol=1e-7)
+
+
+def test_router_empty_batch(cuda_lib):
+    rw = np.zeros((8, 64), np.float32)
+    L = type("L", (), {"router_w": rw, "logit_bias": None})
+    _, ids, tw, kd, me = route_gpu(cuda_lib, np.zeros((0, 64), np.uint16), L, 0, 3)
+    assert int(kd.item()) == 1 and float(me.item()) == 0.0
+
+
+# ----------------------------------------------------------------- permute
+
+@pytest.mark.parametrize("T,kmax,k,E,skew", [(1, 4, 4, 64, False), (64, 4, 4, 64, True),
+                                             (4096, 8, 8, 128, False), (512, 3, 2, 32, False),
+                                             (300, 16, 16, 1024, False), (100, 3, 3, 4, True),
+                                             (0, 2, 2, 8, False)])
+def test_permute_bit_exact(cuda_lib, T, kmax, k, E, skew):
+    rng = np.random.default_rng(T + E)
+    ids = np.full((T, kmax), -1, np.int32)
+    for t in range(T):
+        if skew:
+            p = np.exp(-np.arange(E) * 0.5)
+            ids[t, :k] = rng.choice(E, size=k, replace=False, p=p / p.sum())
+        else:
+            ids[t, :k] = rng.choice(E, size=k, replace=False)
+    ref = oracle.permute(ids, k, E)
+    d = dev()
+    kd = torch.tensor([k], dtype=torch.int32, device=d)
+    cnt, off, srt, inv = cuda_lib.moe_permute(torch.from_numpy(ids).to(d), kd, E)
+    assert np.array_equal(to_np(cnt), ref.counts)
+    assert np.array_equal(to_np(off), ref.offsets)
+    A = T * k
+    assert np.array_equal(to_np(srt)[:A], ref.sorted_assign)
+    if T:
+        assert np.array_equal(to_np(inv)[:T * kmax], ref.inv_pos)
+
+
+def test_permute_flags_bad_expert(cuda_lib):
+    d = dev()
+    cuda_lib.moe_get_device_error(clear=True)
+    ids = torch.tensor([[0, 9], [1, 2]], dtype=torch.int32, device=d)
+    kd = torch.tensor([2], dtype=torch.int32, device=d)
+    cuda_lib.moe_permute(ids, kd, 4)
+    assert cuda_lib.moe_get_device_error(clear=True) & cuda_lib.DEVERR_BAD_EXPERT
+    assert cuda_lib.moe_get_device_error(clear=True) == 0

@@ -53,6 +53,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample", type=int, default=0, help="oracle sample size (calls/tokens)")
+    p.add_argument("--experts", type=int, default=0,
+                   help="smaller expert pool (same per-call work; for profiling captures)")
     return p.parse_args(argv)
 
 
@@ -234,6 +236,8 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     cfg = workloads.CONFIGS[args.config]
+    if args.experts:
+        cfg = cfg.scaled(E=args.experts)
     layer_np = workloads.make_layer(cfg)
     layer = moe.MoELayer.from_workload(layer_np, dev, free_sources=True)
     calls = cfg.calls

@@ -19,6 +19,7 @@ from ._lib import EPILOGUE_RAW, EPILOGUE_SWIGLU, PATH_AUTO, PATH_GEMV, PATH_TC, 
 
 FUSE_ENV = "MOE_GB300_FUSE_GATE_UP"
 TC_MIN_TOKENS_PER_EXPERT = 24  # mirrors the library's automatic path choice
+TC_BUILT = False               # the tensor-core grouped GEMM is not in this build yet
 
 
 @dataclasses.dataclass
@@ -113,7 +114,9 @@ class MoELayer:
     def resolved_path(self, T: int) -> int:
         if self.path != PATH_AUTO:
             return self.path
-        return PATH_TC if (T * self.kmax) // self.E >= TC_MIN_TOKENS_PER_EXPERT else PATH_GEMV
+        if TC_BUILT and (T * self.kmax) // self.E >= TC_MIN_TOKENS_PER_EXPERT:
+            return PATH_TC
+        return PATH_GEMV
 
     def buffers(self, T: int) -> dict:
         key = T

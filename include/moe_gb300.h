@@ -163,6 +163,37 @@ moe_status_t moe_router_topk(const uint16_t* x, const float* w_router, const flo
                              void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * moe_router_topk_noalloc -- moe_router_topk for callers that cannot
+ * allocate device memory.
+ *
+ * No page describes this call; it exists for integration only.  Some callers
+ * cannot get device memory on demand: a model runner that reserves the whole
+ * device pool at start-up and gives a plugged-in layer only its input and
+ * output tensors, or a deployment that forbids allocation after start-up
+ * because cudaMalloc can synchronize the device in the middle of a
+ * latency-bound decode loop.  This call takes no workspace; its scratch is a
+ * static device array inside the library holding 2 floats per token for up
+ * to MOE_ROUTER_NOALLOC_MAX_TOKENS tokens (512 KiB), kept by every GPU that
+ * loads the library until the process exits.  It allocates nothing.
+ *
+ * Arguments, outputs and results are those of moe_router_topk without
+ * workspace/workspace_bytes.  T > MOE_ROUTER_NOALLOC_MAX_TOKENS returns
+ * MOE_ERR_INVALID_ARG and launches nothing.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  All calls
+ * share the array: calls whose executions overlap on the GPU race, so the
+ * caller must order them (one stream, or events).  Nothing in the array
+ * needs clearing between calls.
+ * ---------------------------------------------------------------------- */
+#define MOE_ROUTER_NOALLOC_MAX_TOKENS 65536
+
+moe_status_t moe_router_topk_noalloc(const uint16_t* x, const float* w_router,
+                                     const float* logit_bias, float inv_temperature, int T,
+                                     int H, int E, int k_fixed, int kmax, float thr1, float thr2,
+                                     int renormalize, int32_t* topk_ids, float* topk_w,
+                                     int32_t* k_dev, float* mean_entropy, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * moe_permute -- group the assignments by expert (stable counting sort).
  *
  * Page [C], 如何验证正确性 (the sorted branch that groups token indices by

@@ -324,3 +324,116 @@ extern "C" moe_status_t moe_router_topk(const uint16_t* x, const float* w_router
   }
   return MOE_OK;
 }
+
+// ---------------------------------------------------------------------------
+// moe_router_topk_noalloc: the same router for callers that cannot allocate.
+//
+// Some callers of this layer have no way to obtain device memory on demand:
+// a model runner that reserves the whole device pool for itself at start-up
+// and hands plugins only the tensors of their inputs and outputs, or a
+// deployment that forbids allocation after initialisation because
+// cudaMalloc can synchronize the device and stall a latency-bound decode
+// loop.  This entry point needs nothing beyond its inputs and outputs: the
+// per-token scratch (entropy and softmax denominator, two floats per token)
+// lives in the file-scope array below, sized for
+// MOE_ROUTER_NOALLOC_MAX_TOKENS tokens (512 KiB).  Every GPU that loads the
+// library holds the array until the process exits.
+//
+// Host code must not pass the array's name to a kernel: on the host it is
+// only a stand-in symbol.  Its device address is looked up once per device,
+// with that device current, by the first call on that device
+// (cudaGetSymbolAddress); make that first call before any stream capture.
+// All calls share the array and it keeps the last call's contents; nothing
+// in it needs to start at zero, because every entry a call reads was written
+// earlier by the same call.  Calls whose executions overlap on the GPU (two
+// streams, say) race on the array and must be ordered by the caller.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+static __device__ __align__(256) float g_router_noalloc_scratch[2 * MOE_ROUTER_NOALLOC_MAX_TOKENS];
+
+namespace {
+
+constexpr int kNoallocMaxDevices = 64;
+float* g_noalloc_scratch_ptr[kNoallocMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Device address of the scratch array on the current device.
+moe_status_t noalloc_scratch(float** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev < 0 || dev >= kNoallocMaxDevices) return MOE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_router_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return MOE_ERR_CUDA;
+    g_noalloc_scratch_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_scratch_ptr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_router_topk_noalloc(const uint16_t* x, const float* w_router,
+                                                const float* logit_bias, float inv_temperature,
+                                                int T, int H, int E, int k_fixed, int kmax,
+                                                float thr1, float thr2, int renormalize,
+                                                int32_t* topk_ids, float* topk_w, int32_t* k_dev,
+                                                float* mean_entropy, moe_stream_t stream) {
+  using namespace moe_host;
+  if (T > MOE_ROUTER_NOALLOC_MAX_TOKENS) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || H <= 0 || H % 64 != 0 || E < 1 || E > kMaxExperts || kmax < 1 || kmax > 16)
+    return MOE_ERR_INVALID_ARG;
+  if (k_fixed < 0 || k_fixed > kmax || k_fixed > E) return MOE_ERR_INVALID_ARG;
+  if (k_fixed == 0 && (kmax < kAdaptiveMaxK || E < kAdaptiveMaxK)) return MOE_ERR_INVALID_ARG;
+  if (!(thr1 <= thr2)) return MOE_ERR_INVALID_ARG;
+  if (!k_dev || !mean_entropy) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !w_router || !topk_ids || !topk_w)) return MOE_ERR_INVALID_ARG;
+  if ((x && !aligned16(x)) || (w_router && !aligned16(w_router))) return MOE_ERR_INVALID_ARG;
+  if (logit_bias && (reinterpret_cast<uintptr_t>(logit_bias) & 3u)) return MOE_ERR_INVALID_ARG;
+
+  float* scratch = nullptr;
+  const moe_status_t sst = noalloc_scratch(&scratch);
+  if (sst != MOE_OK) return sst;
+
+  RouterParams p;
+  p.x = x;
+  p.w = w_router;
+  p.bias = logit_bias;
+  p.inv_temp = inv_temperature;
+  p.T = T;
+  p.H = H;
+  p.E = E;
+  p.k_fixed = k_fixed;
+  p.kmax = kmax;
+  p.thr1 = thr1;
+  p.thr2 = thr2;
+  p.renorm = renormalize ? 1 : 0;
+  p.ids = topk_ids;
+  p.topw = topk_w;
+  p.k_dev = k_dev;
+  p.mean_ent = mean_entropy;
+  p.ws_ent = scratch;
+  p.ws_sum = scratch + MOE_ROUTER_NOALLOC_MAX_TOKENS;
+  p.err = device_error_word();
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  const int nblocks = (T + kTokensPerCta - 1) / kTokensPerCta;
+  if (nblocks > 0) {
+    size_t smem = (size_t)kTokensPerCta * E * sizeof(float);
+    if (smem > 48 * 1024) {
+      if (cudaFuncSetAttribute(router_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    }
+    router_topk_kernel<<<nblocks, kRouterThreads, smem, st>>>(p);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+  }
+  if (nblocks != 1) {
+    router_finalize_kernel<<<1, kFinalizeThreads, 0, st>>>(p);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}

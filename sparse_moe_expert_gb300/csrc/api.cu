@@ -107,7 +107,7 @@ extern "C" moe_status_t moe_gate_up_qmm(const uint16_t* x, const int32_t* sorted
                                         moe_stream_t stream) {
   using namespace moe_host;
   if (!common_shape_ok(T, kmax, E)) return MOE_ERR_INVALID_ARG;
-  if (H <= 0 || H % 64 != 0 || n_rows <= 0) return MOE_ERR_INVALID_ARG;
+  if (H <= 0 || H % 64 != 0 || n_rows <= 0 || n_rows % 64 != 0) return MOE_ERR_INVALID_ARG;
   if (bits != 4 && bits != 8) return MOE_ERR_UNSUPPORTED;
   if (epilogue != MOE_EPILOGUE_RAW && epilogue != MOE_EPILOGUE_SWIGLU) return MOE_ERR_INVALID_ARG;
   if (out_dtype != MOE_DTYPE_F32 && out_dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;

@@ -6,26 +6,26 @@
 // activation, down projection); page "Qwen3.5 Block在llama.cpp中的映射与优化
 // 原理", section 4.2 (only the routed experts' weights are touched).
 //
-// Work: an item is (active expert, block of 8 warps x 4 weight rows).  The
-// CTAs of a persistent grid take equal contiguous ranges of the item list.
-// A CTA stages the activations of up to MT rows of the expert's segment in
-// shared memory as fp32 (with per-segment sums, see below) and every warp
-// streams its 4 weight rows once with 128-bit non-allocating loads,
-// prefetching the next segment, and applies them to all staged tokens.
+// Work.  An item is (active expert, block of 8 warps x 4 weight rows); the
+// CTAs of a persistent grid (two per SM) take equal contiguous ranges of the
+// item list.  A CTA stages the activations of up to MT rows of the expert's
+// segment in shared memory; each warp streams its 4 weight rows once with
+// 128-bit loads (one segment ahead) and applies them to every staged token;
+// lane partials are combined by a fixed xor butterfly.  SWIGLU warps hold
+// gate rows n, n+1 and up rows n, n+1, so the activation is applied in
+// registers.
 //
-// Dequantization in registers.  A lane takes a 16-byte segment of a row
-// (32 four-bit or 16 eight-bit codes).  Per group of 64 elements
+// Dequantization in registers.  Per group of 64 elements
 //   sum_i x_i (s q_i + b) = s * sum_i x_i q_i + b * sum_i x_i,
-// so only sum x_i q_i needs the codes.  A code is moved into the top of a
-// float mantissa by one shift and one LOP3: the bit pattern 0x3F800000 |
-// (q << p) is the float 1 + q * 2^(p-23), exact, and x * (1 + q 2^(p-23)) is
-// exact in fp32 as well.  Starting the accumulator at -sum x (staged with the
-// activations) leaves 2^(p-23) * sum x q.  Codes of adjacent elements sit at
-// two positions of one shifted word (4-bit: p = 14 and 18) and are combined
-// with one packed fp32x2 FMA.  Every row is reduced in the same order (lane
-// segments ascending, then an xor butterfly), whatever rows it is computed
-// with, so the fused gate_up product equals the separate gate and up products
-// bit for bit.
+// so only sum x_i q_i needs the codes.  One shift and one LOP3 turn two codes
+// of a word into the bf16 pair (128 + q_j, 128 + q_{j+4}) (exact: bf16 holds
+// 128..255), each half feeding one fp32-accumulating bf16 FMA
+// (fma.rn.f32.bf16) against the bf16 activation.  Activations are staged per
+// token in that pair order together with their sums X per 32 codes, so
+// sum x q = sum x (128 + q) - 128 X.  8-bit codes are read as two 4-bit codes
+// (low, high) against activations (x, 16 x), exact in bf16.  Every row is
+// reduced in the same order whatever rows it is computed with, so the fused
+// gate_up product equals the separate gate and up products bit for bit.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -59,57 +59,131 @@ struct GemvParams {
 };
 
 template <int BITS>
-struct Seg {
-  static constexpr int kElems = 128 / BITS;       // elements per 16-byte segment
-  static constexpr int kVec4 = kElems / 4;        // float4 vectors per segment
-  static constexpr int kSegsPerGroup = 64 / kElems;
+struct Width {
+  static constexpr int kNibPerElem = BITS / 4;            // 1 or 2
+  static constexpr int kSegPerGroup = 64 * kNibPerElem / 32;  // 2 or 4
 };
 
-// sum_i x_i q_i over one segment, given the segment's staged activations
-// (fp32, natural order) and acc0 = (-sum of even-position x, -sum of odd x).
+// acc += a_half * b_half for the low (hi = false) or high halves of two
+// registers holding bf16 pairs; fp32 accumulation.
+__device__ __forceinline__ void bf16_fma(float& acc, uint32_t a_pair, uint32_t b_pair, bool hi) {
+  unsigned short a_lo, a_hi, b_lo, b_hi;
+  asm("mov.b32 {%0,%1}, %2;" : "=h"(a_lo), "=h"(a_hi) : "r"(a_pair));
+  asm("mov.b32 {%0,%1}, %2;" : "=h"(b_lo), "=h"(b_hi) : "r"(b_pair));
+  if (hi)
+    asm("fma.rn.f32.bf16 %0, %1, %2, %0;" : "+f"(acc) : "h"(a_hi), "h"(b_hi));
+  else
+    asm("fma.rn.f32.bf16 %0, %1, %2, %0;" : "+f"(acc) : "h"(a_lo), "h"(b_lo));
+}
+
+// Stage the activations of `nt` rows starting at sorted row r0 into xs (bf16
+// pairs in code-pair order, 16 words per 32-nibble segment, vectors rotated
+// by segment to avoid bank conflicts) and their per-segment sums.
 template <int BITS>
-__device__ __forceinline__ float seg_dot(const uint4& w, const float* x, float2 acc) {
-  const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-  if constexpr (BITS == 4) {
+__device__ void stage_activations(const GemvParams& p, int r0, int nt, uint32_t* xs, float2* xsum,
+                                  int NK, int nseg_row) {
+  const int K = p.K;
+  for (int idx = threadIdx.x; idx < nt * nseg_row; idx += kGemvThreads) {
+    const int t = idx / nseg_row, sg = idx - t * nseg_row;
+    const int64_t r = r0 + t;
+    uint32_t v[32];  // bf16 bits of the 32 nibble-order activation values
+    if (BITS == 4) {
+      const int k0 = sg * 32;
+      if (p.act_kind == kActF32) {
+        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.act) + r * K + k0);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t v = words[i];
-      const uint32_t sh[4] = {v << 14, v << 6, v >> 2, v >> 10};
+        for (int c = 0; c < 8; ++c) {
+          const float4 u = __ldg(src + c);
+          v[4 * c] = f32_to_bf16_rne(u.x);
+          v[4 * c + 1] = f32_to_bf16_rne(u.y);
+          v[4 * c + 2] = f32_to_bf16_rne(u.z);
+          v[4 * c + 3] = f32_to_bf16_rne(u.w);
+        }
+      } else {
+        const int64_t row = p.act_kind == kActXbf16 ? (int64_t)(__ldg(p.sorted + r) / p.kmax) : r;
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.act) + row * K + k0);
 #pragma unroll
-      for (int pq = 0; pq < 4; ++pq) {
-        float a = __uint_as_float((sh[pq] & 0x0003C000u) | 0x3F800000u);  // 1 + q_even/512
-        float b = __uint_as_float((sh[pq] & 0x003C0000u) | 0x3F800000u);  // 1 + q_odd/32
-        acc = ffma2(make_float2(a, b), make_float2(x[8 * i + 2 * pq], x[8 * i + 2 * pq + 1]), acc);
+        for (int c = 0; c < 4; ++c) {
+          const uint4 u = __ldg(src + c);
+          const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            v[8 * c + 2 * q] = w4[q] & 0xFFFFu;
+            v[8 * c + 2 * q + 1] = w4[q] >> 16;
+          }
+        }
+      }
+    } else {
+      // 8-bit: 16 elements; nibble 2i <- x_i, nibble 2i+1 <- 16 x_i
+      const int k0 = sg * 16;
+      float xf[16];
+      if (p.act_kind == kActF32) {
+        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.act) + r * K + k0);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float4 u = __ldg(src + c);
+          xf[4 * c] = bf16_bits_to_f32(f32_to_bf16_rne(u.x));
+          xf[4 * c + 1] = bf16_bits_to_f32(f32_to_bf16_rne(u.y));
+          xf[4 * c + 2] = bf16_bits_to_f32(f32_to_bf16_rne(u.z));
+          xf[4 * c + 3] = bf16_bits_to_f32(f32_to_bf16_rne(u.w));
+        }
+      } else {
+        const int64_t row = p.act_kind == kActXbf16 ? (int64_t)(__ldg(p.sorted + r) / p.kmax) : r;
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.act) + row * K + k0);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const uint4 u = __ldg(src + c);
+          const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = bf16x2_to_f32x2(w4[q]);
+            xf[8 * c + 2 * q] = f.x;
+            xf[8 * c + 2 * q + 1] = f.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        v[2 * i] = __float_as_uint(xf[i]) >> 16;
+        v[2 * i + 1] = __float_as_uint(16.0f * xf[i]) >> 16;
       }
     }
-    return fmaf(512.0f, acc.x, 32.0f * acc.y);
-  } else {
+    float sum = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t v = words[i];
-      float a0 = __uint_as_float(((v << 15) & 0x007F8000u) | 0x3F800000u);  // 1 + byte0/256
-      float b0 = __uint_as_float(((v << 7) & 0x007F8000u) | 0x3F800000u);   // 1 + byte1/256
-      float a1 = __uint_as_float(((v >> 1) & 0x007F8000u) | 0x3F800000u);   // 1 + byte2/256
-      float b1 = __uint_as_float(((v >> 9) & 0x007F8000u) | 0x3F800000u);   // 1 + byte3/256
-      acc = ffma2(make_float2(a0, b0), make_float2(x[4 * i], x[4 * i + 1]), acc);
-      acc = ffma2(make_float2(a1, b1), make_float2(x[4 * i + 2], x[4 * i + 3]), acc);
+    for (int i = 0; i < 32; ++i) sum += bf16_bits_to_f32(v[i]);
+    float esum = sum;
+    if (BITS == 8) {
+      esum = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) esum += bf16_bits_to_f32(v[i]);
     }
-    return 256.0f * (acc.x + acc.y);
+    uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)t * (NK / 2) + (size_t)sg * 16);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint4 o;
+      o.x = v[8 * c + 0] | (v[8 * c + 4] << 16);
+      o.y = v[8 * c + 1] | (v[8 * c + 5] << 16);
+      o.z = v[8 * c + 2] | (v[8 * c + 6] << 16);
+      o.w = v[8 * c + 3] | (v[8 * c + 7] << 16);
+      dst[(c + (sg >> 1)) & 3] = o;
+    }
+    xsum[t * nseg_row + sg] = make_float2(sum, esum);
   }
 }
 
 template <int BITS, int MODE, int MT>
-__global__ void __launch_bounds__(kGemvThreads, 2) gemv_qmm_kernel(GemvParams p) {
-  using S = Seg<BITS>;
-  extern __shared__ __align__(16) float gsm[];
+__global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_qmm_kernel(GemvParams p) {
+  using W = Width<BITS>;
+  extern __shared__ __align__(16) unsigned char gsm[];
   const int K = p.K;
-  const int nseg = K / S::kElems;
-  float* xs = gsm;                                        // [MT][K] swizzled
-  float2* xsum = reinterpret_cast<float2*>(gsm + MT * K);  // [MT][nseg]
+  const int NK = K * W::kNibPerElem;  // nibbles per row
+  const int nseg = NK / 32;           // 16-byte code segments per row
+  const int ngroups = K / 64;
+  uint32_t* xs = reinterpret_cast<uint32_t*>(gsm);                          // [MT][NK/2]
+  float2* xsum = reinterpret_cast<float2*>(gsm + (size_t)MT * (NK / 2) * 4);  // [MT][nseg]
   __shared__ int act_e[1024];
   __shared__ int n_act_sh;
-  // what is staged in xs; every thread keeps the same copy
-  int tag_e = -1, tag_r0 = -1, tag_nt = 0;
+  __shared__ int wtot[kGemvWarps];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = p.E;
@@ -119,9 +193,8 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_qmm_kernel(GemvParams p)
   __syncthreads();
   for (int base = 0; base < E; base += kGemvThreads) {
     const int e = base + tid;
-    const bool act = e < E && (p.offsets[e + 1] - p.offsets[e]) > 0;
+    const bool act = e < E && (__ldg(p.offsets + e + 1) - __ldg(p.offsets + e)) > 0;
     const unsigned bal = __ballot_sync(0xFFFFFFFFu, act);
-    __shared__ int wtot[kGemvWarps];
     if (lane == 0) wtot[warp] = __popc(bal);
     __syncthreads();
     int before = n_act_sh;
@@ -139,16 +212,17 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_qmm_kernel(GemvParams p)
   const int64_t n_items = (int64_t)n_act * p.items_per_expert;
   const int64_t it0 = n_items * blockIdx.x / gridDim.x;
   const int64_t it1 = n_items * (blockIdx.x + 1) / gridDim.x;
-
-  const int ngroups = K / 64;
-  const int64_t row_words = (int64_t)K * BITS / 32;
+  const int64_t row_u4 = (int64_t)NK / 32;  // uint4 per row
   const int half = p.n_rows / 2;
+
+  // what is staged in xs (every thread keeps the same copy)
+  int tag_r0 = -1, tag_nt = -1;
 
   for (int64_t it = it0; it < it1; ++it) {
     const int e = act_e[it / p.items_per_expert];
     const int ub = (int)(it % p.items_per_expert);
-    const int seg_lo = p.offsets[e];
-    const int m = p.offsets[e + 1] - seg_lo;
+    const int seg_lo = __ldg(p.offsets + e);
+    const int m = __ldg(p.offsets + e + 1) - seg_lo;
 
     // this warp's 4 weight rows and output columns
     int wrow[kRowsPerWarp];
@@ -160,18 +234,18 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_qmm_kernel(GemvParams p)
       for (int q = 0; q < 2; ++q) {
         const int u = u0 + q;
         const int uc = u < p.n_out ? u : p.n_out - 1;
-        wrow[q] = uc;            // gate row
-        wrow[2 + q] = half + uc; // up row
+        wrow[q] = uc;             // gate row
+        wrow[2 + q] = half + uc;  // up row
         ocol[q] = u;
         ovalid[q] = u < p.n_out;
         ocol[2 + q] = u;
         ovalid[2 + q] = false;
       }
     } else {
-      const int r0 = ub * p.units_per_item + warp * kRowsPerWarp;
+      const int r0w = ub * p.units_per_item + warp * kRowsPerWarp;
 #pragma unroll
       for (int q = 0; q < kRowsPerWarp; ++q) {
-        const int r = r0 + q;
+        const int r = r0w + q;
         wrow[q] = r < p.n_rows ? r : p.n_rows - 1;
         ocol[q] = r;
         ovalid[q] = r < p.n_rows;
@@ -183,7 +257,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_qmm_kernel(GemvParams p)
 #pragma unroll
     for (int q = 0; q < kRowsPerWarp; ++q) {
       const int64_t grow = (int64_t)e * p.n_rows + wrow[q];
-      wptr[q] = reinterpret_cast<const uint4*>(p.wq + grow * row_words);
+      wptr[q] = reinterpret_cast<const uint4*>(p.wq) + grow * row_u4;
       sptr[q] = p.ws + grow * ngroups;
       bptr[q] = p.wb + grow * ngroups;
     }
@@ -191,66 +265,20 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_qmm_kernel(GemvParams p)
     for (int tc = 0; tc < m; tc += MT) {
       const int nt = min(MT, m - tc);
       const int r0 = seg_lo + tc;
-      // ---- stage activations (skipped when already staged) ----
-      bool same = false;
-      if (p.act_kind == kActXbf16) {
-        // tokens of the staged rows equal those of these rows?
-        same = tag_nt == nt && tag_e >= 0;
-        if (same) {
+      // ---- stage the activations when they changed ----
+      bool same = tag_nt == nt;
+      if (same) {
+        if (p.act_kind == kActXbf16) {
           for (int t = 0; t < nt; ++t)
-            same = same && (p.sorted[tag_r0 + t] / p.kmax) == (p.sorted[r0 + t] / p.kmax);
+            same = same && (__ldg(p.sorted + tag_r0 + t) / p.kmax) == (__ldg(p.sorted + r0 + t) / p.kmax);
+        } else {
+          same = tag_r0 == r0;
         }
-      } else {
-        same = tag_r0 == r0 && tag_nt == nt;
       }
       if (!same) {
         __syncthreads();  // everyone is done with the previous staging
-        for (int idx = tid; idx < nt * nseg; idx += kGemvThreads) {
-          const int t = idx / nseg, sg = idx - t * nseg;
-          float v[S::kElems];
-          if (p.act_kind == kActXbf16) {
-            const int tok = p.sorted[r0 + t] / p.kmax;
-            const uint4* src = reinterpret_cast<const uint4*>(
-                static_cast<const uint16_t*>(p.act) + (int64_t)tok * K + sg * S::kElems);
-#pragma unroll
-            for (int c = 0; c < S::kElems / 8; ++c) {
-              uint4 u = __ldg(src + c);
-              float2 a = bf16x2_to_f32x2(u.x), b = bf16x2_to_f32x2(u.y);
-              float2 cc = bf16x2_to_f32x2(u.z), d = bf16x2_to_f32x2(u.w);
-              v[8 * c + 0] = a.x; v[8 * c + 1] = a.y; v[8 * c + 2] = b.x; v[8 * c + 3] = b.y;
-              v[8 * c + 4] = cc.x; v[8 * c + 5] = cc.y; v[8 * c + 6] = d.x; v[8 * c + 7] = d.y;
-            }
-          } else if (p.act_kind == kActF32) {
-            const float4* src = reinterpret_cast<const float4*>(
-                static_cast<const float*>(p.act) + (int64_t)(r0 + t) * K + sg * S::kElems);
-#pragma unroll
-            for (int c = 0; c < S::kVec4; ++c) {
-              float4 u = __ldg(src + c);
-              v[4 * c] = u.x; v[4 * c + 1] = u.y; v[4 * c + 2] = u.z; v[4 * c + 3] = u.w;
-            }
-          } else {
-            const uint4* src = reinterpret_cast<const uint4*>(
-                static_cast<const uint16_t*>(p.act) + (int64_t)(r0 + t) * K + sg * S::kElems);
-#pragma unroll
-            for (int c = 0; c < S::kElems / 8; ++c) {
-              uint4 u = __ldg(src + c);
-              float2 a = bf16x2_to_f32x2(u.x), b = bf16x2_to_f32x2(u.y);
-              float2 cc = bf16x2_to_f32x2(u.z), d = bf16x2_to_f32x2(u.w);
-              v[8 * c + 0] = a.x; v[8 * c + 1] = a.y; v[8 * c + 2] = b.x; v[8 * c + 3] = b.y;
-              v[8 * c + 4] = cc.x; v[8 * c + 5] = cc.y; v[8 * c + 6] = d.x; v[8 * c + 7] = d.y;
-            }
-          }
-          float se = 0.0f, so = 0.0f;
-#pragma unroll
-          for (int i = 0; i < S::kElems; i += 2) { se += v[i]; so += v[i + 1]; }
-          float4* dst = reinterpret_cast<float4*>(xs + (int64_t)t * K + sg * S::kElems);
-#pragma unroll
-          for (int c = 0; c < S::kVec4; ++c)
-            dst[(c + sg) % S::kVec4] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-          xsum[t * nseg + sg] = make_float2(-se, -so);
-        }
+        stage_activations<BITS>(p, r0, nt, xs, xsum, NK, nseg);
         __syncthreads();
-        tag_e = e;
         tag_r0 = r0;
         tag_nt = nt;
       }
@@ -262,42 +290,69 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_qmm_kernel(GemvParams p)
 #pragma unroll
         for (int t = 0; t < MT; ++t) tot[q][t] = 0.0f;
 
+      // codes, scales and biases of the next segment are loaded one step ahead
       uint4 wn[kRowsPerWarp];
+      uint16_t sn[kRowsPerWarp], bn[kRowsPerWarp];
       if (lane < nseg) {
+        const int g = lane / W::kSegPerGroup;
 #pragma unroll
-        for (int q = 0; q < kRowsPerWarp; ++q) wn[q] = ldg_nc_v4(wptr[q] + lane);
+        for (int q = 0; q < kRowsPerWarp; ++q) {
+          wn[q] = ldg_nc_v4(wptr[q] + lane);
+          sn[q] = __ldg(sptr[q] + g);
+          bn[q] = __ldg(bptr[q] + g);
+        }
       }
       for (int sg = lane; sg < nseg; sg += 32) {
         uint4 wc[kRowsPerWarp];
-#pragma unroll
-        for (int q = 0; q < kRowsPerWarp; ++q) wc[q] = wn[q];
-        if (sg + 32 < nseg) {
-#pragma unroll
-          for (int q = 0; q < kRowsPerWarp; ++q) wn[q] = ldg_nc_v4(wptr[q] + sg + 32);
-        }
-        const int g = sg / S::kSegsPerGroup;
         float sc[kRowsPerWarp], bi[kRowsPerWarp];
 #pragma unroll
         for (int q = 0; q < kRowsPerWarp; ++q) {
-          sc[q] = f16_bits_to_f32(__ldg(sptr[q] + g));
-          bi[q] = f16_bits_to_f32(__ldg(bptr[q] + g));
+          wc[q] = wn[q];
+          sc[q] = f16_bits_to_f32(sn[q]);
+          bi[q] = f16_bits_to_f32(bn[q]);
         }
+        if (sg + 32 < nseg) {
+          const int gn = (sg + 32) / W::kSegPerGroup;
 #pragma unroll
-        for (int t = 0; t < MT; ++t) {
-          if (t < nt) {
-            float xv[S::kElems];
-            const float4* src = reinterpret_cast<const float4*>(xs + (int64_t)t * K + sg * S::kElems);
+          for (int q = 0; q < kRowsPerWarp; ++q) {
+            wn[q] = ldg_nc_v4(wptr[q] + sg + 32);
+            sn[q] = __ldg(sptr[q] + gn);
+            bn[q] = __ldg(bptr[q] + gn);
+          }
+        }
+        const uint4* xsrc0 = reinterpret_cast<const uint4*>(xs + (size_t)sg * 16);
+        const int rot = sg >> 1;
 #pragma unroll
-            for (int c = 0; c < S::kVec4; ++c) {
-              float4 u = src[(c + sg) % S::kVec4];
-              xv[4 * c] = u.x; xv[4 * c + 1] = u.y; xv[4 * c + 2] = u.z; xv[4 * c + 3] = u.w;
-            }
-            const float2 ns = xsum[t * nseg + sg];
-            const float xsum_seg = -(ns.x + ns.y);
+        for (int q = 0; q < kRowsPerWarp; ++q) {
+          // code pairs (128 + q_j, 128 + q_{j+4}) of this row's segment
+          uint32_t ep[16];
+          const uint32_t w4[4] = {wc[q].x, wc[q].y, wc[q].z, wc[q].w};
 #pragma unroll
-            for (int q = 0; q < kRowsPerWarp; ++q) {
-              const float sxq = seg_dot<BITS>(wc[q], xv, ns);
-              tot[q][t] = fmaf(sc[q], sxq, fmaf(bi[q], xsum_seg, tot[q][t]));
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) ep[4 * i + j] = ((w4[i] >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+#pragma unroll
+          for (int t = 0; t < MT; ++t) {
+            if (t < nt) {
+              const uint4* xsrc = xsrc0 + (size_t)t * (NK / 8);
+              uint32_t xp[16];
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const uint4 u = xsrc[(c + rot) & 3];
+                xp[4 * c] = u.x;
+                xp[4 * c + 1] = u.y;
+                xp[4 * c + 2] = u.z;
+                xp[4 * c + 3] = u.w;
+              }
+              const float2 X = xsum[t * nseg + sg];
+              float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                bf16_fma(a0, ep[i], xp[i], false);
+                bf16_fma(a1, ep[i], xp[i], true);
+              }
+              const float sxq = fmaf(-128.0f, X.x, a0 + a1);
+              tot[q][t] = fmaf(sc[q], sxq, fmaf(bi[q], X.y, tot[q][t]));
             }
           }
         }
@@ -336,10 +391,9 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_qmm_kernel(GemvParams p)
 
 template <int BITS, int MODE, int MT>
 moe_status_t launch_gemv(const GemvParams& p, int max_active, cudaStream_t st) {
-  using S = Seg<BITS>;
   auto kern = gemv_qmm_kernel<BITS, MODE, MT>;
-  const int nseg = p.K / S::kElems;
-  const size_t smem = (size_t)MT * p.K * sizeof(float) + (size_t)MT * nseg * sizeof(float2);
+  const int NK = p.K * (BITS / 4);
+  const size_t smem = (size_t)MT * (NK / 2) * 4 + (size_t)MT * (NK / 32) * sizeof(float2);
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
@@ -351,8 +405,8 @@ moe_status_t launch_gemv(const GemvParams& p, int max_active, cudaStream_t st) {
       occ < 1)
     return MOE_ERR_CUDA;
   const int64_t items = (int64_t)max_active * p.items_per_expert;
-  const int64_t slots = (int64_t)moe_host::sm_count() * occ;
   if (items <= 0) return MOE_OK;
+  const int64_t slots = (int64_t)moe_host::sm_count() * occ;
   const int64_t per = (items + slots - 1) / slots;
   const int grid = (int)((items + per - 1) / per);
   kern<<<grid, kGemvThreads, smem, st>>>(p);
@@ -360,16 +414,20 @@ moe_status_t launch_gemv(const GemvParams& p, int max_active, cudaStream_t st) {
 }
 
 template <int MODE>
-moe_status_t dispatch_gemv(const GemvParams& p, int bits, int max_active, cudaStream_t st) {
-  // MT: tokens staged at a time, bounded by ~100 KB of shared memory
-  const int K = p.K;
+moe_status_t dispatch_gemv(const GemvParams& p, int bits, int max_tokens, int max_active,
+                           cudaStream_t st) {
+  // MT: tokens applied per pass over the weights, at most the tokens an expert
+  // can have (max_tokens) and bounded by shared memory
+  const int NK = p.K * (bits / 4);
+  int mt = NK <= 6144 ? 4 : (NK <= 12288 ? 2 : 1);
+  if (max_tokens < mt) mt = max_tokens <= 1 ? 1 : 2;
   if (bits == 4) {
-    if (K <= 6144) return launch_gemv<4, MODE, 4>(p, max_active, st);
-    if (K <= 12288) return launch_gemv<4, MODE, 2>(p, max_active, st);
+    if (mt == 4) return launch_gemv<4, MODE, 4>(p, max_active, st);
+    if (mt == 2) return launch_gemv<4, MODE, 2>(p, max_active, st);
     return launch_gemv<4, MODE, 1>(p, max_active, st);
   } else {
-    if (K <= 6144) return launch_gemv<8, MODE, 4>(p, max_active, st);
-    if (K <= 12288) return launch_gemv<8, MODE, 2>(p, max_active, st);
+    if (mt == 4) return launch_gemv<8, MODE, 4>(p, max_active, st);
+    if (mt == 2) return launch_gemv<8, MODE, 2>(p, max_active, st);
     return launch_gemv<8, MODE, 1>(p, max_active, st);
   }
 }
@@ -402,8 +460,10 @@ moe_status_t gemv_qmm(const void* act, int act_kind, const int32_t* sorted,
   const int64_t slots = (int64_t)T * kmax;
   const int max_active = (int)(slots < E ? slots : E);
   if (max_active == 0) return MOE_OK;
-  return swiglu ? dispatch_gemv<kSwiglu>(p, bits, max_active, st)
-                : dispatch_gemv<kRaw>(p, bits, max_active, st);
+  // an expert's segment holds at most one row per token (its k ids are distinct)
+  const int max_tokens = T;
+  return swiglu ? dispatch_gemv<kSwiglu>(p, bits, max_tokens, max_active, st)
+                : dispatch_gemv<kRaw>(p, bits, max_tokens, max_active, st);
 }
 
 }  // namespace moe

@@ -122,7 +122,9 @@ class MoELayer:
         key = T
         if key not in self._bufs:
             dev, A = self.device, max(T * self.kmax, 1)
-            h_dtype = torch.bfloat16 if self.resolved_path(T) == PATH_TC else torch.float32
+            # both kernel families consume h as bf16 (the GEMV's FMAs take bf16
+            # operands, the tensor cores bf16 tiles)
+            h_dtype = torch.bfloat16
             bufs = dict(
                 topk_ids=torch.empty((T, self.kmax), dtype=torch.int32, device=dev),
                 topk_w=torch.empty((T, self.kmax), dtype=torch.float32, device=dev),

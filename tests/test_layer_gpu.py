@@ -40,6 +40,8 @@ def test_layer_small_configs(cuda_lib, name, path):
         A = len(ref.perm.sorted_assign)
         h = to_np(bufs["h"])[:A]
         y = to_np(bufs["y"])[:A]
+        # h is stored as bf16: its rounding (2^-9 relative, ~1.6e-3 rel L2)
+        # dominates; y is computed from the rounded h
         h_tol = 1e-4 if bufs["h"].dtype == torch.float32 else 4e-3
         assert rel_l2(h, ref.h) <= h_tol, f"h {rel_l2(h, ref.h):.2e}"
         assert rel_l2(y, ref.y) <= 2 * h_tol, f"y {rel_l2(y, ref.y):.2e}"

@@ -215,177 +215,182 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_qmm_kernel
   const int64_t row_u4 = (int64_t)NK / 32;  // uint4 per row
   const int half = p.n_rows / 2;
 
+  // A pass applies one item's rows to one chunk of at most MT of its
+  // tokens.  Passes follow each other without a gap: the first segment of
+  // the next pass is loaded during the last segment of the current one.
+  struct Pass {
+    int it, tc, seg_lo, m;
+    int col0;                // first output column of this warp
+    int grow[kRowsPerWarp];  // weight rows (global index e*n_rows + row)
+  };
+  auto make_pass = [&](int it, int tc, Pass& ps) {
+    ps.it = it;
+    ps.tc = tc;
+    const int e = act_e[it / p.items_per_expert];
+    const int ub = it % p.items_per_expert;
+    ps.seg_lo = __ldg(p.offsets + e);
+    ps.m = __ldg(p.offsets + e + 1) - ps.seg_lo;
+    const int base = e * p.n_rows;
+    if (MODE == kSwiglu) {
+      ps.col0 = ub * p.units_per_item + warp * 2;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int u = ps.col0 + q;
+        const int uc = u < p.n_out ? u : p.n_out - 1;
+        ps.grow[q] = base + uc;             // gate row
+        ps.grow[2 + q] = base + half + uc;  // up row
+      }
+    } else {
+      ps.col0 = ub * p.units_per_item + warp * kRowsPerWarp;
+#pragma unroll
+      for (int q = 0; q < kRowsPerWarp; ++q) {
+        const int r = ps.col0 + q;
+        ps.grow[q] = base + (r < p.n_rows ? r : p.n_rows - 1);
+      }
+    }
+  };
+  // codes, scale and bias of segment sg of the pass's rows
+  uint4 wn[kRowsPerWarp];
+  uint16_t sn[kRowsPerWarp], bn[kRowsPerWarp];
+  auto load_segment = [&](const Pass& ps, int sg) {
+    const int g = sg / W::kSegPerGroup;
+#pragma unroll
+    for (int q = 0; q < kRowsPerWarp; ++q) {
+      const int64_t grow = ps.grow[q];
+      wn[q] = ldg_nc_v4(reinterpret_cast<const uint4*>(p.wq) + grow * row_u4 + sg);
+      sn[q] = __ldg(p.ws + grow * ngroups + g);
+      bn[q] = __ldg(p.wb + grow * ngroups + g);
+    }
+  };
+
   // what is staged in xs (every thread keeps the same copy)
   int tag_r0 = -1, tag_nt = -1;
 
-  for (int64_t it = it0; it < it1; ++it) {
-    const int e = act_e[it / p.items_per_expert];
-    const int ub = (int)(it % p.items_per_expert);
-    const int seg_lo = __ldg(p.offsets + e);
-    const int m = __ldg(p.offsets + e + 1) - seg_lo;
-
-    // this warp's 4 weight rows and output columns
-    int wrow[kRowsPerWarp];
-    int ocol[kRowsPerWarp];
-    bool ovalid[kRowsPerWarp];
-    if (MODE == kSwiglu) {
-      const int u0 = ub * p.units_per_item + warp * 2;
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int u = u0 + q;
-        const int uc = u < p.n_out ? u : p.n_out - 1;
-        wrow[q] = uc;             // gate row
-        wrow[2 + q] = half + uc;  // up row
-        ocol[q] = u;
-        ovalid[q] = u < p.n_out;
-        ocol[2 + q] = u;
-        ovalid[2 + q] = false;
-      }
+  if (it0 >= it1) return;
+  Pass cur, nxt;
+  make_pass((int)it0, 0, cur);
+  if (lane < nseg) load_segment(cur, lane);
+  for (;;) {
+    // the pass after this one
+    bool has_next = true;
+    if (cur.tc + MT < cur.m) {
+      nxt = cur;
+      nxt.tc = cur.tc + MT;
+    } else if (cur.it + 1 < it1) {
+      make_pass(cur.it + 1, 0, nxt);
     } else {
-      const int r0w = ub * p.units_per_item + warp * kRowsPerWarp;
+      has_next = false;
+    }
+    const int nt = min(MT, cur.m - cur.tc);
+    const int r0 = cur.seg_lo + cur.tc;
+    // ---- stage the activations when they changed ----
+    bool same = tag_nt == nt;
+    if (same) {
+      if (p.act_kind == kActXbf16) {
+        for (int t = 0; t < nt; ++t)
+          same = same && (__ldg(p.sorted + tag_r0 + t) / p.kmax) == (__ldg(p.sorted + r0 + t) / p.kmax);
+      } else {
+        same = tag_r0 == r0;
+      }
+    }
+    if (!same) {
+      __syncthreads();  // everyone is done with the previous staging
+      stage_activations<BITS>(p, r0, nt, xs, xsum, NK, nseg);
+      __syncthreads();
+      tag_r0 = r0;
+      tag_nt = nt;
+    }
+
+    // ---- stream the weights ----
+    float tot[kRowsPerWarp][MT];
+#pragma unroll
+    for (int q = 0; q < kRowsPerWarp; ++q)
+#pragma unroll
+      for (int t = 0; t < MT; ++t) tot[q][t] = 0.0f;
+
+    for (int sg = lane; sg < nseg; sg += 32) {
+      uint4 wc[kRowsPerWarp];
+      float sc[kRowsPerWarp], bi[kRowsPerWarp];
 #pragma unroll
       for (int q = 0; q < kRowsPerWarp; ++q) {
-        const int r = r0w + q;
-        wrow[q] = r < p.n_rows ? r : p.n_rows - 1;
-        ocol[q] = r;
-        ovalid[q] = r < p.n_rows;
+        wc[q] = wn[q];
+        sc[q] = f16_bits_to_f32(sn[q]);
+        bi[q] = f16_bits_to_f32(bn[q]);
+      }
+      if (sg + 32 < nseg)
+        load_segment(cur, sg + 32);
+      else if (has_next)
+        load_segment(nxt, lane);
+      const uint4* xsrc0 = reinterpret_cast<const uint4*>(xs + (size_t)sg * 16);
+      const int rot = sg >> 1;
+#pragma unroll
+      for (int q = 0; q < kRowsPerWarp; ++q) {
+        // code pairs (128 + q_j, 128 + q_{j+4}) of this row's segment
+        uint32_t ep[16];
+        const uint32_t w4[4] = {wc[q].x, wc[q].y, wc[q].z, wc[q].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) ep[4 * i + j] = ((w4[i] >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+          if (t < nt) {
+            const uint4* xsrc = xsrc0 + (size_t)t * (NK / 8);
+            uint32_t xp[16];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const uint4 u = xsrc[(c + rot) & 3];
+              xp[4 * c] = u.x;
+              xp[4 * c + 1] = u.y;
+              xp[4 * c + 2] = u.z;
+              xp[4 * c + 3] = u.w;
+            }
+            const float2 X = xsum[t * nseg + sg];
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              bf16_fma(a0, ep[i], xp[i], false);
+              bf16_fma(a1, ep[i], xp[i], true);
+            }
+            const float sxq = fmaf(-128.0f, X.x, a0 + a1);
+            tot[q][t] = fmaf(sc[q], sxq, fmaf(bi[q], X.y, tot[q][t]));
+          }
+        }
       }
     }
-    const uint4* wptr[kRowsPerWarp];
-    const uint16_t* sptr[kRowsPerWarp];
-    const uint16_t* bptr[kRowsPerWarp];
+    // ---- reduce across lanes (fixed xor butterfly) and store ----
 #pragma unroll
-    for (int q = 0; q < kRowsPerWarp; ++q) {
-      const int64_t grow = (int64_t)e * p.n_rows + wrow[q];
-      wptr[q] = reinterpret_cast<const uint4*>(p.wq) + grow * row_u4;
-      sptr[q] = p.ws + grow * ngroups;
-      bptr[q] = p.wb + grow * ngroups;
-    }
-
-    for (int tc = 0; tc < m; tc += MT) {
-      const int nt = min(MT, m - tc);
-      const int r0 = seg_lo + tc;
-      // ---- stage the activations when they changed ----
-      bool same = tag_nt == nt;
-      if (same) {
-        if (p.act_kind == kActXbf16) {
-          for (int t = 0; t < nt; ++t)
-            same = same && (__ldg(p.sorted + tag_r0 + t) / p.kmax) == (__ldg(p.sorted + r0 + t) / p.kmax);
+    for (int q = 0; q < kRowsPerWarp; ++q)
+#pragma unroll
+      for (int t = 0; t < MT; ++t)
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+          tot[q][t] = __fadd_rn(tot[q][t], __shfl_xor_sync(0xFFFFFFFFu, tot[q][t], off));
+    if (lane == 0) {
+      for (int t = 0; t < nt; ++t) {
+        const int64_t r = r0 + t;
+        if (MODE == kSwiglu) {
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const int col = cur.col0 + q;
+            if (col >= p.n_out) continue;
+            const float hv = swiglu_f32(tot[q][t], tot[2 + q][t]);
+            if (p.out_dtype == MOE_DTYPE_BF16)
+              static_cast<uint16_t*>(p.out)[r * p.n_out + col] = f32_to_bf16_rne(hv);
+            else
+              static_cast<float*>(p.out)[r * p.n_out + col] = hv;
+          }
         } else {
-          same = tag_r0 == r0;
-        }
-      }
-      if (!same) {
-        __syncthreads();  // everyone is done with the previous staging
-        stage_activations<BITS>(p, r0, nt, xs, xsum, NK, nseg);
-        __syncthreads();
-        tag_r0 = r0;
-        tag_nt = nt;
-      }
-
-      // ---- stream the weights ----
-      float tot[kRowsPerWarp][MT];
-#pragma unroll
-      for (int q = 0; q < kRowsPerWarp; ++q)
-#pragma unroll
-        for (int t = 0; t < MT; ++t) tot[q][t] = 0.0f;
-
-      // codes, scales and biases of the next segment are loaded one step ahead
-      uint4 wn[kRowsPerWarp];
-      uint16_t sn[kRowsPerWarp], bn[kRowsPerWarp];
-      if (lane < nseg) {
-        const int g = lane / W::kSegPerGroup;
-#pragma unroll
-        for (int q = 0; q < kRowsPerWarp; ++q) {
-          wn[q] = ldg_nc_v4(wptr[q] + lane);
-          sn[q] = __ldg(sptr[q] + g);
-          bn[q] = __ldg(bptr[q] + g);
-        }
-      }
-      for (int sg = lane; sg < nseg; sg += 32) {
-        uint4 wc[kRowsPerWarp];
-        float sc[kRowsPerWarp], bi[kRowsPerWarp];
-#pragma unroll
-        for (int q = 0; q < kRowsPerWarp; ++q) {
-          wc[q] = wn[q];
-          sc[q] = f16_bits_to_f32(sn[q]);
-          bi[q] = f16_bits_to_f32(bn[q]);
-        }
-        if (sg + 32 < nseg) {
-          const int gn = (sg + 32) / W::kSegPerGroup;
 #pragma unroll
           for (int q = 0; q < kRowsPerWarp; ++q) {
-            wn[q] = ldg_nc_v4(wptr[q] + sg + 32);
-            sn[q] = __ldg(sptr[q] + gn);
-            bn[q] = __ldg(bptr[q] + gn);
-          }
-        }
-        const uint4* xsrc0 = reinterpret_cast<const uint4*>(xs + (size_t)sg * 16);
-        const int rot = sg >> 1;
-#pragma unroll
-        for (int q = 0; q < kRowsPerWarp; ++q) {
-          // code pairs (128 + q_j, 128 + q_{j+4}) of this row's segment
-          uint32_t ep[16];
-          const uint32_t w4[4] = {wc[q].x, wc[q].y, wc[q].z, wc[q].w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) ep[4 * i + j] = ((w4[i] >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
-#pragma unroll
-          for (int t = 0; t < MT; ++t) {
-            if (t < nt) {
-              const uint4* xsrc = xsrc0 + (size_t)t * (NK / 8);
-              uint32_t xp[16];
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                const uint4 u = xsrc[(c + rot) & 3];
-                xp[4 * c] = u.x;
-                xp[4 * c + 1] = u.y;
-                xp[4 * c + 2] = u.z;
-                xp[4 * c + 3] = u.w;
-              }
-              const float2 X = xsum[t * nseg + sg];
-              float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                bf16_fma(a0, ep[i], xp[i], false);
-                bf16_fma(a1, ep[i], xp[i], true);
-              }
-              const float sxq = fmaf(-128.0f, X.x, a0 + a1);
-              tot[q][t] = fmaf(sc[q], sxq, fmaf(bi[q], X.y, tot[q][t]));
-            }
-          }
-        }
-      }
-      // ---- reduce across lanes (fixed xor butterfly) and store ----
-#pragma unroll
-      for (int q = 0; q < kRowsPerWarp; ++q)
-#pragma unroll
-        for (int t = 0; t < MT; ++t)
-#pragma unroll
-          for (int off = 16; off >= 1; off >>= 1)
-            tot[q][t] = __fadd_rn(tot[q][t], __shfl_xor_sync(0xFFFFFFFFu, tot[q][t], off));
-      if (lane == 0) {
-        for (int t = 0; t < nt; ++t) {
-          const int64_t r = r0 + t;
-          if (MODE == kSwiglu) {
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              if (!ovalid[q]) continue;
-              const float hv = swiglu_f32(tot[q][t], tot[2 + q][t]);
-              if (p.out_dtype == MOE_DTYPE_BF16)
-                static_cast<uint16_t*>(p.out)[r * p.n_out + ocol[q]] = f32_to_bf16_rne(hv);
-              else
-                static_cast<float*>(p.out)[r * p.n_out + ocol[q]] = hv;
-            }
-          } else {
-#pragma unroll
-            for (int q = 0; q < kRowsPerWarp; ++q)
-              if (ovalid[q]) static_cast<float*>(p.out)[r * p.n_out + ocol[q]] = tot[q][t];
+            const int col = cur.col0 + q;
+            if (col < p.n_rows) static_cast<float*>(p.out)[r * p.n_out + col] = tot[q][t];
           }
         }
       }
     }
+    if (!has_next) break;
+    cur = nxt;
   }
 }
 

@@ -306,11 +306,19 @@ def run_ours(args):
     torch.cuda.synchronize()
     kt = {k: statistics.mean(a.elapsed_time(b) for a, b in v) for k, v in events.items()}
     n_active = int((layer.buffers(T)["counts"] > 0).sum().item())
+    k_run = int(layer.buffers(T)["k_dev"].item())
     peaks, peak_src = load_peaks()
     gu_bytes = active_bytes_per_expert(cfg, "gate_up") * n_active + T * cfg.H * 2
     dn_bytes = active_bytes_per_expert(cfg, "down") * n_active
     gu_gbs = gu_bytes / (kt["gate_up"] * 1e-3) / 1e9
     dn_gbs = dn_bytes / (kt["down"] * 1e-3) / 1e9
+    # algorithmic FLOPs of the two products (2 * rows * assignments * K)
+    A = T * k_run
+    gu_flops = 2.0 * A * 2 * cfg.I * cfg.H
+    dn_flops = 2.0 * A * cfg.I * cfg.H
+    gu_tflops = gu_flops / (kt["gate_up"] * 1e-3) / 1e12
+    dn_tflops = dn_flops / (kt["down"] * 1e-3) / 1e12
+    tensor_bound = layer.resolved_path(T) == moe.PATH_TC and cfg.name == "prefill"
     traffic = None
     try:
         with open(TRAFFIC_FILE) as f:
@@ -350,11 +358,19 @@ def run_ours(args):
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": workload_config(cfg),
-        "roofline": {"bound": "hbm", "achieved": gu_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": gu_gbs / peaks["hbm_gbs"], "traffic": traffic,
-                     "kernel": "gemv_qmm_kernel (gate_up, SiLU*up epilogue)",
-                     "algorithmic_bytes_per_launch": gu_bytes, "peak_source": peak_src},
+        "roofline": ({"bound": "tensor", "achieved": gu_tflops, "peak": peaks["bf16_tflops"],
+                      "unit": "TFLOP/s", "frac": gu_tflops / peaks["bf16_tflops"],
+                      "frac_of_sustained": gu_tflops / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]),
+                      "traffic": traffic, "kernel": "tc_qmm_kernel (gate_up, SiLU*up epilogue)",
+                      "algorithmic_flops_per_launch": gu_flops, "peak_source": peak_src}
+                     if tensor_bound else
+                     {"bound": "hbm", "achieved": gu_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                      "frac": gu_gbs / peaks["hbm_gbs"], "traffic": traffic,
+                      "kernel": ("tc_qmm_kernel" if layer.resolved_path(T) == moe.PATH_TC
+                                 else "gemv_qmm_kernel") + " (gate_up, SiLU*up epilogue)",
+                      "algorithmic_bytes_per_launch": gu_bytes, "peak_source": peak_src}),
         "kernels": {"gate_up_us": kt["gate_up"] * 1e3, "gate_up_gbs": gu_gbs,
+                    "gate_up_tflops": gu_tflops, "down_tflops": dn_tflops, "k": k_run,
                     "down_us": kt["down"] * 1e3, "down_gbs": dn_gbs,
                     "layer_us_per_call": ms * 1e3 / calls,
                     "layer_gbs": (gu_bytes + dn_bytes) / (ms * 1e-3 / calls) / 1e9,

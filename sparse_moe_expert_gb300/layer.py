@@ -19,7 +19,7 @@ from ._lib import EPILOGUE_RAW, EPILOGUE_SWIGLU, PATH_AUTO, PATH_GEMV, PATH_TC, 
 
 FUSE_ENV = "MOE_GB300_FUSE_GATE_UP"
 TC_MIN_TOKENS_PER_EXPERT = 24  # mirrors the library's automatic path choice
-TC_BUILT = False               # the tensor-core grouped GEMM is not in this build yet
+TC_BUILT = True                # the tensor-core grouped GEMM (tcgen05) is available
 
 
 @dataclasses.dataclass

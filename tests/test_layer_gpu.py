@@ -12,7 +12,7 @@ from test_parity_gpu import CFG, SMALL
 
 pytestmark = pytest.mark.gpu
 
-PATHS = ["gemv"]
+PATHS = ["gemv", "tc"]
 
 
 def path_id(moe, name):
@@ -41,10 +41,11 @@ def test_layer_small_configs(cuda_lib, name, path):
         h = to_np(bufs["h"])[:A]
         y = to_np(bufs["y"])[:A]
         # h is stored as bf16: its rounding (2^-9 relative, ~1.6e-3 rel L2)
-        # dominates; y is computed from the rounded h
-        h_tol = 1e-4 if bufs["h"].dtype == torch.float32 else 4e-3
+        # dominates on the GEMV path; the tensor-core path also rounds the
+        # dequantized weights to bf16 (~1.7e-3 per product)
+        h_tol, y_tol = (4e-3, 4e-3) if path == "gemv" else (5e-3, 6e-3)
         assert rel_l2(h, ref.h) <= h_tol, f"h {rel_l2(h, ref.h):.2e}"
-        assert rel_l2(y, ref.y) <= 2 * h_tol, f"y {rel_l2(y, ref.y):.2e}"
+        assert rel_l2(y, ref.y) <= y_tol, f"y {rel_l2(y, ref.y):.2e}"
         assert_layer_close(out, ref.out, f"{name} batch {b}")
         assert cuda_lib.moe_get_device_error() == 0
 
@@ -92,7 +93,8 @@ def test_fused_gate_up_bit_identical_to_two_products(cuda_lib, path, bits, T, k,
         lo, hi = ref.perm.offsets[e], ref.perm.offsets[e + 1]
         if hi > lo:
             want = oracle.qmm_raw(xf[srt[lo:hi] // cfg.slots], gq[e], gs[e], gb[e], bits, cfg.H)
-            assert rel_l2(got[lo:hi], want) <= 1e-5
+            # GEMV: exact weights, fp32 sums; tensor cores: weights rounded to bf16
+            assert rel_l2(got[lo:hi], want) <= (1e-5 if path == "gemv" else 3e-3)
 
 
 @pytest.mark.parametrize("path", PATHS)

@@ -378,7 +378,7 @@ def run_ours(args):
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                    "reasons": clocks["reasons"], "samples": clocks["samples"]},
         "e2e": e2e,
-        "gpu_launches": 5 * calls * args.steps,
+        "gpu_launches": layer.launches_per_call(T) * calls * args.steps,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n = args.cpu_sample or default_sample(cfg)

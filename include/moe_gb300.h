@@ -216,6 +216,25 @@ moe_status_t moe_permute(const int32_t* topk_ids, const int32_t* k_dev, int T, i
                          int32_t* sorted_assign, int32_t* inv_pos, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * moe_permute_rows -- the token rows in expert order.
+ *
+ * Page [C], 如何验证正确性 (the sorted branch: token rows are gathered into
+ * expert order before the gathered product).  x_sorted[r] = x[t] with
+ * t = sorted_assign[r] / kmax, for sorted rows r < T*k; an exact copy.
+ *
+ * x               bf16 [T, H] (H a multiple of 8), 16-byte aligned.
+ * sorted_assign   int32 [T*kmax] from moe_permute.
+ * k_dev           int32 scalar (clamped to [0, kmax]).
+ * x_sorted        out: bf16 [T*kmax, H], 16-byte aligned; rows >= T*k are
+ *                 not written.  The caller owns all buffers.
+ * An entry outside [0, T*kmax) leaves its row unwritten and sets
+ * MOE_DEVERR_BAD_INDEX.
+ * ---------------------------------------------------------------------- */
+moe_status_t moe_permute_rows(const uint16_t* x, const int32_t* sorted_assign,
+                              const int32_t* k_dev, int T, int kmax, int H, uint16_t* x_sorted,
+                              moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * moe_gate_up_qmm -- the fused gate_up product over expert segments.
  *
  * Page [C], 融合原理 and 实现剖析 ④: one gathered quantized product with the
@@ -233,7 +252,10 @@ moe_status_t moe_permute(const int32_t* topk_ids, const int32_t* k_dev, int T, i
  * matrices (n_rows = I each) gives, bit for bit, the two halves of RAW on
  * the fused matrix; moe_swiglu then reproduces the SWIGLU epilogue exactly.
  *
- * x               bf16 [T, H].
+ * x               bf16 [T, H], read through sorted_assign; or, with
+ *                 sorted_assign = NULL, bf16 [T*kmax, H] already in sorted
+ *                 row order (moe_permute_rows), row r read for sorted row r.
+ *                 Both forms give bitwise the same result.
  * sorted_assign, expert_offsets, k_dev  from moe_permute / moe_router_topk.
  * w_q             uint32 [E, n_rows, H*bits/32]; w_s, w_b fp16 [E, n_rows, H/64].
  * bits            4 or 8.

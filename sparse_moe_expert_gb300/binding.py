@@ -120,11 +120,31 @@ def moe_permute(topk_ids, k_dev, E: int, expert_counts=None, expert_offsets=None
     return expert_counts, expert_offsets, sorted_assign, inv_pos
 
 
+def moe_permute_rows(x, sorted_assign, k_dev, kmax: int, x_sorted=None, stream=None):
+    """-> x_sorted bf16 [T*kmax, H]: row r = x[sorted_assign[r] // kmax] for r < T*k."""
+    _need(x, torch.bfloat16, "x")
+    _need(sorted_assign, torch.int32, "sorted_assign")
+    T, H = x.shape
+    if x_sorted is None:
+        x_sorted = torch.empty((max(T * kmax, 1), H), dtype=torch.bfloat16, device=x.device)
+    st = lib().moe_permute_rows(_p(x), _p(sorted_assign), _p(k_dev), T, kmax, H, _p(x_sorted),
+                                _stream(stream))
+    check("moe_permute_rows", st)
+    return x_sorted
+
+
 def moe_gate_up_qmm(x, sorted_assign, expert_offsets, k_dev, kmax: int, w_q, w_s, w_b, bits: int,
                     epilogue: int = EPILOGUE_SWIGLU, out_dtype=torch.float32, out=None,
-                    path: int = PATH_AUTO, stream=None):
+                    path: int = PATH_AUTO, stream=None, T: Optional[int] = None):
+    """x bf16 [T, H] read through sorted_assign, or (sorted_assign None) the
+    rows already in sorted order, [T*kmax, H]; then T must be given."""
     _need(x, torch.bfloat16, "x")
-    T, H = x.shape
+    if sorted_assign is None:
+        if T is None:
+            raise ValueError("T is required when x is already in sorted row order")
+        H = x.shape[1]
+    else:
+        T, H = x.shape
     E, n_rows = w_q.shape[0], w_q.shape[1]
     cols = n_rows // 2 if epilogue == EPILOGUE_SWIGLU else n_rows
     if out is None:

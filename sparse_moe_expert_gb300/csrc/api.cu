@@ -117,19 +117,22 @@ extern "C" moe_status_t moe_gate_up_qmm(const uint16_t* x, const int32_t* sorted
   if (H > 49152) return MOE_ERR_UNSUPPORTED;
   if (!expert_offsets || !k_dev) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
-  const void* ptrs[] = {x, sorted_assign, w_q, w_s, w_b, out};
+  const void* ptrs[] = {x, w_q, w_s, w_b, out};
   for (const void* q : ptrs)
     if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (sorted_assign && !aligned16(sorted_assign)) return MOE_ERR_INVALID_ARG;
+  // x by token through sorted_assign (kind 0), or rows already in sorted order (kind 2)
+  const int act_kind = sorted_assign ? 0 : 2;
   const bool swiglu = epilogue == MOE_EPILOGUE_SWIGLU;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int p = pick_path(path, T, kmax, E);
   if (p == MOE_PATH_TC) {
     if (!moe::tc_available()) return MOE_ERR_UNSUPPORTED;
-    return moe::tc_qmm(x, 0, sorted_assign, expert_offsets, T, kmax, E, H, n_rows, swiglu, w_q,
-                       w_s, w_b, bits, out, out_dtype, st);
+    return moe::tc_qmm(x, act_kind, sorted_assign, expert_offsets, T, kmax, E, H, n_rows, swiglu,
+                       w_q, w_s, w_b, bits, out, out_dtype, st);
   }
-  return moe::gemv_qmm(x, 0, sorted_assign, expert_offsets, T, kmax, E, H, n_rows, swiglu, w_q,
-                       w_s, w_b, bits, out, out_dtype, st);
+  return moe::gemv_qmm(x, act_kind, sorted_assign, expert_offsets, T, kmax, E, H, n_rows, swiglu,
+                       w_q, w_s, w_b, bits, out, out_dtype, st);
 }
 
 extern "C" moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* expert_offsets,

@@ -1,6 +1,7 @@
 // Shared device helpers of libmoe_gb300 (sm_103a).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -26,24 +27,24 @@ __device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
-// fp32 -> bf16, round to nearest even (finite inputs; NaN kept quiet).
+// fp32 -> bf16, round to nearest even (one hardware conversion).
 __device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) {
-  uint32_t u = __float_as_uint(f);
-  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((u >> 16) | 0x40u);
-  u += 0x7FFFu + ((u >> 16) & 1u);
-  return (uint16_t)(u >> 16);
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
 __device__ __forceinline__ float f16_bits_to_f32(uint16_t h) {
   return __half2float(__ushort_as_half(h));
 }
 
-// SiLU(gate) * up, the SwitchGLU activation, in fp32.  Every path that
-// produces h (fused epilogues and the separate swiglu kernel) calls this one
-// function, so the fused and unfused results agree bit for bit.
+// SiLU(gate) * up, the SwitchGLU activation, in fp32: g / (1 + e^-g) * u
+// with the hardware exponential and reciprocal (a few ulp of fp32, far below
+// the bf16 rounding of h that follows).  For g -> -inf, e^-g overflows to inf
+// and the quotient is 0, the limit of SiLU.  Every path that produces h
+// (fused epilogues and the separate swiglu kernel) calls this one function,
+// so the fused and unfused results agree bit for bit.
 __device__ __forceinline__ float swiglu_f32(float g, float u) {
-  float sig_den = __fadd_rn(1.0f, expf(-g));
-  return __fmul_rn(__fdiv_rn(g, sig_den), u);
+  const float sig_den = __fadd_rn(1.0f, __expf(-g));
+  return __fmul_rn(__fdividef(g, sig_den), u);
 }
 
 // Packed fp32x2 fused multiply-add (Blackwell FFMA2): d = a * b + c, lane-wise.

@@ -7,27 +7,36 @@
 // activation, down projection); page "Qwen3.5 Block在llama.cpp中的映射与优化
 // 原理", section 4.2 (each expert only sees the tokens routed to it).
 //
-// Orientation: weights are the MMA's A operand (M = 128 rows of an expert),
-// the expert's tokens are B (N = 128 tokens of its segment), K = the
-// contraction axis, so D[m, n] lands in TMEM lane m, column n.  A SWIGLU tile
-// holds two accumulators, gate rows n0..n0+127 and up rows I+n0..I+n0+127,
-// so the epilogue has both halves of an output in the same thread.
+// Orientation: weights are the MMA's A operand (M = 128 rows), the expert's
+// tokens are B (N = up to 256 tokens of its segment), K = the contraction
+// axis, so D[m, n] lands in TMEM lane m, column n.
+//   RAW tile:    A rows = 128 consecutive weight rows.
+//   SWIGLU tile: A rows 0..63 = gate rows f0..f0+63, rows 64..127 = the up
+//                rows of the same 64 features, so one accumulator holds both
+//                halves of 64 outputs and TMEM (512 columns) still fits two
+//                accumulators of 256 tokens for double buffering.
+// A segment of m tokens is cut into ceil(m/256) tiles of equal size (rounded
+// up to 16, the MMA's N granularity); the MMA's N is set per tile.  Each
+// dequantized weight tile thus feeds up to 256 tokens, so the dequantization
+// (CUDA cores) costs less than the MMA time it feeds.
 //
 // One CTA per SM, persistent over the tiles (active expert, m-tile, n-tile);
 // n-tiles of the same weights are adjacent so neighbouring CTAs share them in
 // L2.  Warp roles:
 //   warp 5      loader: per k-block of 64, TMA loads the packed codes of the
-//               tile's rows (2D tensor map) and the token tile: a 4-row gather
-//               (tile::gather4) of the token rows of x for gate_up, a 2D tile
-//               of h for down, both 128-byte swizzled as the MMA expects;
-//   warps 6-13  dequant: read the codes from shared memory, w = s*q + b in
+//               tile's 128 rows (2D tensor map, two 64-row boxes) and the
+//               token tile: 4-row gathers (tile::gather4) of the token rows
+//               of x for gate_up, 64-row 2D boxes of h for down, both
+//               128-byte swizzled as the MMA expects; all 32 lanes issue;
+//   warps 6-21  dequant: read the codes from shared memory, w = s*q + b in
 //               fp32 (packed FMA), round to bf16, write the A tile in the
 //               128-byte-swizzled K-major layout, proxy fence, arrive;
 //   warp 4      MMA: one thread issues tcgen05.mma (kind::f16, bf16 x bf16 ->
 //               fp32) per 16-wide K slice, commits stage release and
 //               accumulator completion to mbarriers;
-//   warps 0-3   epilogue: tcgen05.ld of the accumulator, SiLU(gate)*up or raw,
-//               store.  TMEM accumulators are double-buffered.
+//   warps 0-3   epilogue: tcgen05.ld of the accumulator, then raw fp32 stores
+//               or SiLU(gate)*up (gate and up lanes sit in different warps:
+//               warp pairs swap half of their columns through shared memory).
 // Every mbarrier wait is bounded; a wait that runs out sets
 // MOE_DEVERR_TIMEOUT, the CTA stops issuing, drains what is in flight and
 // frees its TMEM.
@@ -39,16 +48,33 @@
 #include "async.cuh"
 #include "common.cuh"
 
+// Optional per-role wait accounting (compiled in only with -DMOE_TC_TRACE).
+#ifdef MOE_TC_TRACE
+__device__ unsigned long long g_tc_trace[16];
+#define TC_T0() const long long tc_t0_ = clock64()
+#define TC_ACC(var) var += clock64() - tc_t0_
+#define TC_FLUSH(slot, var) atomicAdd(&g_tc_trace[slot], (unsigned long long)(var))
+#else
+#define TC_T0()
+#define TC_ACC(var)
+#define TC_FLUSH(slot, var) ((void)(var))
+#endif
+
 namespace moe {
 namespace {
 
-constexpr int BM = 128;  // weight rows per accumulator
-constexpr int BN = 128;  // tokens per tile
-constexpr int BK = 64;   // contraction per stage = one scale group = one 128-B swizzle atom
-constexpr int kEpiWarps = 4, kMmaWarp = 4, kLoadWarp = 5, kDeqWarp0 = 6, kDeqWarps = 8;
-constexpr int kTcThreads = (kDeqWarp0 + kDeqWarps) * 32;  // 448
-constexpr int kTileBytes = BM * BK * 2;                   // 16 KB bf16 tile (A or B)
+constexpr int BM = 128;        // accumulator rows = TMEM lanes
+constexpr int BN = 256;        // most tokens per tile
+constexpr int BK = 64;         // contraction per stage = one scale group = one 128-B swizzle atom
+constexpr int kHalfRows = 64;  // SWIGLU: gate rows, then up rows, per A tile
+constexpr int kBoxRows = 64;   // rows per 2D TMA box (codes and token rows)
+constexpr int kEpiWarps = 4, kMmaWarp = 4, kLoadWarp = 5, kDeqWarp0 = 6, kDeqWarps = 16;
+constexpr int kTcThreads = (kDeqWarp0 + kDeqWarps) * 32;  // 704
+constexpr int kATileBytes = BM * BK * 2;                  // 16 KB bf16 weight tile
+constexpr int kBTileBytes = BN * BK * 2;                  // 32 KB bf16 token tile
 constexpr int kMaxStages = 8;
+constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators of up to 256 columns
+constexpr int kScaleLookahead = 4;      // k-blocks of scale/bias in flight per dequant thread
 
 enum TcMode { kTcSwiglu = 0, kTcRaw = 1 };
 enum TcAct { kTcGatherX = 0, kTcRowsH = 1 };
@@ -61,8 +87,9 @@ struct TcParams {
   void* out;
   int out_dtype;
   int kmax, E, K, n_rows, n_out;
-  int stages;
-  int n_mt;  // m-tiles per expert
+  int load_stages;  // ring of TMA-loaded code + token tiles
+  int a_stages;     // ring of dequantized weight tiles
+  int n_mt;         // m-tiles per expert
   unsigned int* err;
 };
 
@@ -173,11 +200,38 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
+// Bounded wait whose outcome is the same in every lane of the warp (a wait
+// that runs out in one lane counts as run out for all), so warp-collective
+// instructions after it are never reached by part of a warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
+                                          const volatile int* abort_flag) {
+  const bool ok = mbar_wait(bar, parity, kWaitBudgetCycles) && *abort_flag == 0;
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Position in a ring of n stages: slot index and the parity of the current
+// pass, advanced incrementally (no division in the pipelined loops).
+struct Ring {
+  int idx = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++idx == n) {
+      idx = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 // ---- tile schedule ----------------------------------------------------------
 
 struct TileInfo {
-  int e, seg_lo, m, mt, nt;
+  int e, seg_lo, mt;
+  int tok0;  // first token of the tile within the segment
+  int nv;    // tokens in the tile
+  int nmma;  // MMA N: nv rounded up to 16
 };
+
+__device__ __forceinline__ int ntiles_of(int m) { return (m + BN - 1) / BN; }
 
 // tile_start[a] = first tile of active expert a (exclusive prefix), n_act entries + 1.
 __device__ __forceinline__ TileInfo tile_info(const TcParams& p, const int* act_e,
@@ -191,62 +245,79 @@ __device__ __forceinline__ TileInfo tile_info(const TcParams& p, const int* act_
   TileInfo ti;
   ti.e = act_e[lo];
   ti.seg_lo = __ldg(p.offsets + ti.e);
-  ti.m = __ldg(p.offsets + ti.e + 1) - ti.seg_lo;
-  const int nnt = (ti.m + BN - 1) / BN;
+  const int m = __ldg(p.offsets + ti.e + 1) - ti.seg_lo;
+  const int nnt = ntiles_of(m);
+  const int tsz = (((m + nnt - 1) / nnt) + 15) & ~15;  // <= 256, and (nnt-1)*tsz < m
   const int local = t - tile_start[lo];
   ti.mt = local / nnt;
-  ti.nt = local % nnt;
+  const int nt = local - ti.mt * nnt;
+  ti.tok0 = nt * tsz;
+  ti.nv = min(tsz, m - ti.tok0);
+  ti.nmma = (ti.nv + 15) & ~15;
   return ti;
 }
 
-// Weight row (within the expert) of accumulator `acc`, tile row r.
+// Weight row (within the expert) of A-tile row r of m-tile mt.
 template <int MODE>
-__device__ __forceinline__ int tile_weight_row(const TcParams& p, int mt, int acc, int r) {
-  return MODE == kTcSwiglu ? acc * (p.n_rows / 2) + mt * BM + r : mt * BM + r;
+__device__ __forceinline__ int tile_weight_row(const TcParams& p, int mt, int r) {
+  if (MODE == kTcSwiglu)
+    return r < kHalfRows ? mt * kHalfRows + r : (p.n_rows >> 1) + mt * kHalfRows + r - kHalfRows;
+  return mt * BM + r;
 }
 
 template <int BITS, int MODE, int ACT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_qmm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                   const __grid_constant__ CUtensorMap tm_act, TcParams p) {
-  constexpr int NACC = MODE == kTcSwiglu ? 2 : 1;
-  constexpr int RAW_ROW_BYTES = BK * BITS / 8;          // code bytes per row per stage
-  constexpr int RAW_BYTES = BM * RAW_ROW_BYTES;         // per accumulator
-  constexpr int STAGE_BYTES = NACC * kTileBytes + kTileBytes + NACC * RAW_BYTES;
-  constexpr uint32_t TMEM_COLS = NACC * BN * 2;         // double-buffered accumulators
+  constexpr int RAW_ROW_BYTES = BK * BITS / 8;         // code bytes per row per k-block
+  constexpr int RAW_BYTES = BM * RAW_ROW_BYTES;        // codes of one stage
+  constexpr int LOAD_BYTES = kBTileBytes + RAW_BYTES;  // token tile + codes
+  // dequant work split: 4 threads per A row, 16 codes each
+  constexpr int DQ_SLICES = kDeqWarps * 32 / BM;  // 4
+  constexpr int DQ_CHUNKS = 8 / DQ_SLICES;        // 16-byte bf16 chunks per thread: 2
+  constexpr int PD = kScaleLookahead;
+  static_assert(DQ_CHUNKS == 2, "dequant split assumes two output chunks per thread");
 
   extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t raw_full[kMaxStages], a_full[kMaxStages], empty_bar[kMaxStages];
+  __shared__ uint64_t load_full[kMaxStages], load_empty[kMaxStages];
+  __shared__ uint64_t a_full[kMaxStages], a_empty[kMaxStages];
   __shared__ uint64_t tmem_full[2], tmem_empty[2];
+  __shared__ uint64_t xfull[2][2][2];  // SWIGLU exchange: [pair][buffer][writer half]
+  __shared__ uint64_t drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int act_e[1024];
   __shared__ int tile_start[1025];
   __shared__ int n_act_sh;
-  __shared__ int tok_table[BN];
+  __shared__ float xbuf[MODE == kTcSwiglu ? 2 * 2 * 2 * 16 * 32 : 1];
   __shared__ volatile int abort_flag;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int S = p.stages;
+  const int SL = p.load_stages, SA = p.a_stages;
   const int nkb = p.K / BK;
 
   // ---- set-up: barriers, TMEM, active experts and their tile ranges ----
   if (tid == 0) {
     abort_flag = 0;
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&raw_full[s], 1);
+    for (int s = 0; s < SL; ++s) {
+      mbar_init(&load_full[s], 1);
+      mbar_init(&load_empty[s], 1);
+    }
+    for (int s = 0; s < SA; ++s) {
       mbar_init(&a_full[s], kDeqWarps);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&a_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tmem_full[b], 1);
       mbar_init(&tmem_empty[b], kEpiWarps);
     }
+    for (int i = 0; i < 8; ++i) mbar_init(&xfull[i >> 2][(i >> 1) & 1][i & 1], 1);
+    mbar_init(&drain_bar, 1);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(&tmem_base_sh, TMEM_COLS);
+    tmem_alloc(&tmem_base_sh, kTmemCols);
     tmem_relinquish();
   }
   if (tid == 0) {
@@ -256,7 +327,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (m > 0) {
         act_e[n] = e;
         tile_start[n] = t;
-        t += p.n_mt * ((m + BN - 1) / BN);
+        t += p.n_mt * ntiles_of(m);
         ++n;
       }
     }
@@ -270,155 +341,207 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int n_act = n_act_sh;
   const int n_tiles = n_act > 0 ? tile_start[n_act] : 0;
 
-  unsigned char* stage_base = smem;
-  auto stage_a = [&](int s, int acc) { return stage_base + (size_t)s * STAGE_BYTES + acc * kTileBytes; };
-  auto stage_b = [&](int s) { return stage_base + (size_t)s * STAGE_BYTES + NACC * kTileBytes; };
-  auto stage_raw = [&](int s, int acc) {
-    return stage_base + (size_t)s * STAGE_BYTES + (NACC + 1) * kTileBytes + acc * RAW_BYTES;
-  };
+  unsigned char* a_base = smem;                             // SA * kATileBytes
+  unsigned char* l_base = smem + (size_t)SA * kATileBytes;  // SL * LOAD_BYTES
+  auto stage_a = [&](int s) { return a_base + (size_t)s * kATileBytes; };
+  auto stage_b = [&](int s) { return l_base + (size_t)s * LOAD_BYTES; };
+  auto stage_raw = [&](int s) { return l_base + (size_t)s * LOAD_BYTES + kBTileBytes; };
 
   if (warp == kLoadWarp) {
     // =============================== loader ===============================
+    long long w_load_empty = 0;
     int64_t issued = 0;
+    Ring ring;
     bool ok = true;
     for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
       const TileInfo ti = tile_info(p, act_e, tile_start, n_act, t);
+      const int64_t code_row0 = (int64_t)ti.e * p.n_rows;
+      const int crow0 = (int)(code_row0 + tile_weight_row<MODE>(p, ti.mt, 0));
+      const int crow1 = (int)(code_row0 + tile_weight_row<MODE>(p, ti.mt, kHalfRows));
+      // this lane's gathers: groups g = lane and lane + 32 of 4 token rows
+      // (columns past the tile repeat its first token)
+      const int ngroups = ti.nmma / 4;
+      int tok[8];
       if (ACT == kTcGatherX) {
-        // token of each column of this tile (invalid columns repeat the first token)
-        for (int n = lane; n < BN; n += 32) {
-          const int col = ti.nt * BN + n;
-          const int r = ti.seg_lo + (col < ti.m ? col : 0);
-          tok_table[n] = __ldg(p.sorted + r) / p.kmax;
-        }
-        __syncwarp();
+        const int first = ti.seg_lo + ti.tok0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int n = 4 * (lane + 32 * h) + i;
+            tok[4 * h + i] = __ldg(p.sorted + first + (n < ti.nv ? n : 0)) / p.kmax;
+          }
       }
+      const int nbox = (ti.nmma + kBoxRows - 1) / kBoxRows;
+      const uint32_t bytes =
+          (uint32_t)RAW_BYTES + (ACT == kTcGatherX ? (uint32_t)ti.nmma * (BK * 2)
+                                                   : (uint32_t)nbox * (kBoxRows * BK * 2));
       for (int kb = 0; kb < nkb; ++kb) {
-        const int s = (int)(issued % S);
-        const uint32_t round = (uint32_t)(issued / S);
-        if (!mbar_wait(&empty_bar[s], (round & 1u) ^ 1u, kWaitBudgetCycles) || abort_flag) {
+        const int s = ring.idx;
+        TC_T0();
+        if (!warp_wait(&load_empty[s], ring.phase ^ 1u, &abort_flag)) {
           ok = false;
           break;
         }
+        TC_ACC(w_load_empty);
         if (lane == 0) {
-          mbar_arrive_expect_tx(&raw_full[s], NACC * RAW_BYTES + kTileBytes);
+          mbar_arrive_expect_tx(&load_full[s], bytes);
           const int code_col = kb * (BK * BITS / 32);  // in uint32 words
+          tma_load_2d(stage_raw(s), &tm_codes, code_col, crow0, &load_full[s]);
+          tma_load_2d(stage_raw(s) + kHalfRows * RAW_ROW_BYTES, &tm_codes, code_col, crow1,
+                      &load_full[s]);
+        }
+        __syncwarp();
+        if (ACT == kTcGatherX) {
 #pragma unroll
-          for (int acc = 0; acc < NACC; ++acc) {
-            const int row = ti.e * p.n_rows + tile_weight_row<MODE>(p, ti.mt, acc, 0);
-            tma_load_2d(stage_raw(s, acc), &tm_codes, code_col, row, &raw_full[s]);
+          for (int h = 0; h < 2; ++h) {
+            const int g = lane + 32 * h;
+            if (g < ngroups)
+              tma_gather4(stage_b(s) + g * 4 * (BK * 2), &tm_act, kb * BK, tok[4 * h],
+                          tok[4 * h + 1], tok[4 * h + 2], tok[4 * h + 3], &load_full[s]);
           }
-          if (ACT == kTcGatherX) {
-            for (int g = 0; g < BN / 4; ++g)
-              tma_gather4(stage_b(s) + g * 512, &tm_act, kb * BK, tok_table[4 * g],
-                          tok_table[4 * g + 1], tok_table[4 * g + 2], tok_table[4 * g + 3],
-                          &raw_full[s]);
-          } else {
-            tma_load_2d(stage_b(s), &tm_act, kb * BK, ti.seg_lo + ti.nt * BN, &raw_full[s]);
-          }
+        } else if (lane < nbox) {
+          tma_load_2d(stage_b(s) + lane * (kBoxRows * BK * 2), &tm_act, kb * BK,
+                      ti.seg_lo + ti.tok0 + lane * kBoxRows, &load_full[s]);
         }
         __syncwarp();
         ++issued;
+        ring.next(SL);
       }
-      __syncwarp();
     }
-    if (!ok) {
-      if (lane == 0) {
-        raise_device_error(p.err, MOE_DEVERR_TIMEOUT);
-        abort_flag = 1;
-        const int64_t from = issued > S ? issued - S : 0;
-        for (int64_t j = from; j < issued; ++j)
-          mbar_wait(&raw_full[j % S], (uint32_t)((j / S) & 1), kWaitBudgetCycles);
+    if (lane == 0) {
+      TC_FLUSH(0, w_load_empty);
+      TC_FLUSH(1, issued);
+    }
+    if (!ok && lane == 0) {
+      raise_device_error(p.err, MOE_DEVERR_TIMEOUT);
+      abort_flag = 1;
+      // the last min(issued, SL) stages may still have copies in flight
+      Ring r = ring;
+      for (int64_t j = 0; j < issued && j < SL; ++j) {
+        r.idx = r.idx == 0 ? SL - 1 : r.idx - 1;
+        if (r.idx == SL - 1) r.phase ^= 1u;
+        mbar_wait(&load_full[r.idx], r.phase, kWaitBudgetCycles);
       }
     }
   } else if (warp >= kDeqWarp0) {
     // =============================== dequant ===============================
-    const int dt = tid - kDeqWarp0 * 32;  // 0..255
-    // SWIGLU: one row of one accumulator per thread; RAW: half a row per thread
-    const int acc = MODE == kTcSwiglu ? dt >> 7 : 0;
-    const int r = dt & 127;
-    const int khalf = MODE == kTcSwiglu ? -1 : (dt >> 7);  // RAW: which 32 of the 64 columns
+    const int dt = tid - kDeqWarp0 * 32;
+    const int r = dt / DQ_SLICES;                 // A-tile row 0 .. 127
+    const int c0 = (dt % DQ_SLICES) * DQ_CHUNKS;  // first 16-byte bf16 chunk of this thread
     const int ngroups = p.K / 64;
-    int64_t consumed = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-      const TileInfo ti = tile_info(p, act_e, tile_start, n_act, t);
-      int wrow = tile_weight_row<MODE>(p, ti.mt, acc, r);
-      if (wrow >= p.n_rows) wrow = p.n_rows - 1;  // rows past the matrix: any valid scale
-      const int64_t grow = (int64_t)ti.e * p.n_rows + wrow;
-      const uint16_t* sp = p.ws + grow * ngroups;
-      const uint16_t* bp = p.wb + grow * ngroups;
-      uint16_t s_next = __ldg(sp), b_next = __ldg(bp);
-      for (int kb = 0; kb < nkb; ++kb) {
-        const float sc = f16_bits_to_f32(s_next), bi = f16_bits_to_f32(b_next);
-        if (kb + 1 < nkb) {
-          s_next = __ldg(sp + kb + 1);
-          b_next = __ldg(bp + kb + 1);
-        }
-        const int s = (int)(consumed % S);
-        const uint32_t round = (uint32_t)(consumed / S);
-        if (!mbar_wait(&raw_full[s], round & 1u, kWaitBudgetCycles) || abort_flag) {
-          ok = false;
-          break;
-        }
-        const unsigned char* raw = stage_raw(s, acc) + r * RAW_ROW_BYTES;
-        unsigned char* atile = stage_a(s, acc);
-        if (BITS == 4) {
-          // 8 codes per word; a word becomes one 16-byte chunk of 8 bf16
-          const float2 mul = make_float2(512.0f * sc, 32.0f * sc);
-          const float2 add = make_float2(bi - 512.0f * sc, bi - 32.0f * sc);
-          const int c0 = MODE == kTcSwiglu ? 0 : khalf * 4;
-          const int nc = MODE == kTcSwiglu ? 8 : 4;
-          for (int c = c0; c < c0 + nc; c += 4) {
-            const uint4 q4 = *reinterpret_cast<const uint4*>(raw + c * 4);
-            const uint32_t wv[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint32_t v = wv[i];
-              const uint32_t sh[4] = {v << 14, v << 6, v >> 2, v >> 10};
-              uint32_t o[4];
-#pragma unroll
-              for (int pq = 0; pq < 4; ++pq) {
-                // (1 + q_even/512, 1 + q_odd/32), then w = s*q + b exactly in fp32
-                const float2 f = make_float2(__uint_as_float((sh[pq] & 0x0003C000u) | 0x3F800000u),
-                                             __uint_as_float((sh[pq] & 0x003C0000u) | 0x3F800000u));
-                const float2 w = __ffma2_rn(f, mul, add);
-                o[pq] = pack_bf16x2(w.x, w.y);
-              }
-              *reinterpret_cast<uint4*>(atile + sw128_offset(r, c + i)) =
-                  make_uint4(o[0], o[1], o[2], o[3]);
-            }
-          }
-        } else {
-          // 4 codes per word; two words become one 16-byte chunk
-          const float2 mul = make_float2(256.0f * sc, 256.0f * sc);
-          const float2 add = make_float2(bi - 256.0f * sc, bi - 256.0f * sc);
-          const int c0 = MODE == kTcSwiglu ? 0 : khalf * 4;
-          const int nc = MODE == kTcSwiglu ? 8 : 4;
-          for (int c = c0; c < c0 + nc; c += 2) {
-            const uint4 q4 = *reinterpret_cast<const uint4*>(raw + c * 8);
-            const uint32_t wv[4] = {q4.x, q4.y, q4.z, q4.w};
-            uint32_t o[8];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint32_t v = wv[i];
-              const float2 f0 = make_float2(__uint_as_float(((v << 15) & 0x007F8000u) | 0x3F800000u),
-                                            __uint_as_float(((v << 7) & 0x007F8000u) | 0x3F800000u));
-              const float2 f1 = make_float2(__uint_as_float(((v >> 1) & 0x007F8000u) | 0x3F800000u),
-                                            __uint_as_float(((v >> 9) & 0x007F8000u) | 0x3F800000u));
-              const float2 w0 = __ffma2_rn(f0, mul, add);
-              const float2 w1 = __ffma2_rn(f1, mul, add);
-              o[2 * i] = pack_bf16x2(w0.x, w0.y);
-              o[2 * i + 1] = pack_bf16x2(w1.x, w1.y);
-            }
-            *reinterpret_cast<uint4*>(atile + sw128_offset(r, c)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(atile + sw128_offset(r, c + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[s]);
-        ++consumed;
+    // this CTA's stages in order, (its tiles) x (k-blocks); the scale and
+    // bias of stage st + PD are fetched while stage st is converted
+    const int my_tiles = blockIdx.x < n_tiles ? (n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int64_t nst = (int64_t)my_tiles * nkb;
+    int la_t = blockIdx.x, la_kb = 0;
+    const uint16_t* la_sp = nullptr;
+    const uint16_t* la_bp = nullptr;
+    auto la_fetch = [&]() -> uint32_t {  // scale | bias << 16 of the look-ahead stage
+      if (la_t >= n_tiles) return 0u;
+      if (la_kb == 0) {
+        const TileInfo ti = tile_info(p, act_e, tile_start, n_act, la_t);
+        int wrow = tile_weight_row<MODE>(p, ti.mt, r);
+        if (wrow >= p.n_rows) wrow = p.n_rows - 1;  // rows past the matrix: any valid scale
+        const int64_t grow = (int64_t)ti.e * p.n_rows + wrow;
+        la_sp = p.ws + grow * ngroups;
+        la_bp = p.wb + grow * ngroups;
       }
+      const uint32_t v = (uint32_t)__ldg(la_sp + la_kb) | ((uint32_t)__ldg(la_bp + la_kb) << 16);
+      if (++la_kb == nkb) {
+        la_kb = 0;
+        la_t += gridDim.x;
+      }
+      return v;
+    };
+    // the ring is indexed by the unrolled position u, so each slot stays in
+    // its own register while its load is in flight
+    uint32_t sb[PD];
+#pragma unroll
+    for (int i = 0; i < PD; ++i) sb[i] = la_fetch();
+
+    long long w_dq_load = 0, w_dq_aempty = 0;
+    Ring rl, ra;
+    bool ok = true;
+    for (int64_t st0 = 0; st0 < nst && ok; st0 += PD) {
+#pragma unroll
+      for (int u = 0; u < PD; ++u) {
+        if (st0 + u < nst && ok) {
+          const uint32_t sbv = sb[u];
+          sb[u] = la_fetch();
+          const int sl = rl.idx, sa = ra.idx;
+          {
+            TC_T0();
+            if (!warp_wait(&load_full[sl], rl.phase, &abort_flag)) ok = false;
+            TC_ACC(w_dq_load);
+          }
+          if (ok) {
+            TC_T0();
+            if (!warp_wait(&a_empty[sa], ra.phase ^ 1u, &abort_flag)) ok = false;
+            TC_ACC(w_dq_aempty);
+          }
+          if (ok) {
+            const float sc = __half2float(__ushort_as_half((uint16_t)(sbv & 0xFFFFu)));
+            const float bi = __half2float(__ushort_as_half((uint16_t)(sbv >> 16)));
+            const unsigned char* raw = stage_raw(sl) + r * RAW_ROW_BYTES;
+            unsigned char* atile = stage_a(sa);
+            if (BITS == 4) {
+              // one 32-bit word = 8 codes = one 16-byte bf16 chunk
+              const float2 mul = make_float2(512.0f * sc, 32.0f * sc);
+              const float2 add = make_float2(bi - 512.0f * sc, bi - 32.0f * sc);
+              const uint2 q2 = *reinterpret_cast<const uint2*>(raw + c0 * 4);
+              const uint32_t wv[2] = {q2.x, q2.y};
+#pragma unroll
+              for (int i = 0; i < DQ_CHUNKS; ++i) {
+                const uint32_t v = wv[i];
+                const uint32_t sh[4] = {v << 14, v << 6, v >> 2, v >> 10};
+                uint32_t o[4];
+#pragma unroll
+                for (int pq = 0; pq < 4; ++pq) {
+                  // (1 + q_even/512, 1 + q_odd/32), then w = s*q + b in fp32
+                  const float2 f =
+                      make_float2(__uint_as_float((sh[pq] & 0x0003C000u) | 0x3F800000u),
+                                  __uint_as_float((sh[pq] & 0x003C0000u) | 0x3F800000u));
+                  const float2 w = __ffma2_rn(f, mul, add);
+                  o[pq] = pack_bf16x2(w.x, w.y);
+                }
+                *reinterpret_cast<uint4*>(atile + sw128_offset(r, c0 + i)) =
+                    make_uint4(o[0], o[1], o[2], o[3]);
+              }
+            } else {
+              // one 32-bit word = 4 codes; two words = one 16-byte bf16 chunk
+              const float2 mul = make_float2(256.0f * sc, 256.0f * sc);
+              const float2 add = make_float2(bi - 256.0f * sc, bi - 256.0f * sc);
+              const uint4 q4 = *reinterpret_cast<const uint4*>(raw + c0 * 8);
+              const uint32_t wv[4] = {q4.x, q4.y, q4.z, q4.w};
+              uint32_t o[8];
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj) {
+                const uint32_t v = wv[jj];
+                const float2 f0 = make_float2(__uint_as_float(((v << 15) & 0x007F8000u) | 0x3F800000u),
+                                              __uint_as_float(((v << 7) & 0x007F8000u) | 0x3F800000u));
+                const float2 f1 = make_float2(__uint_as_float(((v >> 1) & 0x007F8000u) | 0x3F800000u),
+                                              __uint_as_float(((v >> 9) & 0x007F8000u) | 0x3F800000u));
+                const float2 w0 = __ffma2_rn(f0, mul, add);
+                const float2 w1 = __ffma2_rn(f1, mul, add);
+                o[2 * jj] = pack_bf16x2(w0.x, w0.y);
+                o[2 * jj + 1] = pack_bf16x2(w1.x, w1.y);
+              }
+              *reinterpret_cast<uint4*>(atile + sw128_offset(r, c0)) = make_uint4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<uint4*>(atile + sw128_offset(r, c0 + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[sa]);
+            rl.next(SL);
+            ra.next(SA);
+          }
+        }
+      }
+    }
+    if (lane == 0) {
+      TC_FLUSH(2, w_dq_load);
+      TC_FLUSH(3, w_dq_aempty);
     }
     if (!ok && lane == 0) {
       raise_device_error(p.err, MOE_DEVERR_TIMEOUT);
@@ -427,41 +550,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == kMmaWarp) {
     // ================================= MMA =================================
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(BM, BN);
-      int64_t consumed = 0;
+      long long w_mma_tmem = 0, w_mma_afull = 0, w_mma_load = 0;
+      const long long t_mma0 = clock64();
+      int64_t it = 0;
+      Ring rl, ra;
       int j = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++j) {
+        const TileInfo ti = tile_info(p, act_e, tile_start, n_act, t);
+        const uint32_t idesc = idesc_bf16(BM, ti.nmma);
         const int buf = j & 1;
-        if (!mbar_wait(&tmem_empty[buf], (uint32_t)(((j >> 1) & 1) ^ 1), kWaitBudgetCycles) ||
-            abort_flag) {
+        {
+          TC_T0();
+          if (!mbar_wait(&tmem_empty[buf], (uint32_t)(((j >> 1) & 1) ^ 1), kWaitBudgetCycles))
+            ok = false;
+          TC_ACC(w_mma_tmem);
+        }
+        if (!ok || abort_flag) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d0 = tmem_base + (uint32_t)(buf * NACC * BN);
-        for (int kb = 0; kb < nkb; ++kb) {
-          const int s = (int)(consumed % S);
-          const uint32_t round = (uint32_t)(consumed / S);
-          if (!mbar_wait(&a_full[s], round & 1u, kWaitBudgetCycles) ||
-              !mbar_wait(&raw_full[s], round & 1u, kWaitBudgetCycles) || abort_flag) {
+        const uint32_t d0 = tmem_base + (uint32_t)(buf * BN);
+        for (int kb = 0; kb < nkb; ++kb, ++it, rl.next(SL), ra.next(SA)) {
+          const int sl = rl.idx, sa = ra.idx;
+          {
+            TC_T0();
+            if (!mbar_wait(&a_full[sa], ra.phase, kWaitBudgetCycles)) ok = false;
+            TC_ACC(w_mma_afull);
+          }
+          {
+            TC_T0();
+            if (!mbar_wait(&load_full[sl], rl.phase, kWaitBudgetCycles)) ok = false;
+            TC_ACC(w_mma_load);
+          }
+          if (!ok || abort_flag) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint64_t bdesc = smem_desc_sw128(stage_b(s));
+          // operand visibility: the writers' proxy fence (dequant) or the TMA
+          // transaction count (tokens) plus this acquire on the barrier
+          const uint64_t adesc = smem_desc_sw128(stage_a(sa));
+          const uint64_t bdesc = smem_desc_sw128(stage_b(sl));
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-#pragma unroll
-            for (int acc = 0; acc < NACC; ++acc) {
-              const uint64_t adesc = smem_desc_sw128(stage_a(s, acc));
-              // K advance inside the swizzle atom: 16 elements = 32 bytes
-              umma_bf16(d0 + acc * BN, adesc + 2 * kk, bdesc + 2 * kk, idesc,
-                        (kb | kk) != 0 ? 1u : 0u);
-            }
-          }
-          umma_commit(&empty_bar[s]);
-          ++consumed;
+          for (int kk = 0; kk < BK / 16; ++kk)  // K advance in the swizzle atom: 32 bytes
+            umma_bf16(d0, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+          umma_commit(&a_empty[sa]);
+          umma_commit(&load_empty[sl]);
         }
         if (!ok) break;
         umma_commit(&tmem_full[buf]);
@@ -470,57 +605,129 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         raise_device_error(p.err, MOE_DEVERR_TIMEOUT);
         abort_flag = 1;
       }
-      // wait for the last MMAs of this thread before TMEM is released
-      __shared__ uint64_t drain_bar;
-      mbar_init(&drain_bar, 1);
-      fence_barrier_init();
-      umma_commit(&drain_bar);
-      mbar_wait(&drain_bar, 0, kWaitBudgetCycles);
+      // wait for this thread's last MMAs before TMEM is released (a commit
+      // with no MMA issued before it is not relied on to arrive)
+      if (it > 0) {
+        umma_commit(&drain_bar);
+        mbar_wait(&drain_bar, 0, kWaitBudgetCycles);
+      }
+      TC_FLUSH(4, w_mma_tmem);
+      TC_FLUSH(5, w_mma_afull);
+      TC_FLUSH(6, w_mma_load);
+      TC_FLUSH(7, clock64() - t_mma0);
+      TC_FLUSH(8, it);
     }
     __syncwarp();
   } else {
     // =============================== epilogue ===============================
+    long long w_epi = 0;
+    const long long t_epi0 = clock64();
     int j = 0;
+    uint32_t xs = 0;  // SWIGLU exchange steps so far
     bool ok = true;
-    const int m = warp * 32 + lane;  // accumulator row = TMEM lane
+    const int pair = warp & 1, hi = warp >> 1;  // SWIGLU: hi = 0 holds gate lanes, 1 up lanes
     for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++j) {
       const TileInfo ti = tile_info(p, act_e, tile_start, n_act, t);
       const int buf = j & 1;
-      if (!mbar_wait(&tmem_full[buf], (uint32_t)((j >> 1) & 1), kWaitBudgetCycles) || abort_flag) {
-        ok = false;
-        break;
+      {
+        TC_T0();
+        if (!warp_wait(&tmem_full[buf], (uint32_t)((j >> 1) & 1), &abort_flag)) ok = false;
+        TC_ACC(w_epi);
       }
+      if (!ok) break;
       tc_fence_after();
-      const int col = ti.mt * BM + m;  // output column
-      const bool col_ok = col < p.n_out;
-      const int nvalid = min(BN, ti.m - ti.nt * BN);
-      const uint32_t lane_addr = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * NACC * BN);
-      for (int n0 = 0; n0 < BN; n0 += 16) {
-        uint32_t g[16], u[16];
-        tmem_ld16(lane_addr + n0, g);
-        if (MODE == kTcSwiglu) tmem_ld16(lane_addr + BN + n0, u);
-        tmem_ld_wait();
-        if (col_ok) {
+      const int64_t row0 = (int64_t)ti.seg_lo + ti.tok0;  // output row of tile column 0
+      const uint32_t lane_addr =
+          tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * BN);
+      if (MODE == kTcRaw) {
+        const int col = ti.mt * BM + warp * 32 + lane;
+        const bool col_ok = col < p.n_out;
+        const int64_t stride = p.n_out;
+        float* orow = static_cast<float*>(p.out) + row0 * stride + col;  // row n0 of the step
+        for (int n0 = 0; n0 < ti.nv; n0 += 32, orow += 32 * stride) {
+          uint32_t a[16], b[16];
+          tmem_ld16(lane_addr + n0, a);
+          tmem_ld16(lane_addr + n0 + 16, b);
+          tmem_ld_wait();
+          if (col_ok) {
+            float* q = orow;
+            if (n0 + 32 <= ti.nv) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            if (n0 + i < nvalid) {
-              const int64_t row = (int64_t)ti.seg_lo + ti.nt * BN + n0 + i;
-              if (MODE == kTcSwiglu) {
-                const float hv = swiglu_f32(__uint_as_float(g[i]), __uint_as_float(u[i]));
-                if (p.out_dtype == MOE_DTYPE_BF16)
-                  static_cast<uint16_t*>(p.out)[row * p.n_out + col] = f32_to_bf16_rne(hv);
-                else
-                  static_cast<float*>(p.out)[row * p.n_out + col] = hv;
-              } else {
-                static_cast<float*>(p.out)[row * p.n_out + col] = __uint_as_float(g[i]);
-              }
+              for (int i = 0; i < 16; ++i, q += stride) *q = __uint_as_float(a[i]);
+#pragma unroll
+              for (int i = 0; i < 16; ++i, q += stride) *q = __uint_as_float(b[i]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i, q += stride)
+                if (n0 + i < ti.nv) *q = __uint_as_float(a[i]);
+#pragma unroll
+              for (int i = 0; i < 16; ++i, q += stride)
+                if (n0 + 16 + i < ti.nv) *q = __uint_as_float(b[i]);
             }
           }
         }
+      } else {
+        // gate lane f (warp pair, hi = 0) and up lane f (hi = 1) hold the two
+        // halves of feature f.  Per step both load two 16-column chunks; the
+        // gate warp finishes the first chunk, the up warp the second, each
+        // after receiving the partner's half of it through shared memory
+        // (double-buffered: a buffer is rewritten only after the partner's
+        // next arrival, which follows its reads).
+        const int f = ti.mt * kHalfRows + pair * 32 + lane;
+        const bool f_ok = f < p.n_out;
+        for (int c = 0; c * 16 < ti.nv; c += 2, ++xs) {
+          uint32_t a[16], b[16];
+          tmem_ld16(lane_addr + c * 16, a);
+          tmem_ld16(lane_addr + c * 16 + 16, b);
+          tmem_ld_wait();
+          const int xb = (int)(xs & 1u);
+          float* mine = xbuf + ((pair * 2 + xb) * 2 + hi) * (16 * 32);
+          const float* theirs = xbuf + ((pair * 2 + xb) * 2 + (hi ^ 1)) * (16 * 32);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) mine[i * 32 + lane] = __uint_as_float(hi == 0 ? b[i] : a[i]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&xfull[pair][xb][hi]);
+          if (!warp_wait(&xfull[pair][xb][hi ^ 1], (xs >> 1) & 1u, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int chunk = c + hi;
+          if (f_ok) {
+            const int64_t stride = p.n_out;
+            const int64_t first = (row0 + chunk * 16) * stride + f;
+            const int nrem = ti.nv - chunk * 16;  // valid rows of this chunk (may be <= 0)
+            float hv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float other = theirs[i * 32 + lane];
+              const float g = hi == 0 ? __uint_as_float(a[i]) : other;
+              const float u = hi == 0 ? other : __uint_as_float(b[i]);
+              hv[i] = swiglu_f32(g, u);
+            }
+            if (p.out_dtype == MOE_DTYPE_BF16) {
+              uint16_t* q = static_cast<uint16_t*>(p.out) + first;
+#pragma unroll
+              for (int i = 0; i < 16; ++i, q += stride)
+                if (i < nrem) *q = f32_to_bf16_rne(hv[i]);
+            } else {
+              float* q = static_cast<float*>(p.out) + first;
+#pragma unroll
+              for (int i = 0; i < 16; ++i, q += stride)
+                if (i < nrem) *q = hv[i];
+            }
+          }
+          __syncwarp();
+        }
+        if (!ok) break;
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tmem_empty[buf]);
+    }
+    if (lane == 0 && warp == 0) {
+      TC_FLUSH(9, w_epi);
+      TC_FLUSH(10, clock64() - t_epi0);
+      TC_FLUSH(11, j);
     }
     if (!ok && lane == 0) {
       raise_device_error(p.err, MOE_DEVERR_TIMEOUT);
@@ -531,7 +738,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(tmem_base, TMEM_COLS);
+  if (warp == kMmaWarp) tmem_dealloc(tmem_base, kTmemCols);
 }
 
 // ---- host side ----------------------------------------------------------------
@@ -572,14 +779,15 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint6
 template <int BITS, int MODE, int ACT>
 moe_status_t launch_tc(const CUtensorMap& tmc, const CUtensorMap& tma, TcParams p,
                        int64_t max_tiles, cudaStream_t st) {
-  constexpr int NACC = MODE == kTcSwiglu ? 2 : 1;
-  constexpr int STAGE_BYTES = NACC * kTileBytes + kTileBytes + NACC * BM * BK * BITS / 8;
-  const size_t budget = 200 * 1024;
-  int stages = (int)(budget / STAGE_BYTES);
-  if (stages > 6) stages = 6;
-  if (stages < 2) return MOE_ERR_UNSUPPORTED;
-  p.stages = stages;
-  const size_t smem = (size_t)stages * STAGE_BYTES + 1024;  // + alignment slack
+  constexpr int LOAD_BYTES = kBTileBytes + BM * BK * BITS / 8;
+  const int a_stages = 3;
+  const size_t budget = 200 * 1024;  // dynamic part; the static part holds about 25 KB
+  int load_stages = (int)((budget - 1024 - (size_t)a_stages * kATileBytes) / LOAD_BYTES);
+  if (load_stages > 6) load_stages = 6;
+  if (load_stages < 2) return MOE_ERR_UNSUPPORTED;
+  p.load_stages = load_stages;
+  p.a_stages = a_stages;
+  const size_t smem = (size_t)a_stages * kATileBytes + (size_t)load_stages * LOAD_BYTES + 1024;
   auto kern = tc_qmm_kernel<BITS, MODE, ACT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
@@ -602,13 +810,14 @@ moe_status_t tc_qmm(const void* act, int act_kind, const int32_t* sorted,
   // act_kind: 0 = x bf16 [T, K] gathered by token, 2 = h bf16 [T*kmax, K] by sorted row
   if (act_kind != 0 && act_kind != 2) return MOE_ERR_UNSUPPORTED;
   if (K % BK != 0 || n_rows % 64 != 0) return MOE_ERR_INVALID_ARG;
+  if (E > 1024) return MOE_ERR_UNSUPPORTED;
   const bool gather = act_kind == 0;
   const int64_t A = (int64_t)T * kmax;
   if (A == 0) return MOE_OK;
   CUtensorMap tmc, tma;
   const uint64_t row_words = (uint64_t)K * bits / 32;
   if (!make_map_2d(&tmc, CU_TENSOR_MAP_DATA_TYPE_UINT32, wq, row_words, (uint64_t)E * n_rows,
-                   row_words * 4, BK * bits / 32, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
+                   row_words * 4, BK * bits / 32, kBoxRows, CU_TENSOR_MAP_SWIZZLE_NONE))
     return MOE_ERR_CUDA;
   if (gather) {
     if (!make_map_2d(&tma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, K, (uint64_t)T,
@@ -616,7 +825,7 @@ moe_status_t tc_qmm(const void* act, int act_kind, const int32_t* sorted,
       return MOE_ERR_CUDA;
   } else {
     if (!make_map_2d(&tma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, K, (uint64_t)A,
-                     (uint64_t)K * 2, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+                     (uint64_t)K * 2, BK, kBoxRows, CU_TENSOR_MAP_SWIZZLE_128B))
       return MOE_ERR_CUDA;
   }
   TcParams p;
@@ -631,8 +840,9 @@ moe_status_t tc_qmm(const void* act, int act_kind, const int32_t* sorted,
   p.K = K;
   p.n_rows = n_rows;
   p.n_out = swiglu ? n_rows / 2 : n_rows;
-  p.n_mt = (p.n_out + BM - 1) / BM;
-  p.stages = 2;
+  p.n_mt = swiglu ? (p.n_out + kHalfRows - 1) / kHalfRows : (p.n_out + BM - 1) / BM;
+  p.load_stages = 2;
+  p.a_stages = 2;
   p.err = moe_host::device_error_word();
   // upper bound of the tile count: every expert that can be active, plus one
   // partial n-tile each

@@ -170,3 +170,71 @@ extern "C" moe_status_t moe_permute(const int32_t* topk_ids, const int32_t* k_de
   permute_kernel<<<1, kPermuteThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
   return launch_status();
 }
+
+// ---- token rows in expert order ------------------------------------------
+
+namespace moe {
+namespace {
+
+constexpr int kRowsThreads = 256;
+constexpr int kRowsUnroll = 4;
+
+// x_sorted[r] = x[sorted[r] / kmax] for r < T*k, one warp per row, 16-byte
+// vectors, kRowsUnroll loads in flight per lane.
+__global__ void __launch_bounds__(kRowsThreads) permute_rows_kernel(
+    const uint4* __restrict__ x, const int32_t* __restrict__ sorted,
+    const int32_t* __restrict__ k_dev, int T, int kmax, int vec_per_row,
+    uint4* __restrict__ out, unsigned int* err) {
+  const int k = min(max(*k_dev, 0), kmax);
+  const int64_t rows = (int64_t)T * k;
+  const int lane = threadIdx.x & 31;
+  const int64_t wstride = (int64_t)gridDim.x * (kRowsThreads / 32);
+  for (int64_t r = (int64_t)blockIdx.x * (kRowsThreads / 32) + (threadIdx.x >> 5); r < rows;
+       r += wstride) {
+    const int a = __ldg(sorted + r);
+    if (a < 0 || a >= T * kmax) {
+      if (lane == 0) raise_device_error(err, MOE_DEVERR_BAD_INDEX);
+      continue;
+    }
+    const uint4* src = x + (int64_t)(a / kmax) * vec_per_row;
+    uint4* dst = out + r * vec_per_row;
+    for (int c0 = 0; c0 < vec_per_row; c0 += 32 * kRowsUnroll) {
+      uint4 v[kRowsUnroll];
+#pragma unroll
+      for (int u = 0; u < kRowsUnroll; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < vec_per_row) v[u] = ldg_nc_v4(src + c);
+      }
+#pragma unroll
+      for (int u = 0; u < kRowsUnroll; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < vec_per_row) dst[c] = v[u];
+      }
+    }
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_permute_rows(const uint16_t* x, const int32_t* sorted_assign,
+                                         const int32_t* k_dev, int T, int kmax, int H,
+                                         uint16_t* x_sorted, moe_stream_t stream) {
+  using namespace moe_host;
+  if (T < 0 || kmax < 1 || kmax > 16 || (int64_t)T * kmax > (1 << 24)) return MOE_ERR_INVALID_ARG;
+  if (H <= 0 || H % 8 != 0 || !k_dev) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  const void* ptrs[] = {x, sorted_assign, x_sorted};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  const int64_t rows = (int64_t)T * kmax;
+  const int64_t warps_per_block = moe::kRowsThreads / 32;
+  int64_t grid = (rows + warps_per_block - 1) / warps_per_block;
+  const int64_t cap = (int64_t)sm_count() * 8;
+  if (grid > cap) grid = cap;
+  moe::permute_rows_kernel<<<(int)grid, moe::kRowsThreads, 0,
+                             reinterpret_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint4*>(x), sorted_assign, k_dev, T, kmax, H / 8,
+      reinterpret_cast<uint4*>(x_sorted), device_error_word());
+  return launch_status();
+}

@@ -118,6 +118,18 @@ class MoELayer:
             return PATH_TC
         return PATH_GEMV
 
+    def launches_per_call(self, T: int) -> int:
+        """Kernels one forward of T tokens launches: the router (plus its
+        batch finalize when the tokens span more than one 16-token CTA), the
+        permute, the row permute on the tensor-core path, the gate_up
+        product (or two RAW products and the activation when unfused), down
+        and combine."""
+        n = 1 + (0 if (T + 15) // 16 == 1 else 1)
+        n += 1
+        n += 1 if self.resolved_path(T) == PATH_TC else 0
+        n += 1 if self.fused else 3
+        return n + 2
+
     def buffers(self, T: int) -> dict:
         key = T
         if key not in self._bufs:
@@ -136,6 +148,7 @@ class MoELayer:
                 sorted=torch.empty(A, dtype=torch.int32, device=dev),
                 inv_pos=torch.empty(A, dtype=torch.int32, device=dev),
                 h=torch.empty((A, self.I), dtype=h_dtype, device=dev),
+                x_sorted=torch.empty((A, self.H), dtype=torch.bfloat16, device=dev),
                 y=torch.empty((A, self.H), dtype=torch.float32, device=dev),
                 out=torch.empty((T, self.H), dtype=torch.bfloat16, device=dev),
             )
@@ -161,15 +174,24 @@ class MoELayer:
                           b["k_dev"], b["mean_entropy"], b["ws"])
         B.moe_permute(b["topk_ids"], b["k_dev"], self.E, b["counts"], b["offsets"], b["sorted"],
                       b["inv_pos"])
+        # tensor cores: token rows copied once into expert order, so every
+        # tile loads contiguous rows; the GEMV reads x through sorted_assign
+        if path == PATH_TC:
+            ev = _Timer(events, "permute_rows")
+            xs = B.moe_permute_rows(x, b["sorted"], b["k_dev"], self.kmax, b["x_sorted"])
+            ev.stop()
+            srt = None
+        else:
+            xs, srt = x, b["sorted"]
         ev = _Timer(events, "gate_up")
         if self.fused:
             g = self.gate_up
-            B.moe_gate_up_qmm(x, b["sorted"], b["offsets"], b["k_dev"], self.kmax, g.q, g.s, g.b,
-                              self.bits, EPILOGUE_SWIGLU, b["h"].dtype, b["h"], path)
+            B.moe_gate_up_qmm(xs, srt, b["offsets"], b["k_dev"], self.kmax, g.q, g.s, g.b,
+                              self.bits, EPILOGUE_SWIGLU, b["h"].dtype, b["h"], path, T=T)
         else:
             for m, dst in ((self.gate, b["g_raw"]), (self.up, b["u_raw"])):
-                B.moe_gate_up_qmm(x, b["sorted"], b["offsets"], b["k_dev"], self.kmax, m.q, m.s,
-                                  m.b, self.bits, EPILOGUE_RAW, torch.float32, dst, path)
+                B.moe_gate_up_qmm(xs, srt, b["offsets"], b["k_dev"], self.kmax, m.q, m.s,
+                                  m.b, self.bits, EPILOGUE_RAW, torch.float32, dst, path, T=T)
             B.moe_swiglu(b["g_raw"], b["u_raw"], b["k_dev"], T, self.kmax, b["h"].dtype, b["h"])
         ev.stop()
         d = self.down

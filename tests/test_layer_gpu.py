@@ -97,6 +97,52 @@ def test_fused_gate_up_bit_identical_to_two_products(cuda_lib, path, bits, T, k,
             assert rel_l2(got[lo:hi], want) <= (1e-5 if path == "gemv" else 3e-3)
 
 
+@pytest.mark.parametrize("T,k,E,H", [(1, 4, 16, 512), (37, 3, 8, 1024), (300, 8, 64, 256)])
+def test_permute_rows_is_the_sorted_gather(cuda_lib, T, k, E, H):
+    cfg = CFG["tiny"].scaled(H=H, I=256, E=E, k=k, T=T)
+    layer_np = workloads.make_layer(cfg)
+    x_bits = workloads.make_tokens(cfg)
+    d = dev()
+    layer = cuda_lib.MoELayer.from_workload(layer_np, d)
+    x = cuda_lib.bf16_from_bits(x_bits, d)
+    layer(x)
+    b = layer.buffers(T)
+    xs = cuda_lib.moe_permute_rows(x, b["sorted"], b["k_dev"], cfg.slots)
+    torch.cuda.synchronize()
+    ref = oracle.moe_forward(x_bits, layer_np)
+    srt = ref.perm.sorted_assign
+    assert np.array_equal(to_np(xs.view(torch.int16))[:len(srt)].view(np.uint16),
+                          x_bits[srt // cfg.slots])
+    assert cuda_lib.moe_get_device_error() == 0
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("bits", [4, 8])
+def test_gate_up_presorted_rows_match_gathered_bitwise(cuda_lib, path, bits):
+    """x read through sorted_assign and x pre-permuted into sorted rows give
+    the same products bit for bit (a 300-token, ragged-segment case)."""
+    cfg = CFG["tiny"].scaled(H=512, I=384, E=16, k=4, T=300, bits=bits)
+    layer_np = workloads.make_layer(cfg)
+    x_bits = workloads.make_tokens(cfg)
+    d = dev()
+    p = path_id(cuda_lib, path)
+    layer = cuda_lib.MoELayer.from_workload(layer_np, d, path=p)
+    x = cuda_lib.bf16_from_bits(x_bits, d)
+    layer(x)
+    b = layer.buffers(cfg.T)
+    gu = layer.gate_up
+    xs = cuda_lib.moe_permute_rows(x, b["sorted"], b["k_dev"], cfg.slots)
+    A = cfg.T * cfg.k
+    for epi, dt in ((cuda_lib.EPILOGUE_SWIGLU, torch.bfloat16), (cuda_lib.EPILOGUE_RAW, torch.float32)):
+        g = cuda_lib.moe_gate_up_qmm(x, b["sorted"], b["offsets"], b["k_dev"], cfg.slots, gu.q,
+                                     gu.s, gu.b, bits, epi, out_dtype=dt, path=p)
+        r = cuda_lib.moe_gate_up_qmm(xs, None, b["offsets"], b["k_dev"], cfg.slots, gu.q, gu.s,
+                                     gu.b, bits, epi, out_dtype=dt, path=p, T=cfg.T)
+        isz = torch.int32 if dt == torch.float32 else torch.int16
+        assert torch.equal(g[:A].view(isz), r[:A].view(isz)), (epi, dt)
+    assert cuda_lib.moe_get_device_error() == 0
+
+
 @pytest.mark.parametrize("path", PATHS)
 def test_unfused_switch_matches_fused_bitwise(cuda_lib, path):
     cfg = SMALL["batched_s"]

@@ -374,7 +374,8 @@ def run_ours(args):
                     "down_us": kt["down"] * 1e3, "down_gbs": dn_gbs,
                     "layer_us_per_call": ms * 1e3 / calls,
                     "layer_gbs": (gu_bytes + dn_bytes) / (ms * 1e-3 / calls) / 1e9,
-                    "active_experts_last_call": n_active},
+                    "active_experts_last_call": n_active,
+                    "per_kernel_us": {k: v * 1e3 for k, v in kt.items()}},
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                    "reasons": clocks["reasons"], "samples": clocks["samples"]},
         "e2e": e2e,

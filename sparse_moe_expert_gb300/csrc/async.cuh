@@ -42,6 +42,31 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_test, but a thread whose phase is still open may sleep up to
+// `hint_ns` nanoseconds (woken early when the phase completes).
+__device__ __forceinline__ bool mbar_test_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait for waits that may be long: the thread sleeps in the barrier
+// instead of spinning, so it takes no issue slots from the working warps.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, long long budget) {
+  if (mbar_test(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_test_sleep(bar, parity, 20000u)) {
+    if (clock64() - t0 > budget) return false;
+  }
+  return true;
+}
+
 // Wait for the phase of the given parity to complete, for at most
 // `budget` SM clock cycles.  Returns false if the budget ran out.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long budget) {

@@ -23,13 +23,15 @@
 // One CTA per SM, persistent over the tiles (active expert, m-tile, n-tile);
 // n-tiles of the same weights are adjacent so neighbouring CTAs share them in
 // L2.  Warp roles:
-//   warp 5      loader: per k-block of 64, TMA loads the packed codes of the
-//               tile's 128 rows (2D tensor map, two 64-row boxes) and the
-//               token tile: 4-row gathers (tile::gather4) of the token rows
-//               of x for gate_up, 64-row 2D boxes of h for down, both
+//   warp 5      loader: per k-block of 64, TMA loads the token tile: 4-row
+//               gathers (tile::gather4) of the token rows of x, or 64-row 2D
+//               boxes of rows already in sorted order (h, or x permuted),
 //               128-byte swizzled as the MMA expects; all 32 lanes issue;
-//   warps 6-21  dequant: read the codes from shared memory, w = s*q + b in
-//               fp32 (packed FMA), round to bf16, write the A tile in the
+//   warps 6-13  dequant: each thread streams its row slice of packed codes
+//               and the row's scale and bias straight from global memory
+//               into registers, several k-blocks ahead (covering HBM
+//               latency without shared memory), then w = s*q + b in fp32
+//               (packed FMA), rounds to bf16, writes the A tile in the
 //               128-byte-swizzled K-major layout, proxy fence, arrive;
 //   warp 4      MMA: one thread issues tcgen05.mma (kind::f16, bf16 x bf16 ->
 //               fp32) per 16-wide K slice, commits stage release and
@@ -68,13 +70,16 @@ constexpr int BN = 256;        // most tokens per tile
 constexpr int BK = 64;         // contraction per stage = one scale group = one 128-B swizzle atom
 constexpr int kHalfRows = 64;  // SWIGLU: gate rows, then up rows, per A tile
 constexpr int kBoxRows = 64;   // rows per 2D TMA box (codes and token rows)
-constexpr int kEpiWarps = 4, kMmaWarp = 4, kLoadWarp = 5, kDeqWarp0 = 6, kDeqWarps = 16;
-constexpr int kTcThreads = (kDeqWarp0 + kDeqWarps) * 32;  // 704
+constexpr int kEpiWarps = 4, kMmaWarp = 4, kLoadWarp = 5, kDeqWarp0 = 6, kDeqWarps = 8;
+constexpr int kTcThreads = (kDeqWarp0 + kDeqWarps) * 32;  // 448
 constexpr int kATileBytes = BM * BK * 2;                  // 16 KB bf16 weight tile
+constexpr int kKbPerA = 2;                                // k-blocks per A stage
+constexpr int kAStageBytes = kKbPerA * kATileBytes;       // 32 KB
 constexpr int kBTileBytes = BN * BK * 2;                  // 32 KB bf16 token tile
 constexpr int kMaxStages = 8;
 constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators of up to 256 columns
-constexpr int kScaleLookahead = 4;      // k-blocks of scale/bias in flight per dequant thread
+// A stages of codes, scale and bias in flight per dequant thread
+__host__ __device__ constexpr int dequant_lookahead(int bits) { return bits == 4 ? 3 : 2; }
 
 enum TcMode { kTcSwiglu = 0, kTcRaw = 1 };
 enum TcAct { kTcGatherX = 0, kTcRowsH = 1 };
@@ -82,13 +87,14 @@ enum TcAct { kTcGatherX = 0, kTcRowsH = 1 };
 struct TcParams {
   const int32_t* sorted;   // sorted_assign (gate_up)
   const int32_t* offsets;  // [E+1]
+  const uint32_t* wq;      // codes   [E, n_rows, K*bits/32]
   const uint16_t* ws;      // scales  [E, n_rows, K/64]
   const uint16_t* wb;      // biases
   void* out;
   int out_dtype;
   int kmax, E, K, n_rows, n_out;
-  int load_stages;  // ring of TMA-loaded code + token tiles
-  int a_stages;     // ring of dequantized weight tiles
+  int a_stages;  // ring of dequantized weight stages (kKbPerA k-blocks each)
+  int b_stages;  // ring of TMA-loaded token tiles (one k-block each)
   int n_mt;         // m-tiles per expert
   unsigned int* err;
 };
@@ -205,7 +211,7 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
 // instructions after it are never reached by part of a warp.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
                                           const volatile int* abort_flag) {
-  const bool ok = mbar_wait(bar, parity, kWaitBudgetCycles) && *abort_flag == 0;
+  const bool ok = mbar_wait_sleep(bar, parity, kWaitBudgetCycles) && *abort_flag == 0;
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -265,24 +271,29 @@ __device__ __forceinline__ int tile_weight_row(const TcParams& p, int mt, int r)
   return mt * BM + r;
 }
 
+// 14 warps are granted registers as 16, so 128 per thread is the ceiling
+// for one CTA per SM.
 template <int BITS, int MODE, int ACT>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    tc_qmm_kernel(const __grid_constant__ CUtensorMap tm_codes,
-                  const __grid_constant__ CUtensorMap tm_act, TcParams p) {
-  constexpr int RAW_ROW_BYTES = BK * BITS / 8;         // code bytes per row per k-block
-  constexpr int RAW_BYTES = BM * RAW_ROW_BYTES;        // codes of one stage
-  constexpr int LOAD_BYTES = kBTileBytes + RAW_BYTES;  // token tile + codes
-  // dequant work split: 4 threads per A row, 16 codes each
-  constexpr int DQ_SLICES = kDeqWarps * 32 / BM;  // 4
-  constexpr int DQ_CHUNKS = 8 / DQ_SLICES;        // 16-byte bf16 chunks per thread: 2
-  constexpr int PD = kScaleLookahead;
-  static_assert(DQ_CHUNKS == 2, "dequant split assumes two output chunks per thread");
+    tc_qmm_kernel(const __grid_constant__ CUtensorMap tm_act, TcParams p) {
+  // dequant work split: 2 threads per A row, 32 codes of each k-block each
+  constexpr int DQ_SLICES = kDeqWarps * 32 / BM;  // 2
+  constexpr int DQ_CHUNKS = 8 / DQ_SLICES;        // 16-byte bf16 chunks per thread per k-block: 4
+  constexpr int KB_WORDS = BK * BITS / 32;         // code words of one row per k-block
+  constexpr int QV = KB_WORDS / DQ_SLICES / 4;     // 16-byte code loads per thread per k-block
+  constexpr int PD = dequant_lookahead(BITS);      // A stages of codes in flight
+  static_assert(DQ_CHUNKS == 4, "dequant split assumes four output chunks per thread");
 
   extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t load_full[kMaxStages], load_empty[kMaxStages];
+  // A ring (dequantized weights, kKbPerA k-blocks per stage): a_full arrived
+  // by the dequant warps once the stage's token tiles have landed too, so
+  // the MMA thread waits once per A stage; a_empty committed by the MMAs.
+  // B ring (token tiles, one k-block per slot): b_full counts the TMA bytes,
+  // b_empty is committed by the MMAs.
   __shared__ uint64_t a_full[kMaxStages], a_empty[kMaxStages];
+  __shared__ uint64_t b_full[kMaxStages], b_empty[kMaxStages];
   __shared__ uint64_t tmem_full[2], tmem_empty[2];
   __shared__ uint64_t xfull[2][2][2];  // SWIGLU exchange: [pair][buffer][writer half]
   __shared__ uint64_t drain_bar;
@@ -294,19 +305,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ volatile int abort_flag;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int SL = p.load_stages, SA = p.a_stages;
+  const int SA = p.a_stages, SB = p.b_stages;
   const int nkb = p.K / BK;
+  const int nas = (nkb + kKbPerA - 1) / kKbPerA;  // A stages per tile
 
   // ---- set-up: barriers, TMEM, active experts and their tile ranges ----
   if (tid == 0) {
     abort_flag = 0;
-    for (int s = 0; s < SL; ++s) {
-      mbar_init(&load_full[s], 1);
-      mbar_init(&load_empty[s], 1);
-    }
     for (int s = 0; s < SA; ++s) {
       mbar_init(&a_full[s], kDeqWarps);
       mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < SB; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tmem_full[b], 1);
@@ -341,23 +353,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int n_act = n_act_sh;
   const int n_tiles = n_act > 0 ? tile_start[n_act] : 0;
 
-  unsigned char* a_base = smem;                             // SA * kATileBytes
-  unsigned char* l_base = smem + (size_t)SA * kATileBytes;  // SL * LOAD_BYTES
-  auto stage_a = [&](int s) { return a_base + (size_t)s * kATileBytes; };
-  auto stage_b = [&](int s) { return l_base + (size_t)s * LOAD_BYTES; };
-  auto stage_raw = [&](int s) { return l_base + (size_t)s * LOAD_BYTES + kBTileBytes; };
+  unsigned char* a_base = smem;                                     // SA * kAStageBytes
+  unsigned char* b_base = smem + (size_t)SA * kAStageBytes;         // SB * kBTileBytes
+  // k-block h of A stage s: a 128 x 64 K-major SW128 tile
+  auto stage_a = [&](int s, int h) { return a_base + (size_t)s * kAStageBytes + h * kATileBytes; };
+  auto stage_b = [&](int s) { return b_base + (size_t)s * kBTileBytes; };
 
   if (warp == kLoadWarp) {
     // =============================== loader ===============================
     long long w_load_empty = 0;
     int64_t issued = 0;
-    Ring ring;
+    Ring ring;  // B ring
     bool ok = true;
     for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
       const TileInfo ti = tile_info(p, act_e, tile_start, n_act, t);
-      const int64_t code_row0 = (int64_t)ti.e * p.n_rows;
-      const int crow0 = (int)(code_row0 + tile_weight_row<MODE>(p, ti.mt, 0));
-      const int crow1 = (int)(code_row0 + tile_weight_row<MODE>(p, ti.mt, kHalfRows));
       // this lane's gathers: groups g = lane and lane + 32 of 4 token rows
       // (columns past the tile repeat its first token)
       const int ngroups = ti.nmma / 4;
@@ -373,24 +382,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
       }
       const int nbox = (ti.nmma + kBoxRows - 1) / kBoxRows;
-      const uint32_t bytes =
-          (uint32_t)RAW_BYTES + (ACT == kTcGatherX ? (uint32_t)ti.nmma * (BK * 2)
-                                                   : (uint32_t)nbox * (kBoxRows * BK * 2));
+      const uint32_t bytes = ACT == kTcGatherX ? (uint32_t)ti.nmma * (BK * 2)
+                                               : (uint32_t)nbox * (kBoxRows * BK * 2);
       for (int kb = 0; kb < nkb; ++kb) {
         const int s = ring.idx;
         TC_T0();
-        if (!warp_wait(&load_empty[s], ring.phase ^ 1u, &abort_flag)) {
+        if (!warp_wait(&b_empty[s], ring.phase ^ 1u, &abort_flag)) {
           ok = false;
           break;
         }
         TC_ACC(w_load_empty);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&load_full[s], bytes);
-          const int code_col = kb * (BK * BITS / 32);  // in uint32 words
-          tma_load_2d(stage_raw(s), &tm_codes, code_col, crow0, &load_full[s]);
-          tma_load_2d(stage_raw(s) + kHalfRows * RAW_ROW_BYTES, &tm_codes, code_col, crow1,
-                      &load_full[s]);
-        }
+        if (lane == 0) mbar_arrive_expect_tx(&b_full[s], bytes);
         __syncwarp();
         if (ACT == kTcGatherX) {
 #pragma unroll
@@ -398,15 +400,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int g = lane + 32 * h;
             if (g < ngroups)
               tma_gather4(stage_b(s) + g * 4 * (BK * 2), &tm_act, kb * BK, tok[4 * h],
-                          tok[4 * h + 1], tok[4 * h + 2], tok[4 * h + 3], &load_full[s]);
+                          tok[4 * h + 1], tok[4 * h + 2], tok[4 * h + 3], &b_full[s]);
           }
         } else if (lane < nbox) {
           tma_load_2d(stage_b(s) + lane * (kBoxRows * BK * 2), &tm_act, kb * BK,
-                      ti.seg_lo + ti.tok0 + lane * kBoxRows, &load_full[s]);
+                      ti.seg_lo + ti.tok0 + lane * kBoxRows, &b_full[s]);
         }
         __syncwarp();
         ++issued;
-        ring.next(SL);
+        ring.next(SB);
       }
     }
     if (lane == 0) {
@@ -416,133 +418,166 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (!ok && lane == 0) {
       raise_device_error(p.err, MOE_DEVERR_TIMEOUT);
       abort_flag = 1;
-      // the last min(issued, SL) stages may still have copies in flight
+      // the last min(issued, SB) slots may still have copies in flight
       Ring r = ring;
-      for (int64_t j = 0; j < issued && j < SL; ++j) {
-        r.idx = r.idx == 0 ? SL - 1 : r.idx - 1;
-        if (r.idx == SL - 1) r.phase ^= 1u;
-        mbar_wait(&load_full[r.idx], r.phase, kWaitBudgetCycles);
+      for (int64_t j = 0; j < issued && j < SB; ++j) {
+        r.idx = r.idx == 0 ? SB - 1 : r.idx - 1;
+        if (r.idx == SB - 1) r.phase ^= 1u;
+        mbar_wait(&b_full[r.idx], r.phase, kWaitBudgetCycles);
       }
     }
   } else if (warp >= kDeqWarp0) {
     // =============================== dequant ===============================
     const int dt = tid - kDeqWarp0 * 32;
-    const int r = dt / DQ_SLICES;                 // A-tile row 0 .. 127
-    const int c0 = (dt % DQ_SLICES) * DQ_CHUNKS;  // first 16-byte bf16 chunk of this thread
+    const int r = dt / DQ_SLICES;                  // A-tile row 0 .. 127
+    const int slice = dt % DQ_SLICES;
+    const int c0 = slice * DQ_CHUNKS;              // first 16-byte bf16 chunk of this thread
     const int ngroups = p.K / 64;
-    // this CTA's stages in order, (its tiles) x (k-blocks); the scale and
-    // bias of stage st + PD are fetched while stage st is converted
+    const int64_t row_words = (int64_t)p.K * BITS / 32;
+    // this CTA's A stages in order, (its tiles) x (A stages of the tile); the
+    // codes, scales and biases of A stage st + PD are loaded while stage st
+    // is converted
     const int my_tiles = blockIdx.x < n_tiles ? (n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-    const int64_t nst = (int64_t)my_tiles * nkb;
+    const int nst = my_tiles * nas;  // < 2^31: tiles and k-blocks are bounded by int sizes
+    struct Ahead {
+      uint4 q[kKbPerA][QV];   // this thread's code words of each k-block
+      uint32_t sb[kKbPerA];   // scale | bias << 16 of each k-block
+      int nkb;                // k-blocks in the stage (the last of a tile may have fewer)
+    };
     int la_t = blockIdx.x, la_kb = 0;
     const uint16_t* la_sp = nullptr;
     const uint16_t* la_bp = nullptr;
-    auto la_fetch = [&]() -> uint32_t {  // scale | bias << 16 of the look-ahead stage
-      if (la_t >= n_tiles) return 0u;
+    const uint4* la_qp = nullptr;
+    auto la_fetch = [&](Ahead& d) {
+      if (la_t >= n_tiles) {
+        d.nkb = 0;
+#pragma unroll
+        for (int h = 0; h < kKbPerA; ++h) {
+          d.sb[h] = 0u;
+#pragma unroll
+          for (int v = 0; v < QV; ++v) d.q[h][v] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        return;
+      }
       if (la_kb == 0) {
         const TileInfo ti = tile_info(p, act_e, tile_start, n_act, la_t);
         int wrow = tile_weight_row<MODE>(p, ti.mt, r);
-        if (wrow >= p.n_rows) wrow = p.n_rows - 1;  // rows past the matrix: any valid scale
+        if (wrow >= p.n_rows) wrow = p.n_rows - 1;  // rows past the matrix: any valid row
         const int64_t grow = (int64_t)ti.e * p.n_rows + wrow;
         la_sp = p.ws + grow * ngroups;
         la_bp = p.wb + grow * ngroups;
+        la_qp = reinterpret_cast<const uint4*>(p.wq + grow * row_words) + slice * QV;
       }
-      const uint32_t v = (uint32_t)__ldg(la_sp + la_kb) | ((uint32_t)__ldg(la_bp + la_kb) << 16);
-      if (++la_kb == nkb) {
+      d.nkb = min(kKbPerA, nkb - la_kb);
+#pragma unroll
+      for (int h = 0; h < kKbPerA; ++h) {
+        const int kb = h < d.nkb ? la_kb + h : la_kb;  // a missing second k-block repeats the first
+        d.sb[h] = (uint32_t)__ldg(la_sp + kb) | ((uint32_t)__ldg(la_bp + kb) << 16);
+#pragma unroll
+        for (int v = 0; v < QV; ++v) d.q[h][v] = ldg_nc_v4(la_qp + kb * (KB_WORDS / 4) + v);
+      }
+      la_kb += d.nkb;
+      if (la_kb == nkb) {
         la_kb = 0;
         la_t += gridDim.x;
       }
-      return v;
     };
-    // the ring is indexed by the unrolled position u, so each slot stays in
-    // its own register while its load is in flight
-    uint32_t sb[PD];
+    // the ring is indexed by the unrolled position u, so each slot keeps its
+    // own registers while its loads are in flight
+    Ahead ahead[PD];
 #pragma unroll
-    for (int i = 0; i < PD; ++i) sb[i] = la_fetch();
+    for (int i = 0; i < PD; ++i) la_fetch(ahead[i]);
 
-    long long w_dq_load = 0, w_dq_aempty = 0;
-    Ring rl, ra;
+    long long w_dq_aempty = 0;
+    Ring ra, rb;  // A ring, B ring
     bool ok = true;
-    for (int64_t st0 = 0; st0 < nst && ok; st0 += PD) {
+    for (int st0 = 0; st0 < nst && ok; st0 += PD) {
 #pragma unroll
       for (int u = 0; u < PD; ++u) {
         if (st0 + u < nst && ok) {
-          const uint32_t sbv = sb[u];
-          sb[u] = la_fetch();
-          const int sl = rl.idx, sa = ra.idx;
+          const Ahead cur = ahead[u];
+          la_fetch(ahead[u]);
+          const int sa = ra.idx;
           {
-            TC_T0();
-            if (!warp_wait(&load_full[sl], rl.phase, &abort_flag)) ok = false;
-            TC_ACC(w_dq_load);
-          }
-          if (ok) {
             TC_T0();
             if (!warp_wait(&a_empty[sa], ra.phase ^ 1u, &abort_flag)) ok = false;
             TC_ACC(w_dq_aempty);
           }
           if (ok) {
-            const float sc = __half2float(__ushort_as_half((uint16_t)(sbv & 0xFFFFu)));
-            const float bi = __half2float(__ushort_as_half((uint16_t)(sbv >> 16)));
-            const unsigned char* raw = stage_raw(sl) + r * RAW_ROW_BYTES;
-            unsigned char* atile = stage_a(sa);
-            if (BITS == 4) {
-              // one 32-bit word = 8 codes = one 16-byte bf16 chunk
-              const float2 mul = make_float2(512.0f * sc, 32.0f * sc);
-              const float2 add = make_float2(bi - 512.0f * sc, bi - 32.0f * sc);
-              const uint2 q2 = *reinterpret_cast<const uint2*>(raw + c0 * 4);
-              const uint32_t wv[2] = {q2.x, q2.y};
 #pragma unroll
-              for (int i = 0; i < DQ_CHUNKS; ++i) {
-                const uint32_t v = wv[i];
-                const uint32_t sh[4] = {v << 14, v << 6, v >> 2, v >> 10};
-                uint32_t o[4];
+            for (int h = 0; h < kKbPerA; ++h) {
+              if (h < cur.nkb) {
+                const float sc = __half2float(__ushort_as_half((uint16_t)(cur.sb[h] & 0xFFFFu)));
+                const float bi = __half2float(__ushort_as_half((uint16_t)(cur.sb[h] >> 16)));
+                unsigned char* atile = stage_a(sa, h);
+                if (BITS == 4) {
+                  // one 32-bit word = 8 codes = one 16-byte bf16 chunk
+                  const float2 mul = make_float2(512.0f * sc, 32.0f * sc);
+                  const float2 add = make_float2(bi - 512.0f * sc, bi - 32.0f * sc);
+                  const uint32_t wv[4] = {cur.q[h][0].x, cur.q[h][0].y, cur.q[h][0].z, cur.q[h][0].w};
 #pragma unroll
-                for (int pq = 0; pq < 4; ++pq) {
-                  // (1 + q_even/512, 1 + q_odd/32), then w = s*q + b in fp32
-                  const float2 f =
-                      make_float2(__uint_as_float((sh[pq] & 0x0003C000u) | 0x3F800000u),
-                                  __uint_as_float((sh[pq] & 0x003C0000u) | 0x3F800000u));
-                  const float2 w = __ffma2_rn(f, mul, add);
-                  o[pq] = pack_bf16x2(w.x, w.y);
+                  for (int i = 0; i < DQ_CHUNKS; ++i) {
+                    const uint32_t v = wv[i];
+                    const uint32_t sh[4] = {v << 14, v << 6, v >> 2, v >> 10};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int pq = 0; pq < 4; ++pq) {
+                      // (1 + q_even/512, 1 + q_odd/32), then w = s*q + b in fp32
+                      const float2 f =
+                          make_float2(__uint_as_float((sh[pq] & 0x0003C000u) | 0x3F800000u),
+                                      __uint_as_float((sh[pq] & 0x003C0000u) | 0x3F800000u));
+                      const float2 w = __ffma2_rn(f, mul, add);
+                      o[pq] = pack_bf16x2(w.x, w.y);
+                    }
+                    *reinterpret_cast<uint4*>(atile + sw128_offset(r, c0 + i)) =
+                        make_uint4(o[0], o[1], o[2], o[3]);
+                  }
+                } else {
+                  // one 32-bit word = 4 codes; two words = one 16-byte bf16 chunk
+                  const float2 mul = make_float2(256.0f * sc, 256.0f * sc);
+                  const float2 add = make_float2(bi - 256.0f * sc, bi - 256.0f * sc);
+#pragma unroll
+                  for (int i = 0; i < DQ_CHUNKS; i += 2) {
+                    const uint4 q4 = cur.q[h][(i / 2) % QV];
+                    const uint32_t wv[4] = {q4.x, q4.y, q4.z, q4.w};
+                    uint32_t o[8];
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                      const uint32_t v = wv[jj];
+                      const float2 f0 = make_float2(__uint_as_float(((v << 15) & 0x007F8000u) | 0x3F800000u),
+                                                    __uint_as_float(((v << 7) & 0x007F8000u) | 0x3F800000u));
+                      const float2 f1 = make_float2(__uint_as_float(((v >> 1) & 0x007F8000u) | 0x3F800000u),
+                                                    __uint_as_float(((v >> 9) & 0x007F8000u) | 0x3F800000u));
+                      const float2 w0 = __ffma2_rn(f0, mul, add);
+                      const float2 w1 = __ffma2_rn(f1, mul, add);
+                      o[2 * jj] = pack_bf16x2(w0.x, w0.y);
+                      o[2 * jj + 1] = pack_bf16x2(w1.x, w1.y);
+                    }
+                    *reinterpret_cast<uint4*>(atile + sw128_offset(r, c0 + i)) =
+                        make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4*>(atile + sw128_offset(r, c0 + i + 1)) =
+                        make_uint4(o[4], o[5], o[6], o[7]);
+                  }
                 }
-                *reinterpret_cast<uint4*>(atile + sw128_offset(r, c0 + i)) =
-                    make_uint4(o[0], o[1], o[2], o[3]);
               }
-            } else {
-              // one 32-bit word = 4 codes; two words = one 16-byte bf16 chunk
-              const float2 mul = make_float2(256.0f * sc, 256.0f * sc);
-              const float2 add = make_float2(bi - 256.0f * sc, bi - 256.0f * sc);
-              const uint4 q4 = *reinterpret_cast<const uint4*>(raw + c0 * 8);
-              const uint32_t wv[4] = {q4.x, q4.y, q4.z, q4.w};
-              uint32_t o[8];
-#pragma unroll
-              for (int jj = 0; jj < 4; ++jj) {
-                const uint32_t v = wv[jj];
-                const float2 f0 = make_float2(__uint_as_float(((v << 15) & 0x007F8000u) | 0x3F800000u),
-                                              __uint_as_float(((v << 7) & 0x007F8000u) | 0x3F800000u));
-                const float2 f1 = make_float2(__uint_as_float(((v >> 1) & 0x007F8000u) | 0x3F800000u),
-                                              __uint_as_float(((v >> 9) & 0x007F8000u) | 0x3F800000u));
-                const float2 w0 = __ffma2_rn(f0, mul, add);
-                const float2 w1 = __ffma2_rn(f1, mul, add);
-                o[2 * jj] = pack_bf16x2(w0.x, w0.y);
-                o[2 * jj + 1] = pack_bf16x2(w1.x, w1.y);
-              }
-              *reinterpret_cast<uint4*>(atile + sw128_offset(r, c0)) = make_uint4(o[0], o[1], o[2], o[3]);
-              *reinterpret_cast<uint4*>(atile + sw128_offset(r, c0 + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
             }
             fence_proxy_async_smem();
-            __syncwarp();
+            // the A stage is complete once its token tiles have landed too
+#pragma unroll
+            for (int h = 0; h < kKbPerA; ++h) {
+              if (h < cur.nkb && ok) {
+                if (!warp_wait(&b_full[rb.idx], rb.phase, &abort_flag)) ok = false;
+                rb.next(SB);
+              }
+            }
+            if (!ok) break;
             if (lane == 0) mbar_arrive(&a_full[sa]);
-            rl.next(SL);
             ra.next(SA);
           }
         }
       }
     }
-    if (lane == 0) {
-      TC_FLUSH(2, w_dq_load);
-      TC_FLUSH(3, w_dq_aempty);
-    }
+    if (lane == 0) TC_FLUSH(3, w_dq_aempty);
     if (!ok && lane == 0) {
       raise_device_error(p.err, MOE_DEVERR_TIMEOUT);
       abort_flag = 1;
@@ -550,10 +585,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == kMmaWarp) {
     // ================================= MMA =================================
     if (lane == 0) {
-      long long w_mma_tmem = 0, w_mma_afull = 0, w_mma_load = 0;
+      long long w_mma_tmem = 0, w_mma_afull = 0;
       const long long t_mma0 = clock64();
       int64_t it = 0;
-      Ring rl, ra;
+      Ring ra, rb;  // A ring, B ring
       int j = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++j) {
@@ -562,7 +597,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int buf = j & 1;
         {
           TC_T0();
-          if (!mbar_wait(&tmem_empty[buf], (uint32_t)(((j >> 1) & 1) ^ 1), kWaitBudgetCycles))
+          if (!mbar_wait_sleep(&tmem_empty[buf], (uint32_t)(((j >> 1) & 1) ^ 1), kWaitBudgetCycles))
             ok = false;
           TC_ACC(w_mma_tmem);
         }
@@ -572,31 +607,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc_fence_after();
         const uint32_t d0 = tmem_base + (uint32_t)(buf * BN);
-        for (int kb = 0; kb < nkb; ++kb, ++it, rl.next(SL), ra.next(SA)) {
-          const int sl = rl.idx, sa = ra.idx;
+        // one wait per A stage keeps the MMA queue fed
+        for (int as = 0, kb = 0; as < nas; ++as, ra.next(SA)) {
+          const int sa = ra.idx;
           {
             TC_T0();
-            if (!mbar_wait(&a_full[sa], ra.phase, kWaitBudgetCycles)) ok = false;
+            if (!mbar_wait_sleep(&a_full[sa], ra.phase, kWaitBudgetCycles)) ok = false;
             TC_ACC(w_mma_afull);
           }
-          {
-            TC_T0();
-            if (!mbar_wait(&load_full[sl], rl.phase, kWaitBudgetCycles)) ok = false;
-            TC_ACC(w_mma_load);
-          }
-          if (!ok || abort_flag) {
-            ok = false;
-            break;
-          }
-          // operand visibility: the writers' proxy fence (dequant) or the TMA
-          // transaction count (tokens) plus this acquire on the barrier
-          const uint64_t adesc = smem_desc_sw128(stage_a(sa));
-          const uint64_t bdesc = smem_desc_sw128(stage_b(sl));
+          if (!ok) break;
+          // operand visibility: the dequant writers' proxy fence, the token
+          // tiles' transaction counts observed by them, and their release
+          // arrivals acquired by this wait
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)  // K advance in the swizzle atom: 32 bytes
-            umma_bf16(d0, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+          for (int h = 0; h < kKbPerA; ++h) {
+            if (kb < nkb && (h == 0 || as * kKbPerA + h < nkb)) {
+              const uint64_t adesc = smem_desc_sw128(stage_a(sa, h));
+              const uint64_t bdesc = smem_desc_sw128(stage_b(rb.idx));
+#pragma unroll
+              for (int kk = 0; kk < BK / 16; ++kk)  // K advance in the swizzle atom: 32 bytes
+                umma_bf16(d0, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+              umma_commit(&b_empty[rb.idx]);
+              rb.next(SB);
+              ++kb;
+              ++it;
+            }
+          }
           umma_commit(&a_empty[sa]);
-          umma_commit(&load_empty[sl]);
         }
         if (!ok) break;
         umma_commit(&tmem_full[buf]);
@@ -613,7 +650,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       TC_FLUSH(4, w_mma_tmem);
       TC_FLUSH(5, w_mma_afull);
-      TC_FLUSH(6, w_mma_load);
       TC_FLUSH(7, clock64() - t_mma0);
       TC_FLUSH(8, it);
     }
@@ -777,25 +813,34 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint6
 }
 
 template <int BITS, int MODE, int ACT>
-moe_status_t launch_tc(const CUtensorMap& tmc, const CUtensorMap& tma, TcParams p,
-                       int64_t max_tiles, cudaStream_t st) {
-  constexpr int LOAD_BYTES = kBTileBytes + BM * BK * BITS / 8;
-  const int a_stages = 3;
-  const size_t budget = 200 * 1024;  // dynamic part; the static part holds about 25 KB
-  int load_stages = (int)((budget - 1024 - (size_t)a_stages * kATileBytes) / LOAD_BYTES);
-  if (load_stages > 6) load_stages = 6;
-  if (load_stages < 2) return MOE_ERR_UNSUPPORTED;
-  p.load_stages = load_stages;
-  p.a_stages = a_stages;
-  const size_t smem = (size_t)a_stages * kATileBytes + (size_t)load_stages * LOAD_BYTES + 1024;
+moe_status_t launch_tc(const CUtensorMap& tma, TcParams p, int64_t max_tiles, cudaStream_t st) {
   auto kern = tc_qmm_kernel<BITS, MODE, ACT>;
+  // ring depths from the opt-in shared memory left beside the static part
+  static const int stages = [kern] {
+    cudaFuncAttributes fa;
+    int dev = 0, optin = 0;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess)
+      return 0;
+    const long avail = (long)optin - (long)fa.sharedSizeBytes - 1024;
+    const long a_stages = 2;
+    long b_stages = (avail - a_stages * kAStageBytes) / kBTileBytes;
+    if (b_stages > kMaxStages) b_stages = kMaxStages;
+    return b_stages < 2 ? 0 : (int)(a_stages * 16 + b_stages);
+  }();
+  if (stages == 0) return MOE_ERR_UNSUPPORTED;
+  p.a_stages = stages / 16;
+  p.b_stages = stages % 16;
+  const size_t smem =
+      (size_t)p.a_stages * kAStageBytes + (size_t)p.b_stages * kBTileBytes + 1024;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
   const int64_t sms = moe_host::sm_count();
   const int grid = (int)(max_tiles < sms ? max_tiles : sms);
   if (grid <= 0) return MOE_OK;
-  kern<<<grid, kTcThreads, smem, st>>>(tmc, tma, p);
+  kern<<<grid, kTcThreads, smem, st>>>(tma, p);
   return moe_host::launch_status();
 }
 
@@ -814,11 +859,7 @@ moe_status_t tc_qmm(const void* act, int act_kind, const int32_t* sorted,
   const bool gather = act_kind == 0;
   const int64_t A = (int64_t)T * kmax;
   if (A == 0) return MOE_OK;
-  CUtensorMap tmc, tma;
-  const uint64_t row_words = (uint64_t)K * bits / 32;
-  if (!make_map_2d(&tmc, CU_TENSOR_MAP_DATA_TYPE_UINT32, wq, row_words, (uint64_t)E * n_rows,
-                   row_words * 4, BK * bits / 32, kBoxRows, CU_TENSOR_MAP_SWIZZLE_NONE))
-    return MOE_ERR_CUDA;
+  CUtensorMap tma;
   if (gather) {
     if (!make_map_2d(&tma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, K, (uint64_t)T,
                      (uint64_t)K * 2, BK, 1, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -831,6 +872,7 @@ moe_status_t tc_qmm(const void* act, int act_kind, const int32_t* sorted,
   TcParams p;
   p.sorted = sorted;
   p.offsets = offsets;
+  p.wq = wq;
   p.ws = ws;
   p.wb = wb;
   p.out = out;
@@ -841,23 +883,23 @@ moe_status_t tc_qmm(const void* act, int act_kind, const int32_t* sorted,
   p.n_rows = n_rows;
   p.n_out = swiglu ? n_rows / 2 : n_rows;
   p.n_mt = swiglu ? (p.n_out + kHalfRows - 1) / kHalfRows : (p.n_out + BM - 1) / BM;
-  p.load_stages = 2;
   p.a_stages = 2;
+  p.b_stages = 2;
   p.err = moe_host::device_error_word();
   // upper bound of the tile count: every expert that can be active, plus one
   // partial n-tile each
   const int64_t max_active = A < E ? A : E;
   const int64_t max_tiles = (int64_t)p.n_mt * (max_active + (A + BN - 1) / BN);
   if (bits == 4) {
-    if (swiglu) return gather ? launch_tc<4, kTcSwiglu, kTcGatherX>(tmc, tma, p, max_tiles, st)
-                              : launch_tc<4, kTcSwiglu, kTcRowsH>(tmc, tma, p, max_tiles, st);
-    return gather ? launch_tc<4, kTcRaw, kTcGatherX>(tmc, tma, p, max_tiles, st)
-                  : launch_tc<4, kTcRaw, kTcRowsH>(tmc, tma, p, max_tiles, st);
+    if (swiglu) return gather ? launch_tc<4, kTcSwiglu, kTcGatherX>(tma, p, max_tiles, st)
+                              : launch_tc<4, kTcSwiglu, kTcRowsH>(tma, p, max_tiles, st);
+    return gather ? launch_tc<4, kTcRaw, kTcGatherX>(tma, p, max_tiles, st)
+                  : launch_tc<4, kTcRaw, kTcRowsH>(tma, p, max_tiles, st);
   }
-  if (swiglu) return gather ? launch_tc<8, kTcSwiglu, kTcGatherX>(tmc, tma, p, max_tiles, st)
-                            : launch_tc<8, kTcSwiglu, kTcRowsH>(tmc, tma, p, max_tiles, st);
-  return gather ? launch_tc<8, kTcRaw, kTcGatherX>(tmc, tma, p, max_tiles, st)
-                : launch_tc<8, kTcRaw, kTcRowsH>(tmc, tma, p, max_tiles, st);
+  if (swiglu) return gather ? launch_tc<8, kTcSwiglu, kTcGatherX>(tma, p, max_tiles, st)
+                            : launch_tc<8, kTcSwiglu, kTcRowsH>(tma, p, max_tiles, st);
+  return gather ? launch_tc<8, kTcRaw, kTcGatherX>(tma, p, max_tiles, st)
+                : launch_tc<8, kTcRaw, kTcRowsH>(tma, p, max_tiles, st);
 }
 
 }  // namespace moe

@@ -5,14 +5,18 @@
 // the gathered product); page "Qwen3.5-MoE与Qwen3-MoE架构差异深度解析",
 // section 4.2 (per-expert activation counts).
 //
-// One CTA of 1024 threads.  Counts come from shared-memory atomics (integer,
-// so order-independent), the offsets from a block scan.  The scatter walks
-// the assignments in chunks of 1024 in ascending order; inside a chunk an
-// assignment's rank among equal experts is its rank within its warp
+// CTAs of 1024 threads, each owning a contiguous range of assignments
+// (a multiple of 1024).  Every CTA counts all assignments per expert with
+// shared-memory atomics into per-warp histograms (integer, so
+// order-independent), the ones before its range separately, and scans the
+// totals into the offsets.
+// It then places its own range chunk by chunk in ascending order; inside a
+// chunk an assignment's rank among equal experts is its rank within its warp
 // (__match_any_sync) plus the counts of the same expert in lower warps of the
 // chunk (a per-expert column scan over the 32 warp histograms) plus the
-// number already placed by earlier chunks.  The result is unique: for each
-// expert, its assignments in ascending a = t*kmax + j.
+// number before the chunk (earlier CTAs' ranges and earlier chunks).  The
+// result is unique: for each expert, its assignments in ascending
+// a = t*kmax + j.
 #include "common.cuh"
 
 namespace moe {
@@ -32,34 +36,64 @@ struct PermuteParams {
   unsigned int* err;
 };
 
-__global__ void __launch_bounds__(kPermuteThreads) permute_kernel(PermuteParams p) {
+__global__ void __launch_bounds__(kPermuteThreads) permute_kernel(PermuteParams p, int per_block) {
   extern __shared__ int smem_i[];
   const int E = p.E;
   int* cnt = smem_i;              // [E]
   int* off = cnt + E;             // [E]
-  int* run = off + E;             // [E] placed so far
+  int* run = off + E;             // [E] placed before the current chunk
   int* tot = run + E;             // [E] this chunk's count
   int* wcnt = tot + E;            // [32][E] per-warp histograms / prefixes
   __shared__ int warp_sums[kPermuteWarps];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = *p.k_dev;
-  const int64_t slots = (int64_t)p.T * p.kmax;
+  const int slots = p.T * p.kmax;
+  const int lo = blockIdx.x * per_block;
+  const int hi = min(slots, lo + per_block);
 
   for (int i = tid; i < E; i += kPermuteThreads) { cnt[i] = 0; run[i] = 0; }
   for (int i = tid; i < kPermuteWarps * E; i += kPermuteThreads) wcnt[i] = 0;
   __syncthreads();
 
-  // counts
-  for (int64_t a = tid; a < slots; a += kPermuteThreads) {
-    int j = (int)(a % p.kmax);
-    if (j < k) {
-      int e = p.ids[a];
-      if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
-      else raise_device_error(p.err, MOE_DEVERR_BAD_EXPERT);
+  // expert of assignment a, or -1 (slot j >= k, or an id outside [0, E))
+  auto expert_of = [&](int a, bool report) -> int {
+    if (a >= slots || a % p.kmax >= k) return -1;
+    const int v = __ldg(p.ids + a);
+    if (v >= 0 && v < E) return v;
+    if (report) raise_device_error(p.err, MOE_DEVERR_BAD_EXPERT);
+    return -1;
+  };
+
+  // counts: per-warp histogram rows (plain shared atomics, each warp on its
+  // own row) of [0, lo), summed into run[], then of [lo, slots), summed
+  // with run[] into cnt[] (the total).
+  for (int pass = 0; pass < 2; ++pass) {
+    const int from = pass == 0 ? 0 : lo, to = pass == 0 ? lo : slots;
+    int* row = wcnt + warp * E;
+    for (int base = from; base < to; base += 4 * kPermuteThreads) {
+      int eb[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int a = base + u * kPermuteThreads + tid;
+        eb[u] = a < to ? expert_of(a, blockIdx.x == 0) : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (eb[u] >= 0) atomicAdd(row + eb[u], 1);
     }
+    __syncthreads();
+    for (int x = tid; x < E; x += kPermuteThreads) {
+      int sum = 0;
+      for (int w = 0; w < kPermuteWarps; ++w) {
+        sum += wcnt[w * E + x];
+        wcnt[w * E + x] = 0;
+      }
+      if (pass == 0) run[x] = sum;
+      else cnt[x] = run[x] + sum;
+    }
+    __syncthreads();
   }
-  __syncthreads();
 
   // exclusive scan of cnt -> off (E <= 1024 = blockDim)
   {
@@ -86,27 +120,20 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(PermuteParams 
     if (tid < E) {
       int excl = incl - v + warp_sums[warp];
       off[tid] = excl;
-      p.counts[tid] = v;
-      p.offsets[tid] = excl;
-      if (tid == E - 1) p.offsets[E] = excl + v;
+      if (blockIdx.x == 0) {
+        p.counts[tid] = v;
+        p.offsets[tid] = excl;
+        if (tid == E - 1) p.offsets[E] = excl + v;
+      }
     }
   }
   __syncthreads();
 
-  // stable scatter, chunk by chunk
-  for (int64_t base = 0; base < slots; base += kPermuteThreads) {
-    const int64_t a = base + tid;
-    int e = -1;
-    if (a < slots) {
-      int j = (int)(a % p.kmax);
-      if (j < k) {
-        int v = p.ids[a];
-        if (v >= 0 && v < E) e = v;
-        else p.inv_pos[a] = -1;
-      } else {
-        p.inv_pos[a] = -1;
-      }
-    }
+  // stable scatter of [lo, hi), chunk by chunk
+  for (int base = lo; base < hi; base += kPermuteThreads) {
+    const int a = base + tid;
+    const int e = a < hi ? expert_of(a, false) : -1;
+    if (a < hi && e < 0) p.inv_pos[a] = -1;
     const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
     const int rank_in_warp = __popc(peers & lanemask_lt());
     const bool leader = (peers & lanemask_lt()) == 0u;
@@ -167,7 +194,15 @@ extern "C" moe_status_t moe_permute(const int32_t* topk_ids, const int32_t* k_de
                              (int)smem) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
-  permute_kernel<<<1, kPermuteThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  // ranges of whole 1024-assignment chunks; every CTA also reads all ids
+  // once to count, so the CTA count stays moderate
+  const int slots = T * kmax;
+  const int chunks = slots > 0 ? (slots + kPermuteThreads - 1) / kPermuteThreads : 1;
+  const int nb0 = chunks < 64 ? chunks : 64;
+  const int per_block = (chunks + nb0 - 1) / nb0 * kPermuteThreads;
+  const int nb = slots > 0 ? (slots + per_block - 1) / per_block : 1;
+  permute_kernel<<<nb, kPermuteThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
+      p, per_block);
   return launch_status();
 }
 

@@ -4,17 +4,23 @@
 // router without bias, softmax, top-k); page "Qwen3.5-MoE与Qwen3-MoE架构差异
 // 深度解析", sections 2.1-2.2 (top-k routing, entropy-aware k per batch).
 //
-// Kernel 1 (router_topk_kernel): a CTA takes up to kTokensPerCta tokens.
-//   Phase A: every warp computes (token, expert) logits four at a time; lane
-//   l owns the 8-element chunks c = l, l+32, ... of H and chains single-
-//   rounding FMAs over them, then the 32 lane partials are combined by an
-//   xor butterfly (16, 8, 4, 2, 1).  This is the fixed summation order that
-//   makes the ids reproducible bit for bit.
-//   Phase B: one warp per token: max, softmax sums, entropy, top-kmax by
-//   repeated warp argmax (ties to the lower id), weights.
-// Kernel 2 (router_finalize_kernel, or inline when one CTA covers the batch):
-//   mean entropy over the batch in a fixed reduction order, the batch's k,
-//   and for the adaptive rule the normalisation of the chosen k weights.
+// Kernel 1 (router_topk_kernel): a cluster of 8 CTAs takes a group of up to
+// 32 tokens (16 when E > 256); CTA r of the cluster computes the logits of
+// experts [r*E/8, (r+1)*E/8) and stores them into the leader CTA's shared
+// memory (distributed shared memory), so the router weights are streamed by
+// eight SMs at once.
+//   Phase A: the fixed summation order that makes the ids reproducible bit
+//   for bit: lane l of a warp owns the 8-element chunks c = l, l+32, ... of
+//   H and chains single-rounding FMAs over them; the 32 lane partials are
+//   combined by an xor butterfly (16, 8, 4, 2, 1).  A warp computes a tile
+//   of 8 tokens x 4 experts at once (one token x one expert for groups of
+//   fewer than 8 tokens), each (token, expert) value in that same order.
+//   Phase B (leader CTA): one warp per token: max, softmax sums, entropy,
+//   top-kmax by repeated warp argmax (ties to the lower id), weights.
+// Kernel 2 (router_finalize_kernel, or inline when one cluster covers the
+// batch): mean entropy over the batch in a fixed reduction order, the
+// batch's k, and for the adaptive rule the normalisation of the chosen k
+// weights.
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -25,8 +31,11 @@ namespace {
 
 constexpr int kRouterThreads = 512;
 constexpr int kRouterWarps = kRouterThreads / 32;
-constexpr int kTokensPerCta = 16;
+constexpr int kRouterCluster = 8;  // CTAs per token group, splitting the experts
 constexpr int kMaxExperts = 1024;
+
+// Tokens per cluster: the leader holds [tokens][E] fp32 logits.
+__host__ __device__ constexpr int router_group_tokens(int E) { return E <= 256 ? 32 : 16; }
 constexpr int kFinalizeThreads = 256;
 
 struct RouterParams {
@@ -107,68 +116,143 @@ __device__ void finalize_batch(const RouterParams& p) {
   }
 }
 
-__global__ void __launch_bounds__(kRouterThreads) router_topk_kernel(RouterParams p) {
-  extern __shared__ float logits_s[];  // [kTokensPerCta][E]
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int t0 = blockIdx.x * kTokensPerCta;
-  const int nt = min(kTokensPerCta, p.T - t0);
-  const int E = p.E, H = p.H;
-  const int nchunks = H >> 3;
-  const int npairs = nt * E;
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(r)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
 
-  // ---- Phase A: logits ---------------------------------------------------
-  for (int base = warp * 4; base < npairs; base += kRouterWarps * 4) {
-    float acc[4];
-    const uint4* xrow[4];
-    const float4* wrow[4];
-    int tl[4], ex[4];
+// One 8-element chunk of the TM token rows and TN expert rows.
+template <int TM, int TN>
+struct RouterChunk {
+  uint4 x[TM];
+  float4 wa[TN], wb[TN];
+};
+
+template <int TM, int TN>
+__device__ __forceinline__ void load_chunk(RouterChunk<TM, TN>& d, const uint4* const (&xr)[TM],
+                                           const float4* const (&wr)[TN], int c) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      int pidx = min(base + q, npairs - 1);
-      tl[q] = pidx % nt;
-      ex[q] = pidx / nt;
-      xrow[q] = reinterpret_cast<const uint4*>(p.x + (int64_t)(t0 + tl[q]) * H);
-      wrow[q] = reinterpret_cast<const float4*>(p.w + (int64_t)ex[q] * H);
-      acc[q] = 0.0f;
+  for (int m = 0; m < TM; ++m) d.x[m] = __ldg(xr[m] + c);
+#pragma unroll
+  for (int n = 0; n < TN; ++n) {
+    d.wa[n] = __ldg(wr[n] + 2 * c);
+    d.wb[n] = __ldg(wr[n] + 2 * c + 1);
+  }
+}
+
+// acc[m][n] = fma chain over the chunk's elements h = 0..7, in order.
+template <int TM, int TN>
+__device__ __forceinline__ void fma_chunk(float (&acc)[TM][TN], const RouterChunk<TM, TN>& d) {
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    float xf[TM], wf[TN];
+#pragma unroll
+    for (int m = 0; m < TM; ++m) {
+      const uint32_t word = h < 2 ? d.x[m].x : h < 4 ? d.x[m].y : h < 6 ? d.x[m].z : d.x[m].w;
+      xf[m] = (h & 1) ? __uint_as_float(word & 0xFFFF0000u) : __uint_as_float(word << 16);
     }
+#pragma unroll
+    for (int n = 0; n < TN; ++n) {
+      const float4& q = h < 4 ? d.wa[n] : d.wb[n];
+      const int hh = h & 3;
+      wf[n] = hh == 0 ? q.x : hh == 1 ? q.y : hh == 2 ? q.z : q.w;
+    }
+#pragma unroll
+    for (int m = 0; m < TM; ++m)
+#pragma unroll
+      for (int n = 0; n < TN; ++n) acc[m][n] = fmaf(xf[m], wf[n], acc[m][n]);
+  }
+}
+
+// Logits of tokens [t0, t0+nt) x experts [e_lo, e_lo+ne) in warp tiles of
+// TM tokens x TN experts, stored (after bias and temperature) into the
+// leader's [token][E] array at cluster address `lead`.
+template <int TM, int TN>
+__device__ __forceinline__ void router_logit_tiles(const RouterParams& p, int t0, int nt, int e_lo,
+                                                   int ne, uint32_t lead) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int H = p.H, E = p.E;
+  const int nchunks = H >> 3;
+  const int mtiles = (nt + TM - 1) / TM, ntiles = (ne + TN - 1) / TN;
+  for (int tile = warp; tile < mtiles * ntiles; tile += kRouterWarps) {
+    const int tm = tile % mtiles, tn = tile / mtiles;  // neighbouring warps share experts
+    const uint4* xr[TM];
+    const float4* wr[TN];
+#pragma unroll
+    for (int m = 0; m < TM; ++m)
+      xr[m] = reinterpret_cast<const uint4*>(p.x + (int64_t)(t0 + min(tm * TM + m, nt - 1)) * H);
+#pragma unroll
+    for (int n = 0; n < TN; ++n)
+      wr[n] = reinterpret_cast<const float4*>(p.w + (int64_t)(e_lo + min(tn * TN + n, ne - 1)) * H);
+    float acc[TM][TN];
+#pragma unroll
+    for (int m = 0; m < TM; ++m)
+#pragma unroll
+      for (int n = 0; n < TN; ++n) acc[m][n] = 0.0f;
+    // chunks c = lane, lane+32, ...
+#pragma unroll(TM * TN == 1 ? 4 : 1)
     for (int c = lane; c < nchunks; c += 32) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint4 xv = __ldg(xrow[q] + c);
-        float4 w0 = __ldg(wrow[q] + 2 * c), w1 = __ldg(wrow[q] + 2 * c + 1);
-        float2 x01 = bf16x2_to_f32x2(xv.x), x23 = bf16x2_to_f32x2(xv.y);
-        float2 x45 = bf16x2_to_f32x2(xv.z), x67 = bf16x2_to_f32x2(xv.w);
-        float a = acc[q];
-        a = fmaf(x01.x, w0.x, a);
-        a = fmaf(x01.y, w0.y, a);
-        a = fmaf(x23.x, w0.z, a);
-        a = fmaf(x23.y, w0.w, a);
-        a = fmaf(x45.x, w1.x, a);
-        a = fmaf(x45.y, w1.y, a);
-        a = fmaf(x67.x, w1.z, a);
-        a = fmaf(x67.y, w1.w, a);
-        acc[q] = a;
-      }
+      RouterChunk<TM, TN> b;
+      load_chunk(b, xr, wr, c);
+      fma_chunk(acc, b);
     }
+    // every lane ends with the butterfly total; lane m*TN+n stores (m, n)
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int m = 0; m < TM; ++m)
 #pragma unroll
-      for (int off = 16; off >= 1; off >>= 1)
-        acc[q] = __fadd_rn(acc[q], __shfl_xor_sync(0xFFFFFFFFu, acc[q], off));
-    }
-    if (lane == 0) {
+      for (int n = 0; n < TN; ++n) {
+        float v = acc[m][n];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (base + q < npairs) {
-          float v = acc[q];
-          if (p.bias) v = __fadd_rn(v, __ldg(p.bias + ex[q]));
+        for (int off = 16; off >= 1; off >>= 1)
+          v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+        const int tl = tm * TM + m, el = tn * TN + n;
+        if (lane == ((m * TN + n) & 31) && tl < nt && el < ne) {
+          const int e = e_lo + el;
+          if (p.bias) v = __fadd_rn(v, __ldg(p.bias + e));
           v = __fmul_rn(v, p.inv_temp);
-          logits_s[tl[q] * E + ex[q]] = v;
+          st_cluster_f32(lead + (uint32_t)(tl * E + e) * 4u, v);
         }
       }
-    }
   }
-  __syncthreads();
+}
+
+__global__ void __cluster_dims__(kRouterCluster, 1, 1) __launch_bounds__(kRouterThreads)
+    router_topk_kernel(RouterParams p) {
+  extern __shared__ float logits_s[];  // leader: [group tokens][E]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int E = p.E;
+  const int tpc = router_group_tokens(E);
+  const int t0 = (blockIdx.x / kRouterCluster) * tpc;
+  const int nt = min(tpc, p.T - t0);
+  const uint32_t rank = cluster_ctarank();
+  const int e_lo = (int)rank * E / kRouterCluster;
+  const int ne = ((int)rank + 1) * E / kRouterCluster - e_lo;
+
+  // ---- Phase A: logits (every CTA of the cluster, into the leader) -------
+  cluster_sync();  // the leader's shared memory is live before remote stores
+  const uint32_t lead = cluster_map(logits_s, 0);
+  if (ne > 0) {
+    if (nt >= 8) router_logit_tiles<8, 4>(p, t0, nt, e_lo, ne, lead);
+    else router_logit_tiles<1, 1>(p, t0, nt, e_lo, ne, lead);
+  }
+  cluster_sync();  // all logits of the group are in the leader
+  if (rank != 0) return;
 
   // ---- Phase B: softmax, entropy, top-k per token (one warp per token) ---
   const bool adaptive = p.k_fixed == 0;
@@ -242,7 +326,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_topk_kernel(RouterParam
     }
   }
 
-  if (gridDim.x == 1) {
+  if (gridDim.x == kRouterCluster) {
     __syncthreads();
     finalize_batch(p);
   }
@@ -250,6 +334,29 @@ __global__ void __launch_bounds__(kRouterThreads) router_topk_kernel(RouterParam
 
 __global__ void __launch_bounds__(kFinalizeThreads) router_finalize_kernel(RouterParams p) {
   finalize_batch(p);
+}
+
+// Kernel 1 over ceil(T / group) clusters, then the batch finalize unless a
+// single cluster did it inline.
+moe_status_t launch_router(const RouterParams& p, cudaStream_t st) {
+  using namespace moe_host;
+  const int tpc = router_group_tokens(p.E);
+  const int ngroups = (p.T + tpc - 1) / tpc;
+  if (ngroups > 0) {
+    const size_t smem = (size_t)tpc * p.E * sizeof(float);
+    if (smem > 48 * 1024) {
+      if (cudaFuncSetAttribute(router_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    }
+    router_topk_kernel<<<ngroups * kRouterCluster, kRouterThreads, smem, st>>>(p);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+  }
+  if (ngroups != 1) {
+    router_finalize_kernel<<<1, kFinalizeThreads, 0, st>>>(p);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
 }
 
 }  // namespace
@@ -307,22 +414,7 @@ extern "C" moe_status_t moe_router_topk(const uint16_t* x, const float* w_router
   p.err = device_error_word();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
-  const int nblocks = (T + kTokensPerCta - 1) / kTokensPerCta;
-  if (nblocks > 0) {
-    size_t smem = (size_t)kTokensPerCta * E * sizeof(float);
-    if (smem > 48 * 1024) {
-      if (cudaFuncSetAttribute(router_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    }
-    router_topk_kernel<<<nblocks, kRouterThreads, smem, st>>>(p);
-    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
-  }
-  if (nblocks != 1) {
-    router_finalize_kernel<<<1, kFinalizeThreads, 0, st>>>(p);
-    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
-  }
-  return MOE_OK;
+  return launch_router(p, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -420,20 +512,5 @@ extern "C" moe_status_t moe_router_topk_noalloc(const uint16_t* x, const float* 
   p.err = device_error_word();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
-  const int nblocks = (T + kTokensPerCta - 1) / kTokensPerCta;
-  if (nblocks > 0) {
-    size_t smem = (size_t)kTokensPerCta * E * sizeof(float);
-    if (smem > 48 * 1024) {
-      if (cudaFuncSetAttribute(router_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    }
-    router_topk_kernel<<<nblocks, kRouterThreads, smem, st>>>(p);
-    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
-  }
-  if (nblocks != 1) {
-    router_finalize_kernel<<<1, kFinalizeThreads, 0, st>>>(p);
-    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
-  }
-  return MOE_OK;
+  return launch_router(p, st);
 }

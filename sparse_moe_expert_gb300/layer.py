@@ -120,11 +120,12 @@ class MoELayer:
 
     def launches_per_call(self, T: int) -> int:
         """Kernels one forward of T tokens launches: the router (plus its
-        batch finalize when the tokens span more than one 16-token CTA), the
-        permute, the row permute on the tensor-core path, the gate_up
-        product (or two RAW products and the activation when unfused), down
-        and combine."""
-        n = 1 + (0 if (T + 15) // 16 == 1 else 1)
+        batch finalize when the tokens span more than one token group of 32,
+        16 when E > 256), the permute, the row permute on the tensor-core
+        path, the gate_up product (or two RAW products and the activation
+        when unfused), down and combine."""
+        group = 32 if self.E <= 256 else 16
+        n = 1 + (0 if (T + group - 1) // group == 1 else 1)
         n += 1
         n += 1 if self.resolved_path(T) == PATH_TC else 0
         n += 1 if self.fused else 3
@@ -162,18 +163,22 @@ class MoELayer:
                 inv_temperature: Optional[float] = None, events: Optional[dict] = None
                 ) -> torch.Tensor:
         """x: bf16 [T, H] on the device.  Returns bf16 [T, H] (a reused buffer
-        unless ``out`` is given).  ``events``, if given, maps "gate_up" and
-        "down" to lists that receive (start, end) CUDA events around those
-        launches."""
+        unless ``out`` is given).  ``events``, if given, receives per kernel
+        ("router", "permute", "permute_rows", "gate_up", "down", "combine") a
+        list of (start, end) CUDA events around its launches."""
         T = x.shape[0]
         b = self.buffers(T)
         path = self.resolved_path(T)
         it = self.inv_temperature if inv_temperature is None else float(inv_temperature)
+        ev = _Timer(events, "router")
         B.moe_router_topk(x, self.router_w, self.logit_bias, it, self.k_fixed, self.kmax,
                           self.thr[0], self.thr[1], self.renormalize, b["topk_ids"], b["topk_w"],
                           b["k_dev"], b["mean_entropy"], b["ws"])
+        ev.stop()
+        ev = _Timer(events, "permute")
         B.moe_permute(b["topk_ids"], b["k_dev"], self.E, b["counts"], b["offsets"], b["sorted"],
                       b["inv_pos"])
+        ev.stop()
         # tensor cores: token rows copied once into expert order, so every
         # tile loads contiguous rows; the GEMV reads x through sorted_assign
         if path == PATH_TC:
@@ -200,7 +205,9 @@ class MoELayer:
                        b["y"], path)
         ev.stop()
         res = out if out is not None else b["out"]
+        ev = _Timer(events, "combine")
         B.moe_combine(b["y"], b["inv_pos"], b["topk_w"], b["k_dev"], T, self.kmax, res)
+        ev.stop()
         return res
 
     __call__ = forward

@@ -53,6 +53,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample", type=int, default=0, help="oracle sample size (calls/tokens)")
+    p.add_argument("--path", default="auto", choices=["auto", "gemv", "tc", "tc_small"],
+                   help="kernel family for the two quantized products")
     p.add_argument("--experts", type=int, default=0,
                    help="smaller expert pool (same per-call work; for profiling captures)")
     return p.parse_args(argv)
@@ -239,7 +241,9 @@ def run_ours(args):
     if args.experts:
         cfg = cfg.scaled(E=args.experts)
     layer_np = workloads.make_layer(cfg)
-    layer = moe.MoELayer.from_workload(layer_np, dev, free_sources=True)
+    path = {"auto": moe.PATH_AUTO, "gemv": moe.PATH_GEMV, "tc": moe.PATH_TC,
+            "tc_small": moe.PATH_TC_SMALL}[args.path]
+    layer = moe.MoELayer.from_workload(layer_np, dev, free_sources=True, path=path)
     calls = cfg.calls
     T = cfg.T
     starts = shard_calls(calls, rank, world)

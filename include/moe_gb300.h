@@ -69,7 +69,8 @@ enum { MOE_EPILOGUE_RAW = 0, MOE_EPILOGUE_SWIGLU = 1 };
 enum {
   MOE_PATH_AUTO = 0, /* chosen from the mean tokens per expert, T*kmax/E */
   MOE_PATH_GEMV = 1, /* CUDA-core grouped GEMV: decode and small batches */
-  MOE_PATH_TC = 2    /* tcgen05 grouped GEMM (TMEM accumulators) */
+  MOE_PATH_TC = 2,   /* tcgen05 grouped GEMM (TMEM accumulators), many tokens per expert */
+  MOE_PATH_TC_SMALL = 3 /* tcgen05 with the codes in tensor memory, up to 16 tokens per tile */
 };
 /* Device error word bits (moe_get_device_error). */
 enum { MOE_DEVERR_BAD_EXPERT = 1u, MOE_DEVERR_TIMEOUT = 2u, MOE_DEVERR_BAD_INDEX = 4u };

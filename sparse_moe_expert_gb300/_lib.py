@@ -12,7 +12,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 6: "MOE_ERR_DEVICE"}
 DTYPE_F32, DTYPE_BF16 = 0, 1
 EPILOGUE_RAW, EPILOGUE_SWIGLU = 0, 1
-PATH_AUTO, PATH_GEMV, PATH_TC = 0, 1, 2
+PATH_AUTO, PATH_GEMV, PATH_TC, PATH_TC_SMALL = 0, 1, 2, 3
 DEVERR_BAD_EXPERT, DEVERR_TIMEOUT, DEVERR_BAD_INDEX = 1, 2, 4
 QMODE_AFFINE = 0
 SCALE_F16, SCALE_BF16, SCALE_F32 = 0, 1, 2

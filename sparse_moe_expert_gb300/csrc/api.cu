@@ -14,6 +14,10 @@ moe_status_t tc_qmm(const void* act, int act_kind, const int32_t* sorted,
                     const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
                     bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
                     int bits, void* out, int out_dtype, cudaStream_t st);
+moe_status_t tc_small_qmm(const void* act, int act_kind, const int32_t* sorted,
+                          const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
+                          bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
+                          int bits, void* out, int out_dtype, cudaStream_t st);
 bool tc_available();
 }  // namespace moe
 
@@ -113,7 +117,7 @@ extern "C" moe_status_t moe_gate_up_qmm(const uint16_t* x, const int32_t* sorted
   if (out_dtype != MOE_DTYPE_F32 && out_dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
   if (epilogue == MOE_EPILOGUE_RAW && out_dtype != MOE_DTYPE_F32) return MOE_ERR_UNSUPPORTED;
   if (epilogue == MOE_EPILOGUE_SWIGLU && n_rows % 2 != 0) return MOE_ERR_INVALID_ARG;
-  if (path < MOE_PATH_AUTO || path > MOE_PATH_TC) return MOE_ERR_INVALID_ARG;
+  if (path < MOE_PATH_AUTO || path > MOE_PATH_TC_SMALL) return MOE_ERR_INVALID_ARG;
   if (H > 49152) return MOE_ERR_UNSUPPORTED;
   if (!expert_offsets || !k_dev) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
@@ -131,6 +135,9 @@ extern "C" moe_status_t moe_gate_up_qmm(const uint16_t* x, const int32_t* sorted
     return moe::tc_qmm(x, act_kind, sorted_assign, expert_offsets, T, kmax, E, H, n_rows, swiglu,
                        w_q, w_s, w_b, bits, out, out_dtype, st);
   }
+  if (p == MOE_PATH_TC_SMALL)
+    return moe::tc_small_qmm(x, act_kind, sorted_assign, expert_offsets, T, kmax, E, H, n_rows,
+                             swiglu, w_q, w_s, w_b, bits, out, out_dtype, st);
   return moe::gemv_qmm(x, act_kind, sorted_assign, expert_offsets, T, kmax, E, H, n_rows, swiglu,
                        w_q, w_s, w_b, bits, out, out_dtype, st);
 }
@@ -145,7 +152,7 @@ extern "C" moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* 
   if (I <= 0 || I % 64 != 0 || H <= 0 || H % 64 != 0) return MOE_ERR_INVALID_ARG;
   if (bits != 4 && bits != 8) return MOE_ERR_UNSUPPORTED;
   if (h_dtype != MOE_DTYPE_F32 && h_dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
-  if (path < MOE_PATH_AUTO || path > MOE_PATH_TC) return MOE_ERR_INVALID_ARG;
+  if (path < MOE_PATH_AUTO || path > MOE_PATH_TC_SMALL) return MOE_ERR_INVALID_ARG;
   if (I > 49152) return MOE_ERR_UNSUPPORTED;
   if (!expert_offsets || !k_dev) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
@@ -160,6 +167,9 @@ extern "C" moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* 
     return moe::tc_qmm(h, act_kind, nullptr, expert_offsets, T, kmax, E, I, H, false, w_q, w_s,
                        w_b, bits, y, MOE_DTYPE_F32, st);
   }
+  if (p == MOE_PATH_TC_SMALL)
+    return moe::tc_small_qmm(h, act_kind, nullptr, expert_offsets, T, kmax, E, I, H, false, w_q,
+                             w_s, w_b, bits, y, MOE_DTYPE_F32, st);
   return moe::gemv_qmm(h, act_kind, nullptr, expert_offsets, T, kmax, E, I, H, false, w_q, w_s,
                        w_b, bits, y, MOE_DTYPE_F32, st);
 }

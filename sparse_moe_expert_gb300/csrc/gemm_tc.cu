@@ -848,6 +848,13 @@ moe_status_t launch_tc(const CUtensorMap& tma, TcParams p, int64_t max_tiles, cu
 
 bool tc_available() { return encode_fn() != nullptr; }
 
+// 2D tensor map for other kernels of the library (the small-batch path).
+bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                        uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                        CUtensorMapSwizzle sw) {
+  return make_map_2d(m, dt, base, inner, outer, row_bytes, box_inner, box_outer, sw);
+}
+
 moe_status_t tc_qmm(const void* act, int act_kind, const int32_t* sorted,
                     const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
                     bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,

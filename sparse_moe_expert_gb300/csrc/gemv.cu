@@ -439,11 +439,23 @@ moe_status_t dispatch_gemv(const GemvParams& p, int bits, int max_tokens, int ma
 
 }  // namespace
 
-// Entry used by the C-ABI wrappers (api.cu).
+bool gemv_mma_supported(int act_kind, int K, int bits, int T);
+moe_status_t gemv_mma_qmm(const void* act, int act_kind, const int32_t* sorted,
+                          const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
+                          bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
+                          void* out, int out_dtype, cudaStream_t st);
+
+// Entry used by the C-ABI wrappers (api.cu).  4-bit codes with K a multiple
+// of 256, bf16 activations and more than one token take the warp-MMA kernel
+// (gemv_mma.cu); the rest (one token, 8-bit codes, fp32 activations) this
+// file's kernel.
 moe_status_t gemv_qmm(const void* act, int act_kind, const int32_t* sorted,
                       const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
                       bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
                       int bits, void* out, int out_dtype, cudaStream_t st) {
+  if (gemv_mma_supported(act_kind, K, bits, T))
+    return gemv_mma_qmm(act, act_kind, sorted, offsets, T, kmax, E, K, n_rows, swiglu, wq, ws, wb,
+                        out, out_dtype, st);
   GemvParams p;
   p.act = act;
   p.act_kind = act_kind;

@@ -15,7 +15,7 @@ import numpy as np
 import torch
 
 from . import binding as B
-from ._lib import EPILOGUE_RAW, EPILOGUE_SWIGLU, PATH_AUTO, PATH_GEMV, PATH_TC, MoEError
+from ._lib import EPILOGUE_RAW, EPILOGUE_SWIGLU, PATH_AUTO, PATH_GEMV, PATH_TC, PATH_TC_SMALL, MoEError
 
 FUSE_ENV = "MOE_GB300_FUSE_GATE_UP"
 TC_MIN_TOKENS_PER_EXPERT = 24  # mirrors the library's automatic path choice

@@ -855,6 +855,20 @@ bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
   return make_map_2d(m, dt, base, inner, outer, row_bytes, box_inner, box_outer, sw);
 }
 
+// 3D tensor map (the streamed GEMV's code boxes); strides in bytes of dims 1, 2.
+bool make_tensor_map_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base,
+                        const uint64_t (&dims)[3], const uint64_t (&strides)[2],
+                        const uint32_t (&box)[3], CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  const cuuint64_t str[2] = {strides[0], strides[1]};
+  const cuuint32_t bx[3] = {box[0], box[1], box[2]};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void*>(base), d, str, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 moe_status_t tc_qmm(const void* act, int act_kind, const int32_t* sorted,
                     const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
                     bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,

@@ -94,10 +94,12 @@ def test_fused_gate_up_bit_identical_to_two_products(cuda_lib, path, bits, T, k,
         lo, hi = ref.perm.offsets[e], ref.perm.offsets[e + 1]
         if hi > lo:
             want = oracle.qmm_raw(xf[srt[lo:hi] // cfg.slots], gq[e], gs[e], gb[e], bits, cfg.H)
-            # GEMV: exact weights, fp32 sums; small-batch tensor cores: exact
-            # (128 + q) x products, fp32 accumulation, per-group affine in fp32;
-            # prefill tensor cores: weights rounded to bf16
-            tol = {"gemv": 1e-5, "tc_small": 1e-4, "tc": 3e-3}[path]
+            # GEMV and small-batch tensor cores: exact (128 + q) x products
+            # accumulated in fp32 by the tensor cores, then the 128 X offset
+            # removed and the per-group affine applied in fp32 (the offset
+            # cancellation scales the accumulation rounding by about
+            # 128 / mean|q - 7.5|); prefill tensor cores: weights rounded to bf16
+            tol = {"gemv": 1e-4, "tc_small": 1e-4, "tc": 3e-3}[path]
             assert rel_l2(got[lo:hi], want) <= tol
 
 

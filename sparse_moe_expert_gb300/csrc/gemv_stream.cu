@@ -14,11 +14,11 @@
 // so those slots take the token values divided by 16; an 8-bit word masked
 // with 0x00FF00FF is (c_0, c_2) * 2^-24.  One or two integer instructions per
 // A register, then mma.sync.m16n8k16 (fp16 x fp16 -> fp32).  The token
-// values are staged as fp16 x * 2^e, one power of two per token chosen so
-// that max |x| 2^e lies in [2^14, 2^15): exact for bf16 values in range.  So
-// one MMA forms P = 2^(e-24) sum q x over 16 k for 16 weight rows and up to
-// 8 tokens, with no offset to cancel; CUDA cores accumulate s P and b X per
-// group and a tile's partial is (sum s P) * 2^(24-e) + sum b X.
+// values are staged as fp16 x * 2^e, one power of two per token and group
+// chosen so that the group's max |x| 2^e lies in [2^14, 2^15): exact for
+// bf16 values in range.  So one MMA forms P = 2^(e-24) sum q x over 16 k for
+// 16 weight rows and up to 8 tokens, with no offset to cancel; CUDA cores
+// accumulate (s 2^(24-e)) P and b X per group.
 //
 // Data movement.  A tile is 16 weight rows (SWIGLU: 8 gate rows and the 8 up
 // rows of the same features) of one active expert, applied to a chunk of up
@@ -46,12 +46,20 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "async.cuh"
 #include "common.cuh"
 
 // Optional per-role cycle accounting (compiled in only with -DMOE_SV_TRACE).
 #ifdef MOE_SV_TRACE
-__device__ unsigned long long g_sv_trace[16];
+__device__ unsigned long long g_sv_trace[20];
+__device__ unsigned long long g_sv_span[2];  // min entry, max exit (globaltimer ns)
+__device__ __forceinline__ unsigned long long sv_gtime() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 #define SV_CLK() clock64()
 #define SV_ADD(slot, v) atomicAdd(&g_sv_trace[slot], (unsigned long long)(v))
 #else
@@ -69,15 +77,19 @@ bool tc_available();
 namespace {
 
 constexpr int kSvConsumers = 16;
-constexpr int kSvThreads = (kSvConsumers + 2) * 32;
-constexpr int kSvProducer = kSvConsumers;
-constexpr int kSvEpilogue = kSvConsumers + 1;
-constexpr int kSvRowChunk = 1024;               // code bytes of one row per stage
+constexpr int kSvThreads = (kSvConsumers + 3) * 32;
+constexpr int kSvProducer = kSvConsumers;      // codes (TMA)
+constexpr int kSvScaler = kSvConsumers + 1;    // scales and biases (cp.async)
+constexpr int kSvEpilogue = kSvConsumers + 2;
+constexpr int kSvRowChunk = 2048;               // code bytes of one row per stage
 constexpr int kSvCodeBytes = 16 * kSvRowChunk;  // codes of one stage
 constexpr int kSvHalfBytes = 8 * kSvRowChunk;   // tile rows 0-7 | rows 8-15
-constexpr int kSvBoxes = kSvRowChunk / 128;     // 8-row x 128-byte TMA boxes per half
-constexpr int kSvMaxStages = 16;
-constexpr int kSvRedSlots = 2;
+constexpr int kSvBoxes = kSvRowChunk / 128;     // 128-byte blocks per row and stage
+constexpr int kSvMaxStages = 8;
+constexpr int kSvMaxRedSlots = 4;
+
+// Result slots between consumers and epilogue: more when they are small.
+__host__ __device__ constexpr int sv_red_slots(int mts) { return mts == 1 ? 4 : 2; }
 constexpr int kSvMaxE = 1024;
 constexpr int kSvMaxTokens = 8;  // tokens per pass (the n of one MMA)
 
@@ -91,6 +103,7 @@ struct SvShape {
   static constexpr int kGpc = kSvRowChunk / kGroupBytes;  // groups per stage: 32 | 16
   static constexpr int kGpw = kGpc / kSvConsumers;        // groups per consumer warp
   static constexpr int kScaleRow = kGpc * 2 + 16;         // padded bytes per scale row
+  using ScaleVec = typename std::conditional<BITS == 4, uint2, uint32_t>::type;  // kGpw halves
   static constexpr int kScaleBytes = 2 * 16 * kScaleRow;  // scales and biases of 16 rows
 };
 
@@ -118,7 +131,7 @@ struct SvLayout {
 // Shared-memory carve-up, from a 1024-byte aligned base.
 __host__ __device__ inline SvLayout sv_layout(int bits, int K, int mts, int stages, int E) {
   const int ngroups = K / 64;
-  const int gpc = bits == 4 ? 32 : 16;
+  const int gpc = kSvRowChunk / (8 * bits);
   const int scale_bytes = 2 * 16 * (gpc * 2 + 16);
   const int mts2 = mts < 2 ? 2 : mts;
   SvLayout L;
@@ -130,14 +143,14 @@ __host__ __device__ inline SvLayout sv_layout(int bits, int K, int mts, int stag
   L.x = o;
   o += (uint32_t)ngroups * 2 * mts * 4 * 16;
   L.xsum = o;
-  o += (uint32_t)ngroups * mts2 * 4;
+  o += (uint32_t)ngroups * mts2 * 8;
   L.red = o;
-  o += (uint32_t)kSvRedSlots * kSvConsumers * mts * 16 * 4;
+  o += (uint32_t)sv_red_slots(mts) * kSvConsumers * mts * 16 * 4;
   L.act = o;
   o += (uint32_t)4 * (E + 1) * 4;
   o = (o + 7u) & ~7u;
   L.bars = o;
-  o += (uint32_t)(2 * stages + 2 * kSvRedSlots + 2) * 8;
+  o += (uint32_t)(2 * stages + 2 * kSvMaxRedSlots + 2) * 8;
   L.total = o;
   return L;
 }
@@ -153,8 +166,17 @@ struct SvRing {
   }
 };
 
+// Bounded wait of a whole warp; a waiting thread sleeps in the barrier
+// (woken when the phase completes) instead of spinning on issue slots that
+// the working warps of its SM sub-partition need.
 __device__ __forceinline__ bool sv_wait(uint64_t* bar, uint32_t parity) {
-  return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, kWaitBudgetCycles));
+  bool ok = mbar_test(bar, parity);
+  if (!ok) {
+    const long long t0 = clock64();
+    while (!(ok = mbar_test_sleep(bar, parity, 1000u)))
+      if (clock64() - t0 > kWaitBudgetCycles) break;
+  }
+  return __all_sync(0xFFFFFFFFu, ok);
 }
 
 // One 3D box: 32 code words x 8 rows x 8 consecutive 128-byte blocks of the
@@ -190,6 +212,16 @@ __device__ __forceinline__ void cp_async_wait_all_sv() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// d = A B (zero accumulator in)
+__device__ __forceinline__ void mma_sv0(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
 __device__ __forceinline__ void mma_sv(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                        uint32_t b1) {
   asm volatile(
@@ -198,6 +230,13 @@ __device__ __forceinline__ void mma_sv(float (&d)[4], const uint32_t (&a)[4], ui
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+
+// Half i of a packed vector of fp16 scales, as fp32.
+__device__ __forceinline__ float sv_half(uint32_t v, int i) {
+  const __half2 h = *reinterpret_cast<const __half2*>(&v);
+  return (i & 1) ? __high2float(h) : __low2float(h);
+}
+__device__ __forceinline__ float sv_half(uint2 v, int i) { return sv_half(i < 2 ? v.x : v.y, i); }
 
 // Walk over the tile list: active expert a, token chunk c, row tile rt.
 struct SvCursor {
@@ -214,7 +253,7 @@ __global__ void __launch_bounds__(kSvThreads, 1)
   unsigned char* codes = sm + L.codes;
   unsigned char* scales = sm + L.scales;
   uint4* xs = reinterpret_cast<uint4*>(sm + L.x);      // [G][half][n][t] B fragments
-  float* xsum = reinterpret_cast<float*>(sm + L.xsum);  // [G][mts2] sums of x
+  float2* xsum = reinterpret_cast<float2*>(sm + L.xsum);  // [G][mts2] (X, 2^(24-e))
   float* red = reinterpret_cast<float*>(sm + L.red);       // [slot][warp][n][16 rows]
   int* act_e = reinterpret_cast<int*>(sm + L.act);
   int* act_lo = act_e + (p.E + 1);
@@ -223,17 +262,20 @@ __global__ void __launch_bounds__(kSvThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
   uint64_t* empty = full + p.stages;
   uint64_t* red_full = empty + p.stages;
-  uint64_t* red_empty = red_full + kSvRedSlots;
-  uint64_t* xbar = red_empty + kSvRedSlots;  // consumer-only barrier (two phases per restage)
+  const int rslots = sv_red_slots(ONE ? 1 : p.mts);
+  uint64_t* red_empty = red_full + rslots;
+  uint64_t* xbar = red_empty + rslots;  // consumer-only barrier (two phases per restage)
   __shared__ int n_act_sh;
   __shared__ int wtot[kSvThreads / 32];
   __shared__ volatile int abort_flag;
   __shared__ int st_tok[kSvMaxTokens];
   __shared__ int st_nt;
-  __shared__ float st_post[kSvMaxTokens];                // 2^(24 - e) per staged token
-  __shared__ float wmax[kSvConsumers * kSvMaxTokens];    // per-warp max |x| per token
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+#ifdef MOE_SV_TRACE
+  const long long tr_entry = clock64();
+  if (tid == 0) atomicMin(&g_sv_span[0], sv_gtime());
+#endif
   const int stages = p.stages;
   const int mts = ONE ? 1 : p.mts;
   const int mts2 = mts < 2 ? 2 : mts;
@@ -244,7 +286,7 @@ __global__ void __launch_bounds__(kSvThreads, 1)
       mbar_init(&full[s], 33);  // the producer's expect_tx + one cp.async arrival per lane
       mbar_init(&empty[s], kSvConsumers);
     }
-    for (int r = 0; r < kSvRedSlots; ++r) {
+    for (int r = 0; r < rslots; ++r) {
       mbar_init(&red_full[r], kSvConsumers);
       mbar_init(&red_empty[r], 1);
     }
@@ -335,15 +377,18 @@ __global__ void __launch_bounds__(kSvThreads, 1)
   const int row_words = p.K * BITS / 32;
   const int nck = (row_words + kSvRowChunk / 4 - 1) / (kSvRowChunk / 4);  // stages per tile
 
-  if (warp == kSvProducer) {
-    // ================================ producer ================================
+  if (warp == kSvProducer || warp == kSvScaler) {
+    // ======================== producers (codes | scales) ======================
+    // Both walk the same stages; a slot is full once the TMA bytes have landed
+    // and every cp.async lane of the scale warp has arrived.
+    const bool codes_warp = warp == kSvProducer;
     const int64_t tot_rows = (int64_t)p.E * p.n_rows;
     SvRing ring{0, 0u};
     bool ok = true;
     int64_t issued = 0;
     SvCursor cu = cursor_at(u0);
     const int arr = lane >> 4, srow = lane & 15;  // this lane's scale row
-    long long tr_wait = 0, tr_tma = 0, tr_cpa = 0;
+    long long tr_wait = 0, tr_issue = 0;
     const long long tr_start = SV_CLK();
     for (int u = u0; u < u1 && ok; ++u, cursor_next(cu)) {
       const int64_t ebase = (int64_t)act_e[cu.a] * p.n_rows;
@@ -363,50 +408,53 @@ __global__ void __launch_bounds__(kSvThreads, 1)
           ok = false;
           break;
         }
-        tr_wait += SV_CLK() - tr0;
-        const long long trt = SV_CLK();
-        unsigned char* cdst = codes + (size_t)ring.idx * kSvCodeBytes;
-        if (lane == 0) {
-          // blocks past the row end are zero-filled and still counted
-          mbar_arrive_expect_tx(&full[ring.idx], (uint32_t)kSvCodeBytes);
-          tma_load_3d_sv(cdst, &tm_codes, (int)r0, ch * kSvBoxes, &full[ring.idx]);
-          tma_load_3d_sv(cdst + kSvHalfBytes, &tm_codes, (int)r1, ch * kSvBoxes, &full[ring.idx]);
+        const long long tr1 = SV_CLK();
+        tr_wait += tr1 - tr0;
+        if (codes_warp) {
+          unsigned char* cdst = codes + (size_t)ring.idx * kSvCodeBytes;
+          if (lane == 0) {
+            // blocks past the row end are zero-filled and still counted
+            mbar_arrive_expect_tx(&full[ring.idx], (uint32_t)kSvCodeBytes);
+            tma_load_3d_sv(cdst, &tm_codes, (int)r0, ch * kSvBoxes, &full[ring.idx]);
+            tma_load_3d_sv(cdst + kSvHalfBytes, &tm_codes, (int)r1, ch * kSvBoxes,
+                           &full[ring.idx]);
+          }
+          __syncwarp();
+        } else {
+          const int g0 = ch * S::kGpc;
+          const int gbytes = 2 * min(S::kGpc, ngroups - g0);
+          if (grow < tot_rows) {
+            unsigned char* sdst =
+                scales + (size_t)ring.idx * S::kScaleBytes + (arr * 16 + srow) * S::kScaleRow;
+            const unsigned char* src = reinterpret_cast<const unsigned char*>(srcrow + g0);
+            for (int o = 0; o < gbytes; o += p.scale_cw)
+              cp_async_sv(sdst + o, src + o, p.scale_cw);
+          }
+          cp_async_arrive_sv(&full[ring.idx]);
         }
-        __syncwarp();
-        const long long trc = SV_CLK();
-        tr_tma += trc - trt;
-        const int g0 = ch * S::kGpc;
-        const int gbytes = 2 * min(S::kGpc, ngroups - g0);
-        if (grow < tot_rows) {
-          unsigned char* sdst =
-              scales + (size_t)ring.idx * S::kScaleBytes + (arr * 16 + srow) * S::kScaleRow;
-          const unsigned char* src = reinterpret_cast<const unsigned char*>(srcrow + g0);
-          for (int o = 0; o < gbytes; o += p.scale_cw) cp_async_sv(sdst + o, src + o, p.scale_cw);
-        }
-        cp_async_arrive_sv(&full[ring.idx]);
-        __syncwarp();
-        tr_cpa += SV_CLK() - trc;
+        tr_issue += SV_CLK() - tr1;
         ++issued;
         ring.next(stages);
       }
     }
-    cp_async_wait_all_sv();
+    if (!codes_warp) cp_async_wait_all_sv();
     if (lane == 0) {
-      SV_ADD(0, tr_wait);
-      SV_ADD(1, issued);
-      SV_ADD(2, SV_CLK() - tr_start);
-      SV_ADD(11, tr_tma);
-      SV_ADD(12, tr_cpa);
+      SV_ADD(codes_warp ? 0 : 13, tr_wait);
+      SV_ADD(codes_warp ? 1 : 14, issued);
+      SV_ADD(codes_warp ? 2 : 15, SV_CLK() - tr_start);
+      SV_ADD(codes_warp ? 11 : 12, tr_issue);
     }
     if (!ok && lane == 0) {
       raise_device_error(p.err, MOE_DEVERR_TIMEOUT);
       abort_flag = 1;
-      // the last min(issued, stages) slots may still have copies in flight
-      SvRing r = ring;
-      for (int64_t j = 0; j < issued && j < stages; ++j) {
-        r.idx = r.idx == 0 ? stages - 1 : r.idx - 1;
-        if (r.idx == stages - 1) r.phase ^= 1u;
-        mbar_wait(&full[r.idx], r.phase, kWaitBudgetCycles);
+      if (codes_warp) {
+        // the last min(issued, stages) slots may still have copies in flight
+        SvRing r = ring;
+        for (int64_t j = 0; j < issued && j < stages; ++j) {
+          r.idx = r.idx == 0 ? stages - 1 : r.idx - 1;
+          if (r.idx == stages - 1) r.phase ^= 1u;
+          mbar_wait(&full[r.idx], r.phase, kWaitBudgetCycles);
+        }
       }
     }
   } else if (warp < kSvConsumers) {
@@ -459,39 +507,16 @@ __global__ void __launch_bounds__(kSvThreads, 1)
         }
       }
     };
-    // power-of-two exponent e of token n: max |x| 2^e in [2^14, 2^15)
-    auto token_exp = [&](int n) {
-      float m = 0.0f;
-#pragma unroll
-      for (int w = 0; w < kSvConsumers; ++w) m = fmaxf(m, wmax[w * kSvMaxTokens + n]);
-      const int E = (int)((__float_as_uint(m) >> 23) & 0xFFu);
-      int e = m == 0.0f ? 0 : (E == 0 ? 100 : 141 - E);
-      return e < -100 ? -100 : (e > 100 ? 100 : e);
-    };
-    // stage the token values of (expert a, chunk c): fp16 x 2^e in B-fragment
-    // order (4-bit odd-MMA slots take x 2^(e-4), their codes read as 16 q),
-    // the group sums of x and the factor 2^(24-e) that undoes both scalings
+    // stage the token values of (expert a, chunk c) in B-fragment order: per
+    // group of 64 values one power of two 2^e with max |x| 2^e in [2^14,
+    // 2^15) (found by the 4 lanes that hold the group), fp16 x 2^e (4-bit
+    // odd-MMA slots x 2^(e-4): their codes read as 16 q), and per group the
+    // sum X of x and the factor 2^(24-e) that undoes the scalings
     auto stage_x = [&](int a, int c) -> bool {
       const int lo = act_lo[a], m = act_m[a];
       const int nt = min(mts, m - c * mts);
       const int r0 = lo + c * mts;
       if (!consumer_sync()) return false;  // everyone is done with the staged values
-      // pass 1: max |x| per token, per warp
-      for (int n = 0; n < nt; ++n) {
-        float mx = 0.0f;
-        for (int idx = ctid; idx < ngroups * 4; idx += kSvConsumers * 32) {
-          uint32_t v[16];
-          load16(r0, n, idx >> 2, idx & 3, v);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(bf16_bits_to_f32(v[i])));
-        }
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1)
-          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-        if (lane == 0) wmax[warp * kSvMaxTokens + n] = mx;
-      }
-      if (!consumer_sync()) return false;
-      // pass 2: convert and place
       const int total = ngroups * mts2 * 4;
       for (int base = 0; base < total; base += kSvConsumers * 32) {
         const int idx = base + ctid;
@@ -503,19 +528,27 @@ __global__ void __launch_bounds__(kSvThreads, 1)
         uint32_t v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = 0u;
-        int e = 0;
-        if (valid && n < nt) {
-          load16(r0, n, G, tq, v);
-          e = token_exp(n);
-        }
-        const float sc = __uint_as_float((uint32_t)(127 + e) << 23);
-        const float sc16 = __uint_as_float((uint32_t)(123 + e) << 23);
-        uint32_t h[16], h16[16];
-        float xb = 0.0f;
+        if (valid && n < nt) load16(r0, n, G, tq, v);
+        float mx = 0.0f, xb = 0.0f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float f = bf16_bits_to_f32(v[i]);
+          mx = fmaxf(mx, fabsf(f));
           xb += f;
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+        xb += __shfl_xor_sync(0xFFFFFFFFu, xb, 1);
+        xb += __shfl_xor_sync(0xFFFFFFFFu, xb, 2);
+        const int E = (int)((__float_as_uint(mx) >> 23) & 0xFFu);
+        int e = mx == 0.0f ? 0 : (E == 0 ? 100 : 141 - E);
+        e = e < -100 ? -100 : (e > 100 ? 100 : e);
+        const float sc = __uint_as_float((uint32_t)(127 + e) << 23);
+        const float sc16 = __uint_as_float((uint32_t)(123 + e) << 23);
+        uint32_t h[16], h16[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float f = bf16_bits_to_f32(v[i]);
           h[i] = __half_as_ushort(__float2half_rn(f * sc));
           h16[i] = BITS == 4 ? __half_as_ushort(__float2half_rn(f * sc16)) : 0u;
         }
@@ -538,23 +571,37 @@ __global__ void __launch_bounds__(kSvThreads, 1)
             xs[(((size_t)G * 2 + q) * mts + n) * 4 + tq] =
                 make_uint4(regs[4 * q], regs[4 * q + 1], regs[4 * q + 2], regs[4 * q + 3]);
         }
-        xb += __shfl_xor_sync(0xFFFFFFFFu, xb, 1);
-        xb += __shfl_xor_sync(0xFFFFFFFFu, xb, 2);
-        if (valid && tq == 0) xsum[(size_t)G * mts2 + n] = xb;
+        if (valid && tq == 0)
+          xsum[(size_t)G * mts2 + n] =
+              make_float2(xb, __uint_as_float((uint32_t)(151 - e) << 23));
       }
       if (ctid < kSvMaxTokens) {
         const int n = ctid;
-        const int e = n < nt ? token_exp(n) : 0;
-        st_post[n] = __uint_as_float((uint32_t)(151 - e) << 23);  // 2^(24 - e)
         st_tok[n] = (n < nt && p.act_kind == kSvActX) ? __ldg(p.sorted + r0 + n) / p.kmax : -1;
       }
       if (ctid == 0) st_nt = nt;
       return consumer_sync();
     };
 
+    // per-warp constants of the stage loop: groups jb .. jb + kGpw - 1 of
+    // every stage, their code offsets in a slot, the scale-row offset
+    const int jb = S::kGpw * warp;
+    int coff[S::kGpw];
+#pragma unroll
+    for (int i = 0; i < S::kGpw; ++i) {
+      const int o = (jb + i) * S::kGroupBytes + t * (S::kGroupBytes / 4);
+      coff[i] = (o >> 7) * 1024 + rr * 128 + ((((o >> 4) & 7) ^ rr) << 4) + (o & 15);
+    }
+    const int soff = rr * S::kScaleRow + jb * 2;
+    // B column g of a lane: token g, or a copy of a staged token for the
+    // columns past the chunk (their results are never read)
+    const int bn = ONE ? 0 : min(g, mts - 1);
     SvCursor cu = cursor_at(u0);
     long long tr_full = 0, tr_red = 0, tr_stage = 0, tr_work = 0, tr_n = 0;
     const long long tr_start = SV_CLK();
+#ifdef MOE_SV_TRACE
+    if (tid == 0) SV_ADD(16, tr_start - tr_entry);
+#endif
     for (int u = u0; u < u1 && ok; ++u, cursor_next(cu)) {
       const long long trs = SV_CLK();
       if (cu.a != st_a || cu.c != st_c) {
@@ -587,28 +634,31 @@ __global__ void __launch_bounds__(kSvThreads, 1)
         const long long tr1 = SV_CLK();
         tr_full += tr1 - tr0;
         const unsigned char* cst = codes + (size_t)ring.idx * kSvCodeBytes;
-        const unsigned char* sst = scales + (size_t)ring.idx * S::kScaleBytes;
         const int g0 = ch * S::kGpc;
-        const int gv = min(S::kGpc, ngroups - g0);
+        const int nv = min(S::kGpw, ngroups - g0 - jb);  // this warp's groups in the stage
+        if (nv > 0) {
+          // scales and biases of rows g and g + 8 of the warp's groups, one load each
+          const unsigned char* sp = scales + (size_t)ring.idx * S::kScaleBytes + soff;
+          typename S::ScaleVec sv[4];
 #pragma unroll
-        for (int i = 0; i < S::kGpw; ++i) {
-          const int j = warp + kSvConsumers * i;
-          if (j < gv) {
-            const int G = g0 + j;
+          for (int q = 0; q < 4; ++q)
+            sv[q] = *reinterpret_cast<const typename S::ScaleVec*>(sp + q * 8 * S::kScaleRow);
+          const int G0 = g0 + jb;
+          const uint4* xq = xs + (((size_t)G0 * 2 * mts + bn) * 4 + t);
+          const float2* xsp = xsum + (size_t)G0 * mts2 + (ONE ? 0 : 2 * min(t, (mts2 >> 1) - 1));
+          auto group = [&](int i) {
             // this lane's codes of rows g and g + 8 (128-byte swizzled boxes)
-            const int o = j * S::kGroupBytes + t * (S::kGroupBytes / 4);
-            const int off = (o >> 7) * 1024 + rr * 128 + ((((o >> 4) & 7) ^ rr) << 4) + (o & 15);
             uint32_t a0[S::kLaneWords], a1[S::kLaneWords];
             if constexpr (BITS == 4) {
-              const uint2 v0 = *reinterpret_cast<const uint2*>(cst + off);
-              const uint2 v1 = *reinterpret_cast<const uint2*>(cst + kSvHalfBytes + off);
+              const uint2 v0 = *reinterpret_cast<const uint2*>(cst + coff[i]);
+              const uint2 v1 = *reinterpret_cast<const uint2*>(cst + kSvHalfBytes + coff[i]);
               a0[0] = v0.x;
               a0[1] = v0.y;
               a1[0] = v1.x;
               a1[1] = v1.y;
             } else {
-              const uint4 v0 = *reinterpret_cast<const uint4*>(cst + off);
-              const uint4 v1 = *reinterpret_cast<const uint4*>(cst + kSvHalfBytes + off);
+              const uint4 v0 = *reinterpret_cast<const uint4*>(cst + coff[i]);
+              const uint4 v1 = *reinterpret_cast<const uint4*>(cst + kSvHalfBytes + coff[i]);
               a0[0] = v0.x;
               a0[1] = v0.y;
               a0[2] = v0.z;
@@ -619,63 +669,69 @@ __global__ void __launch_bounds__(kSvThreads, 1)
               a1[3] = v1.w;
             }
             uint4 xb[2];
-            const uint4* xq = xs + ((size_t)G * 2 * mts + g) * 4 + t;
-            const bool has = ONE ? g == 0 : g < mts;
-            xb[0] = has ? xq[0] : make_uint4(0u, 0u, 0u, 0u);
-            xb[1] = has ? xq[(size_t)mts * 4] : make_uint4(0u, 0u, 0u, 0u);
-            float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const uint4* xqi = xq + (size_t)i * 2 * mts * 4;
+            xb[0] = xqi[0];
+            xb[1] = xqi[(size_t)mts * 4];
+            // the words shifted right by 8 bits
+            uint32_t a0h[S::kLaneWords], a1h[S::kLaneWords];
+#pragma unroll
+            for (int w = 0; w < S::kLaneWords; ++w) {
+              a0h[w] = a0[w] >> 8;
+              a1h[w] = a1[w] >> 8;
+            }
+            float d[4];
 #pragma unroll
             for (int mm = 0; mm < 4; ++mm) {
               uint32_t af[4];
               if constexpr (BITS == 4) {
                 // fp16 subnormal pairs: (q_m, q_{m+4}) 2^-24, odd m as 16 q
                 const uint32_t mask = (mm & 1) ? 0x00F000F0u : 0x000F000Fu;
-                const int sh = (mm >> 1) * 8;
-                af[0] = (a0[0] >> sh) & mask;
-                af[1] = (a1[0] >> sh) & mask;
-                af[2] = (a0[1] >> sh) & mask;
-                af[3] = (a1[1] >> sh) & mask;
+                af[0] = (mm >= 2 ? a0h[0] : a0[0]) & mask;
+                af[1] = (mm >= 2 ? a1h[0] : a1[0]) & mask;
+                af[2] = (mm >= 2 ? a0h[1] : a0[1]) & mask;
+                af[3] = (mm >= 2 ? a1h[1] : a1[1]) & mask;
               } else {
                 // 8-bit: bytes (c_r, c_{r+2}) of words 2p, 2p + 1
-                const int pp = mm >> 1, sh = (mm & 1) * 8;
-                af[0] = (a0[2 * pp] >> sh) & 0x00FF00FFu;
-                af[1] = (a1[2 * pp] >> sh) & 0x00FF00FFu;
-                af[2] = (a0[2 * pp + 1] >> sh) & 0x00FF00FFu;
-                af[3] = (a1[2 * pp + 1] >> sh) & 0x00FF00FFu;
+                const int pp = mm >> 1;
+                af[0] = ((mm & 1) ? a0h[2 * pp] : a0[2 * pp]) & 0x00FF00FFu;
+                af[1] = ((mm & 1) ? a1h[2 * pp] : a1[2 * pp]) & 0x00FF00FFu;
+                af[2] = ((mm & 1) ? a0h[2 * pp + 1] : a0[2 * pp + 1]) & 0x00FF00FFu;
+                af[3] = ((mm & 1) ? a1h[2 * pp + 1] : a1[2 * pp + 1]) & 0x00FF00FFu;
               }
               const uint4 bq = xb[mm >> 1];
-              if (mm & 1)
-                mma_sv(d, af, bq.z, bq.w);
+              const uint32_t b0 = (mm & 1) ? bq.z : bq.x, b1 = (mm & 1) ? bq.w : bq.y;
+              if (mm == 0)
+                mma_sv0(d, af, b0, b1);
               else
-                mma_sv(d, af, bq.x, bq.y);
+                mma_sv(d, af, b0, b1);
             }
-            const unsigned char* srow0 = sst + rr * S::kScaleRow + j * 2;
-            const float s0 = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(srow0));
-            const float s1 =
-                f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(srow0 + 8 * S::kScaleRow));
-            const float b0 =
-                f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(srow0 + 16 * S::kScaleRow));
-            const float b1 =
-                f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(srow0 + 24 * S::kScaleRow));
+            const float s0 = sv_half(sv[0], i), s1 = sv_half(sv[1], i);
+            const float b0 = sv_half(sv[2], i), b1 = sv_half(sv[3], i);
             if (ONE) {
-              const float X = xsum[(size_t)G * mts2];
-              as[0] = fmaf(s0, d[0], as[0]);
-              as[2] = fmaf(s1, d[2], as[2]);
-              ab[0] = fmaf(b0, X, ab[0]);
-              ab[2] = fmaf(b1, X, ab[2]);
-            } else {
-              const float2 X =
-                  reinterpret_cast<const float2*>(xsum)[(size_t)G * (mts2 >> 1) +
-                                                        min(t, (mts2 >> 1) - 1)];
-              as[0] = fmaf(s0, d[0], as[0]);
-              as[1] = fmaf(s0, d[1], as[1]);
-              as[2] = fmaf(s1, d[2], as[2]);
-              as[3] = fmaf(s1, d[3], as[3]);
+              const float2 X = xsp[(size_t)i * mts2];  // (sum x, 2^(24-e))
+              as[0] = fmaf(s0 * X.y, d[0], as[0]);
+              as[2] = fmaf(s1 * X.y, d[2], as[2]);
               ab[0] = fmaf(b0, X.x, ab[0]);
-              ab[1] = fmaf(b0, X.y, ab[1]);
               ab[2] = fmaf(b1, X.x, ab[2]);
-              ab[3] = fmaf(b1, X.y, ab[3]);
+            } else {
+              const float4 X = *reinterpret_cast<const float4*>(xsp + (size_t)i * mts2);
+              as[0] = fmaf(s0 * X.y, d[0], as[0]);
+              as[1] = fmaf(s0 * X.w, d[1], as[1]);
+              as[2] = fmaf(s1 * X.y, d[2], as[2]);
+              as[3] = fmaf(s1 * X.w, d[3], as[3]);
+              ab[0] = fmaf(b0, X.x, ab[0]);
+              ab[1] = fmaf(b0, X.z, ab[1]);
+              ab[2] = fmaf(b1, X.x, ab[2]);
+              ab[3] = fmaf(b1, X.z, ab[3]);
             }
+          };
+          if (nv == S::kGpw) {
+#pragma unroll
+            for (int i = 0; i < S::kGpw; ++i) group(i);
+          } else {
+#pragma unroll
+            for (int i = 0; i < S::kGpw; ++i)
+              if (i < nv) group(i);
           }
         }
         __syncwarp();
@@ -695,18 +751,16 @@ __global__ void __launch_bounds__(kSvThreads, 1)
       float* rd = red + ((size_t)rs.idx * kSvConsumers + warp) * mts * 16;
       const int n0 = 2 * t, n1 = 2 * t + 1;
       if (n0 < mts) {
-        const float post = st_post[n0];
-        rd[n0 * 16 + rr] = fmaf(as[0], post, ab[0]);
-        rd[n0 * 16 + 8 + rr] = fmaf(as[2], post, ab[2]);
+        rd[n0 * 16 + rr] = as[0] + ab[0];
+        rd[n0 * 16 + 8 + rr] = as[2] + ab[2];
       }
       if (!ONE && n1 < mts) {
-        const float post = st_post[n1];
-        rd[n1 * 16 + rr] = fmaf(as[1], post, ab[1]);
-        rd[n1 * 16 + 8 + rr] = fmaf(as[3], post, ab[3]);
+        rd[n1 * 16 + rr] = as[1] + ab[1];
+        rd[n1 * 16 + 8 + rr] = as[3] + ab[3];
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&red_full[rs.idx]);
-      rs.next(kSvRedSlots);
+      rs.next(rslots);
     }
     if (lane == 0) {
       SV_ADD(3, tr_full);
@@ -733,7 +787,7 @@ __global__ void __launch_bounds__(kSvThreads, 1)
         break;
       }
       const long long tr0 = SV_CLK();
-      const bool got = mbar_wait_sleep(&red_full[rs.idx], rs.phase, kWaitBudgetCycles);
+      const bool got = mbar_wait(&red_full[rs.idx], rs.phase, kWaitBudgetCycles);
       if (!__all_sync(0xFFFFFFFFu, got)) {
         ok = false;
         break;
@@ -743,42 +797,42 @@ __global__ void __launch_bounds__(kSvThreads, 1)
       const int nt = min(mts, m - cu.c * mts);
       const int64_t row0 = (int64_t)act_lo[cu.a] + (int64_t)cu.c * mts;
       const float* rd = red + (size_t)rs.idx * kSvConsumers * mts * 16;
-      if (MODE == kSvSwiglu) {
-        for (int q = lane; q < nt * 8; q += 32) {
-          const int n = q >> 3, i = q & 7;
-          const int col = cu.rt * 8 + i;
-          float gs = 0.0f, us = 0.0f;
+      // lane l: tile row l & 15, consumer warps 8 (l >> 4) .. + 7 in order,
+      // then the two halves added
+      const int ri = lane & 15, wh = (lane >> 4) * 8;
+      for (int n = 0; n < nt; ++n) {
+        float v = 0.0f;
 #pragma unroll
-          for (int w = 0; w < kSvConsumers; ++w) {
-            gs += rd[((size_t)w * mts + n) * 16 + i];
-            us += rd[((size_t)w * mts + n) * 16 + 8 + i];
-          }
-          if (col < p.n_out) {
-            const float hv = swiglu_f32(gs, us);
+        for (int w = 0; w < 8; ++w) v += rd[((size_t)(wh + w) * mts + n) * 16 + ri];
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
+        if (MODE == kSvSwiglu) {
+          const float up = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 8);
+          const int col = cu.rt * 8 + lane;
+          if (lane < 8 && col < p.n_out) {
+            const float hv = swiglu_f32(v, up);
             const int64_t oi = (row0 + n) * p.n_out + col;
             if (p.out_dtype == MOE_DTYPE_BF16)
               static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16_rne(hv);
             else
               static_cast<float*>(p.out)[oi] = hv;
           }
-        }
-      } else {
-        for (int q = lane; q < nt * 16; q += 32) {
-          const int n = q >> 4, i = q & 15;
-          const int col = cu.rt * 16 + i;
-          float s = 0.0f;
-#pragma unroll
-          for (int w = 0; w < kSvConsumers; ++w) s += rd[((size_t)w * mts + n) * 16 + i];
-          if (col < p.n_rows) static_cast<float*>(p.out)[(row0 + n) * p.n_out + col] = s;
+        } else {
+          const int col = cu.rt * 16 + lane;
+          if (lane < 16 && col < p.n_rows)
+            static_cast<float*>(p.out)[(row0 + n) * p.n_out + col] = v;
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&red_empty[rs.idx]);
-      rs.next(kSvRedSlots);
+      rs.next(rslots);
     }
     if (lane == 0) {
       SV_ADD(7, tr_wait);
       SV_ADD(8, SV_CLK() - tr_start);
+#ifdef MOE_SV_TRACE
+      SV_ADD(17, SV_CLK() - tr_entry);
+      atomicMax(&g_sv_span[1], sv_gtime());
+#endif
     }
     if (!ok && lane == 0) {
       raise_device_error(p.err, MOE_DEVERR_TIMEOUT);

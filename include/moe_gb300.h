@@ -217,6 +217,24 @@ moe_status_t moe_permute(const int32_t* topk_ids, const int32_t* k_dev, int T, i
                          int32_t* sorted_assign, int32_t* inv_pos, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * moe_route -- moe_router_topk followed by moe_permute, as one call.
+ *
+ * The two calls above in sequence (their passages), with their arguments and
+ * outputs.  When one cluster of the router covers the batch (T <= 32 tokens
+ * for E <= 256), E <= 256 and T*kmax <= 512, the router's leader CTA sorts
+ * the assignments itself once the batch's k is known: one launch instead of
+ * two, the same outputs bit for bit.  Otherwise the two kernels are launched
+ * one after the other.  Argument errors of either call return
+ * MOE_ERR_INVALID_ARG before anything is launched.
+ * ---------------------------------------------------------------------- */
+moe_status_t moe_route(const uint16_t* x, const float* w_router, const float* logit_bias,
+                       float inv_temperature, int T, int H, int E, int k_fixed, int kmax,
+                       float thr1, float thr2, int renormalize, int32_t* topk_ids, float* topk_w,
+                       int32_t* k_dev, float* mean_entropy, void* workspace,
+                       size_t workspace_bytes, int32_t* expert_counts, int32_t* expert_offsets,
+                       int32_t* sorted_assign, int32_t* inv_pos, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * moe_permute_rows -- the token rows in expert order.
  *
  * Page [C], 如何验证正确性 (the sorted branch: token rows are gathered into

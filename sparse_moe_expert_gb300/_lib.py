@@ -20,7 +20,7 @@ SCALE_F16, SCALE_BF16, SCALE_F32 = 0, 1, 2
 # every symbol the header declares
 EXPORTS = (
     "moe_status_string", "moe_abi_version", "moe_pack_gate_up", "moe_router_workspace_size",
-    "moe_router_topk", "moe_router_topk_noalloc", "moe_permute", "moe_permute_rows", "moe_gate_up_qmm", "moe_down_qmm", "moe_combine",
+    "moe_router_topk", "moe_router_topk_noalloc", "moe_route", "moe_permute", "moe_permute_rows", "moe_gate_up_qmm", "moe_down_qmm", "moe_combine",
     "moe_swiglu", "moe_get_device_error",
 )
 
@@ -59,6 +59,8 @@ def _declare(lib):
                                     vp, vp, vp, vp, sz, vp]
     lib.moe_router_topk_noalloc.argtypes = [vp, vp, vp, f32, i32, i32, i32, i32, i32, f32, f32,
                                             i32, vp, vp, vp, vp, vp]
+    lib.moe_route.argtypes = [vp, vp, vp, f32, i32, i32, i32, i32, i32, f32, f32, i32, vp, vp, vp,
+                              vp, vp, sz, vp, vp, vp, vp, vp]
     lib.moe_permute.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
     lib.moe_permute_rows.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
     lib.moe_gate_up_qmm.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i32, i32,
@@ -68,7 +70,7 @@ def _declare(lib):
     lib.moe_combine.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp]
     lib.moe_swiglu.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp]
     lib.moe_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32, vp]
-    for name in ("moe_pack_gate_up", "moe_router_topk", "moe_router_topk_noalloc",
+    for name in ("moe_pack_gate_up", "moe_router_topk", "moe_router_topk_noalloc", "moe_route",
                  "moe_permute", "moe_permute_rows", "moe_gate_up_qmm",
                  "moe_down_qmm", "moe_combine", "moe_swiglu", "moe_get_device_error"):
         getattr(lib, name).restype = i32

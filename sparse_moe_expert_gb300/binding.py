@@ -100,6 +100,24 @@ def moe_router_topk(x, w_router, logit_bias=None, inv_temperature: float = 1.0, 
     return topk_ids, topk_w, k_dev, mean_entropy
 
 
+def moe_route(x, w_router, logit_bias, inv_temperature: float, k_fixed: int, kmax: int,
+              thr1: float, thr2: float, renormalize: bool, topk_ids, topk_w, k_dev, mean_entropy,
+              workspace, expert_counts, expert_offsets, sorted_assign, inv_pos, stream=None):
+    """moe_router_topk then moe_permute in one call (one launch for small
+    batches); every output buffer is given."""
+    _need(x, torch.bfloat16, "x")
+    _need(w_router, torch.float32, "w_router")
+    T, H = x.shape
+    E = w_router.shape[0]
+    st = lib().moe_route(_p(x), _p(w_router), _p(logit_bias), ctypes.c_float(inv_temperature),
+                         T, H, E, k_fixed, kmax, ctypes.c_float(thr1), ctypes.c_float(thr2),
+                         int(renormalize), _p(topk_ids), _p(topk_w), _p(k_dev), _p(mean_entropy),
+                         _p(workspace), workspace.numel(), _p(expert_counts), _p(expert_offsets),
+                         _p(sorted_assign), _p(inv_pos), _stream(stream))
+    check("moe_route", st)
+    return topk_ids, topk_w, k_dev, mean_entropy, expert_counts, expert_offsets, sorted_assign, inv_pos
+
+
 def moe_permute(topk_ids, k_dev, E: int, expert_counts=None, expert_offsets=None,
                 sorted_assign=None, inv_pos=None, stream=None):
     """-> (expert_counts [E], expert_offsets [E+1], sorted_assign [T*kmax], inv_pos [T*kmax])"""

@@ -15,6 +15,10 @@
 //   combined by an xor butterfly (16, 8, 4, 2, 1).  A warp computes a tile
 //   of 8 tokens x 4 experts at once (one token x one expert for groups of
 //   fewer than 8 tokens), each (token, expert) value in that same order.
+//   Small groups (the cluster's router-weight slice and token rows fit in
+//   shared memory, e.g. decode): each CTA first brings them in with bulk
+//   copies (one round trip to memory instead of one per 8-element chunk) and
+//   runs the same chains from shared memory.
 //   Phase B (leader CTA): one warp per token: max, softmax sums, entropy,
 //   top-kmax by repeated warp argmax (ties to the lower id), weights.
 // Kernel 2 (router_finalize_kernel, or inline when one cluster covers the
@@ -24,6 +28,7 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include "async.cuh"
 #include "common.cuh"
 
 namespace moe {
@@ -37,6 +42,8 @@ constexpr int kMaxExperts = 1024;
 // Tokens per cluster: the leader holds [tokens][E] fp32 logits.
 __host__ __device__ constexpr int router_group_tokens(int E) { return E <= 256 ? 32 : 16; }
 constexpr int kFinalizeThreads = 256;
+// Shared memory a CTA may stage for the small-batch path.
+constexpr size_t kRouterStageBytes = 200 * 1024;
 
 struct RouterParams {
   const uint16_t* x;
@@ -46,12 +53,19 @@ struct RouterParams {
   int T, H, E, k_fixed, kmax;
   float thr1, thr2;
   int renorm;
+  int smem_stage;  // bulk-copy the weight slice and token rows to shared memory
   int32_t* ids;
   float* topw;
   int32_t* k_dev;
   float* mean_ent;
   float* ws_ent;  // [T] per-token entropy
   float* ws_sum;  // [T] softmax denominator over all experts
+  // fused permute (one cluster covers the batch): outputs of moe_permute, or
+  // null when a separate permute follows
+  int32_t* pm_counts;
+  int32_t* pm_offsets;
+  int32_t* pm_sorted;
+  int32_t* pm_inv_pos;
   unsigned int* err;
 };
 
@@ -116,6 +130,73 @@ __device__ void finalize_batch(const RouterParams& p) {
   }
 }
 
+// The stable counting sort of moe_permute, run by the leader CTA once the
+// batch's k is known (T * kmax <= blockDim, E <= 256).  Same result: for each
+// expert, its assignments a = t * kmax + j (j < k) in ascending a.  `sm`
+// holds at least (warps + 1) * E ints.
+__device__ void fused_permute(const RouterParams& p, int* sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int E = p.E, slots = p.T * p.kmax;
+  const int k = *p.k_dev;
+  int* wh = sm;                 // [warp][E]: counts, then exclusive prefixes over warps
+  int* off = wh + nwarps * E;   // [E]: totals, then offsets
+  for (int i = tid; i < nwarps * E; i += blockDim.x) wh[i] = 0;
+  __syncthreads();
+  const int a = tid;
+  int e = -1;
+  if (a < slots && a % p.kmax < k) {
+    const int v = p.ids[a];
+    if (v >= 0 && v < E) e = v;
+    else raise_device_error(p.err, MOE_DEVERR_BAD_EXPERT);
+  }
+  const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+  const int rank = __popc(peers & lanemask_lt());
+  if (e >= 0 && rank == 0) wh[warp * E + e] = __popc(peers);
+  __syncthreads();
+  for (int x = tid; x < E; x += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < nwarps; ++w) {
+      const int c = wh[w * E + x];
+      wh[w * E + x] = run;
+      run += c;
+    }
+    off[x] = run;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int carry = 0;
+    for (int x0 = 0; x0 < E; x0 += 32) {
+      const int x = x0 + lane;
+      const int v = x < E ? off[x] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (x < E) {
+        const int excl = carry + incl - v;
+        off[x] = excl;
+        p.pm_counts[x] = v;
+        p.pm_offsets[x] = excl;
+      }
+      carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (lane == 0) p.pm_offsets[E] = carry;
+  }
+  __syncthreads();
+  if (a < slots) {
+    if (e >= 0) {
+      const int pos = off[e] + wh[warp * E + e] + rank;
+      p.pm_sorted[pos] = a;
+      p.pm_inv_pos[a] = pos;
+    } else {
+      p.pm_inv_pos[a] = -1;
+    }
+  }
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -144,15 +225,15 @@ struct RouterChunk {
   float4 wa[TN], wb[TN];
 };
 
-template <int TM, int TN>
+template <int TM, int TN, bool SMEM>
 __device__ __forceinline__ void load_chunk(RouterChunk<TM, TN>& d, const uint4* const (&xr)[TM],
                                            const float4* const (&wr)[TN], int c) {
 #pragma unroll
-  for (int m = 0; m < TM; ++m) d.x[m] = __ldg(xr[m] + c);
+  for (int m = 0; m < TM; ++m) d.x[m] = SMEM ? xr[m][c] : __ldg(xr[m] + c);
 #pragma unroll
   for (int n = 0; n < TN; ++n) {
-    d.wa[n] = __ldg(wr[n] + 2 * c);
-    d.wb[n] = __ldg(wr[n] + 2 * c + 1);
+    d.wa[n] = SMEM ? wr[n][2 * c] : __ldg(wr[n] + 2 * c);
+    d.wb[n] = SMEM ? wr[n][2 * c + 1] : __ldg(wr[n] + 2 * c + 1);
   }
 }
 
@@ -182,10 +263,12 @@ __device__ __forceinline__ void fma_chunk(float (&acc)[TM][TN], const RouterChun
 
 // Logits of tokens [t0, t0+nt) x experts [e_lo, e_lo+ne) in warp tiles of
 // TM tokens x TN experts, stored (after bias and temperature) into the
-// leader's [token][E] array at cluster address `lead`.
-template <int TM, int TN>
+// leader's [token][E] array at cluster address `lead`.  SMEM: the token rows
+// and weight rows are xs = x[t0 ..] and ws = w[e_lo ..] in shared memory.
+template <int TM, int TN, bool SMEM>
 __device__ __forceinline__ void router_logit_tiles(const RouterParams& p, int t0, int nt, int e_lo,
-                                                   int ne, uint32_t lead) {
+                                                   int ne, uint32_t lead, const uint16_t* xs,
+                                                   const float* ws) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int H = p.H, E = p.E;
   const int nchunks = H >> 3;
@@ -196,10 +279,14 @@ __device__ __forceinline__ void router_logit_tiles(const RouterParams& p, int t0
     const float4* wr[TN];
 #pragma unroll
     for (int m = 0; m < TM; ++m)
-      xr[m] = reinterpret_cast<const uint4*>(p.x + (int64_t)(t0 + min(tm * TM + m, nt - 1)) * H);
+      xr[m] = reinterpret_cast<const uint4*>(
+          SMEM ? xs + (int64_t)min(tm * TM + m, nt - 1) * H
+               : p.x + (int64_t)(t0 + min(tm * TM + m, nt - 1)) * H);
 #pragma unroll
     for (int n = 0; n < TN; ++n)
-      wr[n] = reinterpret_cast<const float4*>(p.w + (int64_t)(e_lo + min(tn * TN + n, ne - 1)) * H);
+      wr[n] = reinterpret_cast<const float4*>(
+          SMEM ? ws + (int64_t)min(tn * TN + n, ne - 1) * H
+               : p.w + (int64_t)(e_lo + min(tn * TN + n, ne - 1)) * H);
     float acc[TM][TN];
 #pragma unroll
     for (int m = 0; m < TM; ++m)
@@ -209,7 +296,7 @@ __device__ __forceinline__ void router_logit_tiles(const RouterParams& p, int t0
 #pragma unroll(TM * TN == 1 ? 4 : 1)
     for (int c = lane; c < nchunks; c += 32) {
       RouterChunk<TM, TN> b;
-      load_chunk(b, xr, wr, c);
+      load_chunk<TM, TN, SMEM>(b, xr, wr, c);
       fma_chunk(acc, b);
     }
     // every lane ends with the butterfly total; lane m*TN+n stores (m, n)
@@ -234,7 +321,8 @@ __device__ __forceinline__ void router_logit_tiles(const RouterParams& p, int t0
 
 __global__ void __cluster_dims__(kRouterCluster, 1, 1) __launch_bounds__(kRouterThreads)
     router_topk_kernel(RouterParams p) {
-  extern __shared__ float logits_s[];  // leader: [group tokens][E]
+  extern __shared__ __align__(16) float logits_s[];  // leader: [group tokens][E]
+  __shared__ __align__(8) uint64_t stage_bar;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int E = p.E;
   const int tpc = router_group_tokens(E);
@@ -245,11 +333,41 @@ __global__ void __cluster_dims__(kRouterCluster, 1, 1) __launch_bounds__(kRouter
   const int ne = ((int)rank + 1) * E / kRouterCluster - e_lo;
 
   // ---- Phase A: logits (every CTA of the cluster, into the leader) -------
+  // staged copies of the weight slice and token rows sit after the logits
+  float* ws_s = logits_s + tpc * E;
+  uint16_t* xs_s = reinterpret_cast<uint16_t*>(ws_s + (size_t)((E + kRouterCluster - 1) /
+                                                              kRouterCluster) * p.H);
+  bool staged_ok = true;
+  if (p.smem_stage) {
+    if (threadIdx.x == 0) {
+      mbar_init(&stage_bar, 1);
+      fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && ne > 0) {
+      const uint32_t wbytes = (uint32_t)ne * p.H * 4u, xbytes = (uint32_t)nt * p.H * 2u;
+      mbar_arrive_expect_tx(&stage_bar, wbytes + xbytes);
+      // one copy per weight row, one for the token rows
+      for (int e = 0; e < ne; ++e)
+        bulk_g2s(ws_s + (size_t)e * p.H, p.w + (int64_t)(e_lo + e) * p.H, (uint32_t)p.H * 4u,
+                 &stage_bar);
+      bulk_g2s(xs_s, p.x + (int64_t)t0 * p.H, xbytes, &stage_bar);
+    }
+  }
   cluster_sync();  // the leader's shared memory is live before remote stores
   const uint32_t lead = cluster_map(logits_s, 0);
-  if (ne > 0) {
-    if (nt >= 8) router_logit_tiles<8, 4>(p, t0, nt, e_lo, ne, lead);
-    else router_logit_tiles<1, 1>(p, t0, nt, e_lo, ne, lead);
+  if (p.smem_stage && ne > 0) {
+    staged_ok = mbar_wait(&stage_bar, 0, kWaitBudgetCycles);
+    if (!staged_ok && threadIdx.x == 0) raise_device_error(p.err, MOE_DEVERR_TIMEOUT);
+  }
+  if (ne > 0 && staged_ok) {
+    if (p.smem_stage) {
+      if (nt >= 8) router_logit_tiles<8, 4, true>(p, t0, nt, e_lo, ne, lead, xs_s, ws_s);
+      else router_logit_tiles<1, 1, true>(p, t0, nt, e_lo, ne, lead, xs_s, ws_s);
+    } else {
+      if (nt >= 8) router_logit_tiles<8, 4, false>(p, t0, nt, e_lo, ne, lead, nullptr, nullptr);
+      else router_logit_tiles<1, 1, false>(p, t0, nt, e_lo, ne, lead, nullptr, nullptr);
+    }
   }
   cluster_sync();  // all logits of the group are in the leader
   if (rank != 0) return;
@@ -329,6 +447,10 @@ __global__ void __cluster_dims__(kRouterCluster, 1, 1) __launch_bounds__(kRouter
   if (gridDim.x == kRouterCluster) {
     __syncthreads();
     finalize_batch(p);
+    if (p.pm_sorted) {
+      __syncthreads();
+      fused_permute(p, reinterpret_cast<int*>(logits_s));  // the logits are no longer needed
+    }
   }
 }
 
@@ -343,13 +465,22 @@ moe_status_t launch_router(const RouterParams& p, cudaStream_t st) {
   const int tpc = router_group_tokens(p.E);
   const int ngroups = (p.T + tpc - 1) / tpc;
   if (ngroups > 0) {
-    const size_t smem = (size_t)tpc * p.E * sizeof(float);
-    if (smem > 48 * 1024) {
+    size_t smem = (size_t)tpc * p.E * sizeof(float);
+    // small batches: the per-CTA weight slice and the token rows in shared memory
+    const int ne_max = (p.E + kRouterCluster - 1) / kRouterCluster;
+    const int nt_max = p.T < tpc ? p.T : tpc;
+    const size_t staged = smem + (size_t)ne_max * p.H * 4 + (size_t)nt_max * p.H * 2;
+    RouterParams q = p;
+    q.smem_stage = (ngroups == 1 && staged <= kRouterStageBytes) ? 1 : 0;
+    if (q.smem_stage) smem = staged;
+    static size_t set_max = 48 * 1024;
+    if (smem > set_max) {
       if (cudaFuncSetAttribute(router_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem) != cudaSuccess)
         return MOE_ERR_CUDA;
+      set_max = smem;
     }
-    router_topk_kernel<<<ngroups * kRouterCluster, kRouterThreads, smem, st>>>(p);
+    router_topk_kernel<<<ngroups * kRouterCluster, kRouterThreads, smem, st>>>(q);
     if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
   }
   if (ngroups != 1) {
@@ -370,13 +501,14 @@ extern "C" size_t moe_router_workspace_size(int T) {
   return 2 * per + 256;
 }
 
-extern "C" moe_status_t moe_router_topk(const uint16_t* x, const float* w_router,
-                                        const float* logit_bias, float inv_temperature, int T,
-                                        int H, int E, int k_fixed, int kmax, float thr1,
-                                        float thr2, int renormalize, int32_t* topk_ids,
-                                        float* topk_w, int32_t* k_dev, float* mean_entropy,
-                                        void* workspace, size_t workspace_bytes,
-                                        moe_stream_t stream) {
+namespace {
+
+// Validates the router arguments and fills the kernel parameters.
+moe_status_t router_params(const uint16_t* x, const float* w_router, const float* logit_bias,
+                           float inv_temperature, int T, int H, int E, int k_fixed, int kmax,
+                           float thr1, float thr2, int renormalize, int32_t* topk_ids,
+                           float* topk_w, int32_t* k_dev, float* mean_entropy, void* workspace,
+                           size_t workspace_bytes, RouterParams* out) {
   using namespace moe_host;
   if (T < 0 || H <= 0 || H % 64 != 0 || E < 1 || E > kMaxExperts || kmax < 1 || kmax > 16)
     return MOE_ERR_INVALID_ARG;
@@ -391,7 +523,7 @@ extern "C" moe_status_t moe_router_topk(const uint16_t* x, const float* w_router
     return MOE_ERR_INVALID_ARG;
   if (logit_bias && (reinterpret_cast<uintptr_t>(logit_bias) & 3u)) return MOE_ERR_INVALID_ARG;
 
-  RouterParams p;
+  RouterParams p{};
   p.x = x;
   p.w = w_router;
   p.bias = logit_bias;
@@ -404,6 +536,7 @@ extern "C" moe_status_t moe_router_topk(const uint16_t* x, const float* w_router
   p.thr1 = thr1;
   p.thr2 = thr2;
   p.renorm = renormalize ? 1 : 0;
+  p.smem_stage = 0;
   p.ids = topk_ids;
   p.topw = topk_w;
   p.k_dev = k_dev;
@@ -411,10 +544,58 @@ extern "C" moe_status_t moe_router_topk(const uint16_t* x, const float* w_router
   size_t per = ((size_t)T * sizeof(float) + 255) / 256 * 256;
   p.ws_ent = reinterpret_cast<float*>(workspace);
   p.ws_sum = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + per);
+  p.pm_counts = p.pm_offsets = p.pm_sorted = p.pm_inv_pos = nullptr;
   p.err = device_error_word();
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  *out = p;
+  return MOE_OK;
+}
 
-  return launch_router(p, st);
+}  // namespace
+
+extern "C" moe_status_t moe_router_topk(const uint16_t* x, const float* w_router,
+                                        const float* logit_bias, float inv_temperature, int T,
+                                        int H, int E, int k_fixed, int kmax, float thr1,
+                                        float thr2, int renormalize, int32_t* topk_ids,
+                                        float* topk_w, int32_t* k_dev, float* mean_entropy,
+                                        void* workspace, size_t workspace_bytes,
+                                        moe_stream_t stream) {
+  RouterParams p{};
+  const moe_status_t s = router_params(x, w_router, logit_bias, inv_temperature, T, H, E, k_fixed,
+                                       kmax, thr1, thr2, renormalize, topk_ids, topk_w, k_dev,
+                                       mean_entropy, workspace, workspace_bytes, &p);
+  if (s != MOE_OK) return s;
+  return launch_router(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" moe_status_t moe_route(const uint16_t* x, const float* w_router,
+                                  const float* logit_bias, float inv_temperature, int T, int H,
+                                  int E, int k_fixed, int kmax, float thr1, float thr2,
+                                  int renormalize, int32_t* topk_ids, float* topk_w,
+                                  int32_t* k_dev, float* mean_entropy, void* workspace,
+                                  size_t workspace_bytes, int32_t* expert_counts,
+                                  int32_t* expert_offsets, int32_t* sorted_assign,
+                                  int32_t* inv_pos, moe_stream_t stream) {
+  RouterParams p{};
+  moe_status_t s = router_params(x, w_router, logit_bias, inv_temperature, T, H, E, k_fixed,
+                                 kmax, thr1, thr2, renormalize, topk_ids, topk_w, k_dev,
+                                 mean_entropy, workspace, workspace_bytes, &p);
+  if (s != MOE_OK) return s;
+  if (!expert_counts || !expert_offsets) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!sorted_assign || !inv_pos)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // one launch when one cluster covers the batch and its leader can sort it
+  const int tpc = router_group_tokens(E);
+  if (T > 0 && T <= tpc && E <= 256 && T * kmax <= kRouterThreads) {
+    p.pm_counts = expert_counts;
+    p.pm_offsets = expert_offsets;
+    p.pm_sorted = sorted_assign;
+    p.pm_inv_pos = inv_pos;
+    return launch_router(p, st);
+  }
+  s = launch_router(p, st);
+  if (s != MOE_OK) return s;
+  return moe_permute(topk_ids, k_dev, T, kmax, E, expert_counts, expert_offsets, sorted_assign,
+                     inv_pos, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -490,7 +671,7 @@ extern "C" moe_status_t moe_router_topk_noalloc(const uint16_t* x, const float* 
   const moe_status_t sst = noalloc_scratch(&scratch);
   if (sst != MOE_OK) return sst;
 
-  RouterParams p;
+  RouterParams p{};
   p.x = x;
   p.w = w_router;
   p.bias = logit_bias;
@@ -503,6 +684,7 @@ extern "C" moe_status_t moe_router_topk_noalloc(const uint16_t* x, const float* 
   p.thr1 = thr1;
   p.thr2 = thr2;
   p.renorm = renormalize ? 1 : 0;
+  p.smem_stage = 0;
   p.ids = topk_ids;
   p.topw = topk_w;
   p.k_dev = k_dev;

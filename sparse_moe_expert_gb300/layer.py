@@ -121,12 +121,14 @@ class MoELayer:
     def launches_per_call(self, T: int) -> int:
         """Kernels one forward of T tokens launches: the router (plus its
         batch finalize when the tokens span more than one token group of 32,
-        16 when E > 256), the permute, the row permute on the tensor-core
-        path, the gate_up product (or two RAW products and the activation
-        when unfused), down and combine."""
+        16 when E > 256), the permute (inside the router when one group
+        covers the batch, E <= 256 and T * kmax <= 512), the row permute on
+        the tensor-core path, the gate_up product (or two RAW products and
+        the activation when unfused), down and combine."""
         group = 32 if self.E <= 256 else 16
-        n = 1 + (0 if (T + group - 1) // group == 1 else 1)
-        n += 1
+        one_group = (T + group - 1) // group == 1
+        n = 1 + (0 if one_group else 1)
+        n += 0 if (one_group and self.E <= 256 and T * self.kmax <= 512) else 1
         n += 1 if self.resolved_path(T) == PATH_TC else 0
         n += 1 if self.fused else 3
         return n + 2
@@ -170,14 +172,12 @@ class MoELayer:
         b = self.buffers(T)
         path = self.resolved_path(T)
         it = self.inv_temperature if inv_temperature is None else float(inv_temperature)
-        ev = _Timer(events, "router")
-        B.moe_router_topk(x, self.router_w, self.logit_bias, it, self.k_fixed, self.kmax,
-                          self.thr[0], self.thr[1], self.renormalize, b["topk_ids"], b["topk_w"],
-                          b["k_dev"], b["mean_entropy"], b["ws"])
-        ev.stop()
-        ev = _Timer(events, "permute")
-        B.moe_permute(b["topk_ids"], b["k_dev"], self.E, b["counts"], b["offsets"], b["sorted"],
-                      b["inv_pos"])
+        # router, top-k and the expert grouping (one launch for small batches)
+        ev = _Timer(events, "route")
+        B.moe_route(x, self.router_w, self.logit_bias, it, self.k_fixed, self.kmax, self.thr[0],
+                    self.thr[1], self.renormalize, b["topk_ids"], b["topk_w"], b["k_dev"],
+                    b["mean_entropy"], b["ws"], b["counts"], b["offsets"], b["sorted"],
+                    b["inv_pos"])
         ev.stop()
         # tensor cores: token rows copied once into expert order, so every
         # tile loads contiguous rows; the GEMV reads x through sorted_assign

@@ -95,6 +95,47 @@ def test_router_empty_batch(cuda_lib):
     assert int(kd.item()) == 1 and float(me.item()) == 0.0
 
 
+@pytest.mark.parametrize("E,k,kmax,T,H", [
+    (64, 4, 4, 1, 4096),      # single-token decode: staged weights, sort in the router
+    (8, 0, 3, 21, 192),       # adaptive k, sorted after the batch's k is chosen
+    (16, 16, 16, 32, 256),    # 512 slots: the largest batch sorted in the router
+    (64, 4, 4, 33, 256),      # two token groups: router, then the permute kernel
+    (300, 2, 2, 5, 128),      # E > 256: router, then the permute kernel
+])
+def test_route_is_router_then_permute(cuda_lib, E, k, kmax, T, H):
+    """moe_route (router with the expert grouping fused in when one cluster
+    covers the batch) gives the oracle's routing and grouping bit for bit."""
+    rng = np.random.default_rng(E + T + H)
+    rw = rng.normal(0, 0.05, (E, H)).astype(np.float32)
+    x_bits = workloads.normal_bf16(3, 5, (T, H), 1.0)
+    ref = oracle.route(x_bits, rw, None, 1.0, k, kmax, True)
+    pref = oracle.permute(ref.ids, ref.k, E)
+    d = dev()
+    x = cuda_lib.bf16_from_bits(x_bits, d)
+    w = torch.from_numpy(rw).to(d)
+    ids = torch.empty((T, kmax), dtype=torch.int32, device=d)
+    tw = torch.empty((T, kmax), dtype=torch.float32, device=d)
+    kd = torch.empty(1, dtype=torch.int32, device=d)
+    me = torch.empty(1, dtype=torch.float32, device=d)
+    ws = torch.empty(cuda_lib.moe_router_workspace_size(T), dtype=torch.uint8, device=d)
+    cnt = torch.empty(E, dtype=torch.int32, device=d)
+    off = torch.empty(E + 1, dtype=torch.int32, device=d)
+    srt = torch.full((T * kmax,), -7, dtype=torch.int32, device=d)
+    inv = torch.empty(T * kmax, dtype=torch.int32, device=d)
+    cuda_lib.moe_route(x, w, None, 1.0, k, kmax, 1.2, 2.5, True, ids, tw, kd, me, ws, cnt, off,
+                       srt, inv)
+    torch.cuda.synchronize()
+    assert int(kd.item()) == ref.k
+    assert np.array_equal(to_np(ids), ref.ids)
+    assert np.allclose(to_np(tw), ref.weights, rtol=1e-6, atol=1e-7)
+    assert np.array_equal(to_np(cnt), pref.counts)
+    assert np.array_equal(to_np(off), pref.offsets)
+    A = T * ref.k
+    assert np.array_equal(to_np(srt)[:A], pref.sorted_assign)
+    assert np.array_equal(to_np(inv), pref.inv_pos)
+    assert cuda_lib.moe_get_device_error() == 0
+
+
 # ----------------------------------------------------------------- permute
 
 @pytest.mark.parametrize("T,kmax,k,E,skew", [(1, 4, 4, 64, False), (64, 4, 4, 64, True),

@@ -41,7 +41,12 @@ import workloads  # noqa: E402
 MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-GEMV_SRC = os.path.join(ROOT, "sparse_moe_expert_gb300", "csrc", "gemv.cu")
+CSRC = os.path.join(ROOT, "sparse_moe_expert_gb300", "csrc")
+# the products' kernel and its source, by the path the layer resolved to
+# (0 automatic, 1 streamed GEMV, 2 tcgen05 grouped GEMM, 3 tcgen05 small tiles)
+KERNEL_NAME = {1: "gemv_stream_kernel", 2: "tc_qmm_kernel", 3: "tc_small_kernel"}
+KERNEL_SRC = {1: os.path.join(CSRC, "gemv_stream.cu"), 2: os.path.join(CSRC, "gemm_tc.cu"),
+              3: os.path.join(CSRC, "gemm_tc_small.cu")}
 
 
 def parse_args(argv=None):
@@ -244,18 +249,25 @@ def run_ours(args):
     path = {"auto": moe.PATH_AUTO, "gemv": moe.PATH_GEMV, "tc": moe.PATH_TC,
             "tc_small": moe.PATH_TC_SMALL}[args.path]
     layer = moe.MoELayer.from_workload(layer_np, dev, free_sources=True, path=path)
-    calls = cfg.calls
     T = cfg.T
-    starts = shard_calls(calls, rank, world)
-    x_bits = workloads.normal_bf16(0, workloads.STREAM_X, (calls * T, cfg.H), cfg.x_std,
-                                   start=starts[0] * T * cfg.H)
+    # one step = every layer call of the workload: 256 single-token calls for
+    # batch-1 decode, one call per activation batch otherwise (the entropy
+    # workload's three batches, each with its own router temperature, so each
+    # of k = 1, 2, 3 runs once per step)
+    n_batches = cfg.batches
+    calls = cfg.calls * n_batches
+    starts = shard_calls(cfg.calls, rank, world)
+    xb = [workloads.normal_bf16(0, workloads.STREAM_X + b, (cfg.calls * T, cfg.H), cfg.x_std,
+                                start=starts[0] * T * cfg.H) for b in range(n_batches)]
+    x_bits = np.concatenate(xb, axis=0)
     x_dev = moe.bf16_from_bits(x_bits, dev)
     out_dev = torch.empty((calls * T, cfg.H), dtype=torch.bfloat16, device=dev)
+    temps = [cfg.inv_temperature(c // cfg.calls) for c in range(calls)]
 
     def step(events=None):
         for c in range(calls):
             layer.forward(x_dev[c * T:(c + 1) * T], out=out_dev[c * T:(c + 1) * T],
-                          events=events)
+                          inv_temperature=temps[c], events=events)
 
     # eager warm-up (sets kernel attributes), then capture one step in a graph
     step()
@@ -301,34 +313,50 @@ def run_ours(args):
     clocks = clk.summary()
 
     # per-kernel durations: the same calls launched eagerly with CUDA events
-    # around the two products (the graph above is not instrumented)
+    # around each kernel (the graph above is not instrumented).  The first
+    # eager step also records each call's active experts and k.
     ksteps = max(1, min(args.steps, 20))
     events = {}
+    torch.cuda.synchronize()
+    per_call = []
+    for c in range(calls):
+        layer.forward(x_dev[c * T:(c + 1) * T], out=out_dev[c * T:(c + 1) * T],
+                      inv_temperature=temps[c])
+        bufs = layer.buffers(T)
+        per_call.append((int((bufs["counts"] > 0).sum().item()), int(bufs["k_dev"].item())))
     torch.cuda.synchronize()
     for _ in range(ksteps):
         step(events)
     torch.cuda.synchronize()
-    kt = {k: statistics.mean(a.elapsed_time(b) for a, b in v) for k, v in events.items()}
-    n_active = int((layer.buffers(T)["counts"] > 0).sum().item())
-    k_run = int(layer.buffers(T)["k_dev"].item())
+    ktot = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in events.items()}
+    kt = {k: ktot[k] / len(v) for k, v in events.items()}
     peaks, peak_src = load_peaks()
-    gu_bytes = active_bytes_per_expert(cfg, "gate_up") * n_active + T * cfg.H * 2
-    dn_bytes = active_bytes_per_expert(cfg, "down") * n_active
-    gu_gbs = gu_bytes / (kt["gate_up"] * 1e-3) / 1e9
-    dn_gbs = dn_bytes / (kt["down"] * 1e-3) / 1e9
+    # algorithmic bytes of the two products, summed over one step's calls:
+    # the active experts' packed weights (codes + fp16 scale + fp16 bias)
+    # plus the token rows read by gate_up
+    gu_step_bytes = sum(active_bytes_per_expert(cfg, "gate_up") * na + T * cfg.H * 2
+                        for na, _ in per_call)
+    dn_step_bytes = sum(active_bytes_per_expert(cfg, "down") * na for na, _ in per_call)
+    gu_bytes = gu_step_bytes / calls          # per launch (average)
+    dn_bytes = dn_step_bytes / calls
+    gu_gbs = gu_step_bytes * ksteps / (ktot["gate_up"] * 1e-3) / 1e9
+    dn_gbs = dn_step_bytes * ksteps / (ktot["down"] * 1e-3) / 1e9
     # algorithmic FLOPs of the two products (2 * rows * assignments * K)
-    A = T * k_run
-    gu_flops = 2.0 * A * 2 * cfg.I * cfg.H
-    dn_flops = 2.0 * A * cfg.I * cfg.H
-    gu_tflops = gu_flops / (kt["gate_up"] * 1e-3) / 1e12
-    dn_tflops = dn_flops / (kt["down"] * 1e-3) / 1e12
-    tensor_bound = layer.resolved_path(T) == moe.PATH_TC and cfg.name == "prefill"
+    gu_step_flops = sum(2.0 * T * k * 2 * cfg.I * cfg.H for _, k in per_call)
+    dn_step_flops = sum(2.0 * T * k * cfg.I * cfg.H for _, k in per_call)
+    gu_flops = gu_step_flops / calls
+    gu_tflops = gu_step_flops * ksteps / (ktot["gate_up"] * 1e-3) / 1e12
+    dn_tflops = dn_step_flops * ksteps / (ktot["down"] * 1e-3) / 1e12
+    path_used = layer.resolved_path(T)
+    tensor_bound = path_used == moe.PATH_TC and cfg.name == "prefill"
+    kernel_src = KERNEL_SRC[path_used]
     traffic = None
     try:
         with open(TRAFFIC_FILE) as f:
-            tr = json.load(f)
-        if tr.get("gemv_sha") == file_sha(GEMV_SRC) and tr.get("config") == cfg.name:
-            traffic = tr.get("gate_up_dram_bytes_per_launch")
+            for rec in json.load(f).get("records", []):
+                if rec.get("config") == cfg.name and rec.get("src") == os.path.basename(kernel_src) \
+                        and rec.get("src_sha") == file_sha(kernel_src):
+                    traffic = rec.get("gate_up_dram_bytes_per_launch")
     except (OSError, ValueError):
         pass
 
@@ -339,7 +367,8 @@ def run_ours(args):
 
     def e2e_step():
         for c in range(calls):
-            layer.forward_host(x_host[c * T:(c + 1) * T], o_host[c * T:(c + 1) * T])
+            layer.forward_host(x_host[c * T:(c + 1) * T], o_host[c * T:(c + 1) * T],
+                               inv_temperature=temps[c])
     e2e_step()
     torch.cuda.synchronize()
     barrier()
@@ -360,25 +389,26 @@ def run_ours(args):
     line = {
         "metric": metric_name(), "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": f"u{cfg.bits} affine weights x bf16 tokens, f32 accumulate",
         "data": "synthetic", "config": workload_config(cfg),
         "roofline": ({"bound": "tensor", "achieved": gu_tflops, "peak": peaks["bf16_tflops"],
                       "unit": "TFLOP/s", "frac": gu_tflops / peaks["bf16_tflops"],
                       "frac_of_sustained": gu_tflops / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]),
-                      "traffic": traffic, "kernel": "tc_qmm_kernel (gate_up, SiLU*up epilogue)",
+                      "traffic": traffic, "kernel": KERNEL_NAME[path_used] + " (gate_up, SiLU*up epilogue)",
                       "algorithmic_flops_per_launch": gu_flops, "peak_source": peak_src}
                      if tensor_bound else
                      {"bound": "hbm", "achieved": gu_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                       "frac": gu_gbs / peaks["hbm_gbs"], "traffic": traffic,
-                      "kernel": ("tc_qmm_kernel" if layer.resolved_path(T) == moe.PATH_TC
-                                 else "gemv_qmm_kernel") + " (gate_up, SiLU*up epilogue)",
+                      "kernel": KERNEL_NAME[path_used] + " (gate_up, SiLU*up epilogue)",
                       "algorithmic_bytes_per_launch": gu_bytes, "peak_source": peak_src}),
         "kernels": {"gate_up_us": kt["gate_up"] * 1e3, "gate_up_gbs": gu_gbs,
-                    "gate_up_tflops": gu_tflops, "down_tflops": dn_tflops, "k": k_run,
+                    "gate_up_tflops": gu_tflops, "down_tflops": dn_tflops,
                     "down_us": kt["down"] * 1e3, "down_gbs": dn_gbs,
                     "layer_us_per_call": ms * 1e3 / calls,
-                    "layer_gbs": (gu_bytes + dn_bytes) / (ms * 1e-3 / calls) / 1e9,
-                    "active_experts_last_call": n_active,
+                    "layer_gbs": (gu_step_bytes + dn_step_bytes) / (ms * 1e-3) / 1e9,
+                    "layer_tflops": (gu_step_flops + dn_step_flops) / (ms * 1e-3) / 1e12,
+                    "active_experts_and_k_per_call": sorted(set(per_call)),
                     "per_kernel_us": {k: v * 1e3 for k, v in kt.items()}},
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                    "reasons": clocks["reasons"], "samples": clocks["samples"]},

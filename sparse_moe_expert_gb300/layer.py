@@ -212,7 +212,8 @@ class MoELayer:
 
     __call__ = forward
 
-    def forward_host(self, x_host: torch.Tensor, out_host: torch.Tensor) -> torch.Tensor:
+    def forward_host(self, x_host: torch.Tensor, out_host: torch.Tensor,
+                     inv_temperature: Optional[float] = None) -> torch.Tensor:
         """End-to-end call with host buffers: copies x (pinned host, bf16
         [T, H]) to the device, runs the layer and copies the result back into
         out_host, all enqueued on the current stream (no synchronization)."""
@@ -221,7 +222,7 @@ class MoELayer:
         if "x_dev" not in b:
             b["x_dev"] = torch.empty((T, self.H), dtype=torch.bfloat16, device=self.device)
         b["x_dev"].copy_(x_host, non_blocking=True)
-        res = self.forward(b["x_dev"])
+        res = self.forward(b["x_dev"], inv_temperature=inv_temperature)
         out_host.copy_(res, non_blocking=True)
         return out_host
 

@@ -318,6 +318,8 @@ def run_ours(args):
     ksteps = max(1, min(args.steps, 20))
     events = {}
     torch.cuda.synchronize()
+    # each kernel on its own: no overlap with the kernel before it
+    pdl_prev = moe.moe_set_launch_overlap(False)
     per_call = []
     for c in range(calls):
         layer.forward(x_dev[c * T:(c + 1) * T], out=out_dev[c * T:(c + 1) * T],
@@ -328,6 +330,7 @@ def run_ours(args):
     for _ in range(ksteps):
         step(events)
     torch.cuda.synchronize()
+    moe.moe_set_launch_overlap(pdl_prev)
     ktot = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in events.items()}
     kt = {k: ktot[k] / len(v) for k, v in events.items()}
     peaks, peak_src = load_peaks()

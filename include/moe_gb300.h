@@ -72,6 +72,26 @@ enum {
   MOE_PATH_TC = 2,   /* tcgen05 grouped GEMM (TMEM accumulators), many tokens per expert */
   MOE_PATH_TC_SMALL = 3 /* tcgen05 with the codes in tensor memory, up to 16 tokens per tile */
 };
+/* ------------------------------------------------------------------------
+ * moe_set_launch_overlap -- whether later launches of this library may
+ * overlap the end of the previous kernel of their stream (programmatic
+ * dependent launch, on by default; the environment variable MOE_GB300_PDL=0
+ * sets the default off).  Results do not depend on it; per-kernel timings
+ * taken with events between kernels are cleaner with it off.  Returns the
+ * previous setting.  Not synchronized with launches in flight on other
+ * threads.
+ * ---------------------------------------------------------------------- */
+int moe_set_launch_overlap(int enable);
+
+/* Flag OR-ed into the `path` argument of moe_down_qmm.  Kernels of this
+ * library are launched with programmatic stream serialization: a kernel may
+ * start while the previous kernel of the stream finishes, and waits for it
+ * before it reads activations or writes results.  With this flag the down
+ * product also reads expert_offsets and streams its weights before that
+ * wait.  Set it only when the kernel issued just before the call on the
+ * stream writes neither expert_offsets nor the down weights (in the layer
+ * sequence that kernel is the gate_up product). */
+enum { MOE_PATH_FLAG_WEIGHTS_EARLY = 0x100 };
 /* Device error word bits (moe_get_device_error). */
 enum { MOE_DEVERR_BAD_EXPERT = 1u, MOE_DEVERR_TIMEOUT = 2u, MOE_DEVERR_BAD_INDEX = 4u };
 
@@ -298,6 +318,7 @@ moe_status_t moe_gate_up_qmm(const uint16_t* x, const int32_t* sorted_assign,
  *           sorted order (as written by moe_gate_up_qmm).
  * w_q       uint32 [E, H, I*bits/32]; w_s, w_b fp16 [E, H, I/64].
  * y         out: fp32 [T*kmax, H], sorted order; rows >= T*k not written.
+ * path      MOE_PATH_*, optionally | MOE_PATH_FLAG_WEIGHTS_EARLY.
  * ---------------------------------------------------------------------- */
 moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* expert_offsets,
                           const int32_t* k_dev, int T, int kmax, int E, int I, int H,

@@ -13,13 +13,14 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 DTYPE_F32, DTYPE_BF16 = 0, 1
 EPILOGUE_RAW, EPILOGUE_SWIGLU = 0, 1
 PATH_AUTO, PATH_GEMV, PATH_TC, PATH_TC_SMALL = 0, 1, 2, 3
+PATH_FLAG_WEIGHTS_EARLY = 0x100  # moe_down_qmm: offsets/weights read before the wait
 DEVERR_BAD_EXPERT, DEVERR_TIMEOUT, DEVERR_BAD_INDEX = 1, 2, 4
 QMODE_AFFINE = 0
 SCALE_F16, SCALE_BF16, SCALE_F32 = 0, 1, 2
 
 # every symbol the header declares
 EXPORTS = (
-    "moe_status_string", "moe_abi_version", "moe_pack_gate_up", "moe_router_workspace_size",
+    "moe_status_string", "moe_abi_version", "moe_set_launch_overlap", "moe_pack_gate_up", "moe_router_workspace_size",
     "moe_router_topk", "moe_router_topk_noalloc", "moe_route", "moe_permute", "moe_permute_rows", "moe_gate_up_qmm", "moe_down_qmm", "moe_combine",
     "moe_swiglu", "moe_get_device_error",
 )
@@ -51,6 +52,8 @@ def _declare(lib):
     lib.moe_status_string.restype = ctypes.c_char_p
     lib.moe_abi_version.argtypes = []
     lib.moe_abi_version.restype = i32
+    lib.moe_set_launch_overlap.argtypes = [i32]
+    lib.moe_set_launch_overlap.restype = i32
     lib.moe_pack_gate_up.argtypes = [ctypes.POINTER(QDesc), ctypes.POINTER(QDesc), vp, vp, vp, vp,
                                      vp, vp, i32, vp, vp, vp, vp]
     lib.moe_router_workspace_size.argtypes = [i32]

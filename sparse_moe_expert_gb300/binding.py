@@ -41,6 +41,12 @@ def moe_abi_version() -> int:
     return int(lib().moe_abi_version())
 
 
+def moe_set_launch_overlap(enable: bool) -> bool:
+    """Programmatic dependent launch on (default) or off for later launches;
+    returns the previous setting."""
+    return bool(lib().moe_set_launch_overlap(int(bool(enable))))
+
+
 def moe_status_string(status: int) -> str:
     return lib().moe_status_string(status).decode()
 

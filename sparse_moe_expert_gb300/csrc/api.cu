@@ -1,6 +1,8 @@
 // C-ABI entry points of libmoe_gb300 that are not defined next to their
 // kernels: status strings, the two quantized products (path selection and
 // argument checks) and the device error word.
+#include <atomic>
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -9,7 +11,7 @@ namespace moe {
 moe_status_t gemv_qmm(const void* act, int act_kind, const int32_t* sorted,
                       const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
                       bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
-                      int bits, void* out, int out_dtype, cudaStream_t st);
+                      int bits, void* out, int out_dtype, bool early, cudaStream_t st);
 moe_status_t tc_qmm(const void* act, int act_kind, const int32_t* sorted,
                     const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
                     bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
@@ -62,6 +64,22 @@ int sm_count() {
   return c.sm;
 }
 
+// -1 until first use: then the environment variable MOE_GB300_PDL ("0" turns
+// programmatic dependent launch off), or the value moe_set_launch_overlap set.
+std::atomic<int> g_pdl{-1};
+
+bool pdl_enabled() {
+  int v = g_pdl.load(std::memory_order_relaxed);
+  if (v < 0) {
+    const char* e = getenv("MOE_GB300_PDL");
+    v = (e && e[0] == '0') ? 0 : 1;
+    int expected = -1;
+    g_pdl.compare_exchange_strong(expected, v);
+    v = g_pdl.load(std::memory_order_relaxed);
+  }
+  return v != 0;
+}
+
 unsigned int* device_error_word() {
   DeviceCache& c = cache_for_current();
   if (c.err == nullptr) {
@@ -89,6 +107,12 @@ extern "C" const char* moe_status_string(moe_status_t s) {
 }
 
 extern "C" int moe_abi_version(void) { return 1; }
+
+extern "C" int moe_set_launch_overlap(int enable) {
+  const int prev = moe_host::pdl_enabled() ? 1 : 0;
+  moe_host::g_pdl.store(enable ? 1 : 0, std::memory_order_relaxed);
+  return prev;
+}
 
 static int pick_path(int path, int T, int kmax, int E) {
   if (path != MOE_PATH_AUTO) return path;
@@ -139,7 +163,7 @@ extern "C" moe_status_t moe_gate_up_qmm(const uint16_t* x, const int32_t* sorted
     return moe::tc_small_qmm(x, act_kind, sorted_assign, expert_offsets, T, kmax, E, H, n_rows,
                              swiglu, w_q, w_s, w_b, bits, out, out_dtype, st);
   return moe::gemv_qmm(x, act_kind, sorted_assign, expert_offsets, T, kmax, E, H, n_rows, swiglu,
-                       w_q, w_s, w_b, bits, out, out_dtype, st);
+                       w_q, w_s, w_b, bits, out, out_dtype, false, st);
 }
 
 extern "C" moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* expert_offsets,
@@ -152,6 +176,8 @@ extern "C" moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* 
   if (I <= 0 || I % 64 != 0 || H <= 0 || H % 64 != 0) return MOE_ERR_INVALID_ARG;
   if (bits != 4 && bits != 8) return MOE_ERR_UNSUPPORTED;
   if (h_dtype != MOE_DTYPE_F32 && h_dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
+  const bool early = (path & MOE_PATH_FLAG_WEIGHTS_EARLY) != 0;
+  path &= ~MOE_PATH_FLAG_WEIGHTS_EARLY;
   if (path < MOE_PATH_AUTO || path > MOE_PATH_TC_SMALL) return MOE_ERR_INVALID_ARG;
   if (I > 49152) return MOE_ERR_UNSUPPORTED;
   if (!expert_offsets || !k_dev) return MOE_ERR_INVALID_ARG;
@@ -171,7 +197,7 @@ extern "C" moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* 
     return moe::tc_small_qmm(h, act_kind, nullptr, expert_offsets, T, kmax, E, I, H, false, w_q,
                              w_s, w_b, bits, y, MOE_DTYPE_F32, st);
   return moe::gemv_qmm(h, act_kind, nullptr, expert_offsets, T, kmax, E, I, H, false, w_q, w_s,
-                       w_b, bits, y, MOE_DTYPE_F32, st);
+                       w_b, bits, y, MOE_DTYPE_F32, early, st);
 }
 
 extern "C" moe_status_t moe_get_device_error(uint32_t* flags, int clear, moe_stream_t stream) {

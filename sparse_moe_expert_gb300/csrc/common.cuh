@@ -69,6 +69,18 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
 
 __device__ __forceinline__ uint16_t ldg_u16(const uint16_t* p) { return __ldg(p); }
 
+// Programmatic dependent launch.  pdl_wait() returns once the kernel this
+// one was launched behind has finished and its memory is visible (at once
+// when there is no such dependency); every thread waits before it reads
+// what an earlier kernel of the stream wrote or overwrites what one reads.
+// pdl_trigger() lets the next kernel of the stream be scheduled before this
+// one ends; it is called only after this kernel's own pdl_wait(), so a
+// dependent that starts early still sees every kernel before this one done.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ unsigned lanemask_lt() {
   unsigned m;
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
@@ -90,6 +102,34 @@ unsigned int* device_error_word();
 
 inline moe_status_t launch_status() {
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Whether kernels are launched with programmatic stream serialization (the
+// environment variable MOE_GB300_PDL=0 turns it off; read once).
+bool pdl_enabled();
+
+// Launch `kern` on `st`, allowed to start while the previous kernel of the
+// stream finishes (when PDL is enabled); the kernel calls moe::pdl_wait()
+// before it touches data of earlier kernels.
+template <typename... KArgs, typename... Args>
+inline moe_status_t launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                           cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
 }
 
 }  // namespace moe_host

@@ -19,6 +19,8 @@ __global__ void __launch_bounds__(kEwThreads) combine_kernel(const float* __rest
                                                              int T, int kmax, int H,
                                                              uint16_t* __restrict__ out,
                                                              unsigned int* err) {
+  pdl_wait();
+  pdl_trigger();
   const int k = *k_dev;
   const int vec_per_row = H / 4;
   const int64_t total = (int64_t)T * vec_per_row;
@@ -50,6 +52,8 @@ __global__ void __launch_bounds__(kEwThreads) swiglu_kernel(const float* __restr
                                                             const int32_t* __restrict__ k_dev,
                                                             int T, int I, int out_dtype,
                                                             void* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t rows = (int64_t)T * (*k_dev);
   const int64_t total = rows * I;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -99,10 +103,9 @@ extern "C" moe_status_t moe_combine(const float* y, const int32_t* inv_pos, cons
   if (T == 0) return MOE_OK;
   if (!y || !inv_pos || !topk_w || !out || !aligned16(y) || !aligned16(out))
     return MOE_ERR_INVALID_ARG;
-  combine_kernel<<<grid_for((int64_t)T * H / 4), kEwThreads, 0,
-                   reinterpret_cast<cudaStream_t>(stream)>>>(y, inv_pos, topk_w, k_dev, T, kmax,
-                                                             H, out, device_error_word());
-  return launch_status();
+  return launch(combine_kernel, grid_for((int64_t)T * H / 4), kEwThreads, 0,
+                reinterpret_cast<cudaStream_t>(stream), y, inv_pos, topk_w, k_dev, T, kmax, H,
+                out, device_error_word());
 }
 
 extern "C" moe_status_t moe_swiglu(const float* gate, const float* up, const int32_t* k_dev,
@@ -116,10 +119,8 @@ extern "C" moe_status_t moe_swiglu(const float* gate, const float* up, const int
   if (T == 0) return MOE_OK;
   if (!gate || !up || !out || !aligned16(gate) || !aligned16(up) || !aligned16(out))
     return MOE_ERR_INVALID_ARG;
-  swiglu_kernel<<<grid_for((int64_t)T * kmax * I), kEwThreads, 0,
-                  reinterpret_cast<cudaStream_t>(stream)>>>(gate, up, k_dev, T, I, out_dtype,
-                                                            out);
-  return launch_status();
+  return launch(swiglu_kernel, grid_for((int64_t)T * kmax * I), kEwThreads, 0,
+                reinterpret_cast<cudaStream_t>(stream), gate, up, k_dev, T, I, out_dtype, out);
 }
 
 extern "C" moe_status_t moe_pack_gate_up(const moe_qdesc_t* gd, const moe_qdesc_t* ud,

@@ -332,6 +332,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tmem_alloc(&tmem_base_sh, kTmemCols);
     tmem_relinquish();
   }
+  // the set-up above overlaps the end of the previous kernel of the stream
+  pdl_wait();
+  pdl_trigger();
   if (tid == 0) {
     int n = 0, t = 0;
     for (int e = 0; e < p.E; ++e) {
@@ -840,8 +843,7 @@ moe_status_t launch_tc(const CUtensorMap& tma, TcParams p, int64_t max_tiles, cu
   const int64_t sms = moe_host::sm_count();
   const int grid = (int)(max_tiles < sms ? max_tiles : sms);
   if (grid <= 0) return MOE_OK;
-  kern<<<grid, kTcThreads, smem, st>>>(tma, p);
-  return moe_host::launch_status();
+  return moe_host::launch(kern, grid, kTcThreads, smem, st, tma, p);
 }
 
 }  // namespace

@@ -444,7 +444,7 @@ bool gemv_stream_supported(int bits, int K, int E);
 moe_status_t gemv_stream_qmm(const void* act, int act_kind, const int32_t* sorted,
                              const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
                              bool swiglu, const uint32_t* wq, const uint16_t* ws,
-                             const uint16_t* wb, int bits, void* out, int out_dtype,
+                             const uint16_t* wb, int bits, void* out, int out_dtype, bool early,
                              cudaStream_t st);
 moe_status_t gemv_mma_qmm(const void* act, int act_kind, const int32_t* sorted,
                           const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
@@ -458,10 +458,10 @@ moe_status_t gemv_mma_qmm(const void* act, int act_kind, const int32_t* sorted,
 moe_status_t gemv_qmm(const void* act, int act_kind, const int32_t* sorted,
                       const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
                       bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
-                      int bits, void* out, int out_dtype, cudaStream_t st) {
+                      int bits, void* out, int out_dtype, bool early, cudaStream_t st) {
   if (gemv_stream_supported(bits, K, E))
     return gemv_stream_qmm(act, act_kind, sorted, offsets, T, kmax, E, K, n_rows, swiglu, wq, ws,
-                           wb, bits, out, out_dtype, st);
+                           wb, bits, out, out_dtype, early, st);
   if (gemv_mma_supported(act_kind, K, bits, T))
     return gemv_mma_qmm(act, act_kind, sorted, offsets, T, kmax, E, K, n_rows, swiglu, wq, ws, wb,
                         out, out_dtype, st);

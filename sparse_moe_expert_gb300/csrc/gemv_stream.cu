@@ -121,6 +121,8 @@ struct SvParams {
   int stages;    // ring slots
   int rt;        // row tiles per (expert, token chunk)
   int scale_cw;  // cp.async width for scales and biases: 4, 8 or 16 bytes
+  int early;     // offsets and weights final before the previous kernel ends:
+                 // stream them before waiting on it (activations after)
   unsigned int* err;
 };
 
@@ -297,6 +299,11 @@ __global__ void __launch_bounds__(kSvThreads, 1)
     fence_barrier_init();
   }
   __syncthreads();
+  // the previous kernel of the stream: waited for here unless the offsets and
+  // weights may be read while it finishes (then each role waits before it
+  // reads activations or writes results, and every thread waits before exit)
+  if (!p.early) pdl_wait();
+  pdl_trigger();
 
   // active experts in id order, with segment start and length
   for (int base = 0; base < p.E; base += kSvThreads) {
@@ -347,7 +354,10 @@ __global__ void __launch_bounds__(kSvThreads, 1)
   const int n_tiles = act_base[n_act];
   const int u0 = (int)((int64_t)n_tiles * blockIdx.x / gridDim.x);
   const int u1 = (int)((int64_t)n_tiles * (blockIdx.x + 1) / gridDim.x);
-  if (u0 >= u1) return;
+  if (u0 >= u1) {
+    pdl_wait();
+    return;
+  }
 
   auto cursor_at = [&](int u) {
     int lo = 0, hi = n_act - 1;  // last a with act_base[a] <= u
@@ -438,6 +448,7 @@ __global__ void __launch_bounds__(kSvThreads, 1)
       }
     }
     if (!codes_warp) cp_async_wait_all_sv();
+    pdl_wait();
     if (lane == 0) {
       SV_ADD(codes_warp ? 0 : 13, tr_wait);
       SV_ADD(codes_warp ? 1 : 14, issued);
@@ -459,6 +470,7 @@ __global__ void __launch_bounds__(kSvThreads, 1)
     }
   } else if (warp < kSvConsumers) {
     // ================================ consumers ===============================
+    pdl_wait();
     const int g = lane >> 2, t = lane & 3;
     // shared-memory row of MMA row g (rows 0,4 | 2,6 | 1,5 | 3,7 per quarter
     // warp keep the swizzled code reads free of bank conflicts)
@@ -776,6 +788,7 @@ __global__ void __launch_bounds__(kSvThreads, 1)
     }
   } else if (warp == kSvEpilogue) {
     // ================================ epilogue ================================
+    pdl_wait();
     SvRing rs{0, 0u};
     bool ok = true;
     SvCursor cu = cursor_at(u0);
@@ -852,8 +865,7 @@ moe_status_t launch_stream_kernel(const CUtensorMap& tm, const SvParams& p, int 
       return MOE_ERR_CUDA;
     set_max = smem;
   }
-  kern<<<moe_host::sm_count(), kSvThreads, smem, st>>>(tm, p);
-  return moe_host::launch_status();
+  return moe_host::launch(kern, moe_host::sm_count(), kSvThreads, smem, st, tm, p);
 }
 
 template <int BITS, int MODE>
@@ -897,7 +909,7 @@ bool gemv_stream_supported(int bits, int K, int E) {
 moe_status_t gemv_stream_qmm(const void* act, int act_kind, const int32_t* sorted,
                              const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
                              bool swiglu, const uint32_t* wq, const uint16_t* ws,
-                             const uint16_t* wb, int bits, void* out, int out_dtype,
+                             const uint16_t* wb, int bits, void* out, int out_dtype, bool early,
                              cudaStream_t st) {
   if (!gemv_stream_supported(bits, K, E)) return MOE_ERR_UNSUPPORTED;
   if (!moe_host::aligned16(act) || !moe_host::aligned16(wq)) return MOE_ERR_INVALID_ARG;
@@ -929,6 +941,7 @@ moe_status_t gemv_stream_qmm(const void* act, int act_kind, const int32_t* sorte
   p.scale_cw = (ngroups % 8 == 0 && (sa & 15u) == 0) ? 16
                : (ngroups % 4 == 0 && (sa & 7u) == 0) ? 8
                                                       : 4;
+  p.early = early ? 1 : 0;
   p.err = moe_host::device_error_word();
   // tile count bound (int32 positions)
   const int64_t max_tiles = (int64_t)p.rt * (A + E);

@@ -38,6 +38,8 @@ struct PermuteParams {
 
 __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(PermuteParams p, int per_block) {
   extern __shared__ int smem_i[];
+  pdl_wait();
+  pdl_trigger();
   const int E = p.E;
   int* cnt = smem_i;              // [E]
   int* off = cnt + E;             // [E]
@@ -201,9 +203,8 @@ extern "C" moe_status_t moe_permute(const int32_t* topk_ids, const int32_t* k_de
   const int nb0 = chunks < 64 ? chunks : 64;
   const int per_block = (chunks + nb0 - 1) / nb0 * kPermuteThreads;
   const int nb = slots > 0 ? (slots + per_block - 1) / per_block : 1;
-  permute_kernel<<<nb, kPermuteThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
-      p, per_block);
-  return launch_status();
+  return launch(permute_kernel, nb, kPermuteThreads, smem, reinterpret_cast<cudaStream_t>(stream),
+                p, per_block);
 }
 
 // ---- token rows in expert order ------------------------------------------
@@ -220,6 +221,8 @@ __global__ void __launch_bounds__(kRowsThreads) permute_rows_kernel(
     const uint4* __restrict__ x, const int32_t* __restrict__ sorted,
     const int32_t* __restrict__ k_dev, int T, int kmax, int vec_per_row,
     uint4* __restrict__ out, unsigned int* err) {
+  moe::pdl_wait();
+  moe::pdl_trigger();
   const int k = min(max(*k_dev, 0), kmax);
   const int64_t rows = (int64_t)T * k;
   const int lane = threadIdx.x & 31;
@@ -267,9 +270,8 @@ extern "C" moe_status_t moe_permute_rows(const uint16_t* x, const int32_t* sorte
   int64_t grid = (rows + warps_per_block - 1) / warps_per_block;
   const int64_t cap = (int64_t)sm_count() * 8;
   if (grid > cap) grid = cap;
-  moe::permute_rows_kernel<<<(int)grid, moe::kRowsThreads, 0,
-                             reinterpret_cast<cudaStream_t>(stream)>>>(
-      reinterpret_cast<const uint4*>(x), sorted_assign, k_dev, T, kmax, H / 8,
-      reinterpret_cast<uint4*>(x_sorted), device_error_word());
-  return launch_status();
+  return launch(moe::permute_rows_kernel, (int)grid, moe::kRowsThreads, 0,
+                reinterpret_cast<cudaStream_t>(stream), reinterpret_cast<const uint4*>(x),
+                sorted_assign, k_dev, T, kmax, H / 8, reinterpret_cast<uint4*>(x_sorted),
+                device_error_word());
 }

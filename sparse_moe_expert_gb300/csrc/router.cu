@@ -347,13 +347,17 @@ __global__ void __cluster_dims__(kRouterCluster, 1, 1) __launch_bounds__(kRouter
     if (threadIdx.x == 0 && ne > 0) {
       const uint32_t wbytes = (uint32_t)ne * p.H * 4u, xbytes = (uint32_t)nt * p.H * 2u;
       mbar_arrive_expect_tx(&stage_bar, wbytes + xbytes);
-      // one copy per weight row, one for the token rows
+      // one copy per weight row (no kernel of this library writes router
+      // weights, so they are read before the wait on the previous kernel)
       for (int e = 0; e < ne; ++e)
         bulk_g2s(ws_s + (size_t)e * p.H, p.w + (int64_t)(e_lo + e) * p.H, (uint32_t)p.H * 4u,
                  &stage_bar);
-      bulk_g2s(xs_s, p.x + (int64_t)t0 * p.H, xbytes, &stage_bar);
     }
   }
+  pdl_wait();
+  pdl_trigger();
+  if (p.smem_stage && threadIdx.x == 0 && ne > 0)
+    bulk_g2s(xs_s, p.x + (int64_t)t0 * p.H, (uint32_t)nt * p.H * 2u, &stage_bar);  // token rows
   cluster_sync();  // the leader's shared memory is live before remote stores
   const uint32_t lead = cluster_map(logits_s, 0);
   if (p.smem_stage && ne > 0) {
@@ -455,6 +459,8 @@ __global__ void __cluster_dims__(kRouterCluster, 1, 1) __launch_bounds__(kRouter
 }
 
 __global__ void __launch_bounds__(kFinalizeThreads) router_finalize_kernel(RouterParams p) {
+  pdl_wait();
+  pdl_trigger();
   finalize_batch(p);
 }
 
@@ -480,12 +486,13 @@ moe_status_t launch_router(const RouterParams& p, cudaStream_t st) {
         return MOE_ERR_CUDA;
       set_max = smem;
     }
-    router_topk_kernel<<<ngroups * kRouterCluster, kRouterThreads, smem, st>>>(q);
-    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    if (launch(router_topk_kernel, ngroups * kRouterCluster, kRouterThreads, smem, st, q) !=
+        MOE_OK)
+      return MOE_ERR_CUDA;
   }
   if (ngroups != 1) {
-    router_finalize_kernel<<<1, kFinalizeThreads, 0, st>>>(p);
-    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    if (launch(router_finalize_kernel, 1, kFinalizeThreads, 0, st, p) != MOE_OK)
+      return MOE_ERR_CUDA;
   }
   return MOE_OK;
 }

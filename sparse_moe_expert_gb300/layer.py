@@ -15,7 +15,8 @@ import numpy as np
 import torch
 
 from . import binding as B
-from ._lib import EPILOGUE_RAW, EPILOGUE_SWIGLU, PATH_AUTO, PATH_GEMV, PATH_TC, PATH_TC_SMALL, MoEError
+from ._lib import (EPILOGUE_RAW, EPILOGUE_SWIGLU, PATH_AUTO, PATH_FLAG_WEIGHTS_EARLY, PATH_GEMV,
+                   PATH_TC, PATH_TC_SMALL, MoEError)
 
 FUSE_ENV = "MOE_GB300_FUSE_GATE_UP"
 TC_MIN_TOKENS_PER_EXPERT = 24  # mirrors the library's automatic path choice
@@ -201,8 +202,10 @@ class MoELayer:
         ev.stop()
         d = self.down
         ev = _Timer(events, "down")
+        # the kernel just before this one (gate_up or the activation) writes
+        # only h: the down weights may stream while it finishes
         B.moe_down_qmm(b["h"], b["offsets"], b["k_dev"], T, self.kmax, d.q, d.s, d.b, self.bits,
-                       b["y"], path)
+                       b["y"], path | PATH_FLAG_WEIGHTS_EARLY)
         ev.stop()
         res = out if out is not None else b["out"]
         ev = _Timer(events, "combine")

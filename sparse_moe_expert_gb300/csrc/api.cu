@@ -114,11 +114,14 @@ extern "C" int moe_set_launch_overlap(int enable) {
   return prev;
 }
 
-static int pick_path(int path, int T, int kmax, int E) {
+// The tensor-core path also needs rows of at least 128 code bytes (K * bits / 8).
+static int pick_path(int path, int T, int kmax, int E, int K, int bits) {
   if (path != MOE_PATH_AUTO) return path;
   const int64_t per_expert = (int64_t)T * kmax / E;
-  return (per_expert >= kTcMinTokensPerExpert && moe::tc_available()) ? MOE_PATH_TC
-                                                                      : MOE_PATH_GEMV;
+  return (per_expert >= kTcMinTokensPerExpert && (int64_t)K * bits / 8 >= 128 &&
+          moe::tc_available())
+             ? MOE_PATH_TC
+             : MOE_PATH_GEMV;
 }
 
 static bool common_shape_ok(int T, int kmax, int E) {
@@ -153,7 +156,7 @@ extern "C" moe_status_t moe_gate_up_qmm(const uint16_t* x, const int32_t* sorted
   const int act_kind = sorted_assign ? 0 : 2;
   const bool swiglu = epilogue == MOE_EPILOGUE_SWIGLU;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int p = pick_path(path, T, kmax, E);
+  const int p = pick_path(path, T, kmax, E, H, bits);
   if (p == MOE_PATH_TC) {
     if (!moe::tc_available()) return MOE_ERR_UNSUPPORTED;
     return moe::tc_qmm(x, act_kind, sorted_assign, expert_offsets, T, kmax, E, H, n_rows, swiglu,
@@ -187,7 +190,7 @@ extern "C" moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* 
     if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
   const int act_kind = h_dtype == MOE_DTYPE_F32 ? 1 : 2;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int p = pick_path(path, T, kmax, E);
+  const int p = pick_path(path, T, kmax, E, I, bits);
   if (p == MOE_PATH_TC) {
     if (!moe::tc_available()) return MOE_ERR_UNSUPPORTED;
     return moe::tc_qmm(h, act_kind, nullptr, expert_offsets, T, kmax, E, I, H, false, w_q, w_s,

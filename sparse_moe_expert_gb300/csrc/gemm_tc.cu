@@ -27,12 +27,16 @@
 //               gathers (tile::gather4) of the token rows of x, or 64-row 2D
 //               boxes of rows already in sorted order (h, or x permuted),
 //               128-byte swizzled as the MMA expects; all 32 lanes issue;
-//   warps 6-13  dequant: each thread streams its row slice of packed codes
-//               and the row's scale and bias straight from global memory
-//               into registers, several k-blocks ahead (covering HBM
-//               latency without shared memory), then w = s*q + b in fp32
-//               (packed FMA), rounds to bf16, writes the A tile in the
-//               128-byte-swizzled K-major layout, proxy fence, arrive;
+//   warp 14     codes: TMA-loads the packed codes of the tile's 128 rows,
+//               128 bytes of each row per slot (4 k-blocks of 4-bit codes,
+//               2 of 8-bit), two 64-row boxes with the 128-byte swizzle,
+//               into a ring of 16 KB slots; bulk copies keep far more bytes
+//               in flight than per-thread loads of 16-64 bytes per row could;
+//   warps 6-13  dequant: each thread reads its row slice of the codes from
+//               the slot and loads the row's scale and bias into registers
+//               a few A stages ahead, then w = s*q + b in fp32 (packed FMA),
+//               rounds to bf16, writes the A tile in the 128-byte-swizzled
+//               K-major layout, proxy fence, arrive;
 //   warp 4      MMA: one thread issues tcgen05.mma (kind::f16, bf16 x bf16 ->
 //               fp32) per 16-wide K slice, commits stage release and
 //               accumulator completion to mbarriers;
@@ -71,15 +75,19 @@ constexpr int BK = 64;         // contraction per stage = one scale group = one 
 constexpr int kHalfRows = 64;  // SWIGLU: gate rows, then up rows, per A tile
 constexpr int kBoxRows = 64;   // rows per 2D TMA box (codes and token rows)
 constexpr int kEpiWarps = 4, kMmaWarp = 4, kLoadWarp = 5, kDeqWarp0 = 6, kDeqWarps = 8;
-constexpr int kTcThreads = (kDeqWarp0 + kDeqWarps) * 32;  // 448
+constexpr int kCodeWarp = kDeqWarp0 + kDeqWarps;           // 14
+constexpr int kTcThreads = (kCodeWarp + 1) * 32;           // 480
 constexpr int kATileBytes = BM * BK * 2;                  // 16 KB bf16 weight tile
 constexpr int kKbPerA = 2;                                // k-blocks per A stage
 constexpr int kAStageBytes = kKbPerA * kATileBytes;       // 32 KB
-constexpr int kBTileBytes = BN * BK * 2;                  // 32 KB bf16 token tile
+constexpr int kBRowBytes = BK * 2;                         // one token row of a k-block
+constexpr int kCodeRowBytes = 128;                         // code bytes of a row per code slot
+constexpr int kCodeSlotBytes = BM * kCodeRowBytes;         // 16 KB
+constexpr int kMaxCodeSlots = 8;
 constexpr int kMaxStages = 8;
 constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators of up to 256 columns
-// A stages of codes, scale and bias in flight per dequant thread
-__host__ __device__ constexpr int dequant_lookahead(int bits) { return bits == 4 ? 3 : 2; }
+// A stages of scales and biases in flight per dequant thread (registers)
+constexpr int kScaleLookahead = 4;
 
 enum TcMode { kTcSwiglu = 0, kTcRaw = 1 };
 enum TcAct { kTcGatherX = 0, kTcRowsH = 1 };
@@ -95,6 +103,8 @@ struct TcParams {
   int kmax, E, K, n_rows, n_out;
   int a_stages;  // ring of dequantized weight stages (kKbPerA k-blocks each)
   int b_stages;  // ring of TMA-loaded token tiles (one k-block each)
+  int c_stages;  // ring of TMA-loaded code slots (kCodeRowBytes of each row)
+  int bn_cap;    // most tokens per tile (a multiple of 16, at most BN)
   int n_mt;         // m-tiles per expert
   unsigned int* err;
 };
@@ -237,7 +247,7 @@ struct TileInfo {
   int nmma;  // MMA N: nv rounded up to 16
 };
 
-__device__ __forceinline__ int ntiles_of(int m) { return (m + BN - 1) / BN; }
+__device__ __forceinline__ int ntiles_of(int m, int cap) { return (m + cap - 1) / cap; }
 
 // tile_start[a] = first tile of active expert a (exclusive prefix), n_act entries + 1.
 __device__ __forceinline__ TileInfo tile_info(const TcParams& p, const int* act_e,
@@ -252,8 +262,8 @@ __device__ __forceinline__ TileInfo tile_info(const TcParams& p, const int* act_
   ti.e = act_e[lo];
   ti.seg_lo = __ldg(p.offsets + ti.e);
   const int m = __ldg(p.offsets + ti.e + 1) - ti.seg_lo;
-  const int nnt = ntiles_of(m);
-  const int tsz = (((m + nnt - 1) / nnt) + 15) & ~15;  // <= 256, and (nnt-1)*tsz < m
+  const int nnt = ntiles_of(m, p.bn_cap);
+  const int tsz = (((m + nnt - 1) / nnt) + 15) & ~15;  // <= bn_cap, and (nnt-1)*tsz < m
   const int local = t - tile_start[lo];
   ti.mt = local / nnt;
   const int nt = local - ti.mt * nnt;
@@ -275,14 +285,18 @@ __device__ __forceinline__ int tile_weight_row(const TcParams& p, int mt, int r)
 // for one CTA per SM.
 template <int BITS, int MODE, int ACT>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    tc_qmm_kernel(const __grid_constant__ CUtensorMap tm_act, TcParams p) {
+    tc_qmm_kernel(const __grid_constant__ CUtensorMap tm_act,
+                  const __grid_constant__ CUtensorMap tm_codes, TcParams p) {
   // dequant work split: 2 threads per A row, 32 codes of each k-block each
   constexpr int DQ_SLICES = kDeqWarps * 32 / BM;  // 2
   constexpr int DQ_CHUNKS = 8 / DQ_SLICES;        // 16-byte bf16 chunks per thread per k-block: 4
   constexpr int KB_WORDS = BK * BITS / 32;         // code words of one row per k-block
-  constexpr int QV = KB_WORDS / DQ_SLICES / 4;     // 16-byte code loads per thread per k-block
-  constexpr int PD = dequant_lookahead(BITS);      // A stages of codes in flight
+  constexpr int QV = KB_WORDS / DQ_SLICES / 4;     // 16-byte code pieces per thread per k-block
+  constexpr int KB_BYTES = BK * BITS / 8;          // code bytes of a row per k-block: 32 | 64
+  constexpr int KPC = kCodeRowBytes / KB_BYTES;    // k-blocks per code slot: 4 | 2
+  constexpr int PD = kScaleLookahead;              // A stages of scales in flight
   static_assert(DQ_CHUNKS == 4, "dequant split assumes four output chunks per thread");
+  static_assert(KPC % kKbPerA == 0, "a code slot holds whole A stages");
 
   extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
   unsigned char* smem =
@@ -294,6 +308,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // b_empty is committed by the MMAs.
   __shared__ uint64_t a_full[kMaxStages], a_empty[kMaxStages];
   __shared__ uint64_t b_full[kMaxStages], b_empty[kMaxStages];
+  __shared__ uint64_t c_full[kMaxCodeSlots], c_empty[kMaxCodeSlots];
   __shared__ uint64_t tmem_full[2], tmem_empty[2];
   __shared__ uint64_t xfull[2][2][2];  // SWIGLU exchange: [pair][buffer][writer half]
   __shared__ uint64_t drain_bar;
@@ -305,7 +320,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ volatile int abort_flag;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int SA = p.a_stages, SB = p.b_stages;
+  const int SA = p.a_stages, SB = p.b_stages, SC = p.c_stages;
   const int nkb = p.K / BK;
   const int nas = (nkb + kKbPerA - 1) / kKbPerA;  // A stages per tile
 
@@ -319,6 +334,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int s = 0; s < SB; ++s) {
       mbar_init(&b_full[s], 1);
       mbar_init(&b_empty[s], 1);
+    }
+    for (int s = 0; s < SC; ++s) {
+      mbar_init(&c_full[s], 1);
+      mbar_init(&c_empty[s], kDeqWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tmem_full[b], 1);
@@ -342,7 +361,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (m > 0) {
         act_e[n] = e;
         tile_start[n] = t;
-        t += p.n_mt * ntiles_of(m);
+        t += p.n_mt * ntiles_of(m, p.bn_cap);
         ++n;
       }
     }
@@ -356,11 +375,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int n_act = n_act_sh;
   const int n_tiles = n_act > 0 ? tile_start[n_act] : 0;
 
+  const int b_tile_bytes = p.bn_cap * kBRowBytes;
   unsigned char* a_base = smem;                                     // SA * kAStageBytes
-  unsigned char* b_base = smem + (size_t)SA * kAStageBytes;         // SB * kBTileBytes
+  unsigned char* c_base = smem + (size_t)SA * kAStageBytes;         // SC * kCodeSlotBytes
+  unsigned char* b_base = c_base + (size_t)SC * kCodeSlotBytes;     // SB * b_tile_bytes
   // k-block h of A stage s: a 128 x 64 K-major SW128 tile
   auto stage_a = [&](int s, int h) { return a_base + (size_t)s * kAStageBytes + h * kATileBytes; };
-  auto stage_b = [&](int s) { return b_base + (size_t)s * kBTileBytes; };
+  auto stage_b = [&](int s) { return b_base + (size_t)s * b_tile_bytes; };
+  auto stage_c = [&](int s) { return c_base + (size_t)s * kCodeSlotBytes; };
 
   if (warp == kLoadWarp) {
     // =============================== loader ===============================
@@ -429,6 +451,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_wait(&b_full[r.idx], r.phase, kWaitBudgetCycles);
       }
     }
+  } else if (warp == kCodeWarp) {
+    // ============================== code loader ==============================
+    // per tile: ceil(nkb / KPC) slots, each the next kCodeRowBytes of the
+    // tile's 128 rows (A rows 0-63 and 64-127 as two 64-row boxes; rows past
+    // the matrix come back zero, rows of the next expert are never stored)
+    int64_t issued = 0;
+    Ring ring;  // code ring
+    bool ok = true;
+    const int nslot = (nkb + KPC - 1) / KPC;
+    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+      const TileInfo ti = tile_info(p, act_e, tile_start, n_act, t);
+      const int r0 = tile_weight_row<MODE>(p, ti.mt, 0);
+      const int r1 = tile_weight_row<MODE>(p, ti.mt, kHalfRows);
+      const int g0 = ti.e * p.n_rows;  // E * n_rows < 2^31 (checked on the host)
+      for (int c = 0; c < nslot; ++c) {
+        const int sc = ring.idx;
+        if (!warp_wait(&c_empty[sc], ring.phase ^ 1u, &abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&c_full[sc], (uint32_t)kCodeSlotBytes);
+          tma_load_2d(stage_c(sc), &tm_codes, c * kCodeRowBytes, g0 + r0, &c_full[sc]);
+          tma_load_2d(stage_c(sc) + kHalfRows * kCodeRowBytes, &tm_codes, c * kCodeRowBytes,
+                      g0 + r1, &c_full[sc]);
+        }
+        __syncwarp();
+        ++issued;
+        ring.next(SC);
+      }
+    }
+    if (!ok && lane == 0) {
+      raise_device_error(p.err, MOE_DEVERR_TIMEOUT);
+      abort_flag = 1;
+      // the last min(issued, SC) slots may still have copies in flight
+      Ring r = ring;
+      for (int64_t j = 0; j < issued && j < SC; ++j) {
+        r.idx = r.idx == 0 ? SC - 1 : r.idx - 1;
+        if (r.idx == SC - 1) r.phase ^= 1u;
+        mbar_wait(&c_full[r.idx], r.phase, kWaitBudgetCycles);
+      }
+    }
   } else if (warp >= kDeqWarp0) {
     // =============================== dequant ===============================
     const int dt = tid - kDeqWarp0 * 32;
@@ -436,30 +500,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int slice = dt % DQ_SLICES;
     const int c0 = slice * DQ_CHUNKS;              // first 16-byte bf16 chunk of this thread
     const int ngroups = p.K / 64;
-    const int64_t row_words = (int64_t)p.K * BITS / 32;
     // this CTA's A stages in order, (its tiles) x (A stages of the tile); the
-    // codes, scales and biases of A stage st + PD are loaded while stage st
-    // is converted
+    // scales and biases of A stage st + PD are loaded while stage st is
+    // converted; the codes come from the code ring
     const int my_tiles = blockIdx.x < n_tiles ? (n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     const int nst = my_tiles * nas;  // < 2^31: tiles and k-blocks are bounded by int sizes
     struct Ahead {
-      uint4 q[kKbPerA][QV];   // this thread's code words of each k-block
       uint32_t sb[kKbPerA];   // scale | bias << 16 of each k-block
       int nkb;                // k-blocks in the stage (the last of a tile may have fewer)
     };
     int la_t = blockIdx.x, la_kb = 0;
     const uint16_t* la_sp = nullptr;
     const uint16_t* la_bp = nullptr;
-    const uint4* la_qp = nullptr;
     auto la_fetch = [&](Ahead& d) {
       if (la_t >= n_tiles) {
         d.nkb = 0;
 #pragma unroll
-        for (int h = 0; h < kKbPerA; ++h) {
-          d.sb[h] = 0u;
-#pragma unroll
-          for (int v = 0; v < QV; ++v) d.q[h][v] = make_uint4(0u, 0u, 0u, 0u);
-        }
+        for (int h = 0; h < kKbPerA; ++h) d.sb[h] = 0u;
         return;
       }
       if (la_kb == 0) {
@@ -469,15 +526,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int64_t grow = (int64_t)ti.e * p.n_rows + wrow;
         la_sp = p.ws + grow * ngroups;
         la_bp = p.wb + grow * ngroups;
-        la_qp = reinterpret_cast<const uint4*>(p.wq + grow * row_words) + slice * QV;
       }
       d.nkb = min(kKbPerA, nkb - la_kb);
 #pragma unroll
       for (int h = 0; h < kKbPerA; ++h) {
         const int kb = h < d.nkb ? la_kb + h : la_kb;  // a missing second k-block repeats the first
         d.sb[h] = (uint32_t)__ldg(la_sp + kb) | ((uint32_t)__ldg(la_bp + kb) << 16);
-#pragma unroll
-        for (int v = 0; v < QV; ++v) d.q[h][v] = ldg_nc_v4(la_qp + kb * (KB_WORDS / 4) + v);
       }
       la_kb += d.nkb;
       if (la_kb == nkb) {
@@ -490,16 +544,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     Ahead ahead[PD];
 #pragma unroll
     for (int i = 0; i < PD; ++i) la_fetch(ahead[i]);
+    // this thread's 16-byte pieces of k-block j of a code slot: row r,
+    // 16-byte chunk j * (KB_BYTES / 16) + slice * QV + v, 128-byte swizzled
+    auto code_piece = [&](const unsigned char* slot, int j, int v) {
+      const int ch = j * (KB_BYTES / 16) + slice * QV + v;
+      return *reinterpret_cast<const uint4*>(slot + r * kCodeRowBytes + ((ch ^ (r & 7)) << 4));
+    };
 
     long long w_dq_aempty = 0;
-    Ring ra, rb;  // A ring, B ring
+    Ring ra, rb, rc;  // A ring, B ring, code ring
+    int akb = 0;      // k-block (within the tile) of the next A stage
     bool ok = true;
     for (int st0 = 0; st0 < nst && ok; st0 += PD) {
 #pragma unroll
       for (int u = 0; u < PD; ++u) {
         if (st0 + u < nst && ok) {
-          const Ahead cur = ahead[u];
+          const Ahead sbc = ahead[u];
           la_fetch(ahead[u]);
+          // the stage's codes: a new slot starts every KPC k-blocks
+          if (akb % KPC == 0 && !warp_wait(&c_full[rc.idx], rc.phase, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          struct {
+            uint4 q[kKbPerA][QV];
+            uint32_t sb[kKbPerA];
+            int nkb;
+          } cur;
+          const unsigned char* cslot = stage_c(rc.idx);
+#pragma unroll
+          for (int h = 0; h < kKbPerA; ++h) {
+            cur.sb[h] = sbc.sb[h];
+#pragma unroll
+            for (int v = 0; v < QV; ++v)
+              cur.q[h][v] = h < sbc.nkb ? code_piece(cslot, (akb + h) % KPC, v)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+          }
+          cur.nkb = sbc.nkb;
           const int sa = ra.idx;
           {
             TC_T0();
@@ -565,6 +646,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               }
             }
             fence_proxy_async_smem();
+            // the code slot is released once its last k-block is converted
+            akb += cur.nkb;
+            const bool tile_end = akb == nkb;
+            if (akb % KPC == 0 || tile_end) {
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&c_empty[rc.idx]);
+              rc.next(SC);
+            }
+            if (tile_end) akb = 0;
             // the A stage is complete once its token tiles have landed too
 #pragma unroll
             for (int h = 0; h < kKbPerA; ++h) {
@@ -816,34 +906,45 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint6
 }
 
 template <int BITS, int MODE, int ACT>
-moe_status_t launch_tc(const CUtensorMap& tma, TcParams p, int64_t max_tiles, cudaStream_t st) {
+moe_status_t launch_tc(const CUtensorMap& tma, const CUtensorMap& tmc, TcParams p,
+                       int64_t max_tiles, cudaStream_t st) {
   auto kern = tc_qmm_kernel<BITS, MODE, ACT>;
-  // ring depths from the opt-in shared memory left beside the static part
-  static const int stages = [kern] {
+  // opt-in shared memory left beside the static part
+  static const long avail = [kern] {
     cudaFuncAttributes fa;
     int dev = 0, optin = 0;
     if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
             cudaSuccess)
-      return 0;
-    const long avail = (long)optin - (long)fa.sharedSizeBytes - 1024;
-    const long a_stages = 2;
-    long b_stages = (avail - a_stages * kAStageBytes) / kBTileBytes;
-    if (b_stages > kMaxStages) b_stages = kMaxStages;
-    return b_stages < 2 ? 0 : (int)(a_stages * 16 + b_stages);
+      return 0L;
+    return (long)optin - (long)fa.sharedSizeBytes - 1024;
   }();
-  if (stages == 0) return MOE_ERR_UNSUPPORTED;
-  p.a_stages = stages / 16;
-  p.b_stages = stages % 16;
-  const size_t smem =
-      (size_t)p.a_stages * kAStageBytes + (size_t)p.b_stages * kBTileBytes + 1024;
+  // ring depths: two A stages, code slots for about 8 k-blocks (at least
+  // 2), and as many token-tile slots as fit (at least 3, else fewer code
+  // slots)
+  const long b_tile = (long)p.bn_cap * kBRowBytes;
+  const long kpc = kCodeRowBytes / (BK * BITS / 8);
+  long c_stages = (8 + kpc - 1) / kpc;
+  if (c_stages < 2) c_stages = 2;
+  long b_stages = 0;
+  for (; c_stages >= 2; --c_stages) {
+    b_stages = (avail - 2L * kAStageBytes - c_stages * kCodeSlotBytes) / b_tile;
+    if (b_stages >= 3) break;
+  }
+  if (b_stages > kMaxStages) b_stages = kMaxStages;
+  if (c_stages < 2 || b_stages < 2) return MOE_ERR_UNSUPPORTED;
+  p.a_stages = 2;
+  p.b_stages = (int)b_stages;
+  p.c_stages = (int)c_stages;
+  const size_t smem = 2 * (size_t)kAStageBytes + (size_t)c_stages * kCodeSlotBytes +
+                      (size_t)b_stages * b_tile + 1024;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
   const int64_t sms = moe_host::sm_count();
   const int grid = (int)(max_tiles < sms ? max_tiles : sms);
   if (grid <= 0) return MOE_OK;
-  return moe_host::launch(kern, grid, kTcThreads, smem, st, tma, p);
+  return moe_host::launch(kern, grid, kTcThreads, smem, st, tma, tmc, p);
 }
 
 }  // namespace
@@ -878,6 +979,7 @@ moe_status_t tc_qmm(const void* act, int act_kind, const int32_t* sorted,
   // act_kind: 0 = x bf16 [T, K] gathered by token, 2 = h bf16 [T*kmax, K] by sorted row
   if (act_kind != 0 && act_kind != 2) return MOE_ERR_UNSUPPORTED;
   if (K % BK != 0 || n_rows % 64 != 0) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)K * bits / 8 < kCodeRowBytes) return MOE_ERR_UNSUPPORTED;  // one code box per row
   if (E > 1024) return MOE_ERR_UNSUPPORTED;
   const bool gather = act_kind == 0;
   const int64_t A = (int64_t)T * kmax;
@@ -908,21 +1010,34 @@ moe_status_t tc_qmm(const void* act, int act_kind, const int32_t* sorted,
   p.n_mt = swiglu ? (p.n_out + kHalfRows - 1) / kHalfRows : (p.n_out + BM - 1) / BM;
   p.a_stages = 2;
   p.b_stages = 2;
+  p.c_stages = 2;
+  // tokens per tile: near the mean segment length, so that a weight tile is
+  // dequantized about once per expert while small segments keep small token
+  // tiles (more token-tile slots fit)
+  const int64_t mean = A / E;
+  p.bn_cap = mean <= 32 ? 64 : (mean <= 64 ? 128 : BN);
   p.err = moe_host::device_error_word();
+  // codes: [E * n_rows rows][K * bits / 8 bytes], 64-row boxes of 128 bytes
+  if ((int64_t)E * n_rows >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  const uint64_t row_bytes = (uint64_t)K * bits / 8;
+  CUtensorMap tmc;
+  if (!make_map_2d(&tmc, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, row_bytes, (uint64_t)E * n_rows,
+                   row_bytes, kCodeRowBytes, kHalfRows, CU_TENSOR_MAP_SWIZZLE_128B))
+    return MOE_ERR_CUDA;
   // upper bound of the tile count: every expert that can be active, plus one
   // partial n-tile each
   const int64_t max_active = A < E ? A : E;
-  const int64_t max_tiles = (int64_t)p.n_mt * (max_active + (A + BN - 1) / BN);
+  const int64_t max_tiles = (int64_t)p.n_mt * (max_active + (A + p.bn_cap - 1) / p.bn_cap);
   if (bits == 4) {
-    if (swiglu) return gather ? launch_tc<4, kTcSwiglu, kTcGatherX>(tma, p, max_tiles, st)
-                              : launch_tc<4, kTcSwiglu, kTcRowsH>(tma, p, max_tiles, st);
-    return gather ? launch_tc<4, kTcRaw, kTcGatherX>(tma, p, max_tiles, st)
-                  : launch_tc<4, kTcRaw, kTcRowsH>(tma, p, max_tiles, st);
+    if (swiglu) return gather ? launch_tc<4, kTcSwiglu, kTcGatherX>(tma, tmc, p, max_tiles, st)
+                              : launch_tc<4, kTcSwiglu, kTcRowsH>(tma, tmc, p, max_tiles, st);
+    return gather ? launch_tc<4, kTcRaw, kTcGatherX>(tma, tmc, p, max_tiles, st)
+                  : launch_tc<4, kTcRaw, kTcRowsH>(tma, tmc, p, max_tiles, st);
   }
-  if (swiglu) return gather ? launch_tc<8, kTcSwiglu, kTcGatherX>(tma, p, max_tiles, st)
-                            : launch_tc<8, kTcSwiglu, kTcRowsH>(tma, p, max_tiles, st);
-  return gather ? launch_tc<8, kTcRaw, kTcGatherX>(tma, p, max_tiles, st)
-                : launch_tc<8, kTcRaw, kTcRowsH>(tma, p, max_tiles, st);
+  if (swiglu) return gather ? launch_tc<8, kTcSwiglu, kTcGatherX>(tma, tmc, p, max_tiles, st)
+                            : launch_tc<8, kTcSwiglu, kTcRowsH>(tma, tmc, p, max_tiles, st);
+  return gather ? launch_tc<8, kTcRaw, kTcGatherX>(tma, tmc, p, max_tiles, st)
+                : launch_tc<8, kTcRaw, kTcRowsH>(tma, tmc, p, max_tiles, st);
 }
 
 }  // namespace moe

@@ -115,7 +115,8 @@ class MoELayer:
     def resolved_path(self, T: int) -> int:
         if self.path != PATH_AUTO:
             return self.path
-        if TC_BUILT and (T * self.kmax) // self.E >= TC_MIN_TOKENS_PER_EXPERT:
+        if (TC_BUILT and (T * self.kmax) // self.E >= TC_MIN_TOKENS_PER_EXPERT
+                and min(self.H, self.I) * self.bits // 8 >= 128):
             return PATH_TC
         return PATH_GEMV
 

@@ -261,6 +261,26 @@ __device__ __forceinline__ void fma_chunk(float (&acc)[TM][TN], const RouterChun
   }
 }
 
+// The xor butterfly (16, 8, 4, 2, 1) of 32 values per lane, as a reduce-
+// scatter: at each step a lane keeps the half of its values that its bit
+// selects and adds the partner's copy of that half.  Every sum is the one
+// the full butterfly forms (a + b = b + a exactly), and lane l ends with the
+// total of value l.
+__device__ __forceinline__ float butterfly_scatter32(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 16, c = 32; off >= 1; off >>= 1, c >>= 1) {
+    const bool hi = (lane & off) != 0;
+#pragma unroll
+    for (int j = 0; j < c / 2; ++j) {
+      const float keep = hi ? v[j + c / 2] : v[j];
+      const float send = hi ? v[j] : v[j + c / 2];
+      v[j] = __fadd_rn(keep, __shfl_xor_sync(0xFFFFFFFFu, send, off));
+    }
+  }
+  return v[0];
+}
+
 // Logits of tokens [t0, t0+nt) x experts [e_lo, e_lo+ne) in warp tiles of
 // TM tokens x TN experts, stored (after bias and temperature) into the
 // leader's [token][E] array at cluster address `lead`.  SMEM: the token rows
@@ -287,6 +307,64 @@ __device__ __forceinline__ void router_logit_tiles(const RouterParams& p, int t0
       wr[n] = reinterpret_cast<const float4*>(
           SMEM ? ws + (int64_t)min(tn * TN + n, ne - 1) * H
                : p.w + (int64_t)(e_lo + min(tn * TN + n, ne - 1)) * H);
+    constexpr bool kPacked = TM * TN == 32 && TM % 2 == 0;
+    if constexpr (kPacked) {
+      float2 acc2[TM / 2][TN];
+#pragma unroll
+      for (int m = 0; m < TM / 2; ++m)
+#pragma unroll
+        for (int n = 0; n < TN; ++n) acc2[m][n] = make_float2(0.0f, 0.0f);
+      // chunks c = lane, lane+32, ...
+#pragma unroll 1
+      for (int c = lane; c < nchunks; c += 32) {
+        // the chunk's token values, then its weights in two halves (h 0-3,
+        // then 4-7), so fewer registers hold loaded data at once
+        uint4 xv[TM];
+        float4 wv[TN];
+#pragma unroll
+        for (int m = 0; m < TM; ++m) xv[m] = SMEM ? xr[m][c] : __ldg(xr[m] + c);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int n = 0; n < TN; ++n) wv[n] = SMEM ? wr[n][2 * c + half] : __ldg(wr[n] + 2 * c + half);
+#pragma unroll
+          for (int hh = 0; hh < 4; ++hh) {
+            const int h = half * 4 + hh;
+            float2 xp[TM / 2];
+#pragma unroll
+            for (int m = 0; m < TM; ++m) {
+              const uint32_t word = h < 2 ? xv[m].x : h < 4 ? xv[m].y : h < 6 ? xv[m].z : xv[m].w;
+              const float f = (h & 1) ? __uint_as_float(word & 0xFFFF0000u) : __uint_as_float(word << 16);
+              if (m & 1) xp[m >> 1].y = f;
+              else xp[m >> 1].x = f;
+            }
+#pragma unroll
+            for (int n = 0; n < TN; ++n) {
+              const float w = hh == 0 ? wv[n].x : hh == 1 ? wv[n].y : hh == 2 ? wv[n].z : wv[n].w;
+              const float2 wp = make_float2(w, w);
+#pragma unroll
+              for (int mp = 0; mp < TM / 2; ++mp) acc2[mp][n] = __ffma2_rn(xp[mp], wp, acc2[mp][n]);
+            }
+          }
+        }
+      }
+      // lane m*TN+n ends with the butterfly total of (m, n)
+      float v[32];
+#pragma unroll
+      for (int m = 0; m < TM; ++m)
+#pragma unroll
+        for (int n = 0; n < TN; ++n) v[m * TN + n] = (m & 1) ? acc2[m >> 1][n].y : acc2[m >> 1][n].x;
+      float tot = butterfly_scatter32(v);
+      const int m = lane / TN, n = lane % TN;
+      const int tl = tm * TM + m, el = tn * TN + n;
+      if (tl < nt && el < ne) {
+        const int e = e_lo + el;
+        if (p.bias) tot = __fadd_rn(tot, __ldg(p.bias + e));
+        tot = __fmul_rn(tot, p.inv_temp);
+        st_cluster_f32(lead + (uint32_t)(tl * E + e) * 4u, tot);
+      }
+      continue;
+    }
     float acc[TM][TN];
 #pragma unroll
     for (int m = 0; m < TM; ++m)

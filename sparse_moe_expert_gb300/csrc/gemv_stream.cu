@@ -116,7 +116,7 @@ struct SvParams {
   const uint16_t* wb;
   void* out;
   int out_dtype;
-  int kmax, E, K, n_rows, n_out;
+  int T, kmax, E, K, n_rows, n_out;
   int mts;       // tokens per pass: 1, 2, 4 or 8
   int stages;    // ring slots
   int rt;        // row tiles per (expert, token chunk)
@@ -503,8 +503,10 @@ __global__ void __launch_bounds__(kSvThreads, 1)
           v[4 * q + 3] = f32_to_bf16_rne(f.w);
         }
       } else {
-        const int64_t row = p.act_kind == kSvActX ? (int64_t)(__ldg(p.sorted + r0 + n) / p.kmax)
-                                                  : (int64_t)(r0 + n);
+        // x by token (a single-token call has only token 0), or h by sorted row
+        const int64_t row = p.act_kind == kSvActX
+                                ? (p.T == 1 ? 0 : (int64_t)(__ldg(p.sorted + r0 + n) / p.kmax))
+                                : (int64_t)(r0 + n);
         const uint4* src =
             reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.act) + row * p.K + col);
 #pragma unroll
@@ -528,7 +530,8 @@ __global__ void __launch_bounds__(kSvThreads, 1)
       const int lo = act_lo[a], m = act_m[a];
       const int nt = min(mts, m - c * mts);
       const int r0 = lo + c * mts;
-      if (!consumer_sync()) return false;  // everyone is done with the staged values
+      // everyone is done with the staged values (nothing staged before the first)
+      if (st_a >= 0 && !consumer_sync()) return false;
       const int total = ngroups * mts2 * 4;
       for (int base = 0; base < total; base += kSvConsumers * 32) {
         const int idx = base + ctid;
@@ -589,7 +592,9 @@ __global__ void __launch_bounds__(kSvThreads, 1)
       }
       if (ctid < kSvMaxTokens) {
         const int n = ctid;
-        st_tok[n] = (n < nt && p.act_kind == kSvActX) ? __ldg(p.sorted + r0 + n) / p.kmax : -1;
+        st_tok[n] = (n < nt && p.act_kind == kSvActX)
+                        ? (p.T == 1 ? 0 : __ldg(p.sorted + r0 + n) / p.kmax)
+                        : -1;
       }
       if (ctid == 0) st_nt = nt;
       return consumer_sync();
@@ -624,7 +629,7 @@ __global__ void __launch_bounds__(kSvThreads, 1)
           const int r0 = lo + cu.c * mts;
           need = nt != st_nt;
           for (int n = 0; n < nt && !need; ++n)
-            need = (__ldg(p.sorted + r0 + n) / p.kmax) != st_tok[n];
+            need = (p.T == 1 ? 0 : __ldg(p.sorted + r0 + n) / p.kmax) != st_tok[n];
         }
         if (need && !stage_x(cu.a, cu.c)) {
           ok = false;
@@ -924,6 +929,7 @@ moe_status_t gemv_stream_qmm(const void* act, int act_kind, const int32_t* sorte
   p.wb = wb;
   p.out = out;
   p.out_dtype = out_dtype;
+  p.T = T;
   p.kmax = kmax;
   p.E = E;
   p.K = K;

@@ -37,6 +37,10 @@ namespace {
 constexpr int kRouterThreads = 512;
 constexpr int kRouterWarps = kRouterThreads / 32;
 constexpr int kRouterCluster = 8;  // CTAs per token group, splitting the experts
+// Batches of many token groups use clusters of 4 (twice the experts per CTA):
+// clusters of 8 CTAs at one CTA per SM leave a fifth of the SMs without a
+// whole cluster's room.
+constexpr int kRouterClusterWide = 4;
 constexpr int kMaxExperts = 1024;
 
 // Tokens per cluster: the leader holds [tokens][E] fp32 logits.
@@ -397,24 +401,24 @@ __device__ __forceinline__ void router_logit_tiles(const RouterParams& p, int t0
   }
 }
 
-__global__ void __cluster_dims__(kRouterCluster, 1, 1) __launch_bounds__(kRouterThreads)
+template <int CL>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kRouterThreads)
     router_topk_kernel(RouterParams p) {
   extern __shared__ __align__(16) float logits_s[];  // leader: [group tokens][E]
   __shared__ __align__(8) uint64_t stage_bar;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int E = p.E;
   const int tpc = router_group_tokens(E);
-  const int t0 = (blockIdx.x / kRouterCluster) * tpc;
+  const int t0 = (blockIdx.x / CL) * tpc;
   const int nt = min(tpc, p.T - t0);
   const uint32_t rank = cluster_ctarank();
-  const int e_lo = (int)rank * E / kRouterCluster;
-  const int ne = ((int)rank + 1) * E / kRouterCluster - e_lo;
+  const int e_lo = (int)rank * E / CL;
+  const int ne = ((int)rank + 1) * E / CL - e_lo;
 
   // ---- Phase A: logits (every CTA of the cluster, into the leader) -------
   // staged copies of the weight slice and token rows sit after the logits
   float* ws_s = logits_s + tpc * E;
-  uint16_t* xs_s = reinterpret_cast<uint16_t*>(ws_s + (size_t)((E + kRouterCluster - 1) /
-                                                              kRouterCluster) * p.H);
+  uint16_t* xs_s = reinterpret_cast<uint16_t*>(ws_s + (size_t)((E + CL - 1) / CL) * p.H);
   bool staged_ok = true;
   if (p.smem_stage) {
     if (threadIdx.x == 0) {
@@ -526,7 +530,7 @@ __global__ void __cluster_dims__(kRouterCluster, 1, 1) __launch_bounds__(kRouter
     }
   }
 
-  if (gridDim.x == kRouterCluster) {
+  if (gridDim.x == CL) {
     __syncthreads();
     finalize_batch(p);
     if (p.pm_sorted) {
@@ -550,23 +554,25 @@ moe_status_t launch_router(const RouterParams& p, cudaStream_t st) {
   const int ngroups = (p.T + tpc - 1) / tpc;
   if (ngroups > 0) {
     size_t smem = (size_t)tpc * p.E * sizeof(float);
+    // more token groups than a wave of 8-CTA clusters fills: clusters of 4
+    const bool wide = (int64_t)ngroups * kRouterCluster > sm_count();
+    const int cl = wide ? kRouterClusterWide : kRouterCluster;
     // small batches: the per-CTA weight slice and the token rows in shared memory
-    const int ne_max = (p.E + kRouterCluster - 1) / kRouterCluster;
+    const int ne_max = (p.E + cl - 1) / cl;
     const int nt_max = p.T < tpc ? p.T : tpc;
     const size_t staged = smem + (size_t)ne_max * p.H * 4 + (size_t)nt_max * p.H * 2;
     RouterParams q = p;
     q.smem_stage = (ngroups == 1 && staged <= kRouterStageBytes) ? 1 : 0;
     if (q.smem_stage) smem = staged;
-    static size_t set_max = 48 * 1024;
-    if (smem > set_max) {
-      if (cudaFuncSetAttribute(router_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem) != cudaSuccess)
+    auto kern = wide ? router_topk_kernel<kRouterClusterWide> : router_topk_kernel<kRouterCluster>;
+    static size_t set_max[2] = {48 * 1024, 48 * 1024};
+    if (smem > set_max[wide]) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess)
         return MOE_ERR_CUDA;
-      set_max = smem;
+      set_max[wide] = smem;
     }
-    if (launch(router_topk_kernel, ngroups * kRouterCluster, kRouterThreads, smem, st, q) !=
-        MOE_OK)
-      return MOE_ERR_CUDA;
+    if (launch(kern, ngroups * cl, kRouterThreads, smem, st, q) != MOE_OK) return MOE_ERR_CUDA;
   }
   if (ngroups != 1) {
     if (launch(router_finalize_kernel, 1, kFinalizeThreads, 0, st, p) != MOE_OK)

@@ -71,6 +71,7 @@ def test_router_single_token_calls(cuda_lib):
     (1024, 4, 4, 9, True, True, 1.0),
     (8, 0, 5, 21, True, False, 3.0),    # adaptive with kmax > 3
     (8, 0, 3, 21, False, True, 0.2),
+    (37, 3, 3, 700, True, True, 0.9),   # 22 token groups: the 4-CTA cluster router
 ])
 def test_router_edge_shapes(cuda_lib, E, k, kmax, T, renorm, bias, it):
     rng = np.random.default_rng(E * 100 + T)

@@ -78,6 +78,27 @@ def shard_calls(n_calls: int, rank: int, world: int):
     return [(rank * n_calls + c) for c in range(n_calls)]
 
 
+def rank_tokens(cfg, rank: int, world: int) -> np.ndarray:
+    """This rank's activations, bf16 bits [batches * calls * T, H]: batch b
+    draws from stream STREAM_X + b at the offset of the rank's first call, so
+    the ranks' tokens are disjoint pieces of one global stream."""
+    starts = shard_calls(cfg.calls, rank, world)
+    xb = [workloads.normal_bf16(0, workloads.STREAM_X + b, (cfg.calls * cfg.T, cfg.H), cfg.x_std,
+                                start=starts[0] * cfg.T * cfg.H) for b in range(cfg.batches)]
+    return np.concatenate(xb, axis=0)
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest value over the ranks (the slowest rank's time)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def load_peaks():
     try:
         with open(MEASURED_PEAKS) as f:
@@ -259,10 +280,7 @@ def run_ours(args):
     # of k = 1, 2, 3 runs once per step)
     n_batches = cfg.batches
     calls = cfg.calls * n_batches
-    starts = shard_calls(cfg.calls, rank, world)
-    xb = [workloads.normal_bf16(0, workloads.STREAM_X + b, (cfg.calls * T, cfg.H), cfg.x_std,
-                                start=starts[0] * T * cfg.H) for b in range(n_batches)]
-    x_bits = np.concatenate(xb, axis=0)
+    x_bits = rank_tokens(cfg, rank, world)
     x_dev = moe.bf16_from_bits(x_bits, dev)
     out_dev = torch.empty((calls * T, cfg.H), dtype=torch.bfloat16, device=dev)
     temps = [cfg.inv_temperature(c // cfg.calls) for c in range(calls)]
@@ -307,10 +325,7 @@ def run_ours(args):
         torch.cuda.synchronize()
     barrier()
     ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     tokens_per_step = calls * T
     value = tokens_per_step * world / (ms / 1000.0)
     clocks = clk.summary()
@@ -383,10 +398,7 @@ def run_ours(args):
         e2e_step()
     torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t0) / esteps
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, world, dev)
     e2e = {"value": tokens_per_step * world / e2e_s, "unit": "tokens/s",
            "h2d_bytes_per_step": tokens_per_step * cfg.H * 2,
            "d2h_bytes_per_step": tokens_per_step * cfg.H * 2,

@@ -27,12 +27,14 @@
 //               gathers (tile::gather4) of the token rows of x, or 64-row 2D
 //               boxes of rows already in sorted order (h, or x permuted),
 //               128-byte swizzled as the MMA expects; all 32 lanes issue;
-//   warp 14     codes: TMA-loads the packed codes of the tile's 128 rows,
+//   code warp   TMA-loads the packed codes of the tile's 128 rows,
 //               128 bytes of each row per slot (4 k-blocks of 4-bit codes,
 //               2 of 8-bit), two 64-row boxes with the 128-byte swizzle,
 //               into a ring of 16 KB slots; bulk copies keep far more bytes
 //               in flight than per-thread loads of 16-64 bytes per row could;
-//   warps 6-13  dequant: each thread reads its row slice of the codes from
+//   warps 6..   dequant (8 warps for 4-bit codes, 16 for 8-bit; the code
+//               warp comes after them): each thread reads its row slice of
+//               the codes from
 //               the slot and loads the row's scale and bias into registers
 //               a few A stages ahead, then w = s*q + b in fp32 (packed FMA),
 //               rounds to bf16, writes the A tile in the 128-byte-swizzled
@@ -74,9 +76,13 @@ constexpr int BN = 256;        // most tokens per tile
 constexpr int BK = 64;         // contraction per stage = one scale group = one 128-B swizzle atom
 constexpr int kHalfRows = 64;  // SWIGLU: gate rows, then up rows, per A tile
 constexpr int kBoxRows = 64;   // rows per 2D TMA box (codes and token rows)
-constexpr int kEpiWarps = 4, kMmaWarp = 4, kLoadWarp = 5, kDeqWarp0 = 6, kDeqWarps = 8;
-constexpr int kCodeWarp = kDeqWarp0 + kDeqWarps;           // 14
-constexpr int kTcThreads = (kCodeWarp + 1) * 32;           // 480
+constexpr int kEpiWarps = 4, kMmaWarp = 4, kLoadWarp = 5, kDeqWarp0 = 6;
+// Dequant warps: 8 for 4-bit codes, 16 for 8-bit (twice the code bytes per
+// weight to convert; measured: 16 warps speed up the 8-bit products and slow
+// the 4-bit ones).  The code warp follows them.
+__host__ __device__ constexpr int deq_warps(int bits) { return bits == 8 ? 16 : 8; }
+__host__ __device__ constexpr int code_warp(int bits) { return kDeqWarp0 + deq_warps(bits); }
+__host__ __device__ constexpr int tc_threads(int bits) { return (code_warp(bits) + 1) * 32; }
 constexpr int kATileBytes = BM * BK * 2;                  // 16 KB bf16 weight tile
 constexpr int kKbPerA = 2;                                // k-blocks per A stage
 constexpr int kAStageBytes = kKbPerA * kATileBytes;       // 32 KB
@@ -281,21 +287,24 @@ __device__ __forceinline__ int tile_weight_row(const TcParams& p, int mt, int r)
   return mt * BM + r;
 }
 
-// 14 warps are granted registers as 16, so 128 per thread is the ceiling
-// for one CTA per SM.
+// One CTA per SM: 15 warps (4-bit) or 23 warps (8-bit) share the register
+// file, so at most 128 or 88 registers per thread.
 template <int BITS, int MODE, int ACT>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(tc_threads(BITS), 1)
     tc_qmm_kernel(const __grid_constant__ CUtensorMap tm_act,
                   const __grid_constant__ CUtensorMap tm_codes, TcParams p) {
-  // dequant work split: 2 threads per A row, 32 codes of each k-block each
-  constexpr int DQ_SLICES = kDeqWarps * 32 / BM;  // 2
-  constexpr int DQ_CHUNKS = 8 / DQ_SLICES;        // 16-byte bf16 chunks per thread per k-block: 4
+  // dequant work split: DQ_SLICES threads per A row, BK / DQ_SLICES codes of
+  // each k-block each
+  constexpr int kDeqWarps = deq_warps(BITS);
+  constexpr int kCodeWarp = code_warp(BITS);
+  constexpr int DQ_SLICES = kDeqWarps * 32 / BM;  // 2 | 4
+  constexpr int DQ_CHUNKS = 8 / DQ_SLICES;        // 16-byte bf16 chunks per thread per k-block
   constexpr int KB_WORDS = BK * BITS / 32;         // code words of one row per k-block
-  constexpr int QV = KB_WORDS / DQ_SLICES / 4;     // 16-byte code pieces per thread per k-block
+  constexpr int CW = KB_WORDS / DQ_SLICES;         // code words per thread per k-block
   constexpr int KB_BYTES = BK * BITS / 8;          // code bytes of a row per k-block: 32 | 64
   constexpr int KPC = kCodeRowBytes / KB_BYTES;    // k-blocks per code slot: 4 | 2
   constexpr int PD = kScaleLookahead;              // A stages of scales in flight
-  static_assert(DQ_CHUNKS == 4, "dequant split assumes four output chunks per thread");
+  static_assert(CW * 4 == 8 || CW % 4 == 0, "a thread reads 8 bytes or whole 16-byte chunks");
   static_assert(KPC % kKbPerA == 0, "a code slot holds whole A stages");
 
   extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
@@ -544,11 +553,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     Ahead ahead[PD];
 #pragma unroll
     for (int i = 0; i < PD; ++i) la_fetch(ahead[i]);
-    // this thread's 16-byte pieces of k-block j of a code slot: row r,
-    // 16-byte chunk j * (KB_BYTES / 16) + slice * QV + v, 128-byte swizzled
-    auto code_piece = [&](const unsigned char* slot, int j, int v) {
-      const int ch = j * (KB_BYTES / 16) + slice * QV + v;
-      return *reinterpret_cast<const uint4*>(slot + r * kCodeRowBytes + ((ch ^ (r & 7)) << 4));
+    // this thread's CW code words of k-block j of a code slot: row r, bytes
+    // j * KB_BYTES + slice * CW * 4 on, 16-byte chunks 128-byte swizzled
+    auto load_codes = [&](const unsigned char* slot, int j, uint32_t (&w)[CW]) {
+      const int byte0 = j * KB_BYTES + slice * CW * 4;
+      const unsigned char* row = slot + r * kCodeRowBytes;
+      if constexpr (CW * 4 >= 16) {
+#pragma unroll
+        for (int v = 0; v < CW / 4; ++v) {
+          const int ch = byte0 / 16 + v;
+          const uint4 t = *reinterpret_cast<const uint4*>(row + ((ch ^ (r & 7)) << 4));
+          w[4 * v] = t.x;
+          w[4 * v + 1] = t.y;
+          w[4 * v + 2] = t.z;
+          w[4 * v + 3] = t.w;
+        }
+      } else {
+        const int ch = byte0 / 16;
+        const uint2 t = *reinterpret_cast<const uint2*>(row + ((ch ^ (r & 7)) << 4) + (byte0 & 15));
+        w[0] = t.x;
+        w[1] = t.y;
+      }
     };
 
     long long w_dq_aempty = 0;
@@ -567,7 +592,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
           struct {
-            uint4 q[kKbPerA][QV];
+            uint32_t q[kKbPerA][CW];
             uint32_t sb[kKbPerA];
             int nkb;
           } cur;
@@ -575,10 +600,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int h = 0; h < kKbPerA; ++h) {
             cur.sb[h] = sbc.sb[h];
+            if (h < sbc.nkb) {
+              load_codes(cslot, (akb + h) % KPC, cur.q[h]);
+            } else {
 #pragma unroll
-            for (int v = 0; v < QV; ++v)
-              cur.q[h][v] = h < sbc.nkb ? code_piece(cslot, (akb + h) % KPC, v)
-                                        : make_uint4(0u, 0u, 0u, 0u);
+              for (int v = 0; v < CW; ++v) cur.q[h][v] = 0u;
+            }
           }
           cur.nkb = sbc.nkb;
           const int sa = ra.idx;
@@ -598,10 +625,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                   // one 32-bit word = 8 codes = one 16-byte bf16 chunk
                   const float2 mul = make_float2(512.0f * sc, 32.0f * sc);
                   const float2 add = make_float2(bi - 512.0f * sc, bi - 32.0f * sc);
-                  const uint32_t wv[4] = {cur.q[h][0].x, cur.q[h][0].y, cur.q[h][0].z, cur.q[h][0].w};
 #pragma unroll
                   for (int i = 0; i < DQ_CHUNKS; ++i) {
-                    const uint32_t v = wv[i];
+                    const uint32_t v = cur.q[h][i];
                     const uint32_t sh[4] = {v << 14, v << 6, v >> 2, v >> 10};
                     uint32_t o[4];
 #pragma unroll
@@ -622,8 +648,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                   const float2 add = make_float2(bi - 256.0f * sc, bi - 256.0f * sc);
 #pragma unroll
                   for (int i = 0; i < DQ_CHUNKS; i += 2) {
-                    const uint4 q4 = cur.q[h][(i / 2) % QV];
-                    const uint32_t wv[4] = {q4.x, q4.y, q4.z, q4.w};
+                    const uint32_t wv[4] = {cur.q[h][2 * i], cur.q[h][2 * i + 1], cur.q[h][2 * i + 2],
+                                            cur.q[h][2 * i + 3]};
                     uint32_t o[8];
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
@@ -944,7 +970,7 @@ moe_status_t launch_tc(const CUtensorMap& tma, const CUtensorMap& tmc, TcParams 
   const int64_t sms = moe_host::sm_count();
   const int grid = (int)(max_tiles < sms ? max_tiles : sms);
   if (grid <= 0) return MOE_OK;
-  return moe_host::launch(kern, grid, kTcThreads, smem, st, tma, tmc, p);
+  return moe_host::launch(kern, grid, tc_threads(BITS), smem, st, tma, tmc, p);
 }
 
 }  // namespace

@@ -344,6 +344,10 @@ def run_ours(args):
                       inv_temperature=temps[c])
         bufs = layer.buffers(T)
         per_call.append((int((bufs["counts"] > 0).sum().item()), int(bufs["k_dev"].item())))
+    cnt = layer.buffers(T)["counts"].double().cpu()
+    count_stats = {"experts": int(cnt.numel()), "active": int((cnt > 0).sum().item()),
+                   "min": int(cnt.min().item()), "max": int(cnt.max().item()),
+                   "std": round(float(cnt.std(unbiased=False).item()), 3)}
     torch.cuda.synchronize()
     for _ in range(ksteps):
         step(events)
@@ -427,6 +431,7 @@ def run_ours(args):
                     "layer_gbs": (gu_step_bytes + dn_step_bytes) / (ms * 1e-3) / 1e9,
                     "layer_tflops": (gu_step_flops + dn_step_flops) / (ms * 1e-3) / 1e12,
                     "active_experts_and_k_per_call": sorted(set(per_call)),
+                    "expert_counts_last_call": count_stats,
                     "per_kernel_us": {k: v * 1e3 for k, v in kt.items()}},
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                    "reasons": clocks["reasons"], "samples": clocks["samples"]},

@@ -357,6 +357,21 @@ moe_status_t moe_swiglu(const float* gate, const float* up, const int32_t* k_dev
  * ---------------------------------------------------------------------- */
 moe_status_t moe_get_device_error(uint32_t* flags, int clear, moe_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * moe_selftest_wait_timeout -- check of the bounded device waits.
+ *
+ * No page has a counterpart: every wait in the library's kernels gives up
+ * after a bounded number of SM clock cycles, reports MOE_DEVERR_TIMEOUT in
+ * the device error word and lets its kernel end, so a stalled pipeline is
+ * reported instead of hanging the GPU.  This call launches one small CTA
+ * whose thread waits, with the same wait routine, on an mbarrier that no
+ * thread ever arrives on, for at most `budget_cycles` cycles (1 ..
+ * 100,000,000, about 50 ms at 2 GHz), then sets MOE_DEVERR_TIMEOUT.  It lets
+ * a caller check that a wait which runs out is reported and that the
+ * context stays usable.  Asynchronous on `stream`.
+ * ---------------------------------------------------------------------- */
+moe_status_t moe_selftest_wait_timeout(uint32_t budget_cycles, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

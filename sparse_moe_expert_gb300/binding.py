@@ -213,6 +213,12 @@ def moe_swiglu(gate, up, k_dev, T: int, kmax: int, out_dtype=torch.float32, out=
     return out
 
 
+def moe_selftest_wait_timeout(budget_cycles: int = 2_000_000, stream=None) -> None:
+    """Launch the bounded-wait self-test (a wait that runs out on purpose)."""
+    check("moe_selftest_wait_timeout",
+          lib().moe_selftest_wait_timeout(int(budget_cycles), _stream(stream)))
+
+
 def moe_get_device_error(clear: bool = True, stream=None) -> int:
     v = ctypes.c_uint32(0)
     st = lib().moe_get_device_error(ctypes.byref(v), int(clear), _stream(stream))

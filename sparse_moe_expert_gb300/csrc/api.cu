@@ -5,6 +5,7 @@
 #include <cstdlib>
 #include <mutex>
 
+#include "async.cuh"
 #include "common.cuh"
 
 namespace moe {
@@ -201,6 +202,32 @@ extern "C" moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* 
                              w_s, w_b, bits, y, MOE_DTYPE_F32, st);
   return moe::gemv_qmm(h, act_kind, nullptr, expert_offsets, T, kmax, E, I, H, false, w_q, w_s,
                        w_b, bits, y, MOE_DTYPE_F32, early, st);
+}
+
+namespace {
+
+// One thread waits on an mbarrier nothing arrives on, for at most `budget`
+// cycles, with the library's bounded wait, and reports the timeout.
+__global__ void wait_timeout_selftest_kernel(unsigned int* err, long long budget) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    moe::mbar_init(&bar, 1);
+    moe::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !moe::mbar_wait(&bar, 0, budget))
+    moe::raise_device_error(err, MOE_DEVERR_TIMEOUT);
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_selftest_wait_timeout(uint32_t budget_cycles, moe_stream_t stream) {
+  if (budget_cycles < 1 || budget_cycles > 100000000u) return MOE_ERR_INVALID_ARG;
+  unsigned int* err = moe_host::device_error_word();
+  if (!err) return MOE_ERR_CUDA;
+  wait_timeout_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      err, (long long)budget_cycles);
+  return moe_host::launch_status();
 }
 
 extern "C" moe_status_t moe_get_device_error(uint32_t* flags, int clear, moe_stream_t stream) {

@@ -172,3 +172,21 @@ def test_permute_flags_bad_expert(cuda_lib):
     cuda_lib.moe_permute(ids, kd, 4)
     assert cuda_lib.moe_get_device_error(clear=True) & cuda_lib.DEVERR_BAD_EXPERT
     assert cuda_lib.moe_get_device_error(clear=True) == 0
+
+
+def test_bounded_wait_reports_timeout_and_context_stays_usable(cuda_lib):
+    """A device wait that runs out (an mbarrier nothing arrives on) sets the
+    timeout bit in the error word; the next layer call still matches the
+    oracle."""
+    cuda_lib.moe_get_device_error(clear=True)
+    cuda_lib.moe_selftest_wait_timeout(2_000_000)   # about a millisecond
+    assert cuda_lib.moe_get_device_error(clear=True) & cuda_lib.DEVERR_TIMEOUT
+    assert cuda_lib.moe_get_device_error(clear=True) == 0
+    cfg = workloads.CONFIGS["tiny"]
+    layer_np = workloads.make_layer(cfg)
+    x_bits = workloads.make_tokens(cfg)
+    layer = cuda_lib.MoELayer.from_workload(layer_np, dev())
+    out = to_np(layer(cuda_lib.bf16_from_bits(x_bits, dev())))
+    ref = oracle.moe_forward(x_bits, layer_np)
+    assert rel_l2(out, ref.out) <= 5e-3
+    assert cuda_lib.moe_get_device_error() == 0

@@ -11,7 +11,7 @@ from . import _build
 
 __all__ = [
     "router_logits", "softmax_entropy", "batch_mean_entropy", "entropy_k", "topk_ids",
-    "routing_weights", "route", "Routing", "permute", "Permutation", "unpack_codes",
+    "routing_weights", "group_top1_ids", "route", "Routing", "permute", "Permutation", "unpack_codes",
     "dequant", "QDesc", "can_fuse", "pack_gate_up", "qmm_raw", "silu", "swiglu",
     "moe_forward", "Forward", "dense_masked_forward", "bf16_to_f64", "ENTROPY_THRESHOLDS",
 ]
@@ -102,6 +102,29 @@ def topk_ids(logits: np.ndarray, k: int) -> np.ndarray:
     return order[:, :k].astype(np.int32)
 
 
+def group_top1_ids(logits: np.ndarray, groups: int) -> np.ndarray:
+    """Group-limited selection, page [A] section 1.1: the E experts form
+    `groups` groups of E/groups consecutive ids and each token takes the best
+    expert of every group (equal logits: the lower id).  The winners are
+    listed largest logit first, equal logits by lower id, as topk_ids lists
+    its choice."""
+    l = np.asarray(logits, dtype=np.float32)
+    T, E = l.shape
+    assert groups > 0 and E % groups == 0
+    gsz = E // groups
+    out = np.empty((T, groups), dtype=np.int32)
+    for t in range(T):
+        winners = []
+        for g in range(groups):
+            lo = g * gsz
+            seg = l[t, lo:lo + gsz]
+            best = lo + int(np.argmax(seg))  # argmax returns the first maximum
+            winners.append(best)
+        winners.sort(key=lambda e: (-float(l[t, e]), e))
+        out[t] = winners
+    return out
+
+
 def routing_weights(logits: np.ndarray, ids: np.ndarray, renormalize: bool = True) -> np.ndarray:
     """Softmax probabilities of the chosen experts in float64, either
     renormalised to sum to 1 over the chosen k, or as plain softmax values."""
@@ -123,9 +146,10 @@ class Routing:
 
 
 def route(x_bits, router_w, logit_bias=None, inv_temperature=1.0, k_fixed=2, kmax=None,
-          renormalize=True, thresholds=ENTROPY_THRESHOLDS) -> Routing:
+          renormalize=True, thresholds=ENTROPY_THRESHOLDS, groups=0) -> Routing:
     """Router logits, softmax, entropy, k (fixed, or adaptive when k_fixed=0)
-    and the top-k ids and weights, padded to kmax slots."""
+    and the top-k ids and weights, padded to kmax slots.  groups > 0: the
+    group-limited rule (one expert per group, k = groups)."""
     logits = router_logits(x_bits, router_w, logit_bias, inv_temperature)
     ent = softmax_entropy(logits)
     hbar = batch_mean_entropy(ent) if len(ent) else np.float32(0.0)
@@ -137,7 +161,11 @@ def route(x_bits, router_w, logit_bias=None, inv_temperature=1.0, k_fixed=2, kma
     ids = np.full((T, kmax), -1, dtype=np.int32)
     w = np.zeros((T, kmax), dtype=np.float64)
     if T:
-        ids[:, :k] = topk_ids(logits, k)
+        if groups > 0:
+            assert k == groups
+            ids[:, :k] = group_top1_ids(logits, groups)
+        else:
+            ids[:, :k] = topk_ids(logits, k)
         w[:, :k] = routing_weights(logits, ids[:, :k], renormalize)
     return Routing(logits, ids, w, k, hbar, ent)
 

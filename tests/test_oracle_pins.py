@@ -144,6 +144,52 @@ def test_topk_brute_force(k):
     assert np.array_equal(oracle.topk_ids(l, k), brute_topk(l, k))
 
 
+@pytest.mark.parametrize("groups", [1, 2, 4, 16])
+def test_group_top1_brute_force(groups):
+    """Page [A] section 1.1: best expert of each group of consecutive ids.
+    Checked against a per-group scan written from the definition; groups=1
+    is plain top-1 and groups=E is the full descending order."""
+    rng = np.random.default_rng(40 + groups)
+    E = 16
+    l = rng.normal(0, 1, (30, E)).astype(np.float32)
+    l[::4, 3] = l[::4, 1]          # ties inside the first group
+    l[5, :] = 1.0                  # all equal
+    got = oracle.group_top1_ids(l, groups)
+    gsz = E // groups
+    for t in range(l.shape[0]):
+        winners = []
+        for g in range(groups):
+            best = g * gsz
+            for e in range(g * gsz, (g + 1) * gsz):
+                if l[t, e] > l[t, best]:
+                    best = e
+            winners.append(best)
+        # order: larger logit first, equal logits lower id first
+        for i in range(len(winners)):
+            for j in range(len(winners) - 1 - i):
+                a, b = winners[j], winners[j + 1]
+                if l[t, b] > l[t, a] or (l[t, b] == l[t, a] and b < a):
+                    winners[j], winners[j + 1] = b, a
+        assert list(got[t]) == winners
+    if groups == 1:
+        assert np.array_equal(got, brute_topk(l, 1))
+    if groups == E:
+        assert np.array_equal(got, brute_topk(l, E))
+
+
+def test_group_routing_weights_and_k():
+    rng = np.random.default_rng(41)
+    H, E, G = 128, 16, 4
+    w = rng.normal(0, 0.05, (E, H)).astype(np.float32)
+    x = bf16(rng.normal(0, 1, (12, H)).astype(np.float32))
+    r = oracle.route(x, w, None, 1.0, k_fixed=G, groups=G)
+    assert r.k == G
+    gsz = E // G
+    for t in range(12):
+        assert sorted(int(e) // gsz for e in r.ids[t]) == list(range(G))  # one per group
+    np.testing.assert_allclose(r.weights.sum(axis=1), 1.0, rtol=0, atol=1e-12)
+
+
 def test_topk_ties_from_duplicated_router_rows():
     rng = np.random.default_rng(5)
     H, E = 256, 8

@@ -255,6 +255,25 @@ moe_status_t moe_route(const uint16_t* x, const float* w_router, const float* lo
                        int32_t* sorted_assign, int32_t* inv_pos, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * moe_route_grouped -- moe_route with group-limited selection.
+ *
+ * Page [A], section 1.1: the E experts form n_groups groups of E / n_groups
+ * consecutive ids and each token takes the best expert of every group, so
+ * k = n_groups.  Within a group the larger logit wins, equal logits go to
+ * the lower id; the chosen ids are listed larger logit first (equal logits:
+ * lower id first), as moe_router_topk lists its top-k.  Weights, entropy,
+ * k_dev and the expert grouping are those of moe_route with k_fixed =
+ * n_groups.  E must be a multiple of n_groups and n_groups <= kmax <= 16.
+ * ---------------------------------------------------------------------- */
+moe_status_t moe_route_grouped(const uint16_t* x, const float* w_router, const float* logit_bias,
+                               float inv_temperature, int T, int H, int E, int n_groups,
+                               int kmax, int renormalize, int32_t* topk_ids, float* topk_w,
+                               int32_t* k_dev, float* mean_entropy, void* workspace,
+                               size_t workspace_bytes, int32_t* expert_counts,
+                               int32_t* expert_offsets, int32_t* sorted_assign,
+                               int32_t* inv_pos, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * moe_permute_rows -- the token rows in expert order.
  *
  * Page [C], 如何验证正确性 (the sorted branch: token rows are gathered into

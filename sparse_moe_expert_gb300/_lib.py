@@ -21,7 +21,7 @@ SCALE_F16, SCALE_BF16, SCALE_F32 = 0, 1, 2
 # every symbol the header declares
 EXPORTS = (
     "moe_status_string", "moe_abi_version", "moe_set_launch_overlap", "moe_pack_gate_up", "moe_router_workspace_size",
-    "moe_router_topk", "moe_router_topk_noalloc", "moe_route", "moe_permute", "moe_permute_rows", "moe_gate_up_qmm", "moe_down_qmm", "moe_combine",
+    "moe_router_topk", "moe_router_topk_noalloc", "moe_route", "moe_route_grouped", "moe_permute", "moe_permute_rows", "moe_gate_up_qmm", "moe_down_qmm", "moe_combine",
     "moe_swiglu", "moe_get_device_error", "moe_selftest_wait_timeout",
 )
 
@@ -65,6 +65,8 @@ def _declare(lib):
     lib.moe_route.argtypes = [vp, vp, vp, f32, i32, i32, i32, i32, i32, f32, f32, i32, vp, vp, vp,
                               vp, vp, sz, vp, vp, vp, vp, vp]
     lib.moe_permute.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
+    lib.moe_route_grouped.argtypes = [vp, vp, vp, f32, i32, i32, i32, i32, i32, i32, vp, vp, vp,
+                                      vp, vp, sz, vp, vp, vp, vp, vp]
     lib.moe_permute_rows.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
     lib.moe_gate_up_qmm.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i32, i32,
                                     i32, vp, i32, vp]
@@ -75,6 +77,7 @@ def _declare(lib):
     lib.moe_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32, vp]
     lib.moe_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
     for name in ("moe_pack_gate_up", "moe_router_topk", "moe_router_topk_noalloc", "moe_route",
+                 "moe_route_grouped",
                  "moe_permute", "moe_permute_rows", "moe_gate_up_qmm",
                  "moe_down_qmm", "moe_combine", "moe_swiglu", "moe_get_device_error",
                  "moe_selftest_wait_timeout"):

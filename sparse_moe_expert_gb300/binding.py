@@ -124,6 +124,25 @@ def moe_route(x, w_router, logit_bias, inv_temperature: float, k_fixed: int, kma
     return topk_ids, topk_w, k_dev, mean_entropy, expert_counts, expert_offsets, sorted_assign, inv_pos
 
 
+def moe_route_grouped(x, w_router, logit_bias, inv_temperature: float, n_groups: int, kmax: int,
+                      renormalize: bool, topk_ids, topk_w, k_dev, mean_entropy, workspace,
+                      expert_counts, expert_offsets, sorted_assign, inv_pos, stream=None):
+    """moe_route with group-limited selection (the best expert of each of
+    n_groups groups of consecutive ids, k = n_groups)."""
+    _need(x, torch.bfloat16, "x")
+    _need(w_router, torch.float32, "w_router")
+    T, H = x.shape
+    E = w_router.shape[0]
+    st = lib().moe_route_grouped(_p(x), _p(w_router), _p(logit_bias),
+                                 ctypes.c_float(inv_temperature), T, H, E, n_groups, kmax,
+                                 int(renormalize), _p(topk_ids), _p(topk_w), _p(k_dev),
+                                 _p(mean_entropy), _p(workspace), workspace.numel(),
+                                 _p(expert_counts), _p(expert_offsets), _p(sorted_assign),
+                                 _p(inv_pos), _stream(stream))
+    check("moe_route_grouped", st)
+    return topk_ids, topk_w, k_dev, mean_entropy, expert_counts, expert_offsets, sorted_assign, inv_pos
+
+
 def moe_permute(topk_ids, k_dev, E: int, expert_counts=None, expert_offsets=None,
                 sorted_assign=None, inv_pos=None, stream=None):
     """-> (expert_counts [E], expert_offsets [E+1], sorted_assign [T*kmax], inv_pos [T*kmax])"""

@@ -58,6 +58,8 @@ struct RouterParams {
   float thr1, thr2;
   int renorm;
   int smem_stage;  // bulk-copy the weight slice and token rows to shared memory
+  int groups;      // > 0: group-limited selection, the best expert of each of
+                   // `groups` groups of E / groups consecutive ids (k = groups)
   int32_t* ids;
   float* topw;
   int32_t* k_dev;
@@ -483,14 +485,19 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kRouterThreads)
     const float ent = __fsub_rn(logf(s), __fdiv_rn(s1, s));
 
     // top-nsel by repeated warp argmax; lane owns e = lane + 32*j
+    // grouped: round r takes the best expert of group r (page "Qwen3.5
+    // Block在llama.cpp中的映射与优化原理", section 1.1), then the winners are
+    // ordered as top-k orders its choice (larger logit, then lower id)
+    const int gsz = p.groups > 0 ? E / p.groups : E;
     unsigned int taken = 0u;
     int sel[16];
-    float selz[16];
+    float selz[16], selv[16];
     for (int r = 0; r < nsel; ++r) {
       float bv = -INFINITY;
       int bi = -1;
       for (int j = 0, e = lane; e < E; ++j, e += 32) {
         if (taken & (1u << j)) continue;
+        if (p.groups > 0 && e / gsz != r) continue;
         float v = row[e];
         if (better(v, e, bv, bi)) { bv = v; bi = e; }
       }
@@ -503,6 +510,20 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kRouterThreads)
       if (bi >= 0 && (bi & 31) == lane) taken |= 1u << (bi >> 5);
       sel[r] = bi;
       selz[r] = expf(__fsub_rn(bv, m));
+      selv[r] = bv;
+    }
+    if (p.groups > 0 && lane == 0) {
+      for (int i = 1; i < nsel; ++i)  // insertion sort: logit descending, id ascending
+        for (int j = i; j > 0 && better(selv[j], sel[j], selv[j - 1], sel[j - 1]); --j) {
+          const float tv = selv[j], tz = selz[j];
+          const int ti = sel[j];
+          selv[j] = selv[j - 1];
+          selz[j] = selz[j - 1];
+          sel[j] = sel[j - 1];
+          selv[j - 1] = tv;
+          selz[j - 1] = tz;
+          sel[j - 1] = ti;
+        }
     }
     if (lane == 0) {
       int32_t* idr = p.ids + (int64_t)t * p.kmax;
@@ -628,6 +649,7 @@ moe_status_t router_params(const uint16_t* x, const float* w_router, const float
   p.thr2 = thr2;
   p.renorm = renormalize ? 1 : 0;
   p.smem_stage = 0;
+  p.groups = 0;
   p.ids = topk_ids;
   p.topw = topk_w;
   p.k_dev = k_dev;
@@ -658,19 +680,23 @@ extern "C" moe_status_t moe_router_topk(const uint16_t* x, const float* w_router
   return launch_router(p, reinterpret_cast<cudaStream_t>(stream));
 }
 
-extern "C" moe_status_t moe_route(const uint16_t* x, const float* w_router,
-                                  const float* logit_bias, float inv_temperature, int T, int H,
-                                  int E, int k_fixed, int kmax, float thr1, float thr2,
-                                  int renormalize, int32_t* topk_ids, float* topk_w,
-                                  int32_t* k_dev, float* mean_entropy, void* workspace,
-                                  size_t workspace_bytes, int32_t* expert_counts,
-                                  int32_t* expert_offsets, int32_t* sorted_assign,
-                                  int32_t* inv_pos, moe_stream_t stream) {
+namespace {
+
+moe_status_t route_impl(const uint16_t* x, const float* w_router, const float* logit_bias,
+                        float inv_temperature, int T, int H, int E, int k_fixed, int kmax,
+                        float thr1, float thr2, int renormalize, int32_t* topk_ids,
+                        float* topk_w, int32_t* k_dev, float* mean_entropy, void* workspace,
+                        size_t workspace_bytes, int32_t* expert_counts, int32_t* expert_offsets,
+                        int32_t* sorted_assign, int32_t* inv_pos, int groups,
+                        moe_stream_t stream) {
   RouterParams p{};
   moe_status_t s = router_params(x, w_router, logit_bias, inv_temperature, T, H, E, k_fixed,
                                  kmax, thr1, thr2, renormalize, topk_ids, topk_w, k_dev,
                                  mean_entropy, workspace, workspace_bytes, &p);
   if (s != MOE_OK) return s;
+  if (groups < 0 || (groups > 0 && (E % groups != 0 || k_fixed != groups)))
+    return MOE_ERR_INVALID_ARG;
+  p.groups = groups;
   if (!expert_counts || !expert_offsets) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!sorted_assign || !inv_pos)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -687,6 +713,37 @@ extern "C" moe_status_t moe_route(const uint16_t* x, const float* w_router,
   if (s != MOE_OK) return s;
   return moe_permute(topk_ids, k_dev, T, kmax, E, expert_counts, expert_offsets, sorted_assign,
                      inv_pos, stream);
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_route(const uint16_t* x, const float* w_router,
+                                  const float* logit_bias, float inv_temperature, int T, int H,
+                                  int E, int k_fixed, int kmax, float thr1, float thr2,
+                                  int renormalize, int32_t* topk_ids, float* topk_w,
+                                  int32_t* k_dev, float* mean_entropy, void* workspace,
+                                  size_t workspace_bytes, int32_t* expert_counts,
+                                  int32_t* expert_offsets, int32_t* sorted_assign,
+                                  int32_t* inv_pos, moe_stream_t stream) {
+  return route_impl(x, w_router, logit_bias, inv_temperature, T, H, E, k_fixed, kmax, thr1, thr2,
+                    renormalize, topk_ids, topk_w, k_dev, mean_entropy, workspace,
+                    workspace_bytes, expert_counts, expert_offsets, sorted_assign, inv_pos, 0,
+                    stream);
+}
+
+extern "C" moe_status_t moe_route_grouped(const uint16_t* x, const float* w_router,
+                                          const float* logit_bias, float inv_temperature, int T,
+                                          int H, int E, int n_groups, int kmax, int renormalize,
+                                          int32_t* topk_ids, float* topk_w, int32_t* k_dev,
+                                          float* mean_entropy, void* workspace,
+                                          size_t workspace_bytes, int32_t* expert_counts,
+                                          int32_t* expert_offsets, int32_t* sorted_assign,
+                                          int32_t* inv_pos, moe_stream_t stream) {
+  if (n_groups < 1) return MOE_ERR_INVALID_ARG;
+  return route_impl(x, w_router, logit_bias, inv_temperature, T, H, E, n_groups, kmax, 1.2f,
+                    2.5f, renormalize, topk_ids, topk_w, k_dev, mean_entropy, workspace,
+                    workspace_bytes, expert_counts, expert_offsets, sorted_assign, inv_pos,
+                    n_groups, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -776,6 +833,7 @@ extern "C" moe_status_t moe_router_topk_noalloc(const uint16_t* x, const float* 
   p.thr2 = thr2;
   p.renorm = renormalize ? 1 : 0;
   p.smem_stage = 0;
+  p.groups = 0;
   p.ids = topk_ids;
   p.topw = topk_w;
   p.k_dev = k_dev;

@@ -63,13 +63,15 @@ class MoELayer:
     the environment variable MOE_GB300_FUSE_GATE_UP, on unless "0") packs
     gate and up once here; unfused layers run two RAW products plus the
     separate activation.  ``path`` forces a kernel family for the products.
+    ``groups`` > 0 routes each token to the best expert of each of ``groups``
+    groups of consecutive expert ids (k_fixed must equal it).
     """
 
     def __init__(self, router_w: torch.Tensor, logit_bias: Optional[torch.Tensor], gate: QTensor,
                  up: QTensor, down: QTensor, k_fixed: int, kmax: Optional[int] = None,
                  inv_temperature: float = 1.0, renormalize: bool = True,
                  thresholds=(1.2, 2.5), fuse_gate_up: Optional[bool] = None,
-                 path: int = PATH_AUTO, free_sources: bool = False):
+                 path: int = PATH_AUTO, free_sources: bool = False, groups: int = 0):
         self.device = router_w.device
         self.router_w = router_w.contiguous()
         self.logit_bias = None if logit_bias is None else logit_bias.contiguous()
@@ -82,6 +84,9 @@ class MoELayer:
         self.renormalize = renormalize
         self.thr = tuple(float(t) for t in thresholds)
         self.path = path
+        self.groups = int(groups)
+        if self.groups > 0 and (self.E % self.groups or k_fixed != self.groups):
+            raise ValueError("group-limited routing needs k_fixed == groups dividing E")
         self.down = down
         if fuse_gate_up is None:
             fuse_gate_up = os.environ.get(FUSE_ENV, "1") != "0"
@@ -176,10 +181,16 @@ class MoELayer:
         it = self.inv_temperature if inv_temperature is None else float(inv_temperature)
         # router, top-k and the expert grouping (one launch for small batches)
         ev = _Timer(events, "route")
-        B.moe_route(x, self.router_w, self.logit_bias, it, self.k_fixed, self.kmax, self.thr[0],
-                    self.thr[1], self.renormalize, b["topk_ids"], b["topk_w"], b["k_dev"],
-                    b["mean_entropy"], b["ws"], b["counts"], b["offsets"], b["sorted"],
-                    b["inv_pos"])
+        if self.groups > 0:
+            B.moe_route_grouped(x, self.router_w, self.logit_bias, it, self.groups, self.kmax,
+                                self.renormalize, b["topk_ids"], b["topk_w"], b["k_dev"],
+                                b["mean_entropy"], b["ws"], b["counts"], b["offsets"],
+                                b["sorted"], b["inv_pos"])
+        else:
+            B.moe_route(x, self.router_w, self.logit_bias, it, self.k_fixed, self.kmax,
+                        self.thr[0], self.thr[1], self.renormalize, b["topk_ids"], b["topk_w"],
+                        b["k_dev"], b["mean_entropy"], b["ws"], b["counts"], b["offsets"],
+                        b["sorted"], b["inv_pos"])
         ev.stop()
         # tensor cores: token rows copied once into expert order, so every
         # tile loads contiguous rows; the GEMV reads x through sorted_assign

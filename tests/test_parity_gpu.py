@@ -190,3 +190,61 @@ def test_bounded_wait_reports_timeout_and_context_stays_usable(cuda_lib):
     ref = oracle.moe_forward(x_bits, layer_np)
     assert rel_l2(out, ref.out) <= 5e-3
     assert cuda_lib.moe_get_device_error() == 0
+
+
+@pytest.mark.parametrize("E,G,T,renorm,bias", [
+    (64, 4, 1, True, False),      # the pages' 4 groups of 16 experts, one decode token
+    (64, 4, 37, True, True),      # two token groups
+    (48, 8, 700, False, True),    # 22 token groups (4-CTA cluster router), raw softmax weights
+    (16, 16, 9, True, False),     # one expert per group: every expert, in logit order
+])
+def test_group_limited_routing_matches_oracle(cuda_lib, E, G, T, renorm, bias):
+    """Group-limited routing (page A section 1.1): ids and grouping bit for
+    bit, weights to fp32 rounding, against the oracle's per-group argmax."""
+    rng = np.random.default_rng(E * 7 + T)
+    H = 256
+    rw = rng.normal(0, 0.05, (E, H)).astype(np.float32)
+    rw[5] = rw[2]                 # an exact tie inside the first group
+    lb = rng.normal(0, 0.5, E).astype(np.float32) if bias else None
+    x_bits = workloads.normal_bf16(3, 11, (T, H), 1.0)
+    ref = oracle.route(x_bits, rw, lb, 0.8, G, G, renorm, groups=G)
+    perm = oracle.permute(ref.ids, G, E)
+    d = dev()
+    x = cuda_lib.bf16_from_bits(x_bits, d)
+    w = torch.from_numpy(rw).to(d)
+    b = None if lb is None else torch.from_numpy(lb).to(d)
+    ids = torch.empty((T, G), dtype=torch.int32, device=d)
+    tw = torch.empty((T, G), dtype=torch.float32, device=d)
+    kd = torch.empty(1, dtype=torch.int32, device=d)
+    me = torch.empty(1, dtype=torch.float32, device=d)
+    ws = torch.empty(cuda_lib.moe_router_workspace_size(T), dtype=torch.uint8, device=d)
+    cnt = torch.empty(E, dtype=torch.int32, device=d)
+    off = torch.empty(E + 1, dtype=torch.int32, device=d)
+    srt = torch.empty(T * G, dtype=torch.int32, device=d)
+    inv = torch.empty(T * G, dtype=torch.int32, device=d)
+    cuda_lib.moe_route_grouped(x, w, b, 0.8, G, G, renorm, ids, tw, kd, me, ws, cnt, off, srt, inv)
+    torch.cuda.synchronize()
+    assert int(kd.item()) == G
+    assert np.array_equal(to_np(ids), ref.ids)
+    assert np.allclose(to_np(tw), ref.weights, rtol=1e-6, atol=1e-7)
+    assert np.array_equal(to_np(cnt), perm.counts)
+    assert np.array_equal(to_np(off), perm.offsets)
+    assert np.array_equal(to_np(srt), perm.sorted_assign)
+    assert np.array_equal(to_np(inv), perm.inv_pos)
+    assert cuda_lib.moe_get_device_error() == 0
+
+
+def test_group_limited_layer_matches_oracle(cuda_lib):
+    """A whole layer with group-limited routing (4 groups of 16 experts, one
+    expert each) against the oracle's forward with the same routing rule."""
+    cfg = workloads.CONFIGS["tiny"].scaled(E=16, k=4)
+    layer_np = workloads.make_layer(cfg)
+    x_bits = workloads.make_tokens(cfg)
+    layer = cuda_lib.MoELayer.from_workload(layer_np, dev(), groups=4)
+    out = to_np(layer(cuda_lib.bf16_from_bits(x_bits, dev())))
+    ref_r = oracle.route(x_bits, layer_np.router_w, None, 1.0, 4, 4, True, groups=4)
+    ids = to_np(layer.buffers(cfg.T)["topk_ids"])
+    assert np.array_equal(ids, ref_r.ids)
+    ref = oracle.moe_forward(x_bits, layer_np, routing=ref_r)
+    assert_layer_close(out, ref.out, "group-limited tiny layer")
+    assert cuda_lib.moe_get_device_error() == 0

@@ -60,6 +60,11 @@ def parse_args(argv=None):
     p.add_argument("--cpu-sample", type=int, default=0, help="oracle sample size (calls/tokens)")
     p.add_argument("--path", default="auto", choices=["auto", "gemv", "tc", "tc_small"],
                    help="kernel family for the two quantized products")
+    p.add_argument("--layers", type=int, default=1,
+                   help="layers chained per call in the timed graph (each layer's output is "
+                        "the next one's input; value counts layer-calls)")
+    p.add_argument("--groups", type=int, default=0,
+                   help="group-limited routing: best expert of each of G groups (k = G)")
     p.add_argument("--experts", type=int, default=0,
                    help="smaller expert pool (same per-call work; for profiling captures)")
     return p.parse_args(argv)
@@ -272,7 +277,8 @@ def run_ours(args):
     layer_np = workloads.make_layer(cfg)
     path = {"auto": moe.PATH_AUTO, "gemv": moe.PATH_GEMV, "tc": moe.PATH_TC,
             "tc_small": moe.PATH_TC_SMALL}[args.path]
-    layer = moe.MoELayer.from_workload(layer_np, dev, free_sources=True, path=path)
+    layer = moe.MoELayer.from_workload(layer_np, dev, free_sources=True, path=path,
+                                       groups=args.groups)
     T = cfg.T
     # one step = every layer call of the workload: 256 single-token calls for
     # batch-1 decode, one call per activation batch otherwise (the entropy
@@ -285,10 +291,22 @@ def run_ours(args):
     out_dev = torch.empty((calls * T, cfg.H), dtype=torch.bfloat16, device=dev)
     temps = [cfg.inv_temperature(c // cfg.calls) for c in range(calls)]
 
+    nl = max(1, args.layers)
+    chain = [torch.empty((T, cfg.H), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+
     def step(events=None):
         for c in range(calls):
-            layer.forward(x_dev[c * T:(c + 1) * T], out=out_dev[c * T:(c + 1) * T],
-                          inv_temperature=temps[c], events=events)
+            if nl == 1 or events is not None:
+                layer.forward(x_dev[c * T:(c + 1) * T], out=out_dev[c * T:(c + 1) * T],
+                              inv_temperature=temps[c], events=events)
+                continue
+            # nl layers in a row: layer l reads layer l-1's output (the same
+            # weights serve every layer; routing follows each layer's input)
+            xin = x_dev[c * T:(c + 1) * T]
+            for li in range(nl):
+                dst = out_dev[c * T:(c + 1) * T] if li == nl - 1 else chain[li % 2]
+                layer.forward(xin, out=dst, inv_temperature=temps[c])
+                xin = dst
 
     # eager warm-up (sets kernel attributes), then capture one step in a graph
     step()
@@ -327,7 +345,7 @@ def run_ours(args):
     ms = e0.elapsed_time(e1) / args.steps
     ms = max_over_ranks(ms, world, dev)
     tokens_per_step = calls * T
-    value = tokens_per_step * world / (ms / 1000.0)
+    value = tokens_per_step * nl * world / (ms / 1000.0)  # layer-calls: tokens x layers
     clocks = clk.summary()
 
     # per-kernel durations: the same calls launched eagerly with CUDA events
@@ -413,7 +431,7 @@ def run_ours(args):
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": f"u{cfg.bits} affine weights x bf16 tokens, f32 accumulate",
-        "data": "synthetic", "config": workload_config(cfg),
+        "data": "synthetic", "config": dict(workload_config(cfg), layers=nl, groups=args.groups),
         "roofline": ({"bound": "tensor", "achieved": gu_tflops, "peak": peaks["bf16_tflops"],
                       "unit": "TFLOP/s", "frac": gu_tflops / peaks["bf16_tflops"],
                       "frac_of_sustained": gu_tflops / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]),
@@ -427,16 +445,16 @@ def run_ours(args):
         "kernels": {"gate_up_us": kt["gate_up"] * 1e3, "gate_up_gbs": gu_gbs,
                     "gate_up_tflops": gu_tflops, "down_tflops": dn_tflops,
                     "down_us": kt["down"] * 1e3, "down_gbs": dn_gbs,
-                    "layer_us_per_call": ms * 1e3 / calls,
-                    "layer_gbs": (gu_step_bytes + dn_step_bytes) / (ms * 1e-3) / 1e9,
-                    "layer_tflops": (gu_step_flops + dn_step_flops) / (ms * 1e-3) / 1e12,
+                    "layer_us_per_call": ms * 1e3 / (calls * nl),
+                    "layer_gbs": (gu_step_bytes + dn_step_bytes) * nl / (ms * 1e-3) / 1e9,
+                    "layer_tflops": (gu_step_flops + dn_step_flops) * nl / (ms * 1e-3) / 1e12,
                     "active_experts_and_k_per_call": sorted(set(per_call)),
                     "expert_counts_last_call": count_stats,
                     "per_kernel_us": {k: v * 1e3 for k, v in kt.items()}},
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                    "reasons": clocks["reasons"], "samples": clocks["samples"]},
         "e2e": e2e,
-        "gpu_launches": layer.launches_per_call(T) * calls * args.steps,
+        "gpu_launches": layer.launches_per_call(T) * calls * nl * args.steps,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # the oracle as it stands, repeated on the same bounded sample until

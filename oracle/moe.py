@@ -12,7 +12,7 @@ from . import _build
 __all__ = [
     "router_logits", "softmax_entropy", "batch_mean_entropy", "entropy_k", "topk_ids",
     "routing_weights", "group_top1_ids", "route", "Routing", "permute", "Permutation", "unpack_codes",
-    "dequant", "QDesc", "can_fuse", "pack_gate_up", "qmm_raw", "silu", "swiglu",
+    "dequant", "DROPPED", "QDesc", "can_fuse", "pack_gate_up", "qmm_raw", "silu", "swiglu",
     "moe_forward", "Forward", "dense_masked_forward", "bf16_to_f64", "ENTROPY_THRESHOLDS",
 ]
 
@@ -180,19 +180,42 @@ class Permutation:
     counts: np.ndarray         # int32 [E]
     offsets: np.ndarray        # int32 [E+1]
     sorted_assign: np.ndarray  # int32 [T*k] flat assignment a = t*kmax + j, grouped by expert
-    inv_pos: np.ndarray        # int32 [T*kmax]: position of a in sorted_assign, -1 if j >= k
+    inv_pos: np.ndarray        # int32 [T*kmax]: position of a in sorted_assign, -1 if j >= k,
+                               # DROPPED if the expert's capacity turned it away
 
 
-def permute(ids: np.ndarray, k: int, E: int) -> Permutation:
-    """Stable sort of the assignments (t, j), j < k, by expert id."""
+# inv_pos of an assignment dropped by an expert's capacity
+DROPPED = -2
+
+
+def permute(ids: np.ndarray, k: int, E: int, capacity: Optional[int] = None) -> Permutation:
+    """Stable sort of the assignments (t, j), j < k, by expert id.
+
+    capacity C (page [B] sections 4.3 and 5.2, expert_capacity): an expert
+    takes at most C assignments per batch, those of the lowest a = t*kmax + j
+    (the first C of its stable group); the rest are dropped, contribute
+    nothing to the output, and the kept weights stay as they are."""
     T, kmax = ids.shape
     flat = (np.arange(T)[:, None] * kmax + np.arange(k)[None, :]).ravel()
     experts = ids[:, :k].ravel().astype(np.int64)
     order = np.argsort(experts, kind="stable")
-    sorted_assign = flat[order].astype(np.int32)
-    counts = np.bincount(experts, minlength=E).astype(np.int32)
-    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    grouped = flat[order].astype(np.int32)
+    full_counts = np.bincount(experts, minlength=E).astype(np.int32)
     inv_pos = np.full(T * kmax, -1, dtype=np.int32)
+    if capacity is None:
+        counts = full_counts
+        sorted_assign = grouped
+    else:
+        assert capacity >= 0
+        counts = np.minimum(full_counts, capacity).astype(np.int32)
+        starts = np.concatenate([[0], np.cumsum(full_counts)])
+        keep = []
+        for e in range(E):
+            seg = grouped[starts[e]:starts[e + 1]]
+            keep.append(seg[:capacity])
+            inv_pos[seg[capacity:]] = DROPPED
+        sorted_assign = (np.concatenate(keep) if keep else grouped[:0]).astype(np.int32)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     inv_pos[sorted_assign] = np.arange(len(sorted_assign), dtype=np.int32)
     return Permutation(counts, offsets, sorted_assign, inv_pos)
 
@@ -291,7 +314,8 @@ class Forward:
 
 
 def moe_forward(x_bits, layer, k_fixed=None, kmax=None, inv_temperature=None, renormalize=True,
-                tokens=None, keep_intermediates=True, routing: Optional[Routing] = None) -> Forward:
+                tokens=None, keep_intermediates=True, routing: Optional[Routing] = None,
+                capacity: Optional[int] = None) -> Forward:
     """Whole-layer forward.  `layer` is a workloads.LayerInputs (gate and up
     are fused here with pack_gate_up).  `tokens` restricts the expert math to
     a subset of token indices (routing always covers the whole batch, since
@@ -309,7 +333,7 @@ def moe_forward(x_bits, layer, k_fixed=None, kmax=None, inv_temperature=None, re
     T, H = x_bits.shape
     I, E, bits = cfg.I, cfg.E, cfg.bits
     k = routing.k
-    perm = permute(routing.ids, k, E)
+    perm = permute(routing.ids, k, E, capacity)
     want = np.ones(T, dtype=bool) if tokens is None else np.isin(np.arange(T), tokens)
     A = len(perm.sorted_assign)
     h_all = np.full((A, I), np.nan) if keep_intermediates else None
@@ -335,7 +359,10 @@ def moe_forward(x_bits, layer, k_fixed=None, kmax=None, inv_temperature=None, re
     for t in np.nonzero(want)[0]:
         acc = np.zeros(H)
         for j in range(k):
-            acc = acc + routing.weights[t, j] * y_all[perm.inv_pos[t * kmax + j]]
+            r = perm.inv_pos[t * kmax + j]
+            if r == DROPPED:
+                continue
+            acc = acc + routing.weights[t, j] * y_all[r]
         out[t] = acc
     return Forward(routing, perm, out, h_all, y_all if keep_intermediates else None,
                    np.nonzero(want)[0])

@@ -250,6 +250,58 @@ def test_permute_brute_force(T, k, kmax, E):
                 assert p.inv_pos[a] == -1
 
 
+@pytest.mark.parametrize("C", [0, 1, 3, 1000])
+def test_permute_capacity_brute_force(C):
+    """Expert capacity: each expert keeps its C lowest assignments a =
+    t*kmax + j; the rest are marked dropped.  C at least the largest count
+    is the plain permutation; C = 0 drops everything."""
+    rng = np.random.default_rng(70 + C)
+    T, k, kmax, E = 40, 3, 4, 6
+    ids = np.full((T, kmax), -1, np.int32)
+    for t in range(T):
+        ids[t, :k] = rng.choice(E, size=k, replace=False)
+    p = oracle.permute(ids, k, E, capacity=C)
+    expect, dropped = [], set()
+    for e in range(E):
+        mine = [t * kmax + j for t in range(T) for j in range(k) if ids[t, j] == e]
+        expect += mine[:C]
+        dropped |= set(mine[C:])
+    assert list(p.sorted_assign) == expect
+    assert list(p.counts) == [min(C, int((ids[:, :k] == e).sum())) for e in range(E)]
+    for t in range(T):
+        for j in range(kmax):
+            a = t * kmax + j
+            if j >= k:
+                assert p.inv_pos[a] == -1
+            elif a in dropped:
+                assert p.inv_pos[a] == oracle.DROPPED
+            else:
+                assert p.sorted_assign[p.inv_pos[a]] == a
+    if C >= T:
+        plain = oracle.permute(ids, k, E)
+        assert np.array_equal(p.sorted_assign, plain.sorted_assign)
+        assert np.array_equal(p.inv_pos, plain.inv_pos)
+
+
+def test_capacity_zero_gives_zero_output_and_large_capacity_changes_nothing():
+    cfg = workloads.CONFIGS["tiny"]
+    layer = workloads.make_layer(cfg)
+    x = workloads.make_tokens(cfg)
+    plain = oracle.moe_forward(x, layer)
+    assert np.array_equal(oracle.moe_forward(x, layer, capacity=cfg.T).out, plain.out)
+    assert np.array_equal(oracle.moe_forward(x, layer, capacity=0).out, np.zeros_like(plain.out))
+    # a capped layer equals the dense masked sum over the kept (token, expert) pairs only
+    fw = oracle.moe_forward(x, layer, capacity=2)
+    kept = oracle.Routing(fw.routing.logits, fw.routing.ids.copy(), fw.routing.weights.copy(),
+                          fw.routing.k, fw.routing.mean_entropy, fw.routing.token_entropy)
+    for t in range(cfg.T):
+        for j in range(fw.routing.k):
+            if fw.perm.inv_pos[t * cfg.slots + j] == oracle.DROPPED:
+                kept.weights[t, j] = 0.0
+    dense = oracle.dense_masked_forward(x, layer, kept)
+    np.testing.assert_allclose(fw.out, dense, rtol=1e-9, atol=1e-12)
+
+
 # ---------------------------------------------------------------- dequant ---
 
 def test_dequant_extreme_codes():

@@ -94,6 +94,9 @@ int moe_set_launch_overlap(int enable);
 enum { MOE_PATH_FLAG_WEIGHTS_EARLY = 0x100 };
 /* Device error word bits (moe_get_device_error). */
 enum { MOE_DEVERR_BAD_EXPERT = 1u, MOE_DEVERR_TIMEOUT = 2u, MOE_DEVERR_BAD_INDEX = 4u };
+/* inv_pos value of an assignment that its expert's capacity turned away
+ * (moe_permute_capped); moe_combine skips it. */
+enum { MOE_DROPPED = -2 };
 
 typedef void* moe_stream_t;
 
@@ -237,6 +240,24 @@ moe_status_t moe_permute(const int32_t* topk_ids, const int32_t* k_dev, int T, i
                          int32_t* sorted_assign, int32_t* inv_pos, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * moe_permute_capped -- moe_permute with an expert capacity.
+ *
+ * Page [B], sections 4.3 and 5.2 (expert_capacity: a limit on the tokens an
+ * expert takes per batch).  Each expert keeps at most `capacity` of its
+ * assignments, those of the lowest a = t*kmax + j, in the same stable order
+ * as moe_permute; the others get inv_pos = MOE_DROPPED, contribute nothing
+ * to the combine, and the kept weights are not renormalised.
+ * expert_counts and expert_offsets describe the kept assignments only;
+ * sorted_assign entries past offsets[E] (up to T*k) hold 0, a valid
+ * assignment, so consumers of T*k sorted rows stay in bounds.
+ * capacity >= 0 (0 drops everything).
+ * ---------------------------------------------------------------------- */
+moe_status_t moe_permute_capped(const int32_t* topk_ids, const int32_t* k_dev, int T, int kmax,
+                                int E, int capacity, int32_t* expert_counts,
+                                int32_t* expert_offsets, int32_t* sorted_assign,
+                                int32_t* inv_pos, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * moe_route -- moe_router_topk followed by moe_permute, as one call.
  *
  * The two calls above in sequence (their passages), with their arguments and
@@ -349,7 +370,8 @@ moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* expert_offs
  *
  * Page [A], section 4.2: y[t] = sum_k w_k * expert_out_k.  Here
  * out[t, m] = bf16_rne( sum_{j<k} topk_w[t, j] * y[inv_pos[t*kmax+j], m] ),
- * accumulated in fp32 in ascending j.
+ * accumulated in fp32 in ascending j.  A slot with inv_pos = MOE_DROPPED
+ * (expert capacity) is skipped.
  *
  * y        fp32 [T*kmax, H] (sorted order).
  * out      out: bf16 [T, H].

@@ -15,13 +15,14 @@ EPILOGUE_RAW, EPILOGUE_SWIGLU = 0, 1
 PATH_AUTO, PATH_GEMV, PATH_TC, PATH_TC_SMALL = 0, 1, 2, 3
 PATH_FLAG_WEIGHTS_EARLY = 0x100  # moe_down_qmm: offsets/weights read before the wait
 DEVERR_BAD_EXPERT, DEVERR_TIMEOUT, DEVERR_BAD_INDEX = 1, 2, 4
+DROPPED = -2  # inv_pos of an assignment dropped by its expert's capacity
 QMODE_AFFINE = 0
 SCALE_F16, SCALE_BF16, SCALE_F32 = 0, 1, 2
 
 # every symbol the header declares
 EXPORTS = (
     "moe_status_string", "moe_abi_version", "moe_set_launch_overlap", "moe_pack_gate_up", "moe_router_workspace_size",
-    "moe_router_topk", "moe_router_topk_noalloc", "moe_route", "moe_route_grouped", "moe_permute", "moe_permute_rows", "moe_gate_up_qmm", "moe_down_qmm", "moe_combine",
+    "moe_router_topk", "moe_router_topk_noalloc", "moe_route", "moe_route_grouped", "moe_permute", "moe_permute_capped", "moe_permute_rows", "moe_gate_up_qmm", "moe_down_qmm", "moe_combine",
     "moe_swiglu", "moe_get_device_error", "moe_selftest_wait_timeout",
 )
 
@@ -65,6 +66,7 @@ def _declare(lib):
     lib.moe_route.argtypes = [vp, vp, vp, f32, i32, i32, i32, i32, i32, f32, f32, i32, vp, vp, vp,
                               vp, vp, sz, vp, vp, vp, vp, vp]
     lib.moe_permute.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
+    lib.moe_permute_capped.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]
     lib.moe_route_grouped.argtypes = [vp, vp, vp, f32, i32, i32, i32, i32, i32, i32, vp, vp, vp,
                                       vp, vp, sz, vp, vp, vp, vp, vp]
     lib.moe_permute_rows.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
@@ -77,7 +79,7 @@ def _declare(lib):
     lib.moe_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32, vp]
     lib.moe_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
     for name in ("moe_pack_gate_up", "moe_router_topk", "moe_router_topk_noalloc", "moe_route",
-                 "moe_route_grouped",
+                 "moe_route_grouped", "moe_permute_capped",
                  "moe_permute", "moe_permute_rows", "moe_gate_up_qmm",
                  "moe_down_qmm", "moe_combine", "moe_swiglu", "moe_get_device_error",
                  "moe_selftest_wait_timeout"):

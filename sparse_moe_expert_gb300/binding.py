@@ -163,6 +163,19 @@ def moe_permute(topk_ids, k_dev, E: int, expert_counts=None, expert_offsets=None
     return expert_counts, expert_offsets, sorted_assign, inv_pos
 
 
+def moe_permute_capped(topk_ids, k_dev, E: int, capacity: int, expert_counts, expert_offsets,
+                       sorted_assign, inv_pos, stream=None):
+    """moe_permute keeping at most `capacity` assignments per expert (the
+    lowest a = t*kmax + j); dropped ones get inv_pos = DROPPED."""
+    _need(topk_ids, torch.int32, "topk_ids")
+    T, kmax = topk_ids.shape
+    st = lib().moe_permute_capped(_p(topk_ids), _p(k_dev), T, kmax, E, int(capacity),
+                                  _p(expert_counts), _p(expert_offsets), _p(sorted_assign),
+                                  _p(inv_pos), _stream(stream))
+    check("moe_permute_capped", st)
+    return expert_counts, expert_offsets, sorted_assign, inv_pos
+
+
 def moe_permute_rows(x, sorted_assign, k_dev, kmax: int, x_sorted=None, stream=None):
     """-> x_sorted bf16 [T*kmax, H]: row r = x[sorted_assign[r] // kmax] for r < T*k."""
     _need(x, torch.bfloat16, "x")

@@ -31,7 +31,10 @@ __global__ void __launch_bounds__(kEwThreads) combine_kernel(const float* __rest
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
       const int r = __ldg(inv_pos + (int64_t)t * kmax + j);
-      if (r < 0) { raise_device_error(err, MOE_DEVERR_BAD_INDEX); continue; }
+      if (r < 0) {  // dropped by its expert's capacity: no contribution
+        if (r != MOE_DROPPED) raise_device_error(err, MOE_DEVERR_BAD_INDEX);
+        continue;
+      }
       const float w = __ldg(topk_w + (int64_t)t * kmax + j);
       const float4 yv = __ldg(reinterpret_cast<const float4*>(y + (int64_t)r * H) + v);
       acc.x = fmaf(w, yv.x, acc.x);

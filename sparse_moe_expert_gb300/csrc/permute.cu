@@ -33,6 +33,7 @@ struct PermuteParams {
   int32_t* offsets;
   int32_t* sorted;
   int32_t* inv_pos;
+  int capacity;  // most assignments an expert keeps (INT32_MAX: no limit)
   unsigned int* err;
 };
 
@@ -97,9 +98,9 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(PermuteParams 
     __syncthreads();
   }
 
-  // exclusive scan of cnt -> off (E <= 1024 = blockDim)
+  // exclusive scan of the kept counts -> off (E <= 1024 = blockDim)
   {
-    int v = tid < E ? cnt[tid] : 0;
+    int v = tid < E ? min(cnt[tid], p.capacity) : 0;
     int incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -152,9 +153,15 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(PermuteParams 
     }
     __syncthreads();
     if (e >= 0) {
-      int pos = off[e] + run[e] + wcnt[warp * E + e] + rank_in_warp;
-      p.sorted[pos] = (int32_t)a;
-      p.inv_pos[a] = pos;
+      // rank of a among its expert's assignments, in ascending a
+      const int rank = run[e] + wcnt[warp * E + e] + rank_in_warp;
+      if (rank < p.capacity) {
+        const int pos = off[e] + rank;
+        p.sorted[pos] = (int32_t)a;
+        p.inv_pos[a] = pos;
+      } else {
+        p.inv_pos[a] = MOE_DROPPED;  // the expert's capacity is full
+      }
     }
     __syncthreads();
     for (int x = tid; x < E; x += kPermuteThreads) {
@@ -163,6 +170,13 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(PermuteParams 
     }
     __syncthreads();
   }
+  // with a capacity, sorted rows past the kept total hold assignment 0 (a
+  // valid one), so consumers of T*k sorted rows stay in bounds
+  if (p.capacity != INT32_MAX && blockIdx.x == 0) {
+    int kept = 0;
+    for (int x = 0; x < E; ++x) kept += min(cnt[x], p.capacity);
+    for (int i = kept + tid; i < p.T * k; i += kPermuteThreads) p.sorted[i] = 0;
+  }
 }
 
 }  // namespace
@@ -170,10 +184,11 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(PermuteParams 
 
 using namespace moe;
 
-extern "C" moe_status_t moe_permute(const int32_t* topk_ids, const int32_t* k_dev, int T,
-                                    int kmax, int E, int32_t* expert_counts,
-                                    int32_t* expert_offsets, int32_t* sorted_assign,
-                                    int32_t* inv_pos, moe_stream_t stream) {
+namespace {
+
+moe_status_t permute_impl(const int32_t* topk_ids, const int32_t* k_dev, int T, int kmax, int E,
+                          int capacity, int32_t* expert_counts, int32_t* expert_offsets,
+                          int32_t* sorted_assign, int32_t* inv_pos, moe_stream_t stream) {
   using namespace moe_host;
   if (T < 0 || E < 1 || E > 1024 || kmax < 1 || kmax > 16) return MOE_ERR_INVALID_ARG;
   if ((int64_t)T * kmax > (1 << 24)) return MOE_ERR_INVALID_ARG;
@@ -189,6 +204,7 @@ extern "C" moe_status_t moe_permute(const int32_t* topk_ids, const int32_t* k_de
   p.offsets = expert_offsets;
   p.sorted = sorted_assign;
   p.inv_pos = inv_pos;
+  p.capacity = capacity;
   p.err = device_error_word();
   size_t smem = (size_t)(4 + kPermuteWarps) * E * sizeof(int);
   if (smem > 48 * 1024) {
@@ -205,6 +221,26 @@ extern "C" moe_status_t moe_permute(const int32_t* topk_ids, const int32_t* k_de
   const int nb = slots > 0 ? (slots + per_block - 1) / per_block : 1;
   return launch(permute_kernel, nb, kPermuteThreads, smem, reinterpret_cast<cudaStream_t>(stream),
                 p, per_block);
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_permute(const int32_t* topk_ids, const int32_t* k_dev, int T,
+                                    int kmax, int E, int32_t* expert_counts,
+                                    int32_t* expert_offsets, int32_t* sorted_assign,
+                                    int32_t* inv_pos, moe_stream_t stream) {
+  return permute_impl(topk_ids, k_dev, T, kmax, E, INT32_MAX, expert_counts, expert_offsets,
+                      sorted_assign, inv_pos, stream);
+}
+
+extern "C" moe_status_t moe_permute_capped(const int32_t* topk_ids, const int32_t* k_dev, int T,
+                                           int kmax, int E, int capacity,
+                                           int32_t* expert_counts, int32_t* expert_offsets,
+                                           int32_t* sorted_assign, int32_t* inv_pos,
+                                           moe_stream_t stream) {
+  if (capacity < 0) return MOE_ERR_INVALID_ARG;
+  return permute_impl(topk_ids, k_dev, T, kmax, E, capacity, expert_counts, expert_offsets,
+                      sorted_assign, inv_pos, stream);
 }
 
 // ---- token rows in expert order ------------------------------------------

@@ -64,14 +64,17 @@ class MoELayer:
     gate and up once here; unfused layers run two RAW products plus the
     separate activation.  ``path`` forces a kernel family for the products.
     ``groups`` > 0 routes each token to the best expert of each of ``groups``
-    groups of consecutive expert ids (k_fixed must equal it).
+    groups of consecutive expert ids (k_fixed must equal it).  ``capacity``
+    limits the assignments each expert takes per call (the lowest token
+    slots stay; the others are dropped).
     """
 
     def __init__(self, router_w: torch.Tensor, logit_bias: Optional[torch.Tensor], gate: QTensor,
                  up: QTensor, down: QTensor, k_fixed: int, kmax: Optional[int] = None,
                  inv_temperature: float = 1.0, renormalize: bool = True,
                  thresholds=(1.2, 2.5), fuse_gate_up: Optional[bool] = None,
-                 path: int = PATH_AUTO, free_sources: bool = False, groups: int = 0):
+                 path: int = PATH_AUTO, free_sources: bool = False, groups: int = 0,
+                 capacity: Optional[int] = None):
         self.device = router_w.device
         self.router_w = router_w.contiguous()
         self.logit_bias = None if logit_bias is None else logit_bias.contiguous()
@@ -85,6 +88,7 @@ class MoELayer:
         self.thr = tuple(float(t) for t in thresholds)
         self.path = path
         self.groups = int(groups)
+        self.capacity = None if capacity is None else int(capacity)
         if self.groups > 0 and (self.E % self.groups or k_fixed != self.groups):
             raise ValueError("group-limited routing needs k_fixed == groups dividing E")
         self.down = down
@@ -181,7 +185,14 @@ class MoELayer:
         it = self.inv_temperature if inv_temperature is None else float(inv_temperature)
         # router, top-k and the expert grouping (one launch for small batches)
         ev = _Timer(events, "route")
-        if self.groups > 0:
+        if self.capacity is not None:
+            # router, then the grouping with each expert's capacity
+            B.moe_router_topk(x, self.router_w, self.logit_bias, it, self.k_fixed, self.kmax,
+                              self.thr[0], self.thr[1], self.renormalize, b["topk_ids"],
+                              b["topk_w"], b["k_dev"], b["mean_entropy"], b["ws"])
+            B.moe_permute_capped(b["topk_ids"], b["k_dev"], self.E, self.capacity, b["counts"],
+                                 b["offsets"], b["sorted"], b["inv_pos"])
+        elif self.groups > 0:
             B.moe_route_grouped(x, self.router_w, self.logit_bias, it, self.groups, self.kmax,
                                 self.renormalize, b["topk_ids"], b["topk_w"], b["k_dev"],
                                 b["mean_entropy"], b["ws"], b["counts"], b["offsets"],

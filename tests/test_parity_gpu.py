@@ -248,3 +248,55 @@ def test_group_limited_layer_matches_oracle(cuda_lib):
     ref = oracle.moe_forward(x_bits, layer_np, routing=ref_r)
     assert_layer_close(out, ref.out, "group-limited tiny layer")
     assert cuda_lib.moe_get_device_error() == 0
+
+
+@pytest.mark.parametrize("T,k,kmax,E,C", [
+    (64, 4, 4, 64, 3),     # batched-decode-like: popular experts overflow
+    (700, 2, 3, 16, 40),   # several CTAs of the grouping kernel
+    (33, 3, 3, 8, 0),      # capacity 0: everything dropped
+    (20, 2, 2, 8, 1000),   # capacity above every count: plain grouping
+])
+def test_permute_capacity_matches_oracle(cuda_lib, T, k, kmax, E, C):
+    """Expert capacity: kept assignments, counts, offsets and the dropped
+    marks bit for bit against the oracle; sorted rows past the kept total
+    hold assignment 0."""
+    rng = np.random.default_rng(T * 13 + C)
+    ids_np = np.full((T, kmax), -1, np.int32)
+    for t in range(T):
+        # skewed: low ids are popular
+        ids_np[t, :k] = rng.choice(E, size=k, replace=False, p=np.arange(E, 0, -1) / (E * (E + 1) / 2))
+    ref = oracle.permute(ids_np, k, E, capacity=C)
+    d = dev()
+    ids = torch.from_numpy(ids_np).to(d)
+    kd = torch.tensor([k], dtype=torch.int32, device=d)
+    cnt = torch.empty(E, dtype=torch.int32, device=d)
+    off = torch.empty(E + 1, dtype=torch.int32, device=d)
+    srt = torch.full((T * kmax,), 12345, dtype=torch.int32, device=d)
+    inv = torch.empty(T * kmax, dtype=torch.int32, device=d)
+    cuda_lib.moe_permute_capped(ids, kd, E, C, cnt, off, srt, inv)
+    torch.cuda.synchronize()
+    kept = int(ref.offsets[-1])
+    assert np.array_equal(to_np(cnt), ref.counts)
+    assert np.array_equal(to_np(off), ref.offsets)
+    assert np.array_equal(to_np(srt)[:kept], ref.sorted_assign)
+    assert np.all(to_np(srt)[kept:T * k] == 0)
+    assert np.array_equal(to_np(inv), ref.inv_pos)
+    assert cuda_lib.moe_get_device_error() == 0
+
+
+@pytest.mark.parametrize("path", ["gemv", "tc"])
+def test_layer_with_capacity_matches_oracle(cuda_lib, path):
+    """A whole layer whose popular experts hit their capacity: dropped slots
+    contribute nothing, against the oracle's forward with the same rule."""
+    cfg = SMALL["batched_s"]
+    layer_np = workloads.make_layer(cfg)
+    x_bits = workloads.make_tokens(cfg)
+    C = 6
+    pid = cuda_lib.PATH_GEMV if path == "gemv" else cuda_lib.PATH_TC
+    layer = cuda_lib.MoELayer.from_workload(layer_np, dev(), path=pid, capacity=C)
+    out = to_np(layer(cuda_lib.bf16_from_bits(x_bits, dev())))
+    ref = oracle.moe_forward(x_bits, layer_np, capacity=C)
+    assert (ref.perm.inv_pos == oracle.DROPPED).sum() > 0   # the case drops something
+    assert np.array_equal(to_np(layer.buffers(cfg.T)["inv_pos"]), ref.perm.inv_pos)
+    assert_layer_close(out, ref.out, f"capacity {C} ({path})")
+    assert cuda_lib.moe_get_device_error() == 0

@@ -135,11 +135,14 @@ class MoELayer:
         16 when E > 256), the permute (inside the router when one group
         covers the batch, E <= 256 and T * kmax <= 512), the row permute on
         the tensor-core path, the gate_up product (or two RAW products and
-        the activation when unfused), down and combine."""
+        the activation when unfused), down and combine.  With a capacity the
+        grouping is always its own kernel."""
         group = 32 if self.E <= 256 else 16
         one_group = (T + group - 1) // group == 1
         n = 1 + (0 if one_group else 1)
-        n += 0 if (one_group and self.E <= 256 and T * self.kmax <= 512) else 1
+        fused_permute = (one_group and self.E <= 256 and T * self.kmax <= 512
+                         and self.capacity is None)
+        n += 0 if fused_permute else 1
         n += 1 if self.resolved_path(T) == PATH_TC else 0
         n += 1 if self.fused else 3
         return n + 2

@@ -532,7 +532,9 @@ __global__ void __launch_bounds__(kSvThreads, 1)
       const int r0 = lo + c * mts;
       // everyone is done with the staged values (nothing staged before the first)
       if (st_a >= 0 && !consumer_sync()) return false;
-      const int total = ngroups * mts2 * 4;
+      // a single-token pass reads only token 0's values and sums (the B
+      // fragments' other columns and xsum's second entry are never used)
+      const int total = ngroups * (ONE ? 1 : mts2) * 4;
       for (int base = 0; base < total; base += kSvConsumers * 32) {
         const int idx = base + ctid;
         const bool valid = idx < total;

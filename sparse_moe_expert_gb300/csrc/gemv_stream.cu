@@ -28,8 +28,10 @@
 //               the codes of each stage into a ring of shared-memory slots,
 //               its lanes copy the scales and biases with cp.async whose
 //               completion arrives on the slot's mbarrier;
-//   warps 0-15  consumers: warp w takes the groups j = w, w + 16 of every
-//               stage, converts the codes in registers and issues the MMAs;
+//   warps 0-15  consumers: each takes one of 16 slots of a tile's groups
+//               (128 contiguous code bytes of every stage; the warp of a
+//               slot rotates from tile to tile), converts the codes in
+//               registers and issues the MMAs;
 //               the token values are staged once per (expert, chunk) in the
 //               B-fragment order, with their group sums;
 //   warp 17     epilogue: adds the 16 consumer partials of a tile in warp
@@ -38,7 +40,7 @@
 // so the weight stream of the whole GPU is split evenly across the SMs.
 //
 // Every row is reduced in the same order whatever rows it shares a tile
-// with (a fixed group -> warp assignment, warp partials added in warp
+// with (a fixed group -> slot assignment, slot partials added in slot
 // order), so the fused gate_up product equals the separate gate and up
 // products bit for bit.  Every mbarrier wait is bounded; a wait that runs
 // out sets MOE_DEVERR_TIMEOUT, the CTA stops and the producer waits for the
@@ -602,16 +604,24 @@ __global__ void __launch_bounds__(kSvThreads, 1)
       return consumer_sync();
     };
 
-    // per-warp constants of the stage loop: groups jb .. jb + kGpw - 1 of
-    // every stage, their code offsets in a slot, the scale-row offset
-    const int jb = S::kGpw * warp;
+    // Group slots.  Logical slot wl takes the groups jb .. jb + kGpw - 1
+    // (jb = kGpw wl) of every stage of a tile and its partial sums go to
+    // reduction slot wl, so each row is summed in the same order whichever
+    // warp holds which slot.  The physical warp of a slot rotates from tile
+    // to tile: the last stage of a tile is partial when a row is not a whole
+    // number of stages (an 11008-code row fills 11 of 16 slots there, a
+    // 1536-code one 6), and the rotation spreads the idle slots over the
+    // warps.  kGpw groups are 128 bytes of a row, so slot wl's code offsets
+    // in a slot are slot 0's plus wl 1024.
     int coff[S::kGpw];
 #pragma unroll
     for (int i = 0; i < S::kGpw; ++i) {
-      const int o = (jb + i) * S::kGroupBytes + t * (S::kGroupBytes / 4);
+      const int o = i * S::kGroupBytes + t * (S::kGroupBytes / 4);
       coff[i] = (o >> 7) * 1024 + rr * 128 + ((((o >> 4) & 7) ^ rr) << 4) + (o & 15);
     }
-    const int soff = rr * S::kScaleRow + jb * 2;
+    static_assert(S::kGpw * S::kGroupBytes == 128, "a slot's groups span one 128-byte block");
+    const int last_groups = ngroups - (nck - 1) * S::kGpc;
+    const int rot_step = (last_groups + S::kGpw - 1) / S::kGpw;  // busy slots of the last stage
     // B column g of a lane: token g, or a copy of a staged token for the
     // columns past the chunk (their results are never read)
     const int bn = ONE ? 0 : min(g, mts - 1);
@@ -641,6 +651,9 @@ __global__ void __launch_bounds__(kSvThreads, 1)
         st_c = cu.c;
       }
       tr_stage += SV_CLK() - trs;
+      const int wl = (warp + u * rot_step) & (kSvConsumers - 1);
+      const int jb = S::kGpw * wl;
+      const int soff = rr * S::kScaleRow + jb * 2;
       // sums of s * P (P = 2^(e-24) sum q x) and of b * X, rows g and g + 8;
       // ONE: token 0 only, else tokens 2t and 2t + 1
       float as[4] = {0.0f, 0.0f, 0.0f, 0.0f}, ab[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -652,7 +665,7 @@ __global__ void __launch_bounds__(kSvThreads, 1)
         }
         const long long tr1 = SV_CLK();
         tr_full += tr1 - tr0;
-        const unsigned char* cst = codes + (size_t)ring.idx * kSvCodeBytes;
+        const unsigned char* cst = codes + (size_t)ring.idx * kSvCodeBytes + wl * 1024;
         const int g0 = ch * S::kGpc;
         const int nv = min(S::kGpw, ngroups - g0 - jb);  // this warp's groups in the stage
         if (nv > 0) {
@@ -767,7 +780,7 @@ __global__ void __launch_bounds__(kSvThreads, 1)
         break;
       }
       tr_red += SV_CLK() - tr2;
-      float* rd = red + ((size_t)rs.idx * kSvConsumers + warp) * mts * 16;
+      float* rd = red + ((size_t)rs.idx * kSvConsumers + wl) * mts * 16;
       const int n0 = 2 * t, n1 = 2 * t + 1;
       if (n0 < mts) {
         rd[n0 * 16 + rr] = as[0] + ab[0];
@@ -817,30 +830,46 @@ __global__ void __launch_bounds__(kSvThreads, 1)
       const int nt = min(mts, m - cu.c * mts);
       const int64_t row0 = (int64_t)act_lo[cu.a] + (int64_t)cu.c * mts;
       const float* rd = red + (size_t)rs.idx * kSvConsumers * mts * 16;
-      // lane l: tile row l & 15, consumer warps 8 (l >> 4) .. + 7 in order,
-      // then the two halves added
-      const int ri = lane & 15, wh = (lane >> 4) * 8;
-      for (int n = 0; n < nt; ++n) {
-        float v = 0.0f;
+      // lane l: token l / 4, tile rows 4 (l & 3) .. + 3; the 16 slot
+      // partials added in slot order (the same order for every row, so a
+      // row's value does not depend on the rows it shares a tile with)
+      const int n = lane >> 2, q = lane & 3;
+      float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (n < nt) {
+        const float4* r4 = reinterpret_cast<const float4*>(rd) + n * 4 + q;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) v += rd[((size_t)(wh + w) * mts + n) * 16 + ri];
-        v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
-        if (MODE == kSvSwiglu) {
-          const float up = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 8);
-          const int col = cu.rt * 8 + lane;
-          if (lane < 8 && col < p.n_out) {
-            const float hv = swiglu_f32(v, up);
-            const int64_t oi = (row0 + n) * p.n_out + col;
-            if (p.out_dtype == MOE_DTYPE_BF16)
-              static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16_rne(hv);
-            else
-              static_cast<float*>(p.out)[oi] = hv;
-          }
-        } else {
-          const int col = cu.rt * 16 + lane;
-          if (lane < 16 && col < p.n_rows)
-            static_cast<float*>(p.out)[(row0 + n) * p.n_out + col] = v;
+        for (int w = 0; w < kSvConsumers; ++w) {
+          const float4 pw = r4[(size_t)w * mts * 4];
+          v.x += pw.x;
+          v.y += pw.y;
+          v.z += pw.z;
+          v.w += pw.w;
         }
+      }
+      if (MODE == kSvSwiglu) {
+        // gate rows 0-7 in quads 0 and 1, the up rows of the same features
+        // in quads 2 and 3
+        float4 up;
+        up.x = __shfl_xor_sync(0xFFFFFFFFu, v.x, 2);
+        up.y = __shfl_xor_sync(0xFFFFFFFFu, v.y, 2);
+        up.z = __shfl_xor_sync(0xFFFFFFFFu, v.z, 2);
+        up.w = __shfl_xor_sync(0xFFFFFFFFu, v.w, 2);
+        const int col0 = cu.rt * 8 + q * 4;
+        if (n < nt && q < 2 && col0 < p.n_out) {
+          const float4 hv = make_float4(swiglu_f32(v.x, up.x), swiglu_f32(v.y, up.y),
+                                        swiglu_f32(v.z, up.z), swiglu_f32(v.w, up.w));
+          const int64_t oi = (row0 + n) * p.n_out + col0;
+          if (p.out_dtype == MOE_DTYPE_BF16)
+            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + oi) =
+                make_uint2((uint32_t)f32_to_bf16_rne(hv.x) | ((uint32_t)f32_to_bf16_rne(hv.y) << 16),
+                           (uint32_t)f32_to_bf16_rne(hv.z) | ((uint32_t)f32_to_bf16_rne(hv.w) << 16));
+          else
+            *reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi) = hv;
+        }
+      } else {
+        const int col0 = cu.rt * 16 + q * 4;
+        if (n < nt && col0 < p.n_rows)
+          *reinterpret_cast<float4*>(static_cast<float*>(p.out) + (row0 + n) * p.n_out + col0) = v;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&red_empty[rs.idx]);

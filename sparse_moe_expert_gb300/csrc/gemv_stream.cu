@@ -830,46 +830,80 @@ __global__ void __launch_bounds__(kSvThreads, 1)
       const int nt = min(mts, m - cu.c * mts);
       const int64_t row0 = (int64_t)act_lo[cu.a] + (int64_t)cu.c * mts;
       const float* rd = red + (size_t)rs.idx * kSvConsumers * mts * 16;
-      // lane l: token l / 4, tile rows 4 (l & 3) .. + 3; the 16 slot
-      // partials added in slot order (the same order for every row, so a
-      // row's value does not depend on the rows it shares a tile with)
-      const int n = lane >> 2, q = lane & 3;
-      float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      if (n < nt) {
-        const float4* r4 = reinterpret_cast<const float4*>(rd) + n * 4 + q;
+      // A row's value is (slot partials 0..7, added in order) + (slots
+      // 8..15, in order), whatever rows and tokens share its tile.
+      if (ONE) {
+        // lane l: tile row l & 15, slots 8 (l >> 4) .. + 7
+        const int ri = lane & 15, wh = (lane >> 4) * 8;
+        float v = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kSvConsumers; ++w) {
-          const float4 pw = r4[(size_t)w * mts * 4];
-          v.x += pw.x;
-          v.y += pw.y;
-          v.z += pw.z;
-          v.w += pw.w;
-        }
-      }
-      if (MODE == kSvSwiglu) {
-        // gate rows 0-7 in quads 0 and 1, the up rows of the same features
-        // in quads 2 and 3
-        float4 up;
-        up.x = __shfl_xor_sync(0xFFFFFFFFu, v.x, 2);
-        up.y = __shfl_xor_sync(0xFFFFFFFFu, v.y, 2);
-        up.z = __shfl_xor_sync(0xFFFFFFFFu, v.z, 2);
-        up.w = __shfl_xor_sync(0xFFFFFFFFu, v.w, 2);
-        const int col0 = cu.rt * 8 + q * 4;
-        if (n < nt && q < 2 && col0 < p.n_out) {
-          const float4 hv = make_float4(swiglu_f32(v.x, up.x), swiglu_f32(v.y, up.y),
-                                        swiglu_f32(v.z, up.z), swiglu_f32(v.w, up.w));
-          const int64_t oi = (row0 + n) * p.n_out + col0;
-          if (p.out_dtype == MOE_DTYPE_BF16)
-            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + oi) =
-                make_uint2((uint32_t)f32_to_bf16_rne(hv.x) | ((uint32_t)f32_to_bf16_rne(hv.y) << 16),
-                           (uint32_t)f32_to_bf16_rne(hv.z) | ((uint32_t)f32_to_bf16_rne(hv.w) << 16));
-          else
-            *reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi) = hv;
+        for (int w = 0; w < 8; ++w) v += rd[(wh + w) * 16 + ri];
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
+        if (MODE == kSvSwiglu) {
+          const float up = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 8);
+          const int col = cu.rt * 8 + lane;
+          if (lane < 8 && col < p.n_out) {
+            const float hv = swiglu_f32(v, up);
+            const int64_t oi = row0 * p.n_out + col;
+            if (p.out_dtype == MOE_DTYPE_BF16)
+              static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16_rne(hv);
+            else
+              static_cast<float*>(p.out)[oi] = hv;
+          }
+        } else {
+          const int col = cu.rt * 16 + lane;
+          if (lane < 16 && col < p.n_rows) static_cast<float*>(p.out)[row0 * p.n_out + col] = v;
         }
       } else {
-        const int col0 = cu.rt * 16 + q * 4;
-        if (n < nt && col0 < p.n_rows)
-          *reinterpret_cast<float4*>(static_cast<float*>(p.out) + (row0 + n) * p.n_out + col0) = v;
+        // lane l: token l / 4, tile rows 4 (l & 3) .. + 3
+        const int n = lane >> 2, q = lane & 3;
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (n < nt) {
+          const float4* r4 = reinterpret_cast<const float4*>(rd) + n * 4 + q;
+          float4 hi = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+          for (int w = 0; w < 8; ++w) {
+            const float4 pl = r4[(size_t)w * mts * 4], ph = r4[(size_t)(w + 8) * mts * 4];
+            v.x += pl.x;
+            v.y += pl.y;
+            v.z += pl.z;
+            v.w += pl.w;
+            hi.x += ph.x;
+            hi.y += ph.y;
+            hi.z += ph.z;
+            hi.w += ph.w;
+          }
+          v.x += hi.x;
+          v.y += hi.y;
+          v.z += hi.z;
+          v.w += hi.w;
+        }
+        if (MODE == kSvSwiglu) {
+          // gate rows 0-7 in quads 0 and 1, the up rows of the same features
+          // in quads 2 and 3
+          float4 up;
+          up.x = __shfl_xor_sync(0xFFFFFFFFu, v.x, 2);
+          up.y = __shfl_xor_sync(0xFFFFFFFFu, v.y, 2);
+          up.z = __shfl_xor_sync(0xFFFFFFFFu, v.z, 2);
+          up.w = __shfl_xor_sync(0xFFFFFFFFu, v.w, 2);
+          const int col0 = cu.rt * 8 + q * 4;
+          if (n < nt && q < 2 && col0 < p.n_out) {
+            const float4 hv = make_float4(swiglu_f32(v.x, up.x), swiglu_f32(v.y, up.y),
+                                          swiglu_f32(v.z, up.z), swiglu_f32(v.w, up.w));
+            const int64_t oi = (row0 + n) * p.n_out + col0;
+            if (p.out_dtype == MOE_DTYPE_BF16)
+              *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + oi) = make_uint2(
+                  (uint32_t)f32_to_bf16_rne(hv.x) | ((uint32_t)f32_to_bf16_rne(hv.y) << 16),
+                  (uint32_t)f32_to_bf16_rne(hv.z) | ((uint32_t)f32_to_bf16_rne(hv.w) << 16));
+            else
+              *reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi) = hv;
+          }
+        } else {
+          const int col0 = cu.rt * 16 + q * 4;
+          if (n < nt && col0 < p.n_rows)
+            *reinterpret_cast<float4*>(static_cast<float*>(p.out) + (row0 + n) * p.n_out + col0) =
+                v;
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&red_empty[rs.idx]);

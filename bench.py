@@ -392,6 +392,11 @@ def run_ours(args):
     dn_tflops = dn_step_flops * ksteps / (ktot["down"] * 1e-3) / 1e12
     path_used = layer.resolved_path(T)
     tensor_bound = path_used == moe.PATH_TC and cfg.name == "prefill"
+    kernel_label = KERNEL_NAME[path_used] + " (gate_up, SiLU*up epilogue)"
+    ks = layer.k_split(T)
+    if ks:
+        kernel_label = (f"{KERNEL_NAME[moe.PATH_GEMV]} for k < {ks}, {KERNEL_NAME[moe.PATH_TC]} "
+                        f"for k >= {ks} (gate_up, SiLU*up epilogue; both queued, gated on k)")
     kernel_src = KERNEL_SRC[path_used]
     traffic = None
     try:
@@ -435,12 +440,12 @@ def run_ours(args):
         "roofline": ({"bound": "tensor", "achieved": gu_tflops, "peak": peaks["bf16_tflops"],
                       "unit": "TFLOP/s", "frac": gu_tflops / peaks["bf16_tflops"],
                       "frac_of_sustained": gu_tflops / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]),
-                      "traffic": traffic, "kernel": KERNEL_NAME[path_used] + " (gate_up, SiLU*up epilogue)",
+                      "traffic": traffic, "kernel": kernel_label,
                       "algorithmic_flops_per_launch": gu_flops, "peak_source": peak_src}
                      if tensor_bound else
                      {"bound": "hbm", "achieved": gu_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                       "frac": gu_gbs / peaks["hbm_gbs"], "traffic": traffic,
-                      "kernel": KERNEL_NAME[path_used] + " (gate_up, SiLU*up epilogue)",
+                      "kernel": kernel_label,
                       "algorithmic_bytes_per_launch": gu_bytes, "peak_source": peak_src}),
         "kernels": {"gate_up_us": kt["gate_up"] * 1e3, "gate_up_gbs": gu_gbs,
                     "gate_up_tflops": gu_tflops, "down_tflops": dn_tflops,

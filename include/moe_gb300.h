@@ -92,6 +92,18 @@ int moe_set_launch_overlap(int enable);
  * stream writes neither expert_offsets nor the down weights (in the layer
  * sequence that kernel is the gate_up product). */
 enum { MOE_PATH_FLAG_WEIGHTS_EARLY = 0x100 };
+/* k-gated launch, OR-ed into the `path` of moe_gate_up_qmm or moe_down_qmm
+ * with an explicit MOE_PATH_GEMV or MOE_PATH_TC: the product runs only if
+ * lo <= *k_dev <= hi (1 <= lo <= hi <= kmax); otherwise its kernel returns
+ * without reading or writing anything but k_dev.  It still waits for the
+ * kernel ahead of it on the stream, so the stream's order holds.  With the
+ * adaptive k of page [B] section 2.2 the host does not know k when it
+ * queues a layer; queuing both kernel families, each gated on the k values
+ * it is faster for, lets the device pick per call without a host round trip.
+ * Only the streamed GEMV (4-bit K a multiple of 256, 8-bit of 128) and the
+ * tensor-core kernel take a gate (else MOE_ERR_UNSUPPORTED). */
+enum { MOE_PATH_FLAG_K_GATED = 0x200 };
+#define MOE_PATH_K_RANGE(lo, hi) (MOE_PATH_FLAG_K_GATED | ((lo) << 16) | ((hi) << 24))
 /* Device error word bits (moe_get_device_error). */
 enum { MOE_DEVERR_BAD_EXPERT = 1u, MOE_DEVERR_TIMEOUT = 2u, MOE_DEVERR_BAD_INDEX = 4u };
 /* inv_pos value of an assignment that its expert's capacity turned away
@@ -338,7 +350,7 @@ moe_status_t moe_permute_rows(const uint16_t* x, const int32_t* sorted_assign,
  * sorted_assign, expert_offsets, k_dev  from moe_permute / moe_router_topk.
  * w_q             uint32 [E, n_rows, H*bits/32]; w_s, w_b fp16 [E, n_rows, H/64].
  * bits            4 or 8.
- * path            MOE_PATH_*.
+ * path            MOE_PATH_*, optionally | MOE_PATH_K_RANGE(lo, hi).
  * ---------------------------------------------------------------------- */
 moe_status_t moe_gate_up_qmm(const uint16_t* x, const int32_t* sorted_assign,
                              const int32_t* expert_offsets, const int32_t* k_dev, int T,
@@ -358,7 +370,8 @@ moe_status_t moe_gate_up_qmm(const uint16_t* x, const int32_t* sorted_assign,
  *           sorted order (as written by moe_gate_up_qmm).
  * w_q       uint32 [E, H, I*bits/32]; w_s, w_b fp16 [E, H, I/64].
  * y         out: fp32 [T*kmax, H], sorted order; rows >= T*k not written.
- * path      MOE_PATH_*, optionally | MOE_PATH_FLAG_WEIGHTS_EARLY.
+ * path      MOE_PATH_*, optionally | MOE_PATH_FLAG_WEIGHTS_EARLY and/or
+ *           | MOE_PATH_K_RANGE(lo, hi).
  * ---------------------------------------------------------------------- */
 moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* expert_offsets,
                           const int32_t* k_dev, int T, int kmax, int E, int I, int H,

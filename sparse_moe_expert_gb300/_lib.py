@@ -14,6 +14,12 @@ DTYPE_F32, DTYPE_BF16 = 0, 1
 EPILOGUE_RAW, EPILOGUE_SWIGLU = 0, 1
 PATH_AUTO, PATH_GEMV, PATH_TC, PATH_TC_SMALL = 0, 1, 2, 3
 PATH_FLAG_WEIGHTS_EARLY = 0x100  # moe_down_qmm: offsets/weights read before the wait
+PATH_FLAG_K_GATED = 0x200  # the product runs only for lo <= k <= hi (MOE_PATH_K_RANGE)
+
+
+def path_k_range(lo: int, hi: int) -> int:
+    """Flags of a k-gated launch: the product runs only if lo <= k <= hi."""
+    return PATH_FLAG_K_GATED | (lo << 16) | (hi << 24)
 DEVERR_BAD_EXPERT, DEVERR_TIMEOUT, DEVERR_BAD_INDEX = 1, 2, 4
 DROPPED = -2  # inv_pos of an assignment dropped by its expert's capacity
 QMODE_AFFINE = 0

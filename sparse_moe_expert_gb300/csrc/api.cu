@@ -12,11 +12,12 @@ namespace moe {
 moe_status_t gemv_qmm(const void* act, int act_kind, const int32_t* sorted,
                       const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
                       bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
-                      int bits, void* out, int out_dtype, bool early, cudaStream_t st);
+                      int bits, void* out, int out_dtype, bool early, KGate gate,
+                      cudaStream_t st);
 moe_status_t tc_qmm(const void* act, int act_kind, const int32_t* sorted,
                     const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
                     bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
-                    int bits, void* out, int out_dtype, cudaStream_t st);
+                    int bits, void* out, int out_dtype, KGate gate, cudaStream_t st);
 moe_status_t tc_small_qmm(const void* act, int act_kind, const int32_t* sorted,
                           const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
                           bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
@@ -125,6 +126,30 @@ static int pick_path(int path, int T, int kmax, int E, int K, int bits) {
              : MOE_PATH_GEMV;
 }
 
+// `path` = kernel family (low byte) | MOE_PATH_FLAG_WEIGHTS_EARLY (where
+// allowed) | an optional k gate (MOE_PATH_K_RANGE: explicit GEMV or TC only).
+static bool split_path(int path, int kmax, const int32_t* k_dev, bool allow_early, int& family,
+                       bool& early, moe::KGate& gate) {
+  const unsigned u = (unsigned)path;
+  const unsigned known = 0xFFu | MOE_PATH_FLAG_WEIGHTS_EARLY | MOE_PATH_FLAG_K_GATED |
+                         (0xFFu << 16) | (0x7Fu << 24);
+  if (u & ~known) return false;
+  early = (u & MOE_PATH_FLAG_WEIGHTS_EARLY) != 0;
+  if (early && !allow_early) return false;
+  family = (int)(u & 0xFFu);
+  if (family < MOE_PATH_AUTO || family > MOE_PATH_TC_SMALL) return false;
+  gate = moe::KGate{nullptr, 0, 0};
+  if (u & MOE_PATH_FLAG_K_GATED) {
+    const int lo = (int)((u >> 16) & 0xFFu), hi = (int)((u >> 24) & 0x7Fu);
+    if (lo < 1 || hi < lo || hi > kmax) return false;
+    if (family != MOE_PATH_GEMV && family != MOE_PATH_TC) return false;
+    gate = moe::KGate{k_dev, lo, hi};
+  } else if (u >> 16) {
+    return false;  // a range without the flag
+  }
+  return true;
+}
+
 static bool common_shape_ok(int T, int kmax, int E) {
   return T >= 0 && kmax >= 1 && kmax <= 16 && E >= 1 && E <= 1024 &&
          (int64_t)T * kmax <= (1 << 24);
@@ -145,7 +170,10 @@ extern "C" moe_status_t moe_gate_up_qmm(const uint16_t* x, const int32_t* sorted
   if (out_dtype != MOE_DTYPE_F32 && out_dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
   if (epilogue == MOE_EPILOGUE_RAW && out_dtype != MOE_DTYPE_F32) return MOE_ERR_UNSUPPORTED;
   if (epilogue == MOE_EPILOGUE_SWIGLU && n_rows % 2 != 0) return MOE_ERR_INVALID_ARG;
-  if (path < MOE_PATH_AUTO || path > MOE_PATH_TC_SMALL) return MOE_ERR_INVALID_ARG;
+  int family = 0;
+  bool early = false;
+  moe::KGate gate{nullptr, 0, 0};
+  if (!split_path(path, kmax, k_dev, false, family, early, gate)) return MOE_ERR_INVALID_ARG;
   if (H > 49152) return MOE_ERR_UNSUPPORTED;
   if (!expert_offsets || !k_dev) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
@@ -157,17 +185,17 @@ extern "C" moe_status_t moe_gate_up_qmm(const uint16_t* x, const int32_t* sorted
   const int act_kind = sorted_assign ? 0 : 2;
   const bool swiglu = epilogue == MOE_EPILOGUE_SWIGLU;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int p = pick_path(path, T, kmax, E, H, bits);
+  const int p = pick_path(family, T, kmax, E, H, bits);
   if (p == MOE_PATH_TC) {
     if (!moe::tc_available()) return MOE_ERR_UNSUPPORTED;
     return moe::tc_qmm(x, act_kind, sorted_assign, expert_offsets, T, kmax, E, H, n_rows, swiglu,
-                       w_q, w_s, w_b, bits, out, out_dtype, st);
+                       w_q, w_s, w_b, bits, out, out_dtype, gate, st);
   }
   if (p == MOE_PATH_TC_SMALL)
     return moe::tc_small_qmm(x, act_kind, sorted_assign, expert_offsets, T, kmax, E, H, n_rows,
                              swiglu, w_q, w_s, w_b, bits, out, out_dtype, st);
   return moe::gemv_qmm(x, act_kind, sorted_assign, expert_offsets, T, kmax, E, H, n_rows, swiglu,
-                       w_q, w_s, w_b, bits, out, out_dtype, false, st);
+                       w_q, w_s, w_b, bits, out, out_dtype, false, gate, st);
 }
 
 extern "C" moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* expert_offsets,
@@ -180,9 +208,10 @@ extern "C" moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* 
   if (I <= 0 || I % 64 != 0 || H <= 0 || H % 64 != 0) return MOE_ERR_INVALID_ARG;
   if (bits != 4 && bits != 8) return MOE_ERR_UNSUPPORTED;
   if (h_dtype != MOE_DTYPE_F32 && h_dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
-  const bool early = (path & MOE_PATH_FLAG_WEIGHTS_EARLY) != 0;
-  path &= ~MOE_PATH_FLAG_WEIGHTS_EARLY;
-  if (path < MOE_PATH_AUTO || path > MOE_PATH_TC_SMALL) return MOE_ERR_INVALID_ARG;
+  int family = 0;
+  bool early = false;
+  moe::KGate gate{nullptr, 0, 0};
+  if (!split_path(path, kmax, k_dev, true, family, early, gate)) return MOE_ERR_INVALID_ARG;
   if (I > 49152) return MOE_ERR_UNSUPPORTED;
   if (!expert_offsets || !k_dev) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
@@ -191,17 +220,17 @@ extern "C" moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* 
     if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
   const int act_kind = h_dtype == MOE_DTYPE_F32 ? 1 : 2;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int p = pick_path(path, T, kmax, E, I, bits);
+  const int p = pick_path(family, T, kmax, E, I, bits);
   if (p == MOE_PATH_TC) {
     if (!moe::tc_available()) return MOE_ERR_UNSUPPORTED;
     return moe::tc_qmm(h, act_kind, nullptr, expert_offsets, T, kmax, E, I, H, false, w_q, w_s,
-                       w_b, bits, y, MOE_DTYPE_F32, st);
+                       w_b, bits, y, MOE_DTYPE_F32, gate, st);
   }
   if (p == MOE_PATH_TC_SMALL)
     return moe::tc_small_qmm(h, act_kind, nullptr, expert_offsets, T, kmax, E, I, H, false, w_q,
                              w_s, w_b, bits, y, MOE_DTYPE_F32, st);
   return moe::gemv_qmm(h, act_kind, nullptr, expert_offsets, T, kmax, E, I, H, false, w_q, w_s,
-                       w_b, bits, y, MOE_DTYPE_F32, early, st);
+                       w_b, bits, y, MOE_DTYPE_F32, early, gate, st);
 }
 
 namespace {

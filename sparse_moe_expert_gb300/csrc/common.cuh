@@ -81,6 +81,26 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// A k-gated launch: the product runs only if lo <= *k (the routing k on the
+// device) <= hi; otherwise its kernel returns at once.  An adaptive-k layer
+// queues both kernel families, each gated on the k values it serves.
+struct KGate {
+  const int32_t* k;  // null: not gated
+  int lo, hi;
+};
+
+// True if a gated kernel must return.  It waits for the previous kernel first
+// (right away, or before returning when `early` lets it read k ahead of that
+// wait), so whatever runs after it sees every earlier kernel completed.
+__device__ __forceinline__ bool k_gate_closed(const int32_t* k, int lo, int hi, bool early) {
+  if (k == nullptr) return false;
+  if (!early) pdl_wait();
+  const int kv = *reinterpret_cast<const volatile int32_t*>(k);
+  if (kv >= lo && kv <= hi) return false;
+  if (early) pdl_wait();
+  return true;
+}
+
 __device__ __forceinline__ unsigned lanemask_lt() {
   unsigned m;
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));

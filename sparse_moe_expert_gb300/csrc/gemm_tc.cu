@@ -112,6 +112,7 @@ struct TcParams {
   int c_stages;  // ring of TMA-loaded code slots (kCodeRowBytes of each row)
   int bn_cap;    // most tokens per tile (a multiple of 16, at most BN)
   int n_mt;         // m-tiles per expert
+  KGate gate;       // k-gated launch (gate.k null: always runs)
   unsigned int* err;
 };
 
@@ -293,6 +294,7 @@ template <int BITS, int MODE, int ACT>
 __global__ void __launch_bounds__(tc_threads(BITS), 1)
     tc_qmm_kernel(const __grid_constant__ CUtensorMap tm_act,
                   const __grid_constant__ CUtensorMap tm_codes, TcParams p) {
+  if (k_gate_closed(p.gate.k, p.gate.lo, p.gate.hi, false)) return;
   // dequant work split: DQ_SLICES threads per A row, BK / DQ_SLICES codes of
   // each k-block each
   constexpr int kDeqWarps = deq_warps(BITS);
@@ -1001,7 +1003,7 @@ bool make_tensor_map_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
 moe_status_t tc_qmm(const void* act, int act_kind, const int32_t* sorted,
                     const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
                     bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
-                    int bits, void* out, int out_dtype, cudaStream_t st) {
+                    int bits, void* out, int out_dtype, KGate gate, cudaStream_t st) {
   // act_kind: 0 = x bf16 [T, K] gathered by token, 2 = h bf16 [T*kmax, K] by sorted row
   if (act_kind != 0 && act_kind != 2) return MOE_ERR_UNSUPPORTED;
   if (K % BK != 0 || n_rows % 64 != 0) return MOE_ERR_INVALID_ARG;
@@ -1042,6 +1044,7 @@ moe_status_t tc_qmm(const void* act, int act_kind, const int32_t* sorted,
   // tiles (more token-tile slots fit)
   const int64_t mean = A / E;
   p.bn_cap = mean <= 32 ? 64 : (mean <= 64 ? 128 : BN);
+  p.gate = gate;
   p.err = moe_host::device_error_word();
   // codes: [E * n_rows rows][K * bits / 8 bytes], 64-row boxes of 128 bytes
   if ((int64_t)E * n_rows >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;

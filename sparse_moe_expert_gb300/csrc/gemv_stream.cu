@@ -125,6 +125,7 @@ struct SvParams {
   int scale_cw;  // cp.async width for scales and biases: 4, 8 or 16 bytes
   int early;     // offsets and weights final before the previous kernel ends:
                  // stream them before waiting on it (activations after)
+  KGate gate;    // k-gated launch (gate.k null: always runs)
   unsigned int* err;
 };
 
@@ -251,6 +252,7 @@ template <int BITS, int MODE, bool ONE>
 __global__ void __launch_bounds__(kSvThreads, 1)
     gemv_stream_kernel(const __grid_constant__ CUtensorMap tm_codes, SvParams p) {
   using S = SvShape<BITS>;
+  if (k_gate_closed(p.gate.k, p.gate.lo, p.gate.hi, p.early != 0)) return;
   extern __shared__ __align__(16) unsigned char sv_raw[];
   unsigned char* sm = sv_raw + ((1024u - (smem_u32(sv_raw) & 1023u)) & 1023u);
   const SvLayout L = sv_layout(BITS, p.K, p.mts, p.stages, p.E);
@@ -980,7 +982,7 @@ moe_status_t gemv_stream_qmm(const void* act, int act_kind, const int32_t* sorte
                              const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
                              bool swiglu, const uint32_t* wq, const uint16_t* ws,
                              const uint16_t* wb, int bits, void* out, int out_dtype, bool early,
-                             cudaStream_t st) {
+                             KGate gate, cudaStream_t st) {
   if (!gemv_stream_supported(bits, K, E)) return MOE_ERR_UNSUPPORTED;
   if (!moe_host::aligned16(act) || !moe_host::aligned16(wq)) return MOE_ERR_INVALID_ARG;
   const int64_t A = (int64_t)T * kmax;
@@ -1013,6 +1015,7 @@ moe_status_t gemv_stream_qmm(const void* act, int act_kind, const int32_t* sorte
                : (ngroups % 4 == 0 && (sa & 7u) == 0) ? 8
                                                       : 4;
   p.early = early ? 1 : 0;
+  p.gate = gate;
   p.err = moe_host::device_error_word();
   // tile count bound (int32 positions)
   const int64_t max_tiles = (int64_t)p.rt * (A + E);

@@ -16,7 +16,7 @@ import torch
 
 from . import binding as B
 from ._lib import (EPILOGUE_RAW, EPILOGUE_SWIGLU, PATH_AUTO, PATH_FLAG_WEIGHTS_EARLY, PATH_GEMV,
-                   PATH_TC, PATH_TC_SMALL, MoEError)
+                   PATH_TC, PATH_TC_SMALL, MoEError, path_k_range)
 
 FUSE_ENV = "MOE_GB300_FUSE_GATE_UP"
 TC_MIN_TOKENS_PER_EXPERT = 24  # mirrors the library's automatic path choice
@@ -122,12 +122,31 @@ class MoELayer:
                    kmax=cfg.slots, **kw)
 
     def resolved_path(self, T: int) -> int:
+        """The kernel family of the products (with an adaptive k, the one for
+        k = kmax; k_split says when smaller k take the other family)."""
         if self.path != PATH_AUTO:
             return self.path
-        if (TC_BUILT and (T * self.kmax) // self.E >= TC_MIN_TOKENS_PER_EXPERT
+        return self._family(T, self.kmax)
+
+    def _family(self, T: int, k: int) -> int:
+        if (TC_BUILT and (T * k) // self.E >= TC_MIN_TOKENS_PER_EXPERT
                 and min(self.H, self.I) * self.bits // 8 >= 128):
             return PATH_TC
         return PATH_GEMV
+
+    def k_split(self, T: int) -> int:
+        """With an adaptive k and the automatic path, the k (if any) from
+        which the products take the tensor cores while smaller k take the
+        streamed GEMV.  k is known only on the device, so both families are
+        queued, each gated on its k values; 0 when one family serves every k."""
+        if self.path != PATH_AUTO or self.k_fixed != 0 or not self.fused or self.E > 1024:
+            return 0
+        if self._family(T, 1) == self._family(T, self.kmax):
+            return 0
+        step = 256 if self.bits == 4 else 128  # the streamed GEMV's row granularity
+        if self.H % step or self.I % step:
+            return 0
+        return next(k for k in range(2, self.kmax + 1) if self._family(T, k) == PATH_TC)
 
     def launches_per_call(self, T: int) -> int:
         """Kernels one forward of T tokens launches: the router (plus its
@@ -136,13 +155,16 @@ class MoELayer:
         covers the batch, E <= 256 and T * kmax <= 512), the row permute on
         the tensor-core path, the gate_up product (or two RAW products and
         the activation when unfused), down and combine.  With a capacity the
-        grouping is always its own kernel."""
+        grouping is always its own kernel.  When k_split is set both kernel
+        families of each product are launched (one of them returns at once)."""
         group = 32 if self.E <= 256 else 16
         one_group = (T + group - 1) // group == 1
         n = 1 + (0 if one_group else 1)
         fused_permute = (one_group and self.E <= 256 and T * self.kmax <= 512
                          and self.capacity is None)
         n += 0 if fused_permute else 1
+        if self.k_split(T):
+            return n + 6  # row permute, two gated gate_up and two gated down launches, combine
         n += 1 if self.resolved_path(T) == PATH_TC else 0
         n += 1 if self.fused else 3
         return n + 2
@@ -206,6 +228,9 @@ class MoELayer:
                         b["k_dev"], b["mean_entropy"], b["ws"], b["counts"], b["offsets"],
                         b["sorted"], b["inv_pos"])
         ev.stop()
+        ks = self.k_split(T)
+        if ks:
+            return self._forward_k_split(x, b, ks, T, out, events)
         # tensor cores: token rows copied once into expert order, so every
         # tile loads contiguous rows; the GEMV reads x through sorted_assign
         if path == PATH_TC:
@@ -232,6 +257,37 @@ class MoELayer:
         # only h: the down weights may stream while it finishes
         B.moe_down_qmm(b["h"], b["offsets"], b["k_dev"], T, self.kmax, d.q, d.s, d.b, self.bits,
                        b["y"], path | PATH_FLAG_WEIGHTS_EARLY)
+        ev.stop()
+        res = out if out is not None else b["out"]
+        ev = _Timer(events, "combine")
+        B.moe_combine(b["y"], b["inv_pos"], b["topk_w"], b["k_dev"], T, self.kmax, res)
+        ev.stop()
+        return res
+
+    def _forward_k_split(self, x, b, ks, T, out, events):
+        """The products after routing when k < ks takes the streamed GEMV and
+        k >= ks the tensor cores: each product's two launches are gated on k,
+        so exactly one of them computes."""
+        lo_gate, hi_gate = path_k_range(1, ks - 1), path_k_range(ks, self.kmax)
+        ev = _Timer(events, "permute_rows")
+        xs = B.moe_permute_rows(x, b["sorted"], b["k_dev"], self.kmax, b["x_sorted"])
+        ev.stop()
+        g = self.gate_up
+        ev = _Timer(events, "gate_up")
+        B.moe_gate_up_qmm(x, b["sorted"], b["offsets"], b["k_dev"], self.kmax, g.q, g.s, g.b,
+                          self.bits, EPILOGUE_SWIGLU, b["h"].dtype, b["h"], PATH_GEMV | lo_gate,
+                          T=T)
+        B.moe_gate_up_qmm(xs, None, b["offsets"], b["k_dev"], self.kmax, g.q, g.s, g.b,
+                          self.bits, EPILOGUE_SWIGLU, b["h"].dtype, b["h"], PATH_TC | hi_gate, T=T)
+        ev.stop()
+        d = self.down
+        ev = _Timer(events, "down")
+        # the GEMV's weights may stream early: the kernel ahead of it (the
+        # gated tensor-core gate_up) writes only h
+        B.moe_down_qmm(b["h"], b["offsets"], b["k_dev"], T, self.kmax, d.q, d.s, d.b, self.bits,
+                       b["y"], PATH_GEMV | PATH_FLAG_WEIGHTS_EARLY | lo_gate)
+        B.moe_down_qmm(b["h"], b["offsets"], b["k_dev"], T, self.kmax, d.q, d.s, d.b, self.bits,
+                       b["y"], PATH_TC | hi_gate)
         ev.stop()
         res = out if out is not None else b["out"]
         ev = _Timer(events, "combine")

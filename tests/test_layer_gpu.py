@@ -224,3 +224,93 @@ def test_full_size_sampled(cuda_lib, full_layers, name):
         assert_layer_close(out[toks], ref.out[toks], f"{name} batch {b}")
         del layer
         torch.cuda.empty_cache()
+
+
+def test_adaptive_k_queues_both_families_and_runs_the_one_for_k(cuda_lib):
+    """Adaptive k with the automatic path: below ks tokens per expert the
+    streamed GEMV, from ks the tensor cores, decided on the device.  Each
+    batch's output equals, bit for bit, the layer forced to the family its k
+    selects, and stays within tolerance of the oracle."""
+    cfg = CFG["entropy"].scaled(H=1024, I=512, E=12, T=144, batches=3,
+                                inv_temperatures=(12.0, 3.0, 0.5))
+    layer_np = workloads.make_layer(cfg)
+    auto = cuda_lib.MoELayer.from_workload(layer_np, dev())
+    assert auto.k_split(cfg.T) == 2  # k = 1: 12 tokens per expert, k = 2: 24
+    forced = {p: cuda_lib.MoELayer.from_workload(layer_np, dev(), path=p)
+              for p in (cuda_lib.PATH_GEMV, cuda_lib.PATH_TC)}
+    seen = set()
+    for bt in range(cfg.batches):
+        x_bits = workloads.make_tokens(cfg, 0, bt)
+        x = cuda_lib.bf16_from_bits(x_bits, dev())
+        it = cfg.inv_temperature(bt)
+        got = auto(x, inv_temperature=it).clone()
+        k = int(auto.buffers(cfg.T)["k_dev"].item())
+        seen.add(k)
+        fam = cuda_lib.PATH_GEMV if k < 2 else cuda_lib.PATH_TC
+        want = forced[fam](x, inv_temperature=it)
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16)), f"batch {bt} (k={k})"
+        ref = oracle.moe_forward(x_bits, layer_np, inv_temperature=it)
+        assert ref.routing.k == k
+        assert_layer_close(to_np(got), ref.out, f"batch {bt}")
+    assert seen == {1, 2}, seen
+    assert cuda_lib.moe_get_device_error() == 0
+
+
+@pytest.mark.parametrize("path", ["gemv", "tc"])
+def test_k_gated_products_run_only_inside_their_range(cuda_lib, path):
+    """A gated product whose range holds the device's k equals the ungated
+    one bit for bit; one whose range misses it leaves its output untouched."""
+    cfg = CFG["tiny"]  # k = kmax = 2
+    layer_np = workloads.make_layer(cfg)
+    layer = cuda_lib.MoELayer.from_workload(layer_np, dev(), path=path_id(cuda_lib, path))
+    x = cuda_lib.bf16_from_bits(workloads.make_tokens(cfg), dev())
+    layer(x)
+    b = layer.buffers(cfg.T)
+    T, kmax, fam = cfg.T, layer.kmax, path_id(cuda_lib, path)
+    g, d = layer.gate_up, layer.down
+    xs, srt = (x, b["sorted"]) if path == "gemv" else (b["x_sorted"], None)
+
+    def gate_up(flags):
+        h = torch.full_like(b["h"], float("nan"))
+        cuda_lib.moe_gate_up_qmm(xs, srt, b["offsets"], b["k_dev"], kmax, g.q, g.s, g.b, cfg.bits,
+                                 cuda_lib.EPILOGUE_SWIGLU, h.dtype, h, fam | flags, T=T)
+        return h
+
+    def down(flags):
+        y = torch.full_like(b["y"], float("nan"))
+        cuda_lib.moe_down_qmm(b["h"], b["offsets"], b["k_dev"], T, kmax, d.q, d.s, d.b, cfg.bits,
+                              y, fam | flags)
+        return y
+
+    A = T * kmax
+    for run in (gate_up, down):
+        ref = run(0)
+        for lo, hi in ((1, 2), (2, 2)):
+            got = run(cuda_lib.path_k_range(lo, hi))
+            assert torch.equal(got[:A].view(torch.int32 if got.dtype == torch.float32
+                                            else torch.int16),
+                               ref[:A].view(torch.int32 if ref.dtype == torch.float32
+                                            else torch.int16)), (run.__name__, lo, hi)
+        skipped = run(cuda_lib.path_k_range(1, 1))
+        torch.cuda.synchronize()
+        assert torch.isnan(skipped.float()).all(), run.__name__
+    assert cuda_lib.moe_get_device_error() == 0
+
+
+def test_k_gate_arguments_are_checked(cuda_lib):
+    cfg = CFG["tiny"]
+    layer = cuda_lib.MoELayer.from_workload(workloads.make_layer(cfg), dev())
+    x = cuda_lib.bf16_from_bits(workloads.make_tokens(cfg), dev())
+    layer(x)
+    b, d = layer.buffers(cfg.T), layer.down
+    bad = [cuda_lib.PATH_GEMV | cuda_lib.path_k_range(0, 1),       # lo < 1
+           cuda_lib.PATH_GEMV | cuda_lib.path_k_range(2, 1),       # hi < lo
+           cuda_lib.PATH_TC | cuda_lib.path_k_range(1, 3),         # hi > kmax
+           cuda_lib.PATH_AUTO | cuda_lib.path_k_range(1, 2),       # gate needs a family
+           cuda_lib.PATH_TC_SMALL | cuda_lib.path_k_range(1, 2),
+           cuda_lib.PATH_GEMV | (1 << 16)]                         # range without the flag
+    for flags in bad:
+        with pytest.raises(cuda_lib.MoEError):
+            cuda_lib.moe_down_qmm(b["h"], b["offsets"], b["k_dev"], cfg.T, layer.kmax, d.q, d.s,
+                                  d.b, cfg.bits, b["y"], flags)

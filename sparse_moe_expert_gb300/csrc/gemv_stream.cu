@@ -248,11 +248,15 @@ struct SvCursor {
   int a, c, rt, nch;
 };
 
-template <int BITS, int MODE, bool ONE>
+// GATED: a k-gated launch (p.gate); a separate instantiation, since even an
+// untaken gate check at the top cost the single-token kernels 3 %.
+template <int BITS, int MODE, bool ONE, bool GATED>
 __global__ void __launch_bounds__(kSvThreads, 1)
     gemv_stream_kernel(const __grid_constant__ CUtensorMap tm_codes, SvParams p) {
   using S = SvShape<BITS>;
-  if (k_gate_closed(p.gate.k, p.gate.lo, p.gate.hi, p.early != 0)) return;
+  if constexpr (GATED) {
+    if (k_gate_closed(p.gate.k, p.gate.lo, p.gate.hi, p.early != 0)) return;
+  }
   extern __shared__ __align__(16) unsigned char sv_raw[];
   unsigned char* sm = sv_raw + ((1024u - (smem_u32(sv_raw) & 1023u)) & 1023u);
   const SvLayout L = sv_layout(BITS, p.K, p.mts, p.stages, p.E);
@@ -926,10 +930,10 @@ __global__ void __launch_bounds__(kSvThreads, 1)
   }
 }
 
-template <int BITS, int MODE, bool ONE>
+template <int BITS, int MODE, bool ONE, bool GATED>
 moe_status_t launch_stream_kernel(const CUtensorMap& tm, const SvParams& p, int smem,
                                   cudaStream_t st) {
-  auto kern = gemv_stream_kernel<BITS, MODE, ONE>;
+  auto kern = gemv_stream_kernel<BITS, MODE, ONE, GATED>;
   static int set_max = 0;
   if (smem > set_max) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
@@ -948,7 +952,7 @@ moe_status_t launch_stream(const CUtensorMap& tm, SvParams p, cudaStream_t st) {
     cudaFuncAttributes fa;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-        cudaFuncGetAttributes(&fa, gemv_stream_kernel<BITS, MODE, false>) != cudaSuccess)
+        cudaFuncGetAttributes(&fa, gemv_stream_kernel<BITS, MODE, false, false>) != cudaSuccess)
       return MOE_ERR_CUDA;
     static_smem = (int)fa.sharedSizeBytes;
     optin = v;
@@ -965,8 +969,9 @@ moe_status_t launch_stream(const CUtensorMap& tm, SvParams p, cudaStream_t st) {
   if (stages < 2) return MOE_ERR_UNSUPPORTED;
   p.stages = stages;
   const int smem = (int)sv_layout(BITS, p.K, p.mts, stages, p.E).total + 1024;
-  return p.mts == 1 ? launch_stream_kernel<BITS, MODE, true>(tm, p, smem, st)
-                    : launch_stream_kernel<BITS, MODE, false>(tm, p, smem, st);
+  if (p.gate.k != nullptr) return launch_stream_kernel<BITS, MODE, false, true>(tm, p, smem, st);
+  return p.mts == 1 ? launch_stream_kernel<BITS, MODE, true, false>(tm, p, smem, st)
+                    : launch_stream_kernel<BITS, MODE, false, false>(tm, p, smem, st);
 }
 
 }  // namespace

@@ -379,6 +379,33 @@ moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* expert_offs
                           int bits, float* y, int path, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Expert health.  Page [B], section 6: a serving-side "MoE health" check on
+ * two numbers per time window (one minute there): the expert activated least
+ * often, and the standard deviation of all experts' activation counts (an
+ * alert when it stays above 20 for five windows in a row); section 4.2 counts
+ * activations per expert with a bincount of the routed expert ids.  Here a
+ * call's activations of expert e are expert_counts[e] as the grouping writes
+ * it (moe_permute, moe_route, moe_permute_capped: the assignments the expert
+ * runs).  The window and the alert rule live in the caller
+ * (sparse_moe_expert_gb300.ExpertHealthMonitor).
+ *
+ * moe_expert_counts_accumulate: window_counts[e] += expert_counts[e], e < E.
+ *   expert_counts   int32 [E] (device); window_counts int64 [E] (device,
+ *   8-byte aligned, zeroed by the caller when a window opens).
+ * moe_expert_health: over c = window_counts[0..E):
+ *   *least_expert = the e of the smallest c_e (equal counts: the lower e);
+ *   mean_std[0] = sum(c) / E; mean_std[1] = sqrt(sum((c_e - mean)^2) / E)
+ *   (population standard deviation), in fp64, sums in a fixed order.
+ *   least_expert int32 scalar, mean_std double [2] (device, 8-byte aligned).
+ * 1 <= E <= 1024 (else MOE_ERR_INVALID_ARG).  Both are asynchronous on
+ * `stream`; the caller owns every buffer.
+ * ---------------------------------------------------------------------- */
+moe_status_t moe_expert_counts_accumulate(const int32_t* expert_counts, int E,
+                                          int64_t* window_counts, moe_stream_t stream);
+moe_status_t moe_expert_health(const int64_t* window_counts, int E, int32_t* least_expert,
+                               double* mean_std, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * moe_combine -- routing-weighted sum back to token order.
  *
  * Page [A], section 4.2: y[t] = sum_k w_k * expert_out_k.  Here

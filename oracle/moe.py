@@ -14,6 +14,7 @@ __all__ = [
     "routing_weights", "group_top1_ids", "route", "Routing", "permute", "Permutation", "unpack_codes",
     "dequant", "DROPPED", "QDesc", "can_fuse", "pack_gate_up", "qmm_raw", "silu", "swiglu",
     "moe_forward", "Forward", "dense_masked_forward", "bf16_to_f64", "ENTROPY_THRESHOLDS",
+    "expert_health",
 ]
 
 # Entropy bands of the adaptive top-k rule, page [B] section 2.2.
@@ -387,3 +388,19 @@ def dense_masked_forward(x_bits, layer, routing: Routing) -> np.ndarray:
         ye = swiglu(xf @ wg.T, xf @ wu.T) @ wd.T
         out = out + mask[:, e:e + 1] * ye
     return out
+
+
+# --------------------------------------------------------------------------
+# Expert health: page [B] section 6 (per window, the least-activated expert
+# and the standard deviation of all experts' activation counts) and section
+# 4.2 (activation counts per expert).
+# --------------------------------------------------------------------------
+def expert_health(window_counts) -> tuple:
+    """(least-activated expert id, mean, population standard deviation) of a
+    window's per-expert activation counts; equal counts go to the lower id."""
+    c = np.asarray(window_counts, dtype=np.int64)
+    E = c.size
+    least = int(np.argmin(c))
+    mean = float(c.sum()) / E
+    std = float(np.sqrt(((c.astype(np.float64) - mean) ** 2).sum() / E))
+    return least, mean, std

@@ -11,16 +11,19 @@ from ._lib import (DEVERR_BAD_EXPERT, DEVERR_BAD_INDEX, DEVERR_TIMEOUT, DROPPED,
                    PATH_FLAG_WEIGHTS_EARLY, PATH_GEMV, PATH_TC, PATH_TC_SMALL, path_k_range,
                    MoEError,
                    lib, lib_path)
-from .binding import (moe_abi_version, moe_combine, moe_down_qmm, moe_gate_up_qmm,
+from .binding import (moe_abi_version, moe_combine, moe_down_qmm, moe_expert_counts_accumulate,
+                      moe_expert_health, moe_gate_up_qmm,
                       moe_get_device_error, moe_pack_gate_up, moe_permute, moe_permute_capped,
                       moe_permute_rows,
                       moe_route, moe_route_grouped, moe_router_topk, moe_selftest_wait_timeout,
                       moe_set_launch_overlap,
                       moe_router_workspace_size, moe_status_string, moe_swiglu, qdesc)
+from .health import ExpertHealthMonitor, WindowHealth
 from .layer import MoELayer, QTensor, bf16_from_bits, qtensor_from_numpy
 
 __all__ = [
-    "MoELayer", "QTensor", "MoEError", "qtensor_from_numpy", "bf16_from_bits", "lib", "lib_path",
+    "MoELayer", "QTensor", "MoEError", "ExpertHealthMonitor", "WindowHealth",
+    "moe_expert_counts_accumulate", "moe_expert_health", "qtensor_from_numpy", "bf16_from_bits", "lib", "lib_path",
     "moe_abi_version", "moe_set_launch_overlap", "moe_status_string", "moe_pack_gate_up", "moe_router_workspace_size",
     "moe_router_topk", "moe_route", "moe_route_grouped", "moe_permute", "moe_permute_capped", "moe_permute_rows", "moe_gate_up_qmm", "moe_down_qmm", "moe_combine",
     "moe_swiglu", "moe_get_device_error", "moe_selftest_wait_timeout", "qdesc", "EXPORTS", "DTYPE_F32", "DTYPE_BF16",

@@ -30,6 +30,7 @@ EXPORTS = (
     "moe_status_string", "moe_abi_version", "moe_set_launch_overlap", "moe_pack_gate_up", "moe_router_workspace_size",
     "moe_router_topk", "moe_router_topk_noalloc", "moe_route", "moe_route_grouped", "moe_permute", "moe_permute_capped", "moe_permute_rows", "moe_gate_up_qmm", "moe_down_qmm", "moe_combine",
     "moe_swiglu", "moe_get_device_error", "moe_selftest_wait_timeout",
+    "moe_expert_counts_accumulate", "moe_expert_health",
 )
 
 
@@ -84,11 +85,14 @@ def _declare(lib):
     lib.moe_swiglu.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp]
     lib.moe_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32, vp]
     lib.moe_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
+    lib.moe_expert_counts_accumulate.argtypes = [vp, i32, vp, vp]
+    lib.moe_expert_health.argtypes = [vp, i32, vp, vp, vp]
     for name in ("moe_pack_gate_up", "moe_router_topk", "moe_router_topk_noalloc", "moe_route",
                  "moe_route_grouped", "moe_permute_capped",
                  "moe_permute", "moe_permute_rows", "moe_gate_up_qmm",
                  "moe_down_qmm", "moe_combine", "moe_swiglu", "moe_get_device_error",
-                 "moe_selftest_wait_timeout"):
+                 "moe_selftest_wait_timeout", "moe_expert_counts_accumulate",
+                 "moe_expert_health"):
         getattr(lib, name).restype = i32
 
 

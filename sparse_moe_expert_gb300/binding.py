@@ -251,6 +251,34 @@ def moe_selftest_wait_timeout(budget_cycles: int = 2_000_000, stream=None) -> No
           lib().moe_selftest_wait_timeout(int(budget_cycles), _stream(stream)))
 
 
+def moe_expert_counts_accumulate(expert_counts, window_counts, stream=None):
+    """window_counts (int64 [E]) += expert_counts (int32 [E]), on the device."""
+    _need(expert_counts, torch.int32, "expert_counts")
+    _need(window_counts, torch.int64, "window_counts")
+    E = window_counts.numel()
+    if expert_counts.numel() != E:
+        raise ValueError("expert_counts and window_counts differ in length")
+    check("moe_expert_counts_accumulate",
+          lib().moe_expert_counts_accumulate(_p(expert_counts), E, _p(window_counts),
+                                             _stream(stream)))
+    return window_counts
+
+
+def moe_expert_health(window_counts, least=None, mean_std=None, stream=None):
+    """Least-activated expert (int32 [1]) and (mean, population std) of the
+    window's counts (float64 [2]), both left on the device."""
+    _need(window_counts, torch.int64, "window_counts")
+    dev = window_counts.device
+    if least is None:
+        least = torch.empty(1, dtype=torch.int32, device=dev)
+    if mean_std is None:
+        mean_std = torch.empty(2, dtype=torch.float64, device=dev)
+    check("moe_expert_health",
+          lib().moe_expert_health(_p(window_counts), window_counts.numel(), _p(least),
+                                  _p(mean_std), _stream(stream)))
+    return least, mean_std
+
+
 def moe_get_device_error(clear: bool = True, stream=None) -> int:
     v = ctypes.c_uint32(0)
     st = lib().moe_get_device_error(ctypes.byref(v), int(clear), _stream(stream))

@@ -442,3 +442,47 @@ def test_generator_is_deterministic_and_sliceable():
     x1 = workloads.normal_bf16(0, 5, (4, 64), 1.0)
     x2 = workloads.normal_bf16(0, 5, (2, 64), 1.0, start=128)
     assert np.array_equal(x1[2:], x2)
+
+
+# --------------------------------------------------------------------------
+# Expert health (page [B] section 6): closed forms of the least-activated
+# expert, the mean and the population standard deviation.
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("E", [1, 2, 7, 64, 1024])
+def test_expert_health_equal_counts(E):
+    least, mean, std = oracle.expert_health(np.full(E, 37, np.int64))
+    assert (least, mean, std) == (0, 37.0, 0.0)
+
+
+@pytest.mark.parametrize("E,hot", [(8, 0), (8, 5), (64, 63), (1024, 300)])
+def test_expert_health_single_busy_expert(E, hot):
+    # one expert takes all n activations: std = n sqrt(E - 1) / E
+    n = 1000
+    c = np.zeros(E, np.int64)
+    c[hot] = n
+    least, mean, std = oracle.expert_health(c)
+    assert least == (1 if hot == 0 else 0)
+    assert mean == n / E
+    assert math.isclose(std, n * math.sqrt(E - 1) / E, rel_tol=1e-14)
+
+
+@pytest.mark.parametrize("E", [2, 5, 64, 1000])
+def test_expert_health_permuted_ramp(E):
+    # counts 0 .. E-1 in any order: variance (E^2 - 1) / 12, least = where the 0 is
+    rng = np.random.default_rng(E)
+    c = rng.permutation(np.arange(E, dtype=np.int64))
+    least, mean, std = oracle.expert_health(c)
+    assert least == int(np.where(c == 0)[0][0])
+    assert mean == (E - 1) / 2
+    assert math.isclose(std, math.sqrt((E * E - 1) / 12.0), rel_tol=1e-13)
+
+
+def test_expert_health_two_levels_and_ties():
+    # half the experts at a, half at b: std = |a - b| / 2; the lowest id of
+    # the lower level is the least-activated expert
+    c = np.array([9, 4, 9, 4, 9, 4, 9, 4], np.int64)
+    least, mean, std = oracle.expert_health(c)
+    assert (least, mean, std) == (1, 6.5, 2.5)
+    # the page's alert level: 20 activations of spread
+    c = np.array([0, 40] * 32, np.int64)
+    assert oracle.expert_health(c)[2] == 20.0

@@ -300,3 +300,58 @@ def test_layer_with_capacity_matches_oracle(cuda_lib, path):
     assert np.array_equal(to_np(layer.buffers(cfg.T)["inv_pos"]), ref.perm.inv_pos)
     assert_layer_close(out, ref.out, f"capacity {C} ({path})")
     assert cuda_lib.moe_get_device_error() == 0
+
+
+@pytest.mark.parametrize("E", [1, 7, 64, 1000, 1024])
+def test_expert_health_kernels_match_oracle(cuda_lib, E):
+    """Window accumulation is exact (int64); the least-activated expert is
+    exact (ties to the lower id); mean and population std within 1e-12."""
+    rng = np.random.default_rng(E)
+    window = torch.zeros(E, dtype=torch.int64, device=dev())
+    total = np.zeros(E, np.int64)
+    for call in range(3):
+        c = rng.integers(0, 50, E).astype(np.int32)
+        c[rng.integers(0, E, max(1, E // 8))] = 0          # ties at the minimum
+        if call == 2:
+            c[: min(E, 4)] = 2**30                          # large counts: int64 window
+        total += c
+        cuda_lib.moe_expert_counts_accumulate(torch.from_numpy(c).to(dev()), window)
+    least, mean_std = cuda_lib.moe_expert_health(window)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(window), total)
+    l_ref, m_ref, s_ref = oracle.expert_health(total)
+    assert int(least.item()) == l_ref
+    ms = mean_std.cpu().numpy()
+    assert abs(ms[0] - m_ref) <= 1e-12 * max(1.0, abs(m_ref))
+    assert abs(ms[1] - s_ref) <= 1e-12 * max(1.0, s_ref)
+
+
+def test_expert_health_monitor_on_layer_counts(cuda_lib):
+    """The monitor on a layer's own expert_counts: a closed window equals the
+    oracle's health of the summed counts of the calls it saw."""
+    cfg = SMALL["batched_s"]
+    layer = cuda_lib.MoELayer.from_workload(workloads.make_layer(cfg), dev())
+    t = [0.0]
+    mon = cuda_lib.ExpertHealthMonitor(cfg.E, dev(), window_s=60.0, clock=lambda: t[0])
+    x_all = workloads.make_tokens(cfg)
+    total = np.zeros(cfg.E, np.int64)
+    for i in range(3):
+        x = cuda_lib.bf16_from_bits(np.roll(x_all, i, axis=0), dev())
+        layer(x)
+        counts = layer.buffers(cfg.T)["counts"]
+        total += to_np(counts).astype(np.int64)
+        t[0] = 20.0 * i
+        mon.record(counts)
+    h = mon.close_window()
+    l_ref, m_ref, s_ref = oracle.expert_health(total)
+    assert h.least_expert == l_ref and abs(h.mean - m_ref) < 1e-9 and abs(h.std - s_ref) < 1e-9
+    assert total.sum() == 3 * cfg.T * cfg.k
+
+
+def test_expert_health_rejects_bad_arguments(cuda_lib):
+    w = torch.zeros(1025, dtype=torch.int64, device=dev())
+    with pytest.raises(cuda_lib.MoEError):
+        cuda_lib.moe_expert_health(w)
+    with pytest.raises(ValueError):
+        cuda_lib.moe_expert_counts_accumulate(torch.zeros(4, dtype=torch.int32, device=dev()),
+                                              torch.zeros(5, dtype=torch.int64, device=dev()))

@@ -10,7 +10,10 @@ on a few experts).
 The counts stay on the device: every layer call adds its expert_counts into
 an int64 window (moe_expert_counts_accumulate), and closing a window runs
 one small kernel (moe_expert_health) and reads back three numbers.  The
-windowing and the alert rule are host logic.
+windowing and the alert rule are host logic.  When data-parallel ranks each
+serve part of the traffic, the gateway's view is the sum over the ranks: with
+a process group, closing a window first sums the ranks' windows (one
+all-reduce of E int64 counts), so every rank reports the same health.
 """
 from __future__ import annotations
 
@@ -44,7 +47,8 @@ class ExpertHealthMonitor:
 
     def __init__(self, E: int, device, window_s: float = 60.0, std_threshold: float = 20.0,
                  alert_windows: int = 5, clock: Callable[[], float] = time.monotonic,
-                 accumulate: Optional[Callable] = None, reduce: Optional[Callable] = None):
+                 accumulate: Optional[Callable] = None, reduce: Optional[Callable] = None,
+                 process_group=None):
         if E < 1 or window_s <= 0 or alert_windows < 1:
             raise ValueError("E >= 1, window_s > 0 and alert_windows >= 1 are required")
         self.E = E
@@ -55,6 +59,7 @@ class ExpertHealthMonitor:
         self.window = torch.zeros(E, dtype=torch.int64, device=device)
         self._accumulate = accumulate or B.moe_expert_counts_accumulate
         self._reduce = reduce or self._device_reduce
+        self.process_group = process_group
         self.history: List[WindowHealth] = []
         self.opened = clock()
 
@@ -69,13 +74,25 @@ class ExpertHealthMonitor:
         return bool(self.history) and self.history[-1].alert
 
     def record(self, expert_counts) -> Optional[WindowHealth]:
-        """Add one call's counts; returns the window's health if it closed."""
+        """Add one call's counts; returns the window's health if it closed.
+        With a process group windows never close here (the ranks' clocks
+        need not agree): every rank calls close_window at the same point."""
         self._accumulate(expert_counts, self.window)
-        if self.clock() - self.opened >= self.window_s:
+        if self.process_group is None and self.clock() - self.opened >= self.window_s:
             return self.close_window()
         return None
 
+    def window_due(self) -> bool:
+        """Whether the open window has lasted window_s on this rank's clock."""
+        return self.clock() - self.opened >= self.window_s
+
     def close_window(self) -> WindowHealth:
+        """Reduce the open window (summed over the ranks of the process
+        group, if any) and start the next.  With a process group every rank
+        must close its windows in the same order."""
+        if self.process_group is not None:
+            import torch.distributed as dist
+            dist.all_reduce(self.window, op=dist.ReduceOp.SUM, group=self.process_group)
         least, mean, std = self._reduce(self.window)
         recent = [h.std for h in self.history[-(self.alert_windows - 1):]] \
             if self.alert_windows > 1 else []

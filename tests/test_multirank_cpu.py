@@ -78,3 +78,45 @@ def test_single_rank_is_the_whole_stream():
     whole = workloads.normal_bf16(0, workloads.STREAM_X, (cfg.calls * cfg.T, cfg.H), cfg.x_std)
     assert np.array_equal(x, whole)
     assert bench.max_over_ranks(2.5, 1) == 2.5
+
+
+def _health_worker(rank, world, port, results):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from sparse_moe_expert_gb300.health import ExpertHealthMonitor
+
+        def accumulate(counts, window):
+            window += counts.to(torch.int64)
+
+        def reduce(window):
+            return oracle.expert_health(window.numpy())
+
+        mon = ExpertHealthMonitor(6, "cpu", clock=lambda: 0.0, accumulate=accumulate,
+                                  reduce=reduce, process_group=dist.group.WORLD)
+        rng = np.random.default_rng(100 + rank)
+        mine = np.zeros(6, np.int64)
+        for _ in range(3):
+            c = rng.integers(0, 20, 6).astype(np.int32)
+            mine += c
+            mon.record(torch.from_numpy(c))
+        h = mon.close_window()
+        results[rank] = (mine, (h.least_expert, h.mean, h.std))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.timeout(300)
+def test_health_window_sums_the_ranks():
+    """With a process group each rank's closed window reports the health of
+    the counts of all ranks together."""
+    port = _free_port()
+    with mp.Manager() as man:
+        results = man.dict()
+        mp.spawn(_health_worker, args=(WORLD, port, results), nprocs=WORLD, join=True)
+        res = dict(results)
+    total = sum(res[r][0] for r in range(WORLD))
+    want = oracle.expert_health(total)
+    for r in range(WORLD):
+        assert res[r][1] == want

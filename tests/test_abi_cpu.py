@@ -111,3 +111,30 @@ def test_workspace_size_grows_with_tokens(L):
     import sparse_moe_expert_gb300 as moe
     assert moe.moe_router_workspace_size(0) > 0
     assert moe.moe_router_workspace_size(4096) >= 2 * 4 * 4096
+
+
+def test_header_constants_match_the_binding(tmp_path):
+    """The header compiles as C, and its path flags, k-range macro, dropped
+    marker and dtype codes agree with the Python binding's constants."""
+    import shutil
+    import subprocess
+    import sparse_moe_expert_gb300 as moe
+    from sparse_moe_expert_gb300 import _lib
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "consts.c"
+    src.write_text(
+        '#include <stdio.h>\n#include "moe_gb300.h"\n'
+        "int main(void) {\n"
+        '  printf("%d %d %d %d %d %d %d\\n", MOE_PATH_GEMV, MOE_PATH_TC, MOE_PATH_FLAG_WEIGHTS_EARLY,\n'
+        "         MOE_PATH_FLAG_K_GATED, MOE_PATH_K_RANGE(2, 3), MOE_DROPPED, MOE_PATH_TC_SMALL);\n"
+        "  return 0;\n}\n")
+    exe = tmp_path / "consts"
+    subprocess.run([cc, "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    vals = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True,
+                                           check=True).stdout.split()]
+    assert vals == [moe.PATH_GEMV, moe.PATH_TC, moe.PATH_FLAG_WEIGHTS_EARLY,
+                    moe.PATH_FLAG_K_GATED, moe.path_k_range(2, 3), moe.DROPPED,
+                    moe.PATH_TC_SMALL]

@@ -227,8 +227,9 @@ def permute(ids: np.ndarray, k: int, E: int, capacity: Optional[int] = None) -> 
 # --------------------------------------------------------------------------
 
 def unpack_codes(q_words: np.ndarray, bits: int, cols: int) -> np.ndarray:
-    """uint32 words -> codes [..., cols]; element i in word i/(32/bits) at bit
-    offset bits*(i mod 32/bits)."""
+    """uint32 words -> codes [..., cols]: element i at bits [bits*i, bits*i +
+    bits) of the row's little-endian bit stream (for 4 and 8 bits: word
+    i/(32/bits), bit offset bits*(i mod 32/bits))."""
     # Little-endian words: byte j of a word holds elements 2j (low nibble) and
     # 2j+1 (high nibble) for 4-bit codes, element j for 8-bit codes.
     q = np.asarray(q_words)
@@ -239,8 +240,13 @@ def unpack_codes(q_words: np.ndarray, bits: int, cols: int) -> np.ndarray:
         codes = np.empty(by.shape[:-1] + (2 * by.shape[-1],), dtype=np.uint8)
         codes[..., 0::2] = by & 0x0F
         codes[..., 1::2] = by >> 4
+    elif bits in (5, 6):
+        # bit j of the stream is bit j % 8 of byte j / 8
+        stream = np.unpackbits(by, axis=-1, bitorder="little")[..., :cols * bits]
+        digits = stream.reshape(stream.shape[:-1] + (cols, bits)).astype(np.uint16)
+        codes = (digits << np.arange(bits, dtype=np.uint16)).sum(-1).astype(np.uint8)
     else:
-        raise ValueError("bits must be 4 or 8")
+        raise ValueError("bits must be 4, 5, 6 or 8")
     return codes.reshape(*q.shape[:-1], cols)
 
 

@@ -305,7 +305,7 @@ def test_capacity_zero_gives_zero_output_and_large_capacity_changes_nothing():
 # ---------------------------------------------------------------- dequant ---
 
 def test_dequant_extreme_codes():
-    for bits in (4, 8):
+    for bits in (4, 5, 6, 8):
         cols = 128
         words = cols * bits // 32
         s = np.array([[0.25, 0.0625]], np.float16)
@@ -329,7 +329,25 @@ def test_unpack_order_single_code():
     assert codes8[0, 9] == 200 and codes8.sum() == 200
 
 
-@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("bits,elem,code,words", [
+    # 5-bit element 6 spans bits 30..34: word 0 bits 30-31, word 1 bits 0-2
+    (5, 6, 0b10111, {0: 0b11 << 30, 1: 0b101}),
+    # 6-bit element 5 spans bits 30..35: word 0 bits 30-31, word 1 bits 0-3
+    (6, 5, 0b101101, {0: 0b01 << 30, 1: 0b1011}),
+    # 5-bit element 7 at bits 35..39, inside word 1
+    (5, 7, 31, {1: 31 << 3}),
+    # 6-bit element 10 at bits 60..65: low 4 bits in word 1 bits 28-31, high 2 in word 2
+    (6, 10, 0b110011, {1: 0b0011 << 28, 2: 0b11}),
+])
+def test_unpack_bit_stream_codes(bits, elem, code, words):
+    q = np.zeros((1, 2 * bits), np.uint32)       # one group of 64 codes
+    for w, v in words.items():
+        q[0, w] = np.uint32(v)
+    codes = oracle.unpack_codes(q, bits, 64)
+    assert codes[0, elem] == code and int(codes.sum()) == code
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
 def test_dequant_within_quantizer_bound(bits):
     qm, wf = workloads.quantized(0, 77, 2, 24, 256, bits, 0.02, return_float=True)
     for e in range(2):

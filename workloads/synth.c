@@ -128,8 +128,7 @@ typedef struct {
 
 static void quantize_rows(const qjob_t* j) {
   const int G = 64;
-  const int per_word = 32 / j->bits;
-  const int words = j->cols / per_word;
+  const int words = j->cols * j->bits / 32;
   const int groups = j->cols / G;
   const uint32_t qmax = (1u << j->bits) - 1u;
   float w[64];
@@ -161,8 +160,13 @@ static void quantize_rows(const qjob_t* j) {
           if (v > (float)qmax) v = (float)qmax;
           qi = (uint32_t)v;
         }
-        int col = g * G + i;
-        qrow[col / per_word] |= qi << (j->bits * (col % per_word));
+        /* element col at bits [bits*col, bits*col + bits) of the row's
+           little-endian bit stream (whole in one word for 4 and 8 bits) */
+        const int col = g * G + i;
+        const int64_t pos = (int64_t)col * j->bits;
+        const int wi = (int)(pos >> 5), off = (int)(pos & 31);
+        qrow[wi] |= qi << off;
+        if (off + j->bits > 32) qrow[wi + 1] |= qi >> (32 - off);
         if (j->w_out) j->w_out[o * (int64_t)j->cols + col] = w[i];
       }
     }
@@ -177,12 +181,15 @@ static void* quantize_thread(void* arg) { quantize_rows((const qjob_t*)arg); ret
  * columns with min-max affine codes: scale = fp16((max-min)/(2^bits-1)),
  * bias = fp16(min), code = clamp(rint((w-bias)/scale), 0, 2^bits-1) using the
  * fp16-rounded scale and bias (scale 0 gives code 0).  Outputs are indexed
- * from row0: q[(r-row0)*cols*bits/32], s/b[(r-row0)*cols/64].
+ * from row0: q[(r-row0)*cols*bits/32], s/b[(r-row0)*cols/64].  bits is 4,
+ * 5, 6 or 8; a row's codes form one little-endian bit stream over its
+ * uint32 words (a 64-code group is 2*bits whole words).
  */
 int synth_quantized(uint64_t seed, uint64_t stream, int64_t row0, int64_t nrows, int cols,
                     int bits, double sigma, uint32_t* q, uint16_t* s, uint16_t* b,
                     float* w_out, int nthreads) {
-  if ((bits != 4 && bits != 8) || cols % 64 != 0 || nrows < 0) return -1;
+  if ((bits != 4 && bits != 5 && bits != 6 && bits != 8) || cols % 64 != 0 || nrows < 0)
+    return -1;
   if (nthreads < 1) nthreads = 1;
   if (nthreads > 256) nthreads = 256;
   if ((int64_t)nthreads > nrows) nthreads = nrows > 0 ? (int)nrows : 1;

@@ -82,6 +82,12 @@ bool pdl_enabled() {
   return v != 0;
 }
 
+int device_index() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxCachedDevices) dev = 0;
+  return dev;
+}
+
 unsigned int* device_error_word() {
   DeviceCache& c = cache_for_current();
   if (c.err == nullptr) {

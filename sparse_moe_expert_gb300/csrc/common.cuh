@@ -116,6 +116,10 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 // Streaming multiprocessor count of the current device (cached per device).
 int sm_count();
+// The current device's index, for per-device caches of launch settings
+// (kernel attributes are set per device); 0 .. kMaxCachedDevices - 1.
+constexpr int kMaxCachedDevices = 64;
+int device_index();
 
 // Device address of the current device's error word (nullptr on failure).
 unsigned int* device_error_word();

@@ -934,12 +934,13 @@ template <int BITS, int MODE, bool ONE, bool GATED>
 moe_status_t launch_stream_kernel(const CUtensorMap& tm, const SvParams& p, int smem,
                                   cudaStream_t st) {
   auto kern = gemv_stream_kernel<BITS, MODE, ONE, GATED>;
-  static int set_max = 0;
-  if (smem > set_max) {
+  static int set_max[moe_host::kMaxCachedDevices] = {};  // per device
+  const int dev = moe_host::device_index();
+  if (smem > set_max[dev]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
-    set_max = smem;
+    set_max[dev] = smem;
   }
   return moe_host::launch(kern, moe_host::sm_count(), kSvThreads, smem, st, tm, p);
 }

@@ -586,12 +586,13 @@ moe_status_t launch_router(const RouterParams& p, cudaStream_t st) {
     q.smem_stage = (ngroups == 1 && staged <= kRouterStageBytes) ? 1 : 0;
     if (q.smem_stage) smem = staged;
     auto kern = wide ? router_topk_kernel<kRouterClusterWide> : router_topk_kernel<kRouterCluster>;
-    static size_t set_max[2] = {48 * 1024, 48 * 1024};
-    if (smem > set_max[wide]) {
+    static size_t set_max[2][kMaxCachedDevices] = {};  // per kernel and device
+    const int dev = device_index();
+    if (smem > 48 * 1024 && smem > set_max[wide][dev]) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
           cudaSuccess)
         return MOE_ERR_CUDA;
-      set_max[wide] = smem;
+      set_max[wide][dev] = smem;
     }
     if (launch(kern, ngroups * cl, kRouterThreads, smem, st, q) != MOE_OK) return MOE_ERR_CUDA;
   }

@@ -22,20 +22,21 @@
 //
 // Data movement.  A tile is 16 weight rows (SWIGLU: 8 gate rows and the 8 up
 // rows of the same features) of one active expert, applied to a chunk of up
-// to 8 of its tokens.  A stage is 1 KB of codes of each of the tile's rows
-// plus their fp16 scales and biases.  One CTA of 18 warps per SM:
+// to 8 of its tokens.  A stage is 2 KB of codes of each of the tile's rows
+// plus their fp16 scales and biases.  One CTA of 19 warps per SM:
 //   warp 16     producer: TMA (cp.async.bulk.tensor, 128-byte swizzle) loads
-//               the codes of each stage into a ring of shared-memory slots,
-//               its lanes copy the scales and biases with cp.async whose
-//               completion arrives on the slot's mbarrier;
+//               the codes of each stage into a ring of shared-memory slots;
+//   warp 17     its lanes copy the stage's scales and biases with cp.async,
+//               whose completion arrives on the same slot mbarrier;
 //   warps 0-15  consumers: each takes one of 16 slots of a tile's groups
 //               (128 contiguous code bytes of every stage; the warp of a
 //               slot rotates from tile to tile), converts the codes in
 //               registers and issues the MMAs;
 //               the token values are staged once per (expert, chunk) in the
 //               B-fragment order, with their group sums;
-//   warp 17     epilogue: adds the 16 consumer partials of a tile in warp
-//               order and writes SiLU(gate) * up or the raw fp32 rows.
+//   warp 18     epilogue: adds the 16 slot partials of each row of a tile
+//               (slots 0-7 and 8-15 each in order, then the two halves) and
+//               writes SiLU(gate) * up or the raw fp32 rows.
 // Each CTA takes an equal contiguous range of the tile list (expert-major),
 // so the weight stream of the whole GPU is split evenly across the SMs.
 //

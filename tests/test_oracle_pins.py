@@ -413,6 +413,8 @@ def test_silu_closed_forms():
     ("tiny", {"H": 128, "I": 64, "E": 3, "k": 2, "T": 5}),
     ("entropy", {"H": 128, "I": 128, "E": 6, "T": 24, "inv_temperatures": (4.0, 1.5, 0.4)}),
     ("batched", {"H": 192, "I": 64, "E": 10, "k": 3, "T": 12}),
+    ("tiny", {"H": 128, "I": 192, "E": 4, "k": 2, "T": 6, "bits": 5}),
+    ("tiny", {"H": 192, "I": 128, "E": 4, "k": 2, "T": 6, "bits": 6}),
 ])
 def test_sparse_matches_dense_masked(name, over):
     cfg = workloads.CONFIGS[name].scaled(**over)

@@ -43,10 +43,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 CSRC = os.path.join(ROOT, "sparse_moe_expert_gb300", "csrc")
 # the products' kernel and its source, by the path the layer resolved to
-# (0 automatic, 1 streamed GEMV, 2 tcgen05 grouped GEMM, 3 tcgen05 small tiles)
-KERNEL_NAME = {1: "gemv_stream_kernel", 2: "tc_qmm_kernel", 3: "tc_small_kernel"}
-KERNEL_SRC = {1: os.path.join(CSRC, "gemv_stream.cu"), 2: os.path.join(CSRC, "gemm_tc.cu"),
-              3: os.path.join(CSRC, "gemm_tc_small.cu")}
+# (0 automatic, 1 streamed GEMV, 2 tcgen05 grouped GEMM)
+KERNEL_NAME = {1: "gemv_stream_kernel", 2: "tc_qmm_kernel"}
+KERNEL_SRC = {1: os.path.join(CSRC, "gemv_stream.cu"), 2: os.path.join(CSRC, "gemm_tc.cu")}
 
 
 def parse_args(argv=None):
@@ -58,7 +57,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample", type=int, default=0, help="oracle sample size (calls/tokens)")
-    p.add_argument("--path", default="auto", choices=["auto", "gemv", "tc", "tc_small"],
+    p.add_argument("--path", default="auto", choices=["auto", "gemv", "tc"],
                    help="kernel family for the two quantized products")
     p.add_argument("--layers", type=int, default=1,
                    help="layers chained per call in the timed graph (each layer's output is "
@@ -275,8 +274,7 @@ def run_ours(args):
     if args.experts:
         cfg = cfg.scaled(E=args.experts)
     layer_np = workloads.make_layer(cfg)
-    path = {"auto": moe.PATH_AUTO, "gemv": moe.PATH_GEMV, "tc": moe.PATH_TC,
-            "tc_small": moe.PATH_TC_SMALL}[args.path]
+    path = {"auto": moe.PATH_AUTO, "gemv": moe.PATH_GEMV, "tc": moe.PATH_TC}[args.path]
     layer = moe.MoELayer.from_workload(layer_np, dev, free_sources=True, path=path,
                                        groups=args.groups)
     T = cfg.T

@@ -69,8 +69,7 @@ enum { MOE_EPILOGUE_RAW = 0, MOE_EPILOGUE_SWIGLU = 1 };
 enum {
   MOE_PATH_AUTO = 0, /* chosen from the mean tokens per expert, T*kmax/E */
   MOE_PATH_GEMV = 1, /* CUDA-core grouped GEMV: decode and small batches */
-  MOE_PATH_TC = 2,   /* tcgen05 grouped GEMM (TMEM accumulators), many tokens per expert */
-  MOE_PATH_TC_SMALL = 3 /* tcgen05 with the codes in tensor memory, up to 16 tokens per tile */
+  MOE_PATH_TC = 2    /* tcgen05 grouped GEMM (TMEM accumulators), many tokens per expert */
 };
 /* ------------------------------------------------------------------------
  * moe_set_launch_overlap -- whether later launches of this library may
@@ -219,7 +218,11 @@ moe_status_t moe_router_topk(const uint16_t* x, const float* w_router, const flo
  * device current; make that first call before any stream capture.  All calls
  * share the array: calls whose executions overlap on the GPU race, so the
  * caller must order them (one stream, or events).  Nothing in the array
- * needs clearing between calls.
+ * needs clearing between calls.  The looked-up address belongs to the
+ * device's current context: after cudaDeviceReset the library's cached
+ * device addresses (this array's and the error word's of
+ * moe_get_device_error) are stale, so no entry point of the library may be
+ * called on that device again in the same process.
  * ---------------------------------------------------------------------- */
 #define MOE_ROUTER_NOALLOC_MAX_TOKENS 65536
 

@@ -8,7 +8,7 @@ does not build anything; calling into it without the built library raises.
 from ._lib import (DEVERR_BAD_EXPERT, DEVERR_BAD_INDEX, DEVERR_TIMEOUT, DROPPED, DTYPE_BF16,
                    DTYPE_F32,
                    EPILOGUE_RAW, EPILOGUE_SWIGLU, EXPORTS, PATH_AUTO, PATH_FLAG_K_GATED,
-                   PATH_FLAG_WEIGHTS_EARLY, PATH_GEMV, PATH_TC, PATH_TC_SMALL, path_k_range,
+                   PATH_FLAG_WEIGHTS_EARLY, PATH_GEMV, PATH_TC, path_k_range,
                    MoEError,
                    lib, lib_path)
 from .binding import (moe_abi_version, moe_combine, moe_down_qmm, moe_expert_counts_accumulate,
@@ -27,6 +27,6 @@ __all__ = [
     "moe_abi_version", "moe_set_launch_overlap", "moe_status_string", "moe_pack_gate_up", "moe_router_workspace_size",
     "moe_router_topk", "moe_route", "moe_route_grouped", "moe_permute", "moe_permute_capped", "moe_permute_rows", "moe_gate_up_qmm", "moe_down_qmm", "moe_combine",
     "moe_swiglu", "moe_get_device_error", "moe_selftest_wait_timeout", "qdesc", "EXPORTS", "DTYPE_F32", "DTYPE_BF16",
-    "EPILOGUE_RAW", "EPILOGUE_SWIGLU", "PATH_AUTO", "PATH_FLAG_K_GATED", "path_k_range", "PATH_FLAG_WEIGHTS_EARLY", "PATH_GEMV", "PATH_TC", "PATH_TC_SMALL",
+    "EPILOGUE_RAW", "EPILOGUE_SWIGLU", "PATH_AUTO", "PATH_FLAG_K_GATED", "path_k_range", "PATH_FLAG_WEIGHTS_EARLY", "PATH_GEMV", "PATH_TC",
     "DEVERR_BAD_EXPERT", "DEVERR_TIMEOUT", "DEVERR_BAD_INDEX", "DROPPED",
 ]

@@ -12,7 +12,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 6: "MOE_ERR_DEVICE"}
 DTYPE_F32, DTYPE_BF16 = 0, 1
 EPILOGUE_RAW, EPILOGUE_SWIGLU = 0, 1
-PATH_AUTO, PATH_GEMV, PATH_TC, PATH_TC_SMALL = 0, 1, 2, 3
+PATH_AUTO, PATH_GEMV, PATH_TC = 0, 1, 2
 PATH_FLAG_WEIGHTS_EARLY = 0x100  # moe_down_qmm: offsets/weights read before the wait
 PATH_FLAG_K_GATED = 0x200  # the product runs only for lo <= k <= hi (MOE_PATH_K_RANGE)
 

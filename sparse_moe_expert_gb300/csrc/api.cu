@@ -18,10 +18,6 @@ moe_status_t tc_qmm(const void* act, int act_kind, const int32_t* sorted,
                     const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
                     bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
                     int bits, void* out, int out_dtype, KGate gate, cudaStream_t st);
-moe_status_t tc_small_qmm(const void* act, int act_kind, const int32_t* sorted,
-                          const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
-                          bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
-                          int bits, void* out, int out_dtype, cudaStream_t st);
 bool tc_available();
 }  // namespace moe
 
@@ -143,7 +139,7 @@ static bool split_path(int path, int kmax, const int32_t* k_dev, bool allow_earl
   early = (u & MOE_PATH_FLAG_WEIGHTS_EARLY) != 0;
   if (early && !allow_early) return false;
   family = (int)(u & 0xFFu);
-  if (family < MOE_PATH_AUTO || family > MOE_PATH_TC_SMALL) return false;
+  if (family < MOE_PATH_AUTO || family > MOE_PATH_TC) return false;
   gate = moe::KGate{nullptr, 0, 0};
   if (u & MOE_PATH_FLAG_K_GATED) {
     const int lo = (int)((u >> 16) & 0xFFu), hi = (int)((u >> 24) & 0x7Fu);
@@ -197,9 +193,6 @@ extern "C" moe_status_t moe_gate_up_qmm(const uint16_t* x, const int32_t* sorted
     return moe::tc_qmm(x, act_kind, sorted_assign, expert_offsets, T, kmax, E, H, n_rows, swiglu,
                        w_q, w_s, w_b, bits, out, out_dtype, gate, st);
   }
-  if (p == MOE_PATH_TC_SMALL)
-    return moe::tc_small_qmm(x, act_kind, sorted_assign, expert_offsets, T, kmax, E, H, n_rows,
-                             swiglu, w_q, w_s, w_b, bits, out, out_dtype, st);
   return moe::gemv_qmm(x, act_kind, sorted_assign, expert_offsets, T, kmax, E, H, n_rows, swiglu,
                        w_q, w_s, w_b, bits, out, out_dtype, false, gate, st);
 }
@@ -232,9 +225,6 @@ extern "C" moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* 
     return moe::tc_qmm(h, act_kind, nullptr, expert_offsets, T, kmax, E, I, H, false, w_q, w_s,
                        w_b, bits, y, MOE_DTYPE_F32, gate, st);
   }
-  if (p == MOE_PATH_TC_SMALL)
-    return moe::tc_small_qmm(h, act_kind, nullptr, expert_offsets, T, kmax, E, I, H, false, w_q,
-                             w_s, w_b, bits, y, MOE_DTYPE_F32, st);
   return moe::gemv_qmm(h, act_kind, nullptr, expert_offsets, T, kmax, E, I, H, false, w_q, w_s,
                        w_b, bits, y, MOE_DTYPE_F32, early, gate, st);
 }

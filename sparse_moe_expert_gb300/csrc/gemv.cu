@@ -439,22 +439,17 @@ moe_status_t dispatch_gemv(const GemvParams& p, int bits, int max_tokens, int ma
 
 }  // namespace
 
-bool gemv_mma_supported(int act_kind, int K, int bits, int T);
 bool gemv_stream_supported(int bits, int K, int E);
 moe_status_t gemv_stream_qmm(const void* act, int act_kind, const int32_t* sorted,
                              const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
                              bool swiglu, const uint32_t* wq, const uint16_t* ws,
                              const uint16_t* wb, int bits, void* out, int out_dtype, bool early,
                              KGate gate, cudaStream_t st);
-moe_status_t gemv_mma_qmm(const void* act, int act_kind, const int32_t* sorted,
-                          const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
-                          bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
-                          void* out, int out_dtype, cudaStream_t st);
 
-// Entry used by the C-ABI wrappers (api.cu).  4-bit codes with K a multiple
-// of 256, bf16 activations and more than one token take the warp-MMA kernel
-// (gemv_mma.cu); the rest (one token, 8-bit codes, fp32 activations) this
-// file's kernel.  Only the streamed kernel takes a k gate.
+// Entry used by the C-ABI wrappers (api.cu).  Rows that are whole 128-byte
+// blocks of codes (4-bit K a multiple of 256, 8-bit of 128) take the
+// streamed kernel (gemv_stream.cu); other rows this file's kernel.  Only the
+// streamed kernel takes a k gate.
 moe_status_t gemv_qmm(const void* act, int act_kind, const int32_t* sorted,
                       const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
                       bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
@@ -464,9 +459,6 @@ moe_status_t gemv_qmm(const void* act, int act_kind, const int32_t* sorted,
     return gemv_stream_qmm(act, act_kind, sorted, offsets, T, kmax, E, K, n_rows, swiglu, wq, ws,
                            wb, bits, out, out_dtype, early, gate, st);
   if (gate.k != nullptr) return MOE_ERR_UNSUPPORTED;
-  if (gemv_mma_supported(act_kind, K, bits, T))
-    return gemv_mma_qmm(act, act_kind, sorted, offsets, T, kmax, E, K, n_rows, swiglu, wq, ws, wb,
-                        out, out_dtype, st);
   GemvParams p;
   p.act = act;
   p.act_kind = act_kind;

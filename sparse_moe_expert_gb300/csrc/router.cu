@@ -403,67 +403,16 @@ __device__ __forceinline__ void router_logit_tiles(const RouterParams& p, int t0
   }
 }
 
-template <int CL>
-__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kRouterThreads)
-    router_topk_kernel(RouterParams p) {
-  extern __shared__ __align__(16) float logits_s[];  // leader: [group tokens][E]
-  __shared__ __align__(8) uint64_t stage_bar;
+// Phase B for tokens [t0, t0 + nt) whose logits are in `logits_s`
+// ([token][E], shared memory): softmax, entropy and top-k, one warp per
+// token (warps 0 .. nwarps - 1 of the CTA).
+__device__ void router_phase_b(const RouterParams& p, const float* logits_s, int t0, int nt,
+                               int nwarps) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int E = p.E;
-  const int tpc = router_group_tokens(E);
-  const int t0 = (blockIdx.x / CL) * tpc;
-  const int nt = min(tpc, p.T - t0);
-  const uint32_t rank = cluster_ctarank();
-  const int e_lo = (int)rank * E / CL;
-  const int ne = ((int)rank + 1) * E / CL - e_lo;
-
-  // ---- Phase A: logits (every CTA of the cluster, into the leader) -------
-  // staged copies of the weight slice and token rows sit after the logits
-  float* ws_s = logits_s + tpc * E;
-  uint16_t* xs_s = reinterpret_cast<uint16_t*>(ws_s + (size_t)((E + CL - 1) / CL) * p.H);
-  bool staged_ok = true;
-  if (p.smem_stage) {
-    if (threadIdx.x == 0) {
-      mbar_init(&stage_bar, 1);
-      fence_barrier_init();
-    }
-    __syncthreads();
-    if (threadIdx.x == 0 && ne > 0) {
-      const uint32_t wbytes = (uint32_t)ne * p.H * 4u, xbytes = (uint32_t)nt * p.H * 2u;
-      mbar_arrive_expect_tx(&stage_bar, wbytes + xbytes);
-      // one copy per weight row (no kernel of this library writes router
-      // weights, so they are read before the wait on the previous kernel)
-      for (int e = 0; e < ne; ++e)
-        bulk_g2s(ws_s + (size_t)e * p.H, p.w + (int64_t)(e_lo + e) * p.H, (uint32_t)p.H * 4u,
-                 &stage_bar);
-    }
-  }
-  pdl_wait();
-  pdl_trigger();
-  if (p.smem_stage && threadIdx.x == 0 && ne > 0)
-    bulk_g2s(xs_s, p.x + (int64_t)t0 * p.H, (uint32_t)nt * p.H * 2u, &stage_bar);  // token rows
-  cluster_sync();  // the leader's shared memory is live before remote stores
-  const uint32_t lead = cluster_map(logits_s, 0);
-  if (p.smem_stage && ne > 0) {
-    staged_ok = mbar_wait(&stage_bar, 0, kWaitBudgetCycles);
-    if (!staged_ok && threadIdx.x == 0) raise_device_error(p.err, MOE_DEVERR_TIMEOUT);
-  }
-  if (ne > 0 && staged_ok) {
-    if (p.smem_stage) {
-      if (nt >= 8) router_logit_tiles<8, 4, true>(p, t0, nt, e_lo, ne, lead, xs_s, ws_s);
-      else router_logit_tiles<1, 1, true>(p, t0, nt, e_lo, ne, lead, xs_s, ws_s);
-    } else {
-      if (nt >= 8) router_logit_tiles<8, 4, false>(p, t0, nt, e_lo, ne, lead, nullptr, nullptr);
-      else router_logit_tiles<1, 1, false>(p, t0, nt, e_lo, ne, lead, nullptr, nullptr);
-    }
-  }
-  cluster_sync();  // all logits of the group are in the leader
-  if (rank != 0) return;
-
-  // ---- Phase B: softmax, entropy, top-k per token (one warp per token) ---
   const bool adaptive = p.k_fixed == 0;
   const int nsel = adaptive ? kAdaptiveMaxK : p.k_fixed;
-  for (int tl = warp; tl < nt; tl += kRouterWarps) {
+  for (int tl = warp; tl < nt; tl += nwarps) {
     const float* row = logits_s + tl * E;
     const int t = t0 + tl;
     float m = -INFINITY;
@@ -551,6 +500,67 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kRouterThreads)
     }
   }
 
+}
+
+template <int CL>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kRouterThreads)
+    router_topk_kernel(RouterParams p) {
+  extern __shared__ __align__(16) float logits_s[];  // leader: [group tokens][E]
+  __shared__ __align__(8) uint64_t stage_bar;
+  const int E = p.E;
+  const int tpc = router_group_tokens(E);
+  const int t0 = (blockIdx.x / CL) * tpc;
+  const int nt = min(tpc, p.T - t0);
+  const uint32_t rank = cluster_ctarank();
+  const int e_lo = (int)rank * E / CL;
+  const int ne = ((int)rank + 1) * E / CL - e_lo;
+
+  // ---- Phase A: logits (every CTA of the cluster, into the leader) -------
+  // staged copies of the weight slice and token rows sit after the logits
+  float* ws_s = logits_s + tpc * E;
+  uint16_t* xs_s = reinterpret_cast<uint16_t*>(ws_s + (size_t)((E + CL - 1) / CL) * p.H);
+  bool staged_ok = true;
+  if (p.smem_stage) {
+    if (threadIdx.x == 0) {
+      mbar_init(&stage_bar, 1);
+      fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && ne > 0) {
+      const uint32_t wbytes = (uint32_t)ne * p.H * 4u, xbytes = (uint32_t)nt * p.H * 2u;
+      mbar_arrive_expect_tx(&stage_bar, wbytes + xbytes);
+      // one copy per weight row (no kernel of this library writes router
+      // weights, so they are read before the wait on the previous kernel)
+      for (int e = 0; e < ne; ++e)
+        bulk_g2s(ws_s + (size_t)e * p.H, p.w + (int64_t)(e_lo + e) * p.H, (uint32_t)p.H * 4u,
+                 &stage_bar);
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
+  if (p.smem_stage && threadIdx.x == 0 && ne > 0)
+    bulk_g2s(xs_s, p.x + (int64_t)t0 * p.H, (uint32_t)nt * p.H * 2u, &stage_bar);  // token rows
+  cluster_sync();  // the leader's shared memory is live before remote stores
+  const uint32_t lead = cluster_map(logits_s, 0);
+  if (p.smem_stage && ne > 0) {
+    staged_ok = mbar_wait(&stage_bar, 0, kWaitBudgetCycles);
+    if (!staged_ok && threadIdx.x == 0) raise_device_error(p.err, MOE_DEVERR_TIMEOUT);
+  }
+  if (ne > 0 && staged_ok) {
+    if (p.smem_stage) {
+      if (nt >= 8) router_logit_tiles<8, 4, true>(p, t0, nt, e_lo, ne, lead, xs_s, ws_s);
+      else router_logit_tiles<1, 1, true>(p, t0, nt, e_lo, ne, lead, xs_s, ws_s);
+    } else {
+      if (nt >= 8) router_logit_tiles<8, 4, false>(p, t0, nt, e_lo, ne, lead, nullptr, nullptr);
+      else router_logit_tiles<1, 1, false>(p, t0, nt, e_lo, ne, lead, nullptr, nullptr);
+    }
+  }
+  cluster_sync();  // all logits of the group are in the leader
+  if (rank != 0) return;
+
+  // ---- Phase B: softmax, entropy, top-k per token (one warp per token) ---
+  router_phase_b(p, logits_s, t0, nt, kRouterWarps);
+
   if (gridDim.x == CL) {
     __syncthreads();
     finalize_batch(p);
@@ -567,10 +577,422 @@ __global__ void __launch_bounds__(kFinalizeThreads) router_finalize_kernel(Route
   finalize_batch(p);
 }
 
+// ---------------------------------------------------------------------------
+// Small batches (decode: up to kSmallMaxT tokens).  The router weight is
+// spread over a cluster of up to 16 CTAs instead of 8, one warp per expert,
+// so each SM brings in E / 16 weight rows (16 KB each for H 4096) before the
+// previous kernel ends; the token rows follow once it has.  Each warp runs
+// the canonical chains for its expert and every token, the leader CTA
+// receives the logits through distributed shared memory and does phase B,
+// the batch finalize and the fused grouping.
+constexpr int kSmallMaxT = 8;
+constexpr size_t kSmallStageBytes = 160 * 1024;  // weight rows + token rows per CTA
+// with the leader's logits (T E floats) or the grouping's scratch ((warps + 1) E ints)
+constexpr size_t kSmallMaxSmem = 200 * 1024;
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// Order-preserving map of fp32 values onto uint32 (larger value, larger key).
+__device__ __forceinline__ uint32_t f32_key(float v) {
+  const uint32_t b = __float_as_uint(v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_f32(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Phase B, the batch finalize and the grouping of a small batch in one warp
+// (T <= kSmallMaxT tokens, E <= 256, T * kmax <= 32): the results of
+// router_phase_b, finalize_batch and fused_permute (sums in the same
+// orders), with the selections in registers and shared memory and no
+// CTA-wide barriers.  Maxima and argmaxima use the warp's hardware
+// reductions on order-preserving keys (equal logits: the lower id).  The
+// batch mean entropy is the pairwise tree over 32 slots, zeros past T.
+// `scratch` is the logits' region: the counts and offsets (2 E words) take
+// its start once the logits are no longer needed, the selected ids and
+// weights (2 T kmax words) lie past max(2 E, T E) words.
+__device__ void router_tail_warp(const RouterParams& p, const float* logits_s, int* scratch) {
+  constexpr int kEL = 8;  // logits per lane
+  const int lane = threadIdx.x & 31;
+  const int E = p.E, T = p.T, kmax = p.kmax;
+  const bool adaptive = p.k_fixed == 0;
+  const int nsel = adaptive ? kAdaptiveMaxK : p.k_fixed;
+  const int gsz = p.groups > 0 ? E / p.groups : E;
+  int* ids_s = scratch + max(2 * E, T * E);                    // [T * kmax], past the logits
+  float* w_s = reinterpret_cast<float*>(ids_s + T * kmax);     // [T * kmax]
+  float ent_mine = 0.0f;  // lane t: token t's entropy
+  float sum_mine = 0.0f;  // lane t: token t's softmax denominator
+  for (int t = 0; t < T; ++t) {
+    const float* row = logits_s + t * E;
+    float lv[kEL];
+#pragma unroll
+    for (int j = 0; j < kEL; ++j) lv[j] = lane + 32 * j < E ? row[lane + 32 * j] : -INFINITY;
+    float ml = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kEL; ++j) ml = fmaxf(ml, lv[j]);
+    const float m = key_f32(__reduce_max_sync(0xFFFFFFFFu, f32_key(ml)));
+    float sm = 0.0f, s1 = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kEL; ++j) {
+      if (lane + 32 * j < E) {
+        const float z = __fsub_rn(lv[j], m);
+        const float ez = expf(z);
+        sm = __fadd_rn(sm, ez);
+        s1 = __fadd_rn(s1, __fmul_rn(ez, z));
+      }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      sm = __fadd_rn(sm, __shfl_xor_sync(0xFFFFFFFFu, sm, off));
+      s1 = __fadd_rn(s1, __shfl_xor_sync(0xFFFFFFFFu, s1, off));
+    }
+    const float ent = __fsub_rn(logf(sm), __fdiv_rn(s1, sm));
+    // top-nsel by repeated warp argmax (grouped: round r within group r)
+    unsigned taken = 0u;
+    int my_id = -1;
+    float my_v = -INFINITY;
+    for (int r = 0; r < nsel; ++r) {
+      float bv = -INFINITY;
+      int bi = 0x7FFFFFFF;
+#pragma unroll
+      for (int j = 0; j < kEL; ++j) {
+        const int e = lane + 32 * j;
+        if (e < E && !(taken & (1u << j)) && (p.groups <= 0 || e / gsz == r) &&
+            (lv[j] > bv || bi == 0x7FFFFFFF)) {
+          bv = lv[j];
+          bi = e;
+        }
+      }
+      const uint32_t mk = __reduce_max_sync(0xFFFFFFFFu, bi == 0x7FFFFFFF ? 0u : f32_key(bv));
+      const int wi = (int)__reduce_min_sync(
+          0xFFFFFFFFu, (bi != 0x7FFFFFFF && f32_key(bv) == mk) ? (unsigned)bi : 0x7FFFFFFFu);
+      if ((wi & 31) == lane) taken |= 1u << (wi >> 5);
+      if (lane == r) {
+        my_id = wi;
+        my_v = key_f32(mk);
+      }
+    }
+    const float my_z = lane < nsel ? expf(__fsub_rn(my_v, m)) : 0.0f;
+    // output slot of lane r's winner: its rank in the top-k order (larger
+    // logit, then lower id); the rounds of plain top-k are already in it
+    int slot = lane;
+    if (p.groups > 0) {
+      slot = 0;
+      for (int q = 0; q < nsel; ++q) {
+        const float qv = __shfl_sync(0xFFFFFFFFu, my_v, q);
+        const int qi = __shfl_sync(0xFFFFFFFFu, my_id, q);
+        if (q != lane && better(qv, qi, my_v, my_id)) ++slot;
+      }
+    }
+    // the selected exponentials in slot order, summed in that order
+    float denom = 0.0f;
+    if (!adaptive) {
+      if (p.renorm) {
+        for (int j = 0; j < nsel; ++j) {
+          const unsigned src = __ballot_sync(0xFFFFFFFFu, lane < nsel && slot == j);
+          denom = __fadd_rn(denom, __shfl_sync(0xFFFFFFFFu, my_z, __ffs(src) - 1));
+        }
+      } else {
+        denom = sm;
+      }
+    }
+    if (lane < nsel) {
+      ids_s[t * kmax + slot] = my_id;
+      w_s[t * kmax + slot] = adaptive ? my_z : __fdiv_rn(my_z, denom);
+    } else if (lane < kmax) {
+      ids_s[t * kmax + lane] = -1;
+      w_s[t * kmax + lane] = 0.0f;
+    }
+    if (lane == t) {
+      ent_mine = ent;
+      sum_mine = sm;
+    }
+  }
+  __syncwarp();
+  // batch mean entropy and k
+  float acc = lane < T ? ent_mine : 0.0f;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_down_sync(0xFFFFFFFFu, acc, off));
+  const float hbar = __fdiv_rn(__shfl_sync(0xFFFFFFFFu, acc, 0), (float)T);
+  int k = p.k_fixed;
+  if (k == 0) k = hbar < p.thr1 ? 1 : (hbar < p.thr2 ? 2 : 3);
+  if (adaptive) {
+    // the chosen k weights of every token renormalised (or over all experts)
+    for (int t = 0; t < T; ++t) {
+      const float ez = lane < kmax ? w_s[t * kmax + lane] : 0.0f;
+      float den = 0.0f;
+      if (p.renorm) {
+        for (int j = 0; j < k; ++j) den = __fadd_rn(den, __shfl_sync(0xFFFFFFFFu, ez, j));
+      } else {
+        den = __shfl_sync(0xFFFFFFFFu, sum_mine, t);
+      }
+      __syncwarp();
+      if (lane < kmax) {
+        if (lane < k) {
+          w_s[t * kmax + lane] = __fdiv_rn(ez, den);
+        } else {
+          w_s[t * kmax + lane] = 0.0f;
+          ids_s[t * kmax + lane] = -1;
+        }
+      }
+    }
+  }
+  __syncwarp();
+  // outputs
+  const int slots = T * kmax;
+  for (int a = lane; a < slots; a += 32) {
+    p.ids[a] = ids_s[a];
+    p.topw[a] = w_s[a];
+  }
+  if (lane < T) {
+    p.ws_ent[lane] = ent_mine;
+    p.ws_sum[lane] = sum_mine;
+  }
+  if (lane == 0) {
+    *p.k_dev = k;
+    *p.mean_ent = hbar;
+  }
+  if (!p.pm_sorted) return;
+  // the stable counting sort of moe_permute: counts, offsets, sorted rows
+  int* cnt = scratch;
+  int* off = scratch + E;
+  for (int x = lane; x < E; x += 32) cnt[x] = 0;
+  __syncwarp();
+  const int a = lane;
+  int e = -1;
+  if (a < slots && a % kmax < k) {
+    const int v = ids_s[a];
+    if (v >= 0 && v < E) e = v;
+    else raise_device_error(p.err, MOE_DEVERR_BAD_EXPERT);
+  }
+  if (e >= 0) atomicAdd(&cnt[e], 1);
+  __syncwarp();
+  const int chunk = (E + 31) / 32;
+  const int x0 = min(E, lane * chunk), x1 = min(E, x0 + chunk);
+  int run = 0;
+  for (int x = x0; x < x1; ++x) run += cnt[x];
+  int incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  int pos0 = incl - run;
+  for (int x = x0; x < x1; ++x) {
+    const int c = cnt[x];
+    off[x] = pos0;
+    p.pm_counts[x] = c;
+    p.pm_offsets[x] = pos0;
+    pos0 += c;
+  }
+  if (lane == 31) p.pm_offsets[E] = incl;
+  __syncwarp();
+  const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+  const int rank = __popc(peers & lanemask_lt());
+  if (a < slots) {
+    if (e >= 0) {
+      const int pos = off[e] + rank;
+      p.pm_sorted[pos] = a;
+      p.pm_inv_pos[a] = pos;
+    } else {
+      p.pm_inv_pos[a] = -1;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(512) router_small_kernel(RouterParams p, int lg_floats) {
+  extern __shared__ __align__(16) float rs_smem[];
+  float* logits_s = rs_smem;                 // leader: [T][E]; then the grouping's scratch
+  float* ws_s = rs_smem + lg_floats;         // this CTA's weight rows [ne][H]
+  __shared__ __align__(8) uint64_t wbar, xbar;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int E = p.E, H = p.H, nt = p.T;
+  const uint32_t rank = cluster_ctarank();
+  const int CL = (int)(gridDim.x);  // one cluster
+  const int e_lo = (int)rank * E / CL;
+  const int ne = ((int)rank + 1) * E / CL - e_lo;
+  uint16_t* xs_s = reinterpret_cast<uint16_t*>(ws_s + (size_t)ne * H);
+  cluster_arrive_relaxed();  // this CTA is running (waited for before remote stores)
+  if (threadIdx.x == 0) {
+    mbar_init(&wbar, 1);
+    mbar_init(&xbar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && ne > 0) {
+    // the weight rows: no kernel of this library writes router weights, so
+    // they are read before the wait on the previous kernel
+    mbar_arrive_expect_tx(&wbar, (uint32_t)ne * H * 4u);
+    for (int e = 0; e < ne; ++e)
+      bulk_g2s(ws_s + (size_t)e * H, p.w + (int64_t)(e_lo + e) * H, (uint32_t)H * 4u, &wbar);
+  }
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x == 0 && ne > 0) {
+    mbar_arrive_expect_tx(&xbar, (uint32_t)nt * H * 2u);
+    bulk_g2s(xs_s, p.x, (uint32_t)nt * H * 2u, &xbar);
+  }
+  bool ok = true;
+  if (ne > 0) {
+    ok = mbar_wait(&wbar, 0, kWaitBudgetCycles) && mbar_wait(&xbar, 0, kWaitBudgetCycles);
+    if (!ok && lane == 0) raise_device_error(p.err, MOE_DEVERR_TIMEOUT);
+  }
+  cluster_wait();
+  const uint32_t lead = cluster_map(logits_s, 0);
+  // ---- logits: warp w takes experts e_lo + w, + nwarps, ...; lane l the
+  // chunks l, l + 32, ... of every token, in the canonical order
+  const int nchunks = H >> 3;
+  for (int el = warp; ok && el < ne; el += nwarps) {
+    const float4* wr = reinterpret_cast<const float4*>(ws_s + (size_t)el * H);
+    const int e = e_lo + el;
+    const float bias = p.bias ? __ldg(p.bias + e) : 0.0f;
+    for (int t = 0; t < nt; ++t) {
+      const uint4* xr = reinterpret_cast<const uint4*>(xs_s + (size_t)t * H);
+      float acc = 0.0f;
+      for (int c = lane; c < nchunks; c += 32) {
+        const float4 wa = wr[2 * c], wb = wr[2 * c + 1];
+        const uint4 xv = xr[c];
+        const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          const float xf = (h & 1) ? __uint_as_float(xw[h >> 1] & 0xFFFF0000u)
+                                   : __uint_as_float(xw[h >> 1] << 16);
+          acc = fmaf(xf, wv[h], acc);
+        }
+      }
+      float v = acc;
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+      if (lane == 0) {
+        if (p.bias) v = __fadd_rn(v, bias);
+        v = __fmul_rn(v, p.inv_temp);
+        st_cluster_f32(lead + (uint32_t)(t * E + e) * 4u, v);
+      }
+    }
+  }
+  cluster_sync();  // every logit is in the leader
+  if (rank != 0) return;
+  if (E <= 256 && nt * p.kmax <= 32) {
+    if (warp == 0) router_tail_warp(p, logits_s, reinterpret_cast<int*>(logits_s));
+    return;
+  }
+  router_phase_b(p, logits_s, 0, nt, nwarps);
+  __syncthreads();
+  finalize_batch(p);
+  if (p.pm_sorted) {
+    __syncthreads();
+    fused_permute(p, reinterpret_cast<int*>(logits_s));  // the logits are no longer needed
+  }
+}
+
+// The cluster size for the small-batch router: 16 CTAs where the device can
+// co-schedule such a cluster and E >= 16, else 8 (or E when smaller).
+int small_router_cluster(int E, int threads, size_t smem) {
+  static int can16[moe_host::kMaxCachedDevices] = {};  // 0 unknown, 1 yes, -1 no
+  const int dev = moe_host::device_index();
+  if (E >= 16 && can16[dev] == 0) {
+    can16[dev] = -1;
+    // the occupancy query honours the kernel's shared-memory limit: raise it
+    // to the most this launcher asks for first
+    if (cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmallMaxSmem) == cudaSuccess &&
+        cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                             1) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(16);
+      cfg.blockDim = dim3(threads);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 16;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, router_small_kernel, &cfg) == cudaSuccess && n > 0)
+        can16[dev] = 1;
+    }
+    cudaGetLastError();
+  }
+  if (E >= 16 && can16[dev] > 0) return 16;
+  return E >= 8 ? 8 : E;
+}
+
+// Launches the small-batch router if the batch qualifies; false: use the
+// general kernels.
+bool launch_router_small(const RouterParams& p, cudaStream_t st, moe_status_t* status) {
+  if (p.T < 1 || p.T > kSmallMaxT || p.groups < 0) return false;
+  const int wcl = p.E >= 16 ? 16 : (p.E >= 8 ? 8 : p.E);  // widest cluster considered
+  const int ne_max = (p.E + 7) / 8;                        // experts per CTA at 8 CTAs
+  const size_t stage = (size_t)ne_max * p.H * 4 + (size_t)p.T * p.H * 2;
+  if (stage > kSmallStageBytes) return false;
+  // the leader's logits, then the grouping's scratch ((warps + 1) E ints)
+  const int warps_max = (p.E + 7) / 8 > 16 ? 16 : (p.E + 7) / 8;
+  if (p.pm_sorted && (p.T * p.kmax > 32 * warps_max || p.E > 256)) return false;
+  int cl = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    const int c = pass == 0 ? wcl : (wcl == 16 ? 8 : wcl);
+    const int ne = (p.E + c - 1) / c;
+    const int warps = ne > 16 ? 16 : (ne < 1 ? 1 : ne);
+    // the leader's logits, the block grouping's scratch, or the one-warp
+    // tail's scratch (counts, offsets, ids and weights)
+    int lg = p.T > warps + 1 ? p.T * p.E : (warps + 1) * p.E;
+    lg = max(lg, max(2 * p.E, p.T * p.E) + 2 * p.T * p.kmax);
+    lg = (lg + 3) & ~3;  // the weight rows after it start 16-byte aligned
+    const size_t smem = (size_t)lg * 4 + (size_t)ne * p.H * 4 + (size_t)p.T * p.H * 2;
+    if (pass == 0) {
+      const int got = small_router_cluster(p.E, warps * 32, smem);
+      if (got != c) continue;
+    }
+    if (p.pm_sorted && p.T * p.kmax > warps * 32) return false;
+    cl = c;
+    static bool set_max[moe_host::kMaxCachedDevices] = {};
+    const int dev = moe_host::device_index();
+    if (smem > kSmallMaxSmem) return false;
+    if (!set_max[dev]) {
+      if (cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kSmallMaxSmem) != cudaSuccess) {
+        *status = MOE_ERR_CUDA;
+        return true;
+      }
+      set_max[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cl);
+    cfg.blockDim = dim3(warps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = moe_host::pdl_enabled() ? 2 : 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, router_small_kernel, p, lg);
+    if (e != cudaSuccess) cudaGetLastError();
+    *status = e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    return true;
+  }
+  return false;
+}
+
 // Kernel 1 over ceil(T / group) clusters, then the batch finalize unless a
 // single cluster did it inline.
 moe_status_t launch_router(const RouterParams& p, cudaStream_t st) {
   using namespace moe_host;
+  moe_status_t small_status = MOE_OK;
+  if (launch_router_small(p, st, &small_status)) return small_status;
   const int tpc = router_group_tokens(p.E);
   const int ngroups = (p.T + tpc - 1) / tpc;
   if (ngroups > 0) {

@@ -43,7 +43,14 @@ class ExpertHealthMonitor:
     ``window_s`` of ``clock`` time have passed since it opened.  An alert is
     raised when the last ``alert_windows`` closed windows all have a
     standard deviation above ``std_threshold``.  ``accumulate`` and
-    ``reduce`` default to the library's device entry points."""
+    ``reduce`` default to the library's device entry points.
+
+    For a layer with an expert capacity, the ``counts`` buffer holds the
+    assignments each expert kept, never more than the capacity, so an
+    overloaded expert shows as a count at the capacity rather than as its
+    full demand and the deviation understates the imbalance.  To watch the
+    demand of a capped layer, record the per-expert counts of the routed ids
+    (``topk_ids``) instead."""
 
     def __init__(self, E: int, device, window_s: float = 60.0, std_threshold: float = 20.0,
                  alert_windows: int = 5, clock: Callable[[], float] = time.monotonic,

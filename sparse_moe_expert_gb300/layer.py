@@ -16,7 +16,7 @@ import torch
 
 from . import binding as B
 from ._lib import (EPILOGUE_RAW, EPILOGUE_SWIGLU, PATH_AUTO, PATH_FLAG_WEIGHTS_EARLY, PATH_GEMV,
-                   PATH_TC, PATH_TC_SMALL, MoEError, path_k_range)
+                   PATH_TC, MoEError, path_k_range)
 
 FUSE_ENV = "MOE_GB300_FUSE_GATE_UP"
 TC_MIN_TOKENS_PER_EXPERT = 24  # mirrors the library's automatic path choice
@@ -160,9 +160,12 @@ class MoELayer:
         group = 32 if self.E <= 256 else 16
         one_group = (T + group - 1) // group == 1
         n = 1 + (0 if one_group else 1)
-        fused_permute = (one_group and self.E <= 256 and T * self.kmax <= 512
-                         and self.capacity is None)
-        n += 0 if fused_permute else 1
+        fused = one_group and self.E <= 256 and T * self.kmax <= 512
+        if self.capacity is None:
+            n += 0 if fused else 1
+        else:
+            # the capped grouping, after the group-limited route's own grouping
+            n += 1 + ((0 if fused else 1) if self.groups > 0 else 0)
         if self.k_split(T):
             return n + 6  # row permute, two gated gate_up and two gated down launches, combine
         n += 1 if self.resolved_path(T) == PATH_TC else 0
@@ -211,10 +214,18 @@ class MoELayer:
         # router, top-k and the expert grouping (one launch for small batches)
         ev = _Timer(events, "route")
         if self.capacity is not None:
-            # router, then the grouping with each expert's capacity
-            B.moe_router_topk(x, self.router_w, self.logit_bias, it, self.k_fixed, self.kmax,
-                              self.thr[0], self.thr[1], self.renormalize, b["topk_ids"],
-                              b["topk_w"], b["k_dev"], b["mean_entropy"], b["ws"])
+            # router (group-limited or top-k), then the grouping with each
+            # expert's capacity (it replaces the uncapped grouping that the
+            # group-limited route also writes)
+            if self.groups > 0:
+                B.moe_route_grouped(x, self.router_w, self.logit_bias, it, self.groups,
+                                    self.kmax, self.renormalize, b["topk_ids"], b["topk_w"],
+                                    b["k_dev"], b["mean_entropy"], b["ws"], b["counts"],
+                                    b["offsets"], b["sorted"], b["inv_pos"])
+            else:
+                B.moe_router_topk(x, self.router_w, self.logit_bias, it, self.k_fixed, self.kmax,
+                                  self.thr[0], self.thr[1], self.renormalize, b["topk_ids"],
+                                  b["topk_w"], b["k_dev"], b["mean_entropy"], b["ws"])
             B.moe_permute_capped(b["topk_ids"], b["k_dev"], self.E, self.capacity, b["counts"],
                                  b["offsets"], b["sorted"], b["inv_pos"])
         elif self.groups > 0:

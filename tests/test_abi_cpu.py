@@ -130,7 +130,7 @@ def test_header_constants_match_the_binding(tmp_path):
         '#include <stdio.h>\n#include "moe_gb300.h"\n'
         "int main(void) {\n"
         '  printf("%d %d %d %d %d %d %d\\n", MOE_PATH_GEMV, MOE_PATH_TC, MOE_PATH_FLAG_WEIGHTS_EARLY,\n'
-        "         MOE_PATH_FLAG_K_GATED, MOE_PATH_K_RANGE(2, 3), MOE_DROPPED, MOE_PATH_TC_SMALL);\n"
+        "         MOE_PATH_FLAG_K_GATED, MOE_PATH_K_RANGE(2, 3), MOE_DROPPED, MOE_PATH_AUTO);\n"
         "  return 0;\n}\n")
     exe = tmp_path / "consts"
     subprocess.run([cc, "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
@@ -139,4 +139,4 @@ def test_header_constants_match_the_binding(tmp_path):
                                            check=True).stdout.split()]
     assert vals == [moe.PATH_GEMV, moe.PATH_TC, moe.PATH_FLAG_WEIGHTS_EARLY,
                     moe.PATH_FLAG_K_GATED, moe.path_k_range(2, 3), moe.DROPPED,
-                    moe.PATH_TC_SMALL]
+                    moe.PATH_AUTO]

@@ -12,11 +12,11 @@ from test_parity_gpu import CFG, SMALL
 
 pytestmark = pytest.mark.gpu
 
-PATHS = ["gemv", "tc", "tc_small"]
+PATHS = ["gemv", "tc"]
 
 
 def path_id(moe, name):
-    return {"gemv": moe.PATH_GEMV, "tc": moe.PATH_TC, "tc_small": moe.PATH_TC_SMALL}[name]
+    return {"gemv": moe.PATH_GEMV, "tc": moe.PATH_TC}[name]
 
 
 def run_layer(moe, layer_np, x_bits, path, batch=0, **kw):
@@ -99,7 +99,7 @@ def test_fused_gate_up_bit_identical_to_two_products(cuda_lib, path, bits, T, k,
             # removed and the per-group affine applied in fp32 (the offset
             # cancellation scales the accumulation rounding by about
             # 128 / mean|q - 7.5|); prefill tensor cores: weights rounded to bf16
-            tol = {"gemv": 1e-4, "tc_small": 1e-4, "tc": 3e-3}[path]
+            tol = {"gemv": 1e-4, "tc": 3e-3}[path]
             assert rel_l2(got[lo:hi], want) <= tol
 
 
@@ -308,7 +308,8 @@ def test_k_gate_arguments_are_checked(cuda_lib):
            cuda_lib.PATH_GEMV | cuda_lib.path_k_range(2, 1),       # hi < lo
            cuda_lib.PATH_TC | cuda_lib.path_k_range(1, 3),         # hi > kmax
            cuda_lib.PATH_AUTO | cuda_lib.path_k_range(1, 2),       # gate needs a family
-           cuda_lib.PATH_TC_SMALL | cuda_lib.path_k_range(1, 2),
+           3 | cuda_lib.path_k_range(1, 2),                         # no such family
+           3,
            cuda_lib.PATH_GEMV | (1 << 16)]                         # range without the flag
     for flags in bad:
         with pytest.raises(cuda_lib.MoEError):

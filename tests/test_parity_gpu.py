@@ -302,6 +302,28 @@ def test_layer_with_capacity_matches_oracle(cuda_lib, path):
     assert cuda_lib.moe_get_device_error() == 0
 
 
+def test_group_limited_layer_with_capacity_matches_oracle(cuda_lib):
+    """Group-limited routing and an expert capacity together: the ids follow
+    the per-group rule and the grouping keeps each expert's C lowest
+    assignments, against the oracle's grouped routing with its capacity."""
+    cfg = SMALL["batched_s"].scaled(E=24, k=4)
+    layer_np = workloads.make_layer(cfg)
+    x_bits = workloads.make_tokens(cfg)
+    C = 5
+    layer = cuda_lib.MoELayer.from_workload(layer_np, dev(), groups=4, capacity=C)
+    out = to_np(layer(cuda_lib.bf16_from_bits(x_bits, dev())))
+    ref_r = oracle.route(x_bits, layer_np.router_w, layer_np.logit_bias,
+                         cfg.inv_temperature(0), 4, 4, True, groups=4)
+    ref = oracle.moe_forward(x_bits, layer_np, routing=ref_r, capacity=C)
+    b = layer.buffers(cfg.T)
+    assert np.array_equal(to_np(b["topk_ids"]), ref_r.ids)
+    assert (ref.perm.inv_pos == oracle.DROPPED).sum() > 0   # the case drops something
+    assert np.array_equal(to_np(b["counts"]), ref.perm.counts)
+    assert np.array_equal(to_np(b["inv_pos"]), ref.perm.inv_pos)
+    assert_layer_close(out, ref.out, f"groups 4, capacity {C}")
+    assert cuda_lib.moe_get_device_error() == 0
+
+
 @pytest.mark.parametrize("E", [1, 7, 64, 1000, 1024])
 def test_expert_health_kernels_match_oracle(cuda_lib, E):
     """Window accumulation is exact (int64); the least-activated expert is

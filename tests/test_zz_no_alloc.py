@@ -14,6 +14,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -82,6 +83,32 @@ def test_noalloc_matches_workspace_router_on_two_calls(cuda_lib, case):
         assert int(got[2].item()) == int(ref[2].item())
         assert np.allclose(got[1].cpu().numpy(), ref[1].cpu().numpy(), rtol=1e-6, atol=1e-7)
         assert abs(float(got[3].item()) - float(ref[3].item())) <= 1e-6
+
+
+@pytest.mark.parametrize("case", [CASES[0], CASES[2]], ids=["decode_token", "adaptive"])
+def test_noalloc_matches_oracle_on_two_calls(cuda_lib, case):
+    """The allocation-free router against the oracle directly: ids and the
+    batch's k exactly, weights and the mean entropy within the router's
+    tolerances, on two calls in a row (the adaptive case also exercises the
+    entropy and softmax sums that live in the shared scratch)."""
+    name, T, H, E, k_fixed, kmax, renorm, use_bias, it = case
+    lib = cuda_lib.lib()
+    dev = torch.device("cuda:0")
+    w_np = workloads.normal_f32(3, 1, (E, H), 0.05)
+    b_np = workloads.normal_f32(3, 2, (E,), 0.5) if use_bias else None
+    w = torch.from_numpy(w_np).to(dev)
+    bias = torch.from_numpy(b_np).to(dev) if use_bias else None
+    for call in range(2):
+        x_bits = workloads.normal_bf16(3, 20 + call, (T, H), 1.0)
+        x = torch.from_numpy(x_bits).view(torch.bfloat16).to(dev)
+        got = _outputs(T, kmax, dev)
+        assert _call_noalloc(lib, x, w, bias, it, k_fixed, kmax, renorm, got) == 0
+        torch.cuda.synchronize()
+        ref = oracle.route(x_bits, w_np, b_np, it, k_fixed, kmax, renorm)
+        assert np.array_equal(got[0].cpu().numpy(), ref.ids), f"{name} call {call}: ids"
+        assert int(got[2].item()) == ref.k
+        assert np.allclose(got[1].cpu().numpy(), ref.weights, rtol=1e-6, atol=1e-7)
+        assert abs(float(got[3].item()) - float(ref.mean_entropy)) <= 1e-4
 
 
 def test_noalloc_rejects_batches_above_its_scratch(cuda_lib):

@@ -66,6 +66,8 @@ def parse_args(argv=None):
                    help="group-limited routing: best expert of each of G groups (k = G)")
     p.add_argument("--experts", type=int, default=0,
                    help="smaller expert pool (same per-call work; for profiling captures)")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the other workloads and the decode launch variants")
     return p.parse_args(argv)
 
 
@@ -259,37 +261,25 @@ def workload_config(cfg):
 
 # ----------------------------------------------------------------- ours
 
-def run_ours(args):
+def workload_measure(moe, cfg, dev, rank, world, steps, warmup, layer_kw, nl=1, clocks_gpu=None,
+                     per_kernel=True, layer_np=None):
+    """One workload on this GPU: every layer call of a step (256 single-token
+    calls for batch-1 decode, one call per activation batch otherwise)
+    captured once in a CUDA graph and replayed `steps` times after `warmup`
+    replays; then the same calls launched eagerly with CUDA events around
+    each kernel (launch overlap off) for per-kernel durations, and the
+    algorithmic bytes and FLOPs of the active experts.  Returns the layer,
+    its inputs and a dict of results."""
     import torch
-    import torch.distributed as dist
-
-    import sparse_moe_expert_gb300 as moe
-
-    rank, world, local = dist_env()
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    cfg = workloads.CONFIGS[args.config]
-    if args.experts:
-        cfg = cfg.scaled(E=args.experts)
-    layer_np = workloads.make_layer(cfg)
-    path = {"auto": moe.PATH_AUTO, "gemv": moe.PATH_GEMV, "tc": moe.PATH_TC}[args.path]
-    layer = moe.MoELayer.from_workload(layer_np, dev, free_sources=True, path=path,
-                                       groups=args.groups)
+    if layer_np is None:
+        layer_np = workloads.make_layer(cfg)
+    layer = moe.MoELayer.from_workload(layer_np, dev, **layer_kw)
     T = cfg.T
-    # one step = every layer call of the workload: 256 single-token calls for
-    # batch-1 decode, one call per activation batch otherwise (the entropy
-    # workload's three batches, each with its own router temperature, so each
-    # of k = 1, 2, 3 runs once per step)
-    n_batches = cfg.batches
-    calls = cfg.calls * n_batches
+    calls = cfg.calls * cfg.batches
     x_bits = rank_tokens(cfg, rank, world)
     x_dev = moe.bf16_from_bits(x_bits, dev)
     out_dev = torch.empty((calls * T, cfg.H), dtype=torch.bfloat16, device=dev)
     temps = [cfg.inv_temperature(c // cfg.calls) for c in range(calls)]
-
-    nl = max(1, args.layers)
     chain = [torch.empty((T, cfg.H), dtype=torch.bfloat16, device=dev) for _ in range(2)]
 
     def step(events=None):
@@ -318,84 +308,160 @@ def run_ours(args):
     with torch.cuda.graph(graph):
         step()
     torch.cuda.synchronize()
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, warmup)):
         graph.replay()
     torch.cuda.synchronize()
-    gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
-    gpu_id = str(gpu_id) if gpu_id is not None else str(local)
-    if gpu_id and not gpu_id.startswith("GPU-") and "-" in gpu_id:
-        gpu_id = "GPU-" + gpu_id
-    barrier()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(gpu_id) as clk:
-        e0.record()
-        for _ in range(args.steps):
-            graph.replay()
-        e1.record()
-        torch.cuda.synchronize()
-    barrier()
-    ms = e0.elapsed_time(e1) / args.steps
-    ms = max_over_ranks(ms, world, dev)
-    tokens_per_step = calls * T
-    value = tokens_per_step * nl * world / (ms / 1000.0)  # layer-calls: tokens x layers
-    clocks = clk.summary()
-
-    # per-kernel durations: the same calls launched eagerly with CUDA events
-    # around each kernel (the graph above is not instrumented).  The first
-    # eager step also records each call's active experts and k.
-    ksteps = max(1, min(args.steps, 20))
-    events = {}
+    clk = ClockSampler(clocks_gpu) if clocks_gpu else None
+    if clk:
+        clk.__enter__()
+    e0.record()
+    for _ in range(steps):
+        graph.replay()
+    e1.record()
     torch.cuda.synchronize()
-    # each kernel on its own: no overlap with the kernel before it
-    pdl_prev = moe.moe_set_launch_overlap(False)
+    if clk:
+        clk.__exit__()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, world, dev)
+    del graph
+    res = {"ms": ms, "calls": calls, "T": T, "nl": nl,
+           "clocks": clk.summary() if clk else None}
+    # per-call active experts and k (one eager pass)
     per_call = []
     for c in range(calls):
         layer.forward(x_dev[c * T:(c + 1) * T], out=out_dev[c * T:(c + 1) * T],
                       inv_temperature=temps[c])
         bufs = layer.buffers(T)
         per_call.append((int((bufs["counts"] > 0).sum().item()), int(bufs["k_dev"].item())))
+    res["per_call"] = per_call
     cnt = layer.buffers(T)["counts"].double().cpu()
-    count_stats = {"experts": int(cnt.numel()), "active": int((cnt > 0).sum().item()),
-                   "min": int(cnt.min().item()), "max": int(cnt.max().item()),
-                   "std": round(float(cnt.std(unbiased=False).item()), 3)}
-    torch.cuda.synchronize()
-    for _ in range(ksteps):
-        step(events)
-    torch.cuda.synchronize()
-    moe.moe_set_launch_overlap(pdl_prev)
-    ktot = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in events.items()}
-    kt = {k: ktot[k] / len(v) for k, v in events.items()}
-    peaks, peak_src = load_peaks()
+    res["count_stats"] = {"experts": int(cnt.numel()), "active": int((cnt > 0).sum().item()),
+                          "min": int(cnt.min().item()), "max": int(cnt.max().item()),
+                          "std": round(float(cnt.std(unbiased=False).item()), 3)}
     # algorithmic bytes of the two products, summed over one step's calls:
     # the active experts' packed weights (codes + fp16 scale + fp16 bias)
-    # plus the token rows read by gate_up
-    gu_step_bytes = sum(active_bytes_per_expert(cfg, "gate_up") * na + T * cfg.H * 2
-                        for na, _ in per_call)
-    dn_step_bytes = sum(active_bytes_per_expert(cfg, "down") * na for na, _ in per_call)
-    gu_bytes = gu_step_bytes / calls          # per launch (average)
-    dn_bytes = dn_step_bytes / calls
-    gu_gbs = gu_step_bytes * ksteps / (ktot["gate_up"] * 1e-3) / 1e9
-    dn_gbs = dn_step_bytes * ksteps / (ktot["down"] * 1e-3) / 1e9
-    # algorithmic FLOPs of the two products (2 * rows * assignments * K)
-    gu_step_flops = sum(2.0 * T * k * 2 * cfg.I * cfg.H for _, k in per_call)
-    dn_step_flops = sum(2.0 * T * k * cfg.I * cfg.H for _, k in per_call)
-    gu_flops = gu_step_flops / calls
-    gu_tflops = gu_step_flops * ksteps / (ktot["gate_up"] * 1e-3) / 1e12
-    dn_tflops = dn_step_flops * ksteps / (ktot["down"] * 1e-3) / 1e12
+    # plus the token rows read by gate_up; FLOPs 2 * rows * assignments * K
+    res["gu_step_bytes"] = sum(active_bytes_per_expert(cfg, "gate_up") * na + T * cfg.H * 2
+                               for na, _ in per_call)
+    res["dn_step_bytes"] = sum(active_bytes_per_expert(cfg, "down") * na for na, _ in per_call)
+    res["gu_step_flops"] = sum(2.0 * T * k * 2 * cfg.I * cfg.H for _, k in per_call)
+    res["dn_step_flops"] = sum(2.0 * T * k * cfg.I * cfg.H for _, k in per_call)
+    if per_kernel:
+        ksteps = max(1, min(steps, 20))
+        events = {}
+        torch.cuda.synchronize()
+        # each kernel on its own: no overlap with the kernel before it
+        pdl_prev = moe.moe_set_launch_overlap(False)
+        for _ in range(ksteps):
+            step(events)
+        torch.cuda.synchronize()
+        moe.moe_set_launch_overlap(pdl_prev)
+        res["ktot"] = {k: sum(a.elapsed_time(b) for a, b in v) / ksteps for k, v in events.items()}
+        res["kavg"] = {k: sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in events.items()}
+    return layer, layer_np, x_bits, temps, res
+
+
+def workload_summary(moe, cfg, layer, res, peaks, peak_src):
+    """The measured numbers of one workload as the JSON fields of its line."""
+    calls, T, nl, ms = res["calls"], res["T"], res["nl"], res["ms"]
+    kt = res.get("ktot", {})
+    gu_b, dn_b = res["gu_step_bytes"], res["dn_step_bytes"]
+    gu_f, dn_f = res["gu_step_flops"], res["dn_step_flops"]
     path_used = layer.resolved_path(T)
-    tensor_bound = path_used == moe.PATH_TC and cfg.name == "prefill"
-    kernel_label = KERNEL_NAME[path_used] + " (gate_up, SiLU*up epilogue)"
     ks = layer.k_split(T)
+    kernel_label = KERNEL_NAME[path_used] + " (gate_up, SiLU*up epilogue)"
     if ks:
         kernel_label = (f"{KERNEL_NAME[moe.PATH_GEMV]} for k < {ks}, {KERNEL_NAME[moe.PATH_TC]} "
                         f"for k >= {ks} (gate_up, SiLU*up epilogue; both queued, gated on k)")
-    kernel_src = KERNEL_SRC[path_used]
+    gu_ms = kt.get("gate_up", 0.0)
+    dn_ms = kt.get("down", 0.0)
+    gu_gbs = gu_b / (gu_ms * 1e-3) / 1e9 if gu_ms else None
+    dn_gbs = dn_b / (dn_ms * 1e-3) / 1e9 if dn_ms else None
+    gu_tflops = gu_f / (gu_ms * 1e-3) / 1e12 if gu_ms else None
+    dn_tflops = dn_f / (dn_ms * 1e-3) / 1e12 if dn_ms else None
+    layer_gbs = (gu_b + dn_b) * nl / (ms * 1e-3) / 1e9
+    layer_tflops = (gu_f + dn_f) * nl / (ms * 1e-3) / 1e12
+    tensor_bound = path_used == moe.PATH_TC and cfg.name == "prefill"
+    if tensor_bound:
+        roof = {"bound": "tensor", "achieved": gu_tflops, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": gu_tflops / peaks["bf16_tflops"] if gu_tflops else None,
+                "frac_of_sustained": (gu_tflops / peaks.get("bf16_tflops_sustained",
+                                                            peaks["bf16_tflops"])
+                                      if gu_tflops else None),
+                "layer_frac": layer_tflops / peaks["bf16_tflops"],
+                "kernel": kernel_label, "algorithmic_flops_per_launch": gu_f / calls,
+                "peak_source": peak_src}
+    else:
+        roof = {"bound": "hbm", "achieved": gu_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gu_gbs / peaks["hbm_gbs"] if gu_gbs else None,
+                "layer_frac": layer_gbs / peaks["hbm_gbs"],
+                "kernel": kernel_label, "algorithmic_bytes_per_launch": gu_b / calls,
+                "peak_source": peak_src}
+    kern = {"gate_up_us": gu_ms * 1e3 / calls if gu_ms else None,
+            "down_us": dn_ms * 1e3 / calls if dn_ms else None,
+            "gate_up_gbs": gu_gbs, "down_gbs": dn_gbs,
+            "gate_up_tflops": gu_tflops, "down_tflops": dn_tflops,
+            "layer_us_per_call": ms * 1e3 / (calls * nl), "layer_gbs": layer_gbs,
+            "layer_tflops": layer_tflops,
+            "active_experts_and_k_per_call": sorted(set(res["per_call"])),
+            "expert_counts_last_call": res["count_stats"],
+            "per_kernel_us": {k: v * 1e3 for k, v in res.get("kavg", {}).items()}}
+    return roof, kern
+
+
+def oracle_one_thread(cfg_name, n):
+    """The oracle sample timed in a fresh process with one BLAS/OpenMP thread."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    out = subprocess.run([sys.executable, os.path.abspath(__file__), "--impl", "reference",
+                          "--config", cfg_name, "--steps", "1", "--warmup", "0",
+                          "--cpu-sample", str(n)], capture_output=True, text=True, env=env,
+                         cwd=ROOT, timeout=600)
+    for line in out.stdout.splitlines():
+        if line.startswith("{"):
+            d = json.loads(line)
+            return {"value": d["value"], "cores": d["cpu_baseline"]["cores"],
+                    "sample": d["cpu_baseline"]["sample"]}
+    return None
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import sparse_moe_expert_gb300 as moe
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = workloads.CONFIGS[args.config]
+    if args.experts:
+        cfg = cfg.scaled(E=args.experts)
+    path = {"auto": moe.PATH_AUTO, "gemv": moe.PATH_GEMV, "tc": moe.PATH_TC}[args.path]
+    gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    gpu_id = str(gpu_id) if gpu_id is not None else str(local)
+    if gpu_id and not gpu_id.startswith("GPU-") and "-" in gpu_id:
+        gpu_id = "GPU-" + gpu_id
+    nl = max(1, args.layers)
+    peaks, peak_src = load_peaks()
+
+    layer, layer_np, x_bits, temps, res = workload_measure(
+        moe, cfg, dev, rank, world, args.steps, args.warmup,
+        dict(free_sources=True, path=path, groups=args.groups), nl=nl, clocks_gpu=gpu_id)
+    T, calls, ms = res["T"], res["calls"], res["ms"]
+    tokens_per_step = calls * T
+    value = tokens_per_step * nl * world / (ms / 1000.0)  # layer-calls: tokens x layers
+    clocks = res["clocks"]
+    roof, kern = workload_summary(moe, cfg, layer, res, peaks, peak_src)
+    kernel_src = KERNEL_SRC[layer.resolved_path(T)]
     traffic = None
     try:
         with open(TRAFFIC_FILE) as f:
@@ -405,6 +471,7 @@ def run_ours(args):
                     traffic = rec.get("gate_up_dram_bytes_per_launch")
     except (OSError, ValueError):
         pass
+    roof["traffic"] = traffic
 
     # end to end through the public API with pinned host buffers
     x_host = torch.from_numpy(x_bits).view(torch.bfloat16).pin_memory()
@@ -417,7 +484,8 @@ def run_ours(args):
                                inv_temperature=temps[c])
     e2e_step()
     torch.cuda.synchronize()
-    barrier()
+    if world > 1:
+        dist.barrier()
     t0 = time.perf_counter()
     for _ in range(esteps):
         e2e_step()
@@ -435,33 +503,60 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": f"u{cfg.bits} affine weights x bf16 tokens, f32 accumulate",
         "data": "synthetic", "config": dict(workload_config(cfg), layers=nl, groups=args.groups),
-        "roofline": ({"bound": "tensor", "achieved": gu_tflops, "peak": peaks["bf16_tflops"],
-                      "unit": "TFLOP/s", "frac": gu_tflops / peaks["bf16_tflops"],
-                      "frac_of_sustained": gu_tflops / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]),
-                      "traffic": traffic, "kernel": kernel_label,
-                      "algorithmic_flops_per_launch": gu_flops, "peak_source": peak_src}
-                     if tensor_bound else
-                     {"bound": "hbm", "achieved": gu_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                      "frac": gu_gbs / peaks["hbm_gbs"], "traffic": traffic,
-                      "kernel": kernel_label,
-                      "algorithmic_bytes_per_launch": gu_bytes, "peak_source": peak_src}),
-        "kernels": {"gate_up_us": kt["gate_up"] * 1e3, "gate_up_gbs": gu_gbs,
-                    "gate_up_tflops": gu_tflops, "down_tflops": dn_tflops,
-                    "down_us": kt["down"] * 1e3, "down_gbs": dn_gbs,
-                    "layer_us_per_call": ms * 1e3 / (calls * nl),
-                    "layer_gbs": (gu_step_bytes + dn_step_bytes) * nl / (ms * 1e-3) / 1e9,
-                    "layer_tflops": (gu_step_flops + dn_step_flops) * nl / (ms * 1e-3) / 1e12,
-                    "active_experts_and_k_per_call": sorted(set(per_call)),
-                    "expert_counts_last_call": count_stats,
-                    "per_kernel_us": {k: v * 1e3 for k, v in kt.items()}},
+        "roofline": roof, "kernels": kern,
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                    "reasons": clocks["reasons"], "samples": clocks["samples"]},
         "e2e": e2e,
         "gpu_launches": layer.launches_per_call(T) * calls * nl * args.steps,
     }
+    del layer
+    torch.cuda.empty_cache()
+
+    if world == 1 and not args.no_configs and args.config == "decode" and not args.experts \
+            and nl == 1 and args.groups == 0 and path == moe.PATH_AUTO:
+        # the other workloads of the layer, measured the same way in this run
+        cfgs = {}
+        csteps = max(3, min(args.steps, 20))
+        for name in ("tiny", "batched", "prefill", "entropy"):
+            c = workloads.CONFIGS[name]
+            lay, _, _, _, r = workload_measure(moe, c, dev, rank, world, csteps, args.warmup,
+                                               dict(free_sources=True), clocks_gpu=gpu_id)
+            rf, kn = workload_summary(moe, c, lay, r, peaks, peak_src)
+            cfgs[name] = {"config": workload_config(c), "value": r["calls"] * r["T"] / (r["ms"] / 1e3),
+                          "unit": "tokens/s", "ms_per_step": r["ms"], "steps": csteps,
+                          "roofline": rf, "kernels": kn,
+                          "clocks": {k: r["clocks"][k] for k in ("sm_mhz", "sm_max_mhz", "reasons",
+                                                                  "samples")},
+                          "gpu_launches": lay.launches_per_call(r["T"]) * r["calls"] * csteps}
+            del lay
+            torch.cuda.empty_cache()
+        line["configs"] = cfgs
+        # the decode layer's launch-count variants (page "oMLX MoE gate/up 融合
+        # 优化", 总结: one fewer launch per layer with gate and up fused): the
+        # unfused product (gate, up, activation) and launches without overlap,
+        # per layer call and for four chained layers
+        ab = {}
+        for label, kw, nlay, pdl in (("fused", {}, 1, True),
+                                     ("unfused", {"fuse_gate_up": False}, 1, True),
+                                     ("fused_no_overlap", {}, 1, False),
+                                     ("fused_4_chained", {}, 4, True),
+                                     ("unfused_4_chained", {"fuse_gate_up": False}, 4, True)):
+            prev = moe.moe_set_launch_overlap(pdl)
+            lay, _, _, _, r = workload_measure(moe, cfg, dev, rank, world, csteps, args.warmup,
+                                               dict(free_sources=False, **kw), nl=nlay,
+                                               clocks_gpu=None, per_kernel=False,
+                                               layer_np=layer_np)
+            moe.moe_set_launch_overlap(prev)
+            ab[label] = {"layer_us_per_call": r["ms"] * 1e3 / (r["calls"] * nlay),
+                         "kernels_per_layer": lay.launches_per_call(r["T"]), "layers": nlay}
+            del lay
+            torch.cuda.empty_cache()
+        line["decode_launch_variants"] = ab
+
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # the oracle as it stands, repeated on the same bounded sample until
-        # about ten seconds of host work have been timed
+        # about ten seconds of host work have been timed; then the same sample
+        # with one thread in a fresh process
         n = args.cpu_sample or default_sample(cfg)
         tok = wall = cpu = 0.0
         reps = 0
@@ -473,6 +568,10 @@ def run_ours(args):
                                 "cores": round(cpu / wall, 1), "kind": "oracle",
                                 "sample": f"{n} {unit} of the same workload, {reps} times "
                                           f"({wall:.1f} s)"}
+        one = oracle_one_thread(cfg.name, n)
+        if one:
+            line["cpu_baseline"]["one_thread"] = {"value": one["value"], "unit": "tokens/s",
+                                                  "cores": one["cores"], "sample": one["sample"]}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -13,8 +13,8 @@ __all__ = [
     "router_logits", "softmax_entropy", "batch_mean_entropy", "entropy_k", "topk_ids",
     "routing_weights", "group_top1_ids", "route", "Routing", "permute", "Permutation", "unpack_codes",
     "dequant", "DROPPED", "QDesc", "can_fuse", "pack_gate_up", "qmm_raw", "silu", "swiglu",
-    "moe_forward", "Forward", "dense_masked_forward", "bf16_to_f64", "ENTROPY_THRESHOLDS",
-    "expert_health",
+    "moe_forward", "Forward", "dense_masked_forward", "bf16_to_f64", "f64_to_bf16_bits",
+    "ENTROPY_THRESHOLDS", "expert_health",
 ]
 
 # Entropy bands of the adaptive top-k rule, page [B] section 2.2.
@@ -38,6 +38,16 @@ def _router_lib():
 def bf16_to_f64(x_bits: np.ndarray) -> np.ndarray:
     """Raw bf16 bit patterns (uint16) -> float64, exactly."""
     return (np.asarray(x_bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def f64_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """float64 -> raw bf16 bit patterns, through fp32: round to nearest even
+    to fp32, then to nearest even to bf16 (the layer rounds its fp32 output
+    the same way; a chained layer's input is the previous layer's output).
+    Finite values only."""
+    b = np.asarray(a, dtype=np.float64).astype(np.float32).view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    return b.astype(np.uint16)
 
 
 # --------------------------------------------------------------------------

@@ -315,3 +315,53 @@ def test_k_gate_arguments_are_checked(cuda_lib):
         with pytest.raises(cuda_lib.MoEError):
             cuda_lib.moe_down_qmm(b["h"], b["offsets"], b["k_dev"], cfg.T, layer.kmax, d.q, d.s,
                                   d.b, cfg.bits, b["y"], flags)
+
+
+@pytest.mark.parametrize("name,T", [("decode", 1), ("batched", 24)])
+def test_three_chained_layers_in_one_graph_match_the_oracle(cuda_lib, name, T):
+    """Three layers captured in one CUDA graph, layer l's bf16 output feeding
+    layer l+1 (the launches of consecutive layers overlap): every layer's
+    output matches the oracle applied to that layer's input.  (The oracle's
+    own three-layer chain is no reference for the end result: the per-layer
+    rounding differences compound and can move a routing near a tie.)"""
+    cfg = CFG[name].scaled(H=1024, I=1536, E=16, T=T, calls=1)
+    layer_np = workloads.make_layer(cfg)
+    x_bits = workloads.make_tokens(cfg)[:T]
+    d = dev()
+    layer = cuda_lib.MoELayer.from_workload(layer_np, d)
+    x0 = cuda_lib.bf16_from_bits(x_bits, d)
+    outs = [torch.empty_like(x0) for _ in range(3)]
+
+    def chain():
+        inp = x0
+        for o in outs:
+            layer.forward(inp, out=o)
+            inp = o
+
+    chain()
+    torch.cuda.synchronize()
+    for o in outs:
+        o.zero_()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            chain()
+    torch.cuda.current_stream().wait_stream(s)
+    graph.replay()
+    torch.cuda.synchronize()
+
+    def bits(t):
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+    inp = x_bits
+    for li, o in enumerate(outs):
+        got = to_np(o)
+        ref = oracle.moe_forward(inp, layer_np)
+        ids = to_np(layer.buffers(T)["topk_ids"]) if li == len(outs) - 1 else None
+        if ids is not None:   # the buffers hold the last layer's routing
+            assert np.array_equal(ids, ref.routing.ids)
+        assert_layer_close(got, ref.out, f"{name} chained layer {li}")
+        inp = bits(o)
+    assert cuda_lib.moe_get_device_error() == 0

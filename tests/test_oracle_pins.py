@@ -506,3 +506,22 @@ def test_expert_health_two_levels_and_ties():
     # the page's alert level: 20 activations of spread
     c = np.array([0, 40] * 32, np.int64)
     assert oracle.expert_health(c)[2] == 20.0
+
+
+def test_f64_to_bf16_bits_rounds_to_nearest_even():
+    """bf16 keeps 8 significant bits.  Halfway cases go to the even
+    neighbour: 1 + 2^-8 lies between 1 (even) and 1 + 2^-7 and goes to 1;
+    1 + 3 2^-8 lies between 1 + 2^-7 and 1 + 2^-6 (even) and goes up; just
+    above a halfway point rounds up; any other value lands within half a
+    unit in the last place."""
+    cases = [(1.0, 1.0), (1.0 + 2.0 ** -8, 1.0), (1.0 + 3 * 2.0 ** -8, 1.0 + 2.0 ** -6),
+             (1.0 + 2.0 ** -8 + 2.0 ** -20, 1.0 + 2.0 ** -7), (-2.5, -2.5), (0.0, 0.0),
+             (3.0e38, 2.0 ** 127 * (1 + 98 / 128))]
+    for v, want in cases:
+        got = oracle.bf16_to_f64(oracle.f64_to_bf16_bits(np.array([v])))[0]
+        assert got == want, (v, got, want)
+    rng = np.random.default_rng(5)
+    v = rng.normal(0, 3, 1000) * 10.0 ** rng.integers(-8, 8, 1000)
+    got = oracle.bf16_to_f64(oracle.f64_to_bf16_bits(v))
+    ulp = 2.0 ** (np.floor(np.log2(np.abs(v))) - 7)
+    assert np.all(np.abs(got - v) <= ulp / 2 * (1 + 1e-9))

@@ -31,8 +31,12 @@
  * - Tensors are dense, row-major, with the shapes given below.  Every
  *   pointer must be 16-byte aligned.
  * - bf16 and fp16 values travel as their raw 16-bit patterns (uint16_t).
- * - Packed codes: a row of `cols` b-bit codes (b = 4 or 8) is stored as
- *   uint32 words; element i sits in word i/(32/b) at bit b*(i mod (32/b)).
+ * - Packed codes: a row of `cols` b-bit codes (b = 4, 5, 6 or 8) is one
+ *   little-endian bit stream over uint32 words: element i occupies bits
+ *   [b*i, b*i + b) of the row (for 4 and 8 bits: word i/(32/b), bit
+ *   b*(i mod (32/b))).  A group of 64 codes is 2b whole words.  5- and 6-bit
+ *   codes take the GEMV family only (MOE_PATH_TC returns MOE_ERR_UNSUPPORTED)
+ *   and no k gate.
  *   Dequantized weight = scale * code + bias, where scale and bias are fp16
  *   and shared by 64 consecutive elements of the row (group size 64 along
  *   the contraction axis).  Page [C], section 融合原理.
@@ -136,7 +140,7 @@ int moe_abi_version(void);
  * gu_s, gu_b          out: fp16 [E, 2*I, H/64].
  * Returns MOE_ERR_INCOMPATIBLE (nothing written) when the descriptors
  * differ -- the caller keeps the unfused path; MOE_ERR_UNSUPPORTED for a
- * descriptor this library cannot run (not quantized, bits not 4/8, group
+ * descriptor this library cannot run (not quantized, bits not 4/5/6/8, group
  * not 64, mode not affine, a linear bias, scale dtype not fp16).
  * ---------------------------------------------------------------------- */
 enum { MOE_QMODE_AFFINE = 0 };
@@ -352,7 +356,7 @@ moe_status_t moe_permute_rows(const uint16_t* x, const int32_t* sorted_assign,
  *                 Both forms give bitwise the same result.
  * sorted_assign, expert_offsets, k_dev  from moe_permute / moe_router_topk.
  * w_q             uint32 [E, n_rows, H*bits/32]; w_s, w_b fp16 [E, n_rows, H/64].
- * bits            4 or 8.
+ * bits            4, 5, 6 or 8 (5 and 6: the GEMV family, no k gate).
  * path            MOE_PATH_*, optionally | MOE_PATH_K_RANGE(lo, hi).
  * ---------------------------------------------------------------------- */
 moe_status_t moe_gate_up_qmm(const uint16_t* x, const int32_t* sorted_assign,

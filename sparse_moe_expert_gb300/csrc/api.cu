@@ -18,6 +18,10 @@ moe_status_t tc_qmm(const void* act, int act_kind, const int32_t* sorted,
                     const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
                     bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
                     int bits, void* out, int out_dtype, KGate gate, cudaStream_t st);
+moe_status_t gemv_bits_qmm(const void* act, int act_kind, const int32_t* sorted,
+                           const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
+                           bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
+                           int bits, void* out, int out_dtype, cudaStream_t st);
 bool tc_available();
 }  // namespace moe
 
@@ -118,9 +122,11 @@ extern "C" int moe_set_launch_overlap(int enable) {
   return prev;
 }
 
-// The tensor-core path also needs rows of at least 128 code bytes (K * bits / 8).
+// The tensor-core path also needs rows of at least 128 code bytes (K * bits / 8)
+// and 4- or 8-bit codes; 5- and 6-bit codes always take the GEMV family.
 static int pick_path(int path, int T, int kmax, int E, int K, int bits) {
   if (path != MOE_PATH_AUTO) return path;
+  if (bits != 4 && bits != 8) return MOE_PATH_GEMV;
   const int64_t per_expert = (int64_t)T * kmax / E;
   return (per_expert >= kTcMinTokensPerExpert && (int64_t)K * bits / 8 >= 128 &&
           moe::tc_available())
@@ -167,7 +173,7 @@ extern "C" moe_status_t moe_gate_up_qmm(const uint16_t* x, const int32_t* sorted
   using namespace moe_host;
   if (!common_shape_ok(T, kmax, E)) return MOE_ERR_INVALID_ARG;
   if (H <= 0 || H % 64 != 0 || n_rows <= 0 || n_rows % 64 != 0) return MOE_ERR_INVALID_ARG;
-  if (bits != 4 && bits != 8) return MOE_ERR_UNSUPPORTED;
+  if (bits != 4 && bits != 5 && bits != 6 && bits != 8) return MOE_ERR_UNSUPPORTED;
   if (epilogue != MOE_EPILOGUE_RAW && epilogue != MOE_EPILOGUE_SWIGLU) return MOE_ERR_INVALID_ARG;
   if (out_dtype != MOE_DTYPE_F32 && out_dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
   if (epilogue == MOE_EPILOGUE_RAW && out_dtype != MOE_DTYPE_F32) return MOE_ERR_UNSUPPORTED;
@@ -189,7 +195,7 @@ extern "C" moe_status_t moe_gate_up_qmm(const uint16_t* x, const int32_t* sorted
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int p = pick_path(family, T, kmax, E, H, bits);
   if (p == MOE_PATH_TC) {
-    if (!moe::tc_available()) return MOE_ERR_UNSUPPORTED;
+    if (!moe::tc_available() || (bits != 4 && bits != 8)) return MOE_ERR_UNSUPPORTED;
     return moe::tc_qmm(x, act_kind, sorted_assign, expert_offsets, T, kmax, E, H, n_rows, swiglu,
                        w_q, w_s, w_b, bits, out, out_dtype, gate, st);
   }
@@ -205,7 +211,7 @@ extern "C" moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* 
   using namespace moe_host;
   if (!common_shape_ok(T, kmax, E)) return MOE_ERR_INVALID_ARG;
   if (I <= 0 || I % 64 != 0 || H <= 0 || H % 64 != 0) return MOE_ERR_INVALID_ARG;
-  if (bits != 4 && bits != 8) return MOE_ERR_UNSUPPORTED;
+  if (bits != 4 && bits != 5 && bits != 6 && bits != 8) return MOE_ERR_UNSUPPORTED;
   if (h_dtype != MOE_DTYPE_F32 && h_dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
   int family = 0;
   bool early = false;
@@ -221,7 +227,7 @@ extern "C" moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int p = pick_path(family, T, kmax, E, I, bits);
   if (p == MOE_PATH_TC) {
-    if (!moe::tc_available()) return MOE_ERR_UNSUPPORTED;
+    if (!moe::tc_available() || (bits != 4 && bits != 8)) return MOE_ERR_UNSUPPORTED;
     return moe::tc_qmm(h, act_kind, nullptr, expert_offsets, T, kmax, E, I, H, false, w_q, w_s,
                        w_b, bits, y, MOE_DTYPE_F32, gate, st);
   }

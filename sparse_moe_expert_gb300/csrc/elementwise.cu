@@ -141,7 +141,8 @@ extern "C" moe_status_t moe_pack_gate_up(const moe_qdesc_t* gd, const moe_qdesc_
       gd->group_size != ud->group_size || gd->mode != ud->mode || gd->has_bias != ud->has_bias ||
       gd->rows != ud->rows || gd->cols != ud->cols || gd->scale_dtype != ud->scale_dtype)
     return MOE_ERR_INCOMPATIBLE;
-  if (gd->quantized != 1 || (gd->bits != 4 && gd->bits != 8) || gd->group_size != 64 ||
+  if (gd->quantized != 1 || (gd->bits != 4 && gd->bits != 5 && gd->bits != 6 && gd->bits != 8) ||
+      gd->group_size != 64 ||
       gd->mode != MOE_QMODE_AFFINE || gd->has_bias != 0 || gd->scale_dtype != MOE_SCALE_F16)
     return MOE_ERR_UNSUPPORTED;
   const int I = gd->rows, H = gd->cols;

@@ -445,16 +445,26 @@ moe_status_t gemv_stream_qmm(const void* act, int act_kind, const int32_t* sorte
                              bool swiglu, const uint32_t* wq, const uint16_t* ws,
                              const uint16_t* wb, int bits, void* out, int out_dtype, bool early,
                              KGate gate, cudaStream_t st);
+moe_status_t gemv_bits_qmm(const void* act, int act_kind, const int32_t* sorted,
+                           const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
+                           bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
+                           int bits, void* out, int out_dtype, cudaStream_t st);
 
-// Entry used by the C-ABI wrappers (api.cu).  Rows that are whole 128-byte
-// blocks of codes (4-bit K a multiple of 256, 8-bit of 128) take the
-// streamed kernel (gemv_stream.cu); other rows this file's kernel.  Only the
-// streamed kernel takes a k gate.
+// Entry used by the C-ABI wrappers (api.cu).  5- and 6-bit codes take their
+// own kernel (gemv_bits.cu); 4- and 8-bit rows that are whole 128-byte
+// blocks of codes (4-bit K a multiple of 256, 8-bit of 128) the streamed
+// kernel (gemv_stream.cu); other rows this file's kernel.  Only the streamed
+// kernel takes a k gate.
 moe_status_t gemv_qmm(const void* act, int act_kind, const int32_t* sorted,
                       const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
                       bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
                       int bits, void* out, int out_dtype, bool early, KGate gate,
                       cudaStream_t st) {
+  if (bits == 5 || bits == 6) {
+    if (gate.k != nullptr) return MOE_ERR_UNSUPPORTED;
+    return gemv_bits_qmm(act, act_kind, sorted, offsets, T, kmax, E, K, n_rows, swiglu, wq, ws, wb,
+                         bits, out, out_dtype, st);
+  }
   if (gemv_stream_supported(bits, K, E))
     return gemv_stream_qmm(act, act_kind, sorted, offsets, T, kmax, E, K, n_rows, swiglu, wq, ws,
                            wb, bits, out, out_dtype, early, gate, st);

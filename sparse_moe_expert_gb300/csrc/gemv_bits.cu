@@ -1,0 +1,248 @@
+// Grouped GEMV for 5- and 6-bit affine codes: the two quantized products
+// when the codes are not 4 or 8 bits wide.
+//
+// Page "oMLX MoE gate/up 融合优化：qwen35_moe_gate_up 实现剖析", 如何验证正确性
+// (its test list covers the 5-, 6- and 8-bit families besides 4-bit) and
+// 融合原理 (the gathered product with the [gate; up] matrix, split,
+// SwitchGLU activation, down projection).
+//
+// Codes.  A row's codes form one little-endian bit stream over its uint32
+// words: element i sits at bits [b i, b i + b).  A group of 64 codes is 2b
+// whole words (10 for 5 bits, 12 for 6), so groups start on word
+// boundaries and a row's scales and biases index groups as for 4 and 8 bits.
+//
+// Work.  An item is (active expert, chunk of up to kBtTokens of its tokens,
+// block of 8 weight features); the persistent CTAs (two per SM) take equal
+// contiguous ranges of the item list.  Warp w of an item computes feature
+// f = 8 block + w: for SwiGLU its gate row f and up row n_out + f, else row f.
+// Lane l takes codes 2l and 2l + 1 of every group (one funnel shift over the
+// group's words brings both), dequantizes them in fp32 (s q + b, s and b
+// exact from fp16) and accumulates them against each token's two values;
+// the 32 lane partials are added by a fixed xor butterfly.  A row's value
+// depends only on its own codes, scales, biases and the tokens, so the fused
+// gate_up product equals the separate gate and up products bit for bit.
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBtThreads = 256;
+constexpr int kBtWarps = kBtThreads / 32;
+constexpr int kBtTokens = 8;  // tokens per item
+constexpr int kBtMaxE = 1024;
+
+enum BtMode { kBtSwiglu = 0, kBtRaw = 1 };
+enum BtAct { kBtActX = 0, kBtActF32 = 1, kBtActBf16 = 2 };
+
+struct BtParams {
+  const void* act;  // x [T, K] bf16 (gathered by token), or h [rows, K] (by sorted row)
+  int act_kind;
+  const int32_t* sorted;   // sorted_assign (kBtActX)
+  const int32_t* offsets;  // [E+1]
+  int T, kmax, E, K;
+  int n_rows;  // weight rows per expert
+  int n_out;   // output columns: n_rows / 2 (SWIGLU) or n_rows
+  int blocks;  // feature blocks of 8 per (expert, chunk)
+  const uint32_t* wq;
+  const uint16_t* ws;
+  const uint16_t* wb;
+  void* out;
+  int out_dtype;
+  unsigned int* err;
+};
+
+// Activation value k of row `row` as fp32 (bf16 rounding for fp32 rows, as
+// the other GEMV paths apply).
+__device__ __forceinline__ float bt_act(const BtParams& p, int64_t row, int64_t k) {
+  if (p.act_kind == kBtActF32)
+    return bf16_bits_to_f32(f32_to_bf16_rne(__ldg(static_cast<const float*>(p.act) + row * p.K + k)));
+  return bf16_bits_to_f32(__ldg(static_cast<const uint16_t*>(p.act) + row * p.K + k));
+}
+
+template <int BITS, int MODE>
+__global__ void __launch_bounds__(kBtThreads) gemv_bits_kernel(BtParams p) {
+  constexpr int kGroupWords = 2 * BITS;  // 64 codes of a group
+  constexpr uint32_t kMask = (1u << BITS) - 1u;
+  __shared__ int act_e[kBtMaxE + 1], act_lo[kBtMaxE + 1], act_m[kBtMaxE + 1], act_base[kBtMaxE + 1];
+  __shared__ int n_act_sh;
+  __shared__ int wtot[kBtWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();
+  pdl_trigger();
+
+  // active experts in id order, with segment start and length
+  if (tid == 0) n_act_sh = 0;
+  __syncthreads();
+  for (int base = 0; base < p.E; base += kBtThreads) {
+    const int e = base + tid;
+    int lo = 0, m = 0;
+    if (e < p.E) {
+      lo = __ldg(p.offsets + e);
+      m = __ldg(p.offsets + e + 1) - lo;
+    }
+    const bool act = m > 0;
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, act);
+    if (lane == 0) wtot[warp] = __popc(bal);
+    __syncthreads();
+    int before = n_act_sh;
+    for (int w = 0; w < warp; ++w) before += wtot[w];
+    if (act) {
+      const int a = before + __popc(bal & lanemask_lt());
+      act_e[a] = e;
+      act_lo[a] = lo;
+      act_m[a] = m;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int s = 0;
+      for (int w = 0; w < kBtWarps; ++w) s += wtot[w];
+      n_act_sh += s;
+    }
+    __syncthreads();
+  }
+  const int n_act = n_act_sh;
+  // items before each active expert: chunks of kBtTokens tokens x feature blocks
+  if (warp == 0) {
+    int carry = 0;
+    for (int a0 = 0; a0 < n_act; a0 += 32) {
+      const int a = a0 + lane;
+      int v = a < n_act ? ((act_m[a] + kBtTokens - 1) / kBtTokens) * p.blocks : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, v, off);
+        if (lane >= off) v += y;
+      }
+      if (a < n_act) act_base[a + 1] = carry + v;
+      carry += __shfl_sync(0xFFFFFFFFu, v, 31);
+    }
+    if (lane == 0) act_base[0] = 0;
+  }
+  __syncthreads();
+  const int64_t n_items = act_base[n_act];
+  const int64_t it0 = n_items * blockIdx.x / gridDim.x;
+  const int64_t it1 = n_items * (blockIdx.x + 1) / gridDim.x;
+  const int ngroups = p.K / 64;
+  const int64_t row_words = (int64_t)p.K * BITS / 32;
+  // this lane's codes 2 lane, 2 lane + 1 of a group: bits [2 lane b, 2 lane b + 2b)
+  const int bit0 = 2 * lane * BITS;
+  const int w0 = bit0 >> 5, sh = bit0 & 31;
+
+  for (int64_t it = it0; it < it1; ++it) {
+    int lo = 0, hi = n_act - 1;  // last a with act_base[a] <= it
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (act_base[mid] <= it) lo = mid;
+      else hi = mid - 1;
+    }
+    const int a = lo;
+    const int local = (int)(it - act_base[a]);
+    const int c = local / p.blocks, blk = local - c * p.blocks;
+    const int r0 = act_lo[a] + c * kBtTokens;  // first sorted row of the chunk
+    const int nt = min(kBtTokens, act_m[a] - c * kBtTokens);
+    const int f = blk * 8 + warp;              // this warp's feature
+    if (f >= p.n_out) continue;
+    // activation rows of the chunk's tokens
+    int64_t arow[kBtTokens];
+#pragma unroll
+    for (int n = 0; n < kBtTokens; ++n) {
+      const int r = r0 + min(n, nt - 1);
+      arow[n] = p.act_kind == kBtActX ? (int64_t)(__ldg(p.sorted + r) / p.kmax) : (int64_t)r;
+    }
+    const int64_t ebase = (int64_t)act_e[a] * p.n_rows;
+    constexpr int kRows = MODE == kBtSwiglu ? 2 : 1;
+    int64_t wrow[kRows];
+    wrow[0] = ebase + f;
+    if (MODE == kBtSwiglu) wrow[kRows - 1] = ebase + p.n_out + f;
+    float acc[kRows][kBtTokens];
+#pragma unroll
+    for (int q = 0; q < kRows; ++q)
+#pragma unroll
+      for (int n = 0; n < kBtTokens; ++n) acc[q][n] = 0.0f;
+    for (int g = 0; g < ngroups; ++g) {
+      // this lane's two token values of group g, per token
+      float x0[kBtTokens], x1[kBtTokens];
+#pragma unroll
+      for (int n = 0; n < kBtTokens; ++n) {
+        x0[n] = n < nt ? bt_act(p, arow[n], (int64_t)g * 64 + 2 * lane) : 0.0f;
+        x1[n] = n < nt ? bt_act(p, arow[n], (int64_t)g * 64 + 2 * lane + 1) : 0.0f;
+      }
+#pragma unroll
+      for (int q = 0; q < kRows; ++q) {
+        const uint32_t* gw = p.wq + wrow[q] * row_words + (int64_t)g * kGroupWords;
+        const uint32_t lo_w = __ldg(gw + w0);
+        const uint32_t hi_w = w0 + 1 < kGroupWords ? __ldg(gw + w0 + 1) : 0u;
+        const uint32_t v = __funnelshift_r(lo_w, hi_w, sh);
+        const float q0 = (float)(v & kMask), q1 = (float)((v >> BITS) & kMask);
+        const float s = f16_bits_to_f32(__ldg(p.ws + wrow[q] * ngroups + g));
+        const float b = f16_bits_to_f32(__ldg(p.wb + wrow[q] * ngroups + g));
+        const float d0 = fmaf(s, q0, b), d1 = fmaf(s, q1, b);
+#pragma unroll
+        for (int n = 0; n < kBtTokens; ++n) acc[q][n] = fmaf(d1, x1[n], fmaf(d0, x0[n], acc[q][n]));
+      }
+    }
+    // the 32 lane partials of every row and token, by a fixed xor butterfly
+#pragma unroll
+    for (int q = 0; q < kRows; ++q)
+#pragma unroll
+      for (int n = 0; n < kBtTokens; ++n)
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+          acc[q][n] = __fadd_rn(acc[q][n], __shfl_xor_sync(0xFFFFFFFFu, acc[q][n], off));
+#pragma unroll
+    for (int n = 0; n < kBtTokens; ++n) {
+      if (lane != n || n >= nt) continue;
+      const int64_t orow = (int64_t)r0 + n;
+      if (MODE == kBtSwiglu) {
+        const float hv = swiglu_f32(acc[0][n], acc[kRows - 1][n]);
+        if (p.out_dtype == MOE_DTYPE_BF16)
+          static_cast<uint16_t*>(p.out)[orow * p.n_out + f] = f32_to_bf16_rne(hv);
+        else
+          static_cast<float*>(p.out)[orow * p.n_out + f] = hv;
+      } else {
+        static_cast<float*>(p.out)[orow * p.n_out + f] = acc[0][n];
+      }
+    }
+  }
+}
+
+template <int BITS, int MODE>
+moe_status_t launch_bits(const BtParams& p, cudaStream_t st) {
+  return moe_host::launch(gemv_bits_kernel<BITS, MODE>, 2 * moe_host::sm_count(), kBtThreads, 0,
+                          st, p);
+}
+
+}  // namespace
+
+moe_status_t gemv_bits_qmm(const void* act, int act_kind, const int32_t* sorted,
+                           const int32_t* offsets, int T, int kmax, int E, int K, int n_rows,
+                           bool swiglu, const uint32_t* wq, const uint16_t* ws, const uint16_t* wb,
+                           int bits, void* out, int out_dtype, cudaStream_t st) {
+  if ((bits != 5 && bits != 6) || K % 64 != 0 || E > kBtMaxE) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)T * kmax == 0) return MOE_OK;
+  BtParams p;
+  p.act = act;
+  p.act_kind = act_kind;
+  p.sorted = sorted;
+  p.offsets = offsets;
+  p.T = T;
+  p.kmax = kmax;
+  p.E = E;
+  p.K = K;
+  p.n_rows = n_rows;
+  p.n_out = swiglu ? n_rows / 2 : n_rows;
+  p.blocks = (p.n_out + 7) / 8;
+  p.wq = wq;
+  p.ws = ws;
+  p.wb = wb;
+  p.out = out;
+  p.out_dtype = out_dtype;
+  p.err = moe_host::device_error_word();
+  if ((int64_t)p.blocks * ((int64_t)T * kmax + E) >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  if (bits == 5)
+    return swiglu ? launch_bits<5, kBtSwiglu>(p, st) : launch_bits<5, kBtRaw>(p, st);
+  return swiglu ? launch_bits<6, kBtSwiglu>(p, st) : launch_bits<6, kBtRaw>(p, st);
+}
+
+}  // namespace moe

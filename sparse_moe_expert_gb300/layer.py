@@ -129,6 +129,8 @@ class MoELayer:
         return self._family(T, self.kmax)
 
     def _family(self, T: int, k: int) -> int:
+        if self.bits not in (4, 8):  # 5- and 6-bit codes: the GEMV family only
+            return PATH_GEMV
         if (TC_BUILT and (T * k) // self.E >= TC_MIN_TOKENS_PER_EXPERT
                 and min(self.H, self.I) * self.bits // 8 >= 128):
             return PATH_TC

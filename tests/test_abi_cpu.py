@@ -80,8 +80,10 @@ def test_qmm_and_pack_reject_before_launch(L):
     base = [vp(GOOD), vp(GOOD), vp(GOOD), vp(GOOD), 4, 2, 8, 256, 512, vp(GOOD), vp(GOOD),
             vp(GOOD)]
     assert g(*base, 3, 1, 0, vp(GOOD), 0, None) == 2                    # bits 3 unsupported
-    for bits in (5, 6):                                                 # no device kernels yet
-        assert g(*base, bits, 1, 0, vp(GOOD), 0, None) == 2
+    gated = moe.PATH_GEMV | moe.path_k_range(1, 2)
+    for bits in (5, 6):           # the GEMV family only, and without a k gate
+        assert g(*base, bits, 1, 0, vp(GOOD), moe.PATH_TC, None) == 2
+        assert g(*base, bits, 1, 0, vp(GOOD), gated, None) == 2
     assert g(*base, 4, 0, 1, vp(GOOD), 0, None) == 2                    # RAW needs fp32 out
     assert g(*base, 4, 7, 0, vp(GOOD), 0, None) == 1                    # bad epilogue
     assert g(*base, 4, 1, 0, vp(GOOD), 9, None) == 1                    # bad path

@@ -365,3 +365,47 @@ def test_three_chained_layers_in_one_graph_match_the_oracle(cuda_lib, name, T):
         assert_layer_close(got, ref.out, f"{name} chained layer {li}")
         inp = bits(o)
     assert cuda_lib.moe_get_device_error() == 0
+
+
+@pytest.mark.parametrize("bits", [5, 6])
+@pytest.mark.parametrize("T,k,E,H,I", [(1, 4, 16, 1024, 768), (40, 2, 8, 512, 384),
+                                       (37, 3, 12, 192, 320)])
+def test_five_and_six_bit_layers_match_the_oracle(cuda_lib, bits, T, k, E, H, I):
+    """5- and 6-bit codes (a row's little-endian bit stream) on the GEMV
+    family: h, y and the layer output against the oracle, and the fused
+    gate_up product equal to the two separate products bit for bit (raw and
+    with the activation)."""
+    cfg = CFG["tiny"].scaled(H=H, I=I, E=E, k=k, T=T, bits=bits)
+    layer_np = workloads.make_layer(cfg)
+    x_bits = workloads.make_tokens(cfg)
+    d = dev()
+    moe = cuda_lib
+    layer = moe.MoELayer.from_workload(layer_np, d)
+    assert layer.fused and layer.resolved_path(T) == moe.PATH_GEMV
+    x = moe.bf16_from_bits(x_bits, d)
+    out = to_np(layer(x))
+    ref = oracle.moe_forward(x_bits, layer_np)
+    b = layer.buffers(T)
+    A = len(ref.perm.sorted_assign)
+    assert np.array_equal(to_np(b["topk_ids"]), ref.routing.ids)
+    assert rel_l2(to_np(b["h"])[:A], ref.h) <= 4e-3
+    assert rel_l2(to_np(b["y"])[:A], ref.y) <= 4e-3
+    assert_layer_close(out, ref.out, f"{bits}-bit layer T={T}")
+    gu = layer.gate_up
+    raw_f = moe.moe_gate_up_qmm(x, b["sorted"], b["offsets"], b["k_dev"], cfg.slots, gu.q, gu.s,
+                                gu.b, bits, moe.EPILOGUE_RAW)
+    raw_g = moe.moe_gate_up_qmm(x, b["sorted"], b["offsets"], b["k_dev"], cfg.slots, layer.gate.q,
+                                layer.gate.s, layer.gate.b, bits, moe.EPILOGUE_RAW)
+    raw_u = moe.moe_gate_up_qmm(x, b["sorted"], b["offsets"], b["k_dev"], cfg.slots, layer.up.q,
+                                layer.up.s, layer.up.b, bits, moe.EPILOGUE_RAW)
+    assert torch.equal(raw_f[:A, :I].view(torch.int32), raw_g[:A].view(torch.int32))
+    assert torch.equal(raw_f[:A, I:].view(torch.int32), raw_u[:A].view(torch.int32))
+    fused = moe.moe_gate_up_qmm(x, b["sorted"], b["offsets"], b["k_dev"], cfg.slots, gu.q, gu.s,
+                                gu.b, bits, moe.EPILOGUE_SWIGLU, out_dtype=torch.bfloat16)
+    sep = moe.moe_swiglu(raw_g, raw_u, b["k_dev"], T, cfg.slots, out_dtype=torch.bfloat16)
+    assert torch.equal(fused[:A].view(torch.int16), sep[:A].view(torch.int16))
+    # the tensor-core family does not take these widths
+    with pytest.raises(moe.MoEError):
+        moe.moe_gate_up_qmm(x, b["sorted"], b["offsets"], b["k_dev"], cfg.slots, gu.q, gu.s, gu.b,
+                            bits, moe.EPILOGUE_RAW, path=moe.PATH_TC)
+    assert moe.moe_get_device_error() == 0

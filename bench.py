@@ -247,13 +247,12 @@ def metric_name():
 
 
 def workload_config(cfg):
-    desc = {
-        "decode": "batch-1 decode: H4096 I11008 E64 top-4, 4-bit affine g64, 256 calls x 1 token",
-        "batched": "batched decode: H4096 I1536 E64 top-4 T64, 4-bit, Zipf(1.1) log-prior",
-        "prefill": "prefill: H2048 I768 E128 top-8 T4096, 4-bit",
-        "entropy": "entropy-adaptive: H4096 I1536 E32 T512, 8-bit, k from batch entropy",
-        "tiny": "tiny: H256 I512 E8 top-2 T16, 4-bit",
-    }[cfg.name]
+    kdesc = f"top-{cfg.k}" if cfg.k else "k from batch entropy"
+    extra = {"batched": ", Zipf(1.1) log-prior",
+             "decode": f", {cfg.calls} calls x 1 token"}.get(cfg.name, "")
+    toks = "" if cfg.name == "decode" else f" T{cfg.T}"
+    desc = (f"{cfg.name}: H{cfg.H} I{cfg.I} E{cfg.E} {kdesc}{toks}, {cfg.bits}-bit affine g64"
+            f"{extra}")
     return {"workload": desc, "H": cfg.H, "I": cfg.I, "E": cfg.E, "k": cfg.k or "adaptive",
             "tokens_per_call": cfg.T, "calls_per_step": cfg.calls, "bits": cfg.bits,
             "l2": "inputs larger than L2 (expert weights stream from HBM every call)"}
@@ -376,7 +375,8 @@ def workload_summary(moe, cfg, layer, res, peaks, peak_src):
     gu_f, dn_f = res["gu_step_flops"], res["dn_step_flops"]
     path_used = layer.resolved_path(T)
     ks = layer.k_split(T)
-    kernel_label = KERNEL_NAME[path_used] + " (gate_up, SiLU*up epilogue)"
+    kname = "gemv_bits_kernel" if cfg.bits not in (4, 8) else KERNEL_NAME[path_used]
+    kernel_label = kname + " (gate_up, SiLU*up epilogue)"
     if ks:
         kernel_label = (f"{KERNEL_NAME[moe.PATH_GEMV]} for k < {ks}, {KERNEL_NAME[moe.PATH_TC]} "
                         f"for k >= {ks} (gate_up, SiLU*up epilogue; both queued, gated on k)")
@@ -517,8 +517,10 @@ def run_ours(args):
         # the other workloads of the layer, measured the same way in this run
         cfgs = {}
         csteps = max(3, min(args.steps, 20))
-        for name in ("tiny", "batched", "prefill", "entropy"):
-            c = workloads.CONFIGS[name]
+        extra = {"batched_5bit": workloads.CONFIGS["batched"].scaled(bits=5),
+                 "batched_6bit": workloads.CONFIGS["batched"].scaled(bits=6)}
+        for name in ("tiny", "batched", "prefill", "entropy", "batched_5bit", "batched_6bit"):
+            c = extra.get(name) or workloads.CONFIGS[name]
             lay, _, _, _, r = workload_measure(moe, c, dev, rank, world, csteps, args.warmup,
                                                dict(free_sources=True), clocks_gpu=gpu_id)
             rf, kn = workload_summary(moe, c, lay, r, peaks, peak_src)

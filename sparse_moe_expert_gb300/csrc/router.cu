@@ -58,6 +58,7 @@ struct RouterParams {
   float thr1, thr2;
   int renorm;
   int smem_stage;  // bulk-copy the weight slice and token rows to shared memory
+  int tpc;         // tokens per cluster (token group)
   int groups;      // > 0: group-limited selection, the best expert of each of
                    // `groups` groups of E / groups consecutive ids (k = groups)
   int32_t* ids;
@@ -508,7 +509,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kRouterThreads)
   extern __shared__ __align__(16) float logits_s[];  // leader: [group tokens][E]
   __shared__ __align__(8) uint64_t stage_bar;
   const int E = p.E;
-  const int tpc = router_group_tokens(E);
+  const int tpc = p.tpc;
   const int t0 = (blockIdx.x / CL) * tpc;
   const int nt = min(tpc, p.T - t0);
   const uint32_t rank = cluster_ctarank();
@@ -547,11 +548,19 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kRouterThreads)
     if (!staged_ok && threadIdx.x == 0) raise_device_error(p.err, MOE_DEVERR_TIMEOUT);
   }
   if (ne > 0 && staged_ok) {
+    // tiles of 8 tokens x 4 experts unless that leaves fewer than 4 warps
+    // busy; then 8 tokens x 1 expert (more warps on a small group; each
+    // re-reads the token rows, which costs more than idle warps otherwise)
+    const bool wide_tiles = ((nt + 7) / 8) * ((ne + 3) / 4) >= 4;
     if (p.smem_stage) {
-      if (nt >= 8) router_logit_tiles<8, 4, true>(p, t0, nt, e_lo, ne, lead, xs_s, ws_s);
+      if (nt >= 8 && wide_tiles) router_logit_tiles<8, 4, true>(p, t0, nt, e_lo, ne, lead, xs_s, ws_s);
+      else if (nt >= 8) router_logit_tiles<8, 1, true>(p, t0, nt, e_lo, ne, lead, xs_s, ws_s);
       else router_logit_tiles<1, 1, true>(p, t0, nt, e_lo, ne, lead, xs_s, ws_s);
     } else {
-      if (nt >= 8) router_logit_tiles<8, 4, false>(p, t0, nt, e_lo, ne, lead, nullptr, nullptr);
+      if (nt >= 8 && wide_tiles)
+        router_logit_tiles<8, 4, false>(p, t0, nt, e_lo, ne, lead, nullptr, nullptr);
+      else if (nt >= 8)
+        router_logit_tiles<8, 1, false>(p, t0, nt, e_lo, ne, lead, nullptr, nullptr);
       else router_logit_tiles<1, 1, false>(p, t0, nt, e_lo, ne, lead, nullptr, nullptr);
     }
   }
@@ -571,10 +580,18 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kRouterThreads)
   }
 }
 
-__global__ void __launch_bounds__(kFinalizeThreads) router_finalize_kernel(RouterParams p) {
+// The batch finalize; with the grouping requested (E <= 256, T kmax <= the
+// CTA's threads) the stable counting sort follows in the same CTA.
+constexpr int kFinalizePermuteThreads = 512;
+__global__ void __launch_bounds__(kFinalizePermuteThreads) router_finalize_kernel(RouterParams p) {
+  __shared__ int fp_scratch[(kFinalizePermuteThreads / 32 + 1) * 256];
   pdl_wait();
   pdl_trigger();
   finalize_batch(p);
+  if (p.pm_sorted) {
+    __syncthreads();
+    fused_permute(p, fp_scratch);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -989,11 +1006,24 @@ bool launch_router_small(const RouterParams& p, cudaStream_t st, moe_status_t* s
 
 // Kernel 1 over ceil(T / group) clusters, then the batch finalize unless a
 // single cluster did it inline.
+// Tokens per cluster: one group of 32 (16 when E > 256) for small batches;
+// for larger ones groups as small as 8 tokens, so that the clusters cover the
+// SMs (a 64-token batch takes 8 clusters rather than 2).
+int router_tokens_per_group(int T, int E) {
+  const int base = router_group_tokens(E);
+  if (T <= base) return base;
+  const int want = (int)(((int64_t)T * kRouterCluster + moe_host::sm_count() - 1) /
+                         moe_host::sm_count());
+  int tpc = 8;
+  while (tpc < want && tpc < base) tpc <<= 1;
+  return tpc;
+}
+
 moe_status_t launch_router(const RouterParams& p, cudaStream_t st) {
   using namespace moe_host;
   moe_status_t small_status = MOE_OK;
   if (launch_router_small(p, st, &small_status)) return small_status;
-  const int tpc = router_group_tokens(p.E);
+  const int tpc = router_tokens_per_group(p.T, p.E);
   const int ngroups = (p.T + tpc - 1) / tpc;
   if (ngroups > 0) {
     size_t smem = (size_t)tpc * p.E * sizeof(float);
@@ -1005,6 +1035,7 @@ moe_status_t launch_router(const RouterParams& p, cudaStream_t st) {
     const int nt_max = p.T < tpc ? p.T : tpc;
     const size_t staged = smem + (size_t)ne_max * p.H * 4 + (size_t)nt_max * p.H * 2;
     RouterParams q = p;
+    q.tpc = tpc;
     q.smem_stage = (ngroups == 1 && staged <= kRouterStageBytes) ? 1 : 0;
     if (q.smem_stage) smem = staged;
     auto kern = wide ? router_topk_kernel<kRouterClusterWide> : router_topk_kernel<kRouterCluster>;
@@ -1019,8 +1050,12 @@ moe_status_t launch_router(const RouterParams& p, cudaStream_t st) {
     if (launch(kern, ngroups * cl, kRouterThreads, smem, st, q) != MOE_OK) return MOE_ERR_CUDA;
   }
   if (ngroups != 1) {
-    if (launch(router_finalize_kernel, 1, kFinalizeThreads, 0, st, p) != MOE_OK)
-      return MOE_ERR_CUDA;
+    // the grouping rides along when the caller asked for it (route_impl
+    // checks that it fits one CTA)
+    RouterParams q = p;
+    q.tpc = tpc;
+    const int threads = q.pm_sorted ? kFinalizePermuteThreads : kFinalizeThreads;
+    if (launch(router_finalize_kernel, 1, threads, 0, st, q) != MOE_OK) return MOE_ERR_CUDA;
   }
   return MOE_OK;
 }
@@ -1123,9 +1158,9 @@ moe_status_t route_impl(const uint16_t* x, const float* w_router, const float* l
   if (!expert_counts || !expert_offsets) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!sorted_assign || !inv_pos)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // one launch when one cluster covers the batch and its leader can sort it
-  const int tpc = router_group_tokens(E);
-  if (T > 0 && T <= tpc && E <= 256 && T * kmax <= kRouterThreads) {
+  // the grouping inside the router's launches when it fits one CTA: the
+  // leader of a single cluster, or the batch finalize of several clusters
+  if (T > 0 && E <= 256 && T * kmax <= kRouterThreads) {
     p.pm_counts = expert_counts;
     p.pm_offsets = expert_offsets;
     p.pm_sorted = sorted_assign;

@@ -153,16 +153,17 @@ class MoELayer:
     def launches_per_call(self, T: int) -> int:
         """Kernels one forward of T tokens launches: the router (plus its
         batch finalize when the tokens span more than one token group of 32,
-        16 when E > 256), the permute (inside the router when one group
-        covers the batch, E <= 256 and T * kmax <= 512), the row permute on
-        the tensor-core path, the gate_up product (or two RAW products and
-        the activation when unfused), down and combine.  With a capacity the
-        grouping is always its own kernel.  When k_split is set both kernel
-        families of each product are launched (one of them returns at once)."""
+        16 when E > 256), the grouping (inside those launches when E <= 256
+        and T * kmax <= 512, else its own kernel), the row permute on the
+        tensor-core path, the gate_up product (or two RAW products and the
+        activation when unfused), down and combine.  With a capacity the
+        capped grouping is a kernel of its own.  When k_split is set both
+        kernel families of each product are launched (one of them returns at
+        once)."""
         group = 32 if self.E <= 256 else 16
         one_group = (T + group - 1) // group == 1
         n = 1 + (0 if one_group else 1)
-        fused = one_group and self.E <= 256 and T * self.kmax <= 512
+        fused = self.E <= 256 and T * self.kmax <= 512
         if self.capacity is None:
             n += 0 if fused else 1
         else:

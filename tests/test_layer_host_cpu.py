@@ -53,6 +53,9 @@ def test_launch_counts():
     assert bare_layer(e, path=PATH_TC).launches_per_call(e.T) == 3 + 1 + 1 + 2
     d = CFG["decode"]
     assert bare_layer(d).launches_per_call(1) == 4   # router with the grouping, gate_up, down, combine
+    b = CFG["batched"]
+    # T 64 spans several token groups: router, then the finalize with the grouping
+    assert bare_layer(b).launches_per_call(b.T) == 2 + 3
 
 
 def test_k_range_flags_encode_the_header_layout():

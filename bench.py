@@ -66,6 +66,9 @@ def parse_args(argv=None):
                    help="group-limited routing: best expert of each of G groups (k = G)")
     p.add_argument("--experts", type=int, default=0,
                    help="smaller expert pool (same per-call work; for profiling captures)")
+    p.add_argument("--y-dtype", default="auto", choices=["auto", "f32", "bf16"],
+                   help="storage of the down product's rows before combine (auto: bf16 on the "
+                        "tensor-core path)")
     p.add_argument("--no-configs", action="store_true",
                    help="skip the other workloads and the decode launch variants")
     return p.parse_args(argv)
@@ -446,6 +449,7 @@ def run_ours(args):
     if args.experts:
         cfg = cfg.scaled(E=args.experts)
     path = {"auto": moe.PATH_AUTO, "gemv": moe.PATH_GEMV, "tc": moe.PATH_TC}[args.path]
+    y_dtype = {"auto": None, "f32": torch.float32, "bf16": torch.bfloat16}[args.y_dtype]
     gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
     gpu_id = str(gpu_id) if gpu_id is not None else str(local)
     if gpu_id and not gpu_id.startswith("GPU-") and "-" in gpu_id:
@@ -455,7 +459,8 @@ def run_ours(args):
 
     layer, layer_np, x_bits, temps, res = workload_measure(
         moe, cfg, dev, rank, world, args.steps, args.warmup,
-        dict(free_sources=True, path=path, groups=args.groups), nl=nl, clocks_gpu=gpu_id)
+        dict(free_sources=True, path=path, groups=args.groups, y_dtype=y_dtype), nl=nl,
+        clocks_gpu=gpu_id)
     T, calls, ms = res["T"], res["calls"], res["ms"]
     tokens_per_step = calls * T
     value = tokens_per_step * nl * world / (ms / 1000.0)  # layer-calls: tokens x layers
@@ -502,7 +507,8 @@ def run_ours(args):
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": f"u{cfg.bits} affine weights x bf16 tokens, f32 accumulate",
-        "data": "synthetic", "config": dict(workload_config(cfg), layers=nl, groups=args.groups),
+        "data": "synthetic", "config": dict(workload_config(cfg), layers=nl, groups=args.groups,
+                                            y_storage=str(layer.y_storage(T)).replace("torch.", "")),
         "roofline": roof, "kernels": kern,
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                    "reasons": clocks["reasons"], "samples": clocks["samples"]},
@@ -513,18 +519,26 @@ def run_ours(args):
     torch.cuda.empty_cache()
 
     if world == 1 and not args.no_configs and args.config == "decode" and not args.experts \
-            and nl == 1 and args.groups == 0 and path == moe.PATH_AUTO:
+            and nl == 1 and args.groups == 0 and path == moe.PATH_AUTO and y_dtype is None:
         # the other workloads of the layer, measured the same way in this run
         cfgs = {}
         csteps = max(3, min(args.steps, 20))
         extra = {"batched_5bit": workloads.CONFIGS["batched"].scaled(bits=5),
-                 "batched_6bit": workloads.CONFIGS["batched"].scaled(bits=6)}
-        for name in ("tiny", "batched", "prefill", "entropy", "batched_5bit", "batched_6bit"):
+                 "batched_6bit": workloads.CONFIGS["batched"].scaled(bits=6),
+                 "prefill_y_f32": workloads.CONFIGS["prefill"]}
+        for name in ("tiny", "batched", "prefill", "entropy", "batched_5bit", "batched_6bit",
+                     "prefill_y_f32"):
             c = extra.get(name) or workloads.CONFIGS[name]
-            lay, _, _, _, r = workload_measure(moe, c, dev, rank, world, csteps, args.warmup,
-                                               dict(free_sources=True), clocks_gpu=gpu_id)
+            # prefill_y_f32: the prefill layer with y kept in fp32 (the A/B of
+            # the bf16 storage the tensor-core path uses by default)
+            kw = dict(free_sources=True,
+                      y_dtype=torch.float32 if name == "prefill_y_f32" else None)
+            lay, _, _, _, r = workload_measure(moe, c, dev, rank, world, csteps, args.warmup, kw,
+                                               clocks_gpu=gpu_id)
             rf, kn = workload_summary(moe, c, lay, r, peaks, peak_src)
-            cfgs[name] = {"config": workload_config(c), "value": r["calls"] * r["T"] / (r["ms"] / 1e3),
+            cfgs[name] = {"config": dict(workload_config(c),
+                                         y_storage=str(lay.y_storage(r["T"])).replace("torch.", "")),
+                          "value": r["calls"] * r["T"] / (r["ms"] / 1e3),
                           "unit": "tokens/s", "ms_per_step": r["ms"], "steps": csteps,
                           "roofline": rf, "kernels": kn,
                           "clocks": {k: r["clocks"][k] for k in ("sm_mhz", "sm_max_mhz", "reasons",

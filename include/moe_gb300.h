@@ -376,14 +376,18 @@ moe_status_t moe_gate_up_qmm(const uint16_t* x, const int32_t* sorted_assign,
  * h         [T*kmax, I] of h_dtype (MOE_DTYPE_F32 or MOE_DTYPE_BF16), rows in
  *           sorted order (as written by moe_gate_up_qmm).
  * w_q       uint32 [E, H, I*bits/32]; w_s, w_b fp16 [E, H, I/64].
- * y         out: fp32 [T*kmax, H], sorted order; rows >= T*k not written.
+ * y         out: [T*kmax, H] of y_dtype, sorted order; rows >= T*k not
+ *           written.  MOE_DTYPE_F32 stores the fp32 sums; MOE_DTYPE_BF16
+ *           stores each sum rounded to bf16 (nearest even), bit for bit the
+ *           rounding of the fp32 result, at half the bytes written here and
+ *           read again by moe_combine.
  * path      MOE_PATH_*, optionally | MOE_PATH_FLAG_WEIGHTS_EARLY and/or
  *           | MOE_PATH_K_RANGE(lo, hi).
  * ---------------------------------------------------------------------- */
 moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* expert_offsets,
                           const int32_t* k_dev, int T, int kmax, int E, int I, int H,
                           const uint32_t* w_q, const uint16_t* w_s, const uint16_t* w_b,
-                          int bits, float* y, int path, moe_stream_t stream);
+                          int bits, void* y, int y_dtype, int path, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Expert health.  Page [B], section 6: a serving-side "MoE health" check on
@@ -420,12 +424,14 @@ moe_status_t moe_expert_health(const int64_t* window_counts, int E, int32_t* lea
  * accumulated in fp32 in ascending j.  A slot with inv_pos = MOE_DROPPED
  * (expert capacity) is skipped.
  *
- * y        fp32 [T*kmax, H] (sorted order).
+ * y        [T*kmax, H] of y_dtype (MOE_DTYPE_F32 or MOE_DTYPE_BF16, as
+ *          moe_down_qmm wrote it), sorted order; bf16 values enter the sum
+ *          as their exact fp32 values.
  * out      out: bf16 [T, H].
  * ---------------------------------------------------------------------- */
-moe_status_t moe_combine(const float* y, const int32_t* inv_pos, const float* topk_w,
-                         const int32_t* k_dev, int T, int kmax, int H, uint16_t* out,
-                         moe_stream_t stream);
+moe_status_t moe_combine(const void* y, int y_dtype, const int32_t* inv_pos,
+                         const float* topk_w, const int32_t* k_dev, int T, int kmax, int H,
+                         uint16_t* out, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * moe_swiglu -- the activation on its own, for the unfused two-product path.

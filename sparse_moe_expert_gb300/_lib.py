@@ -80,8 +80,8 @@ def _declare(lib):
     lib.moe_gate_up_qmm.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i32, i32,
                                     i32, vp, i32, vp]
     lib.moe_down_qmm.argtypes = [vp, i32, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i32, vp,
-                                 i32, vp]
-    lib.moe_combine.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp]
+                                 i32, i32, vp]
+    lib.moe_combine.argtypes = [vp, i32, vp, vp, vp, i32, i32, i32, vp, vp]
     lib.moe_swiglu.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp]
     lib.moe_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32, vp]
     lib.moe_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]

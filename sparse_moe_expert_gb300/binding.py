@@ -213,13 +213,15 @@ def moe_gate_up_qmm(x, sorted_assign, expert_offsets, k_dev, kmax: int, w_q, w_s
 
 
 def moe_down_qmm(h, expert_offsets, k_dev, T: int, kmax: int, w_q, w_s, w_b, bits: int, y=None,
-                 path: int = PATH_AUTO, stream=None):
+                 path: int = PATH_AUTO, stream=None, y_dtype=torch.float32):
+    """y: fp32 or bf16 [T*kmax, H] (allocated as ``y_dtype`` when not given)."""
     E, H = w_q.shape[0], w_q.shape[1]
     I = h.shape[1]
     if y is None:
-        y = torch.empty((max(T * kmax, 1), H), dtype=torch.float32, device=h.device)
+        y = torch.empty((max(T * kmax, 1), H), dtype=y_dtype, device=h.device)
     st = lib().moe_down_qmm(_p(h), _DT[h.dtype], _p(expert_offsets), _p(k_dev), T, kmax, E, I, H,
-                            _p(w_q), _p(w_s), _p(w_b), bits, _p(y), path, _stream(stream))
+                            _p(w_q), _p(w_s), _p(w_b), bits, _p(y), _DT[y.dtype], path,
+                            _stream(stream))
     check("moe_down_qmm", st)
     return y
 
@@ -228,8 +230,8 @@ def moe_combine(y, inv_pos, topk_w, k_dev, T: int, kmax: int, out=None, stream=N
     H = y.shape[1]
     if out is None:
         out = torch.empty((T, H), dtype=torch.bfloat16, device=y.device)
-    st = lib().moe_combine(_p(y), _p(inv_pos), _p(topk_w), _p(k_dev), T, kmax, H, _p(out),
-                           _stream(stream))
+    st = lib().moe_combine(_p(y), _DT[y.dtype], _p(inv_pos), _p(topk_w), _p(k_dev), T, kmax, H,
+                           _p(out), _stream(stream))
     check("moe_combine", st)
     return out
 

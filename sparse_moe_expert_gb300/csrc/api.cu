@@ -114,7 +114,7 @@ extern "C" const char* moe_status_string(moe_status_t s) {
   return "unknown status";
 }
 
-extern "C" int moe_abi_version(void) { return 1; }
+extern "C" int moe_abi_version(void) { return 2; }
 
 extern "C" int moe_set_launch_overlap(int enable) {
   const int prev = moe_host::pdl_enabled() ? 1 : 0;
@@ -206,13 +206,14 @@ extern "C" moe_status_t moe_gate_up_qmm(const uint16_t* x, const int32_t* sorted
 extern "C" moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* expert_offsets,
                                      const int32_t* k_dev, int T, int kmax, int E, int I, int H,
                                      const uint32_t* w_q, const uint16_t* w_s,
-                                     const uint16_t* w_b, int bits, float* y, int path,
-                                     moe_stream_t stream) {
+                                     const uint16_t* w_b, int bits, void* y, int y_dtype,
+                                     int path, moe_stream_t stream) {
   using namespace moe_host;
   if (!common_shape_ok(T, kmax, E)) return MOE_ERR_INVALID_ARG;
   if (I <= 0 || I % 64 != 0 || H <= 0 || H % 64 != 0) return MOE_ERR_INVALID_ARG;
   if (bits != 4 && bits != 5 && bits != 6 && bits != 8) return MOE_ERR_UNSUPPORTED;
   if (h_dtype != MOE_DTYPE_F32 && h_dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
+  if (y_dtype != MOE_DTYPE_F32 && y_dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
   int family = 0;
   bool early = false;
   moe::KGate gate{nullptr, 0, 0};
@@ -229,10 +230,10 @@ extern "C" moe_status_t moe_down_qmm(const void* h, int h_dtype, const int32_t* 
   if (p == MOE_PATH_TC) {
     if (!moe::tc_available() || (bits != 4 && bits != 8)) return MOE_ERR_UNSUPPORTED;
     return moe::tc_qmm(h, act_kind, nullptr, expert_offsets, T, kmax, E, I, H, false, w_q, w_s,
-                       w_b, bits, y, MOE_DTYPE_F32, gate, st);
+                       w_b, bits, y, y_dtype, gate, st);
   }
   return moe::gemv_qmm(h, act_kind, nullptr, expert_offsets, T, kmax, E, I, H, false, w_q, w_s,
-                       w_b, bits, y, MOE_DTYPE_F32, early, gate, st);
+                       w_b, bits, y, y_dtype, early, gate, st);
 }
 
 namespace {

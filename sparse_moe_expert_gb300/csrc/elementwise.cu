@@ -11,24 +11,29 @@ constexpr int kEwThreads = 256;
 
 // out[t, m] = bf16( sum_{j<k} w[t, j] * y[inv_pos[t*kmax + j], m] ), fp32, j ascending.
 // Page "Qwen3.5 Block在llama.cpp中的映射与优化原理", section 4.2 (weighted sum of
-// the chosen experts' outputs).  One thread per 4 consecutive m of one token.
-__global__ void __launch_bounds__(kEwThreads) combine_kernel(const float* __restrict__ y,
+// the chosen experts' outputs).  One thread per V consecutive m of one token:
+// V = 4 for fp32 y (one 16-byte load per row), 8 for bf16 y (also 16 bytes).
+template <bool BF16_Y>
+__global__ void __launch_bounds__(kEwThreads) combine_kernel(const void* __restrict__ y,
                                                              const int32_t* __restrict__ inv_pos,
                                                              const float* __restrict__ topk_w,
                                                              const int32_t* __restrict__ k_dev,
                                                              int T, int kmax, int H,
                                                              uint16_t* __restrict__ out,
                                                              unsigned int* err) {
+  constexpr int V = BF16_Y ? 8 : 4;
   pdl_wait();
   pdl_trigger();
   const int k = *k_dev;
-  const int vec_per_row = H / 4;
+  const int vec_per_row = H / V;
   const int64_t total = (int64_t)T * vec_per_row;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int t = (int)(i / vec_per_row);
     const int v = (int)(i - (int64_t)t * vec_per_row);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float acc[V];
+#pragma unroll
+    for (int e = 0; e < V; ++e) acc[e] = 0.0f;
     for (int j = 0; j < k; ++j) {
       const int r = __ldg(inv_pos + (int64_t)t * kmax + j);
       if (r < 0) {  // dropped by its expert's capacity: no contribution
@@ -36,16 +41,35 @@ __global__ void __launch_bounds__(kEwThreads) combine_kernel(const float* __rest
         continue;
       }
       const float w = __ldg(topk_w + (int64_t)t * kmax + j);
-      const float4 yv = __ldg(reinterpret_cast<const float4*>(y + (int64_t)r * H) + v);
-      acc.x = fmaf(w, yv.x, acc.x);
-      acc.y = fmaf(w, yv.y, acc.y);
-      acc.z = fmaf(w, yv.z, acc.z);
-      acc.w = fmaf(w, yv.w, acc.w);
+      float yv[V];
+      if constexpr (BF16_Y) {
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(
+                                  static_cast<const uint16_t*>(y) + (int64_t)r * H) + v);
+        const uint32_t q4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          yv[2 * e] = __uint_as_float(q4[e] << 16);
+          yv[2 * e + 1] = __uint_as_float(q4[e] & 0xFFFF0000u);
+        }
+      } else {
+        const float4 q = __ldg(reinterpret_cast<const float4*>(
+                                   static_cast<const float*>(y) + (int64_t)r * H) + v);
+        yv[0] = q.x;
+        yv[1] = q.y;
+        yv[2] = q.z;
+        yv[3] = q.w;
+      }
+#pragma unroll
+      for (int e = 0; e < V; ++e) acc[e] = fmaf(w, yv[e], acc[e]);
     }
-    uint2 o;
-    o.x = (uint32_t)f32_to_bf16_rne(acc.x) | ((uint32_t)f32_to_bf16_rne(acc.y) << 16);
-    o.y = (uint32_t)f32_to_bf16_rne(acc.z) | ((uint32_t)f32_to_bf16_rne(acc.w) << 16);
-    reinterpret_cast<uint2*>(out + (int64_t)t * H)[v] = o;
+    uint32_t o[V / 2];
+#pragma unroll
+    for (int e = 0; e < V / 2; ++e)
+      o[e] = (uint32_t)f32_to_bf16_rne(acc[2 * e]) | ((uint32_t)f32_to_bf16_rne(acc[2 * e + 1]) << 16);
+    if constexpr (BF16_Y)
+      reinterpret_cast<uint4*>(out + (int64_t)t * H)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    else
+      reinterpret_cast<uint2*>(out + (int64_t)t * H)[v] = make_uint2(o[0], o[1]);
   }
 }
 
@@ -96,19 +120,23 @@ int grid_for(int64_t work) {
 
 using namespace moe;
 
-extern "C" moe_status_t moe_combine(const float* y, const int32_t* inv_pos, const float* topk_w,
-                                    const int32_t* k_dev, int T, int kmax, int H, uint16_t* out,
-                                    moe_stream_t stream) {
+extern "C" moe_status_t moe_combine(const void* y, int y_dtype, const int32_t* inv_pos,
+                                    const float* topk_w, const int32_t* k_dev, int T, int kmax,
+                                    int H, uint16_t* out, moe_stream_t stream) {
   using namespace moe_host;
   if (T < 0 || H <= 0 || H % 64 != 0 || kmax < 1 || kmax > 16) return MOE_ERR_INVALID_ARG;
   if ((int64_t)T * kmax > (1 << 24)) return MOE_ERR_INVALID_ARG;
+  if (y_dtype != MOE_DTYPE_F32 && y_dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
   if (!k_dev) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!y || !inv_pos || !topk_w || !out || !aligned16(y) || !aligned16(out))
     return MOE_ERR_INVALID_ARG;
-  return launch(combine_kernel, grid_for((int64_t)T * H / 4), kEwThreads, 0,
-                reinterpret_cast<cudaStream_t>(stream), y, inv_pos, topk_w, k_dev, T, kmax, H,
-                out, device_error_word());
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (y_dtype == MOE_DTYPE_BF16)
+    return launch(combine_kernel<true>, grid_for((int64_t)T * H / 8), kEwThreads, 0, st, y,
+                  inv_pos, topk_w, k_dev, T, kmax, H, out, device_error_word());
+  return launch(combine_kernel<false>, grid_for((int64_t)T * H / 4), kEwThreads, 0, st, y,
+                inv_pos, topk_w, k_dev, T, kmax, H, out, device_error_word());
 }
 
 extern "C" moe_status_t moe_swiglu(const float* gate, const float* up, const int32_t* k_dev,

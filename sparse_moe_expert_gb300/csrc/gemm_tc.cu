@@ -800,26 +800,33 @@ __global__ void __launch_bounds__(tc_threads(BITS), 1)
         const int col = ti.mt * BM + warp * 32 + lane;
         const bool col_ok = col < p.n_out;
         const int64_t stride = p.n_out;
-        float* orow = static_cast<float*>(p.out) + row0 * stride + col;  // row n0 of the step
-        for (int n0 = 0; n0 < ti.nv; n0 += 32, orow += 32 * stride) {
+        const bool bf16_out = p.out_dtype == MOE_DTYPE_BF16;
+        // element (row n0 + i, col) of the output, fp32 or rounded to bf16
+        auto put = [&](int64_t oi, uint32_t v) {
+          if (bf16_out)
+            static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16_rne(__uint_as_float(v));
+          else
+            static_cast<float*>(p.out)[oi] = __uint_as_float(v);
+        };
+        for (int n0 = 0; n0 < ti.nv; n0 += 32) {
           uint32_t a[16], b[16];
           tmem_ld16(lane_addr + n0, a);
           tmem_ld16(lane_addr + n0 + 16, b);
           tmem_ld_wait();
           if (col_ok) {
-            float* q = orow;
+            const int64_t o0 = (row0 + n0) * stride + col;
             if (n0 + 32 <= ti.nv) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i, q += stride) *q = __uint_as_float(a[i]);
+              for (int i = 0; i < 16; ++i) put(o0 + i * stride, a[i]);
 #pragma unroll
-              for (int i = 0; i < 16; ++i, q += stride) *q = __uint_as_float(b[i]);
+              for (int i = 0; i < 16; ++i) put(o0 + (16 + i) * stride, b[i]);
             } else {
 #pragma unroll
-              for (int i = 0; i < 16; ++i, q += stride)
-                if (n0 + i < ti.nv) *q = __uint_as_float(a[i]);
+              for (int i = 0; i < 16; ++i)
+                if (n0 + i < ti.nv) put(o0 + i * stride, a[i]);
 #pragma unroll
-              for (int i = 0; i < 16; ++i, q += stride)
-                if (n0 + 16 + i < ti.nv) *q = __uint_as_float(b[i]);
+              for (int i = 0; i < 16; ++i)
+                if (n0 + 16 + i < ti.nv) put(o0 + (16 + i) * stride, b[i]);
             }
           }
         }

@@ -384,7 +384,11 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_qmm_kernel
 #pragma unroll
           for (int q = 0; q < kRowsPerWarp; ++q) {
             const int col = cur.col0 + q;
-            if (col < p.n_rows) static_cast<float*>(p.out)[r * p.n_out + col] = tot[q][t];
+            if (col >= p.n_rows) continue;
+            if (p.out_dtype == MOE_DTYPE_BF16)
+              static_cast<uint16_t*>(p.out)[r * p.n_out + col] = f32_to_bf16_rne(tot[q][t]);
+            else
+              static_cast<float*>(p.out)[r * p.n_out + col] = tot[q][t];
           }
         }
       }

@@ -200,6 +200,8 @@ __global__ void __launch_bounds__(kBtThreads) gemv_bits_kernel(BtParams p) {
           static_cast<uint16_t*>(p.out)[orow * p.n_out + f] = f32_to_bf16_rne(hv);
         else
           static_cast<float*>(p.out)[orow * p.n_out + f] = hv;
+      } else if (p.out_dtype == MOE_DTYPE_BF16) {
+        static_cast<uint16_t*>(p.out)[orow * p.n_out + f] = f32_to_bf16_rne(acc[0][n]);
       } else {
         static_cast<float*>(p.out)[orow * p.n_out + f] = acc[0][n];
       }

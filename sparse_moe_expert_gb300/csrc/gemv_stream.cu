@@ -859,7 +859,13 @@ __global__ void __launch_bounds__(kSvThreads, 1)
           }
         } else {
           const int col = cu.rt * 16 + lane;
-          if (lane < 16 && col < p.n_rows) static_cast<float*>(p.out)[row0 * p.n_out + col] = v;
+          if (lane < 16 && col < p.n_rows) {
+            const int64_t oi = row0 * p.n_out + col;
+            if (p.out_dtype == MOE_DTYPE_BF16)
+              static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16_rne(v);
+            else
+              static_cast<float*>(p.out)[oi] = v;
+          }
         }
       } else {
         // lane l: token l / 4, tile rows 4 (l & 3) .. + 3
@@ -907,9 +913,15 @@ __global__ void __launch_bounds__(kSvThreads, 1)
           }
         } else {
           const int col0 = cu.rt * 16 + q * 4;
-          if (n < nt && col0 < p.n_rows)
-            *reinterpret_cast<float4*>(static_cast<float*>(p.out) + (row0 + n) * p.n_out + col0) =
-                v;
+          if (n < nt && col0 < p.n_rows) {
+            const int64_t oi = (row0 + n) * p.n_out + col0;
+            if (p.out_dtype == MOE_DTYPE_BF16)
+              *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + oi) = make_uint2(
+                  (uint32_t)f32_to_bf16_rne(v.x) | ((uint32_t)f32_to_bf16_rne(v.y) << 16),
+                  (uint32_t)f32_to_bf16_rne(v.z) | ((uint32_t)f32_to_bf16_rne(v.w) << 16));
+            else
+              *reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi) = v;
+          }
         }
       }
       __syncwarp();

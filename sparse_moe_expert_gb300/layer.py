@@ -66,7 +66,11 @@ class MoELayer:
     ``groups`` > 0 routes each token to the best expert of each of ``groups``
     groups of consecutive expert ids (k_fixed must equal it).  ``capacity``
     limits the assignments each expert takes per call (the lowest token
-    slots stay; the others are dropped).
+    slots stay; the others are dropped).  ``y_dtype`` is the storage type of
+    the down product's rows between the down and combine kernels: None
+    stores bf16 when a call's products run on the tensor cores (large
+    batches, where y is hundreds of MB written and read again) and fp32
+    otherwise.
     """
 
     def __init__(self, router_w: torch.Tensor, logit_bias: Optional[torch.Tensor], gate: QTensor,
@@ -74,7 +78,7 @@ class MoELayer:
                  inv_temperature: float = 1.0, renormalize: bool = True,
                  thresholds=(1.2, 2.5), fuse_gate_up: Optional[bool] = None,
                  path: int = PATH_AUTO, free_sources: bool = False, groups: int = 0,
-                 capacity: Optional[int] = None):
+                 capacity: Optional[int] = None, y_dtype: Optional[torch.dtype] = None):
         self.device = router_w.device
         self.router_w = router_w.contiguous()
         self.logit_bias = None if logit_bias is None else logit_bias.contiguous()
@@ -89,6 +93,9 @@ class MoELayer:
         self.path = path
         self.groups = int(groups)
         self.capacity = None if capacity is None else int(capacity)
+        if y_dtype not in (None, torch.float32, torch.bfloat16):
+            raise ValueError("y_dtype must be None, torch.float32 or torch.bfloat16")
+        self.y_dtype = y_dtype
         if self.groups > 0 and (self.E % self.groups or k_fixed != self.groups):
             raise ValueError("group-limited routing needs k_fixed == groups dividing E")
         self.down = down
@@ -150,6 +157,13 @@ class MoELayer:
             return 0
         return next(k for k in range(2, self.kmax + 1) if self._family(T, k) == PATH_TC)
 
+    def y_storage(self, T: int) -> torch.dtype:
+        """Storage type of y for calls of T tokens."""
+        if self.y_dtype is not None:
+            return self.y_dtype
+        tc = self.k_split(T) or self.resolved_path(T) == PATH_TC
+        return torch.bfloat16 if tc else torch.float32
+
     def launches_per_call(self, T: int) -> int:
         """Kernels one forward of T tokens launches: the router (plus its
         batch finalize when the tokens span more than one token group of 32,
@@ -194,7 +208,7 @@ class MoELayer:
                 inv_pos=torch.empty(A, dtype=torch.int32, device=dev),
                 h=torch.empty((A, self.I), dtype=h_dtype, device=dev),
                 x_sorted=torch.empty((A, self.H), dtype=torch.bfloat16, device=dev),
-                y=torch.empty((A, self.H), dtype=torch.float32, device=dev),
+                y=torch.empty((A, self.H), dtype=self.y_storage(T), device=dev),
                 out=torch.empty((T, self.H), dtype=torch.bfloat16, device=dev),
             )
             if not self.fused:

@@ -39,7 +39,7 @@ def test_exports_every_declared_function(L):
 
 def test_status_strings_and_version(L):
     import sparse_moe_expert_gb300 as moe
-    assert moe.moe_abi_version() == 1
+    assert moe.moe_abi_version() == 2
     assert moe.moe_status_string(0) == "ok"
     assert moe.moe_status_string(3) == "gate and up cannot be fused"
     assert moe.moe_status_string(99) == "unknown status"
@@ -92,7 +92,9 @@ def test_qmm_and_pack_reject_before_launch(L):
     assert g(*bad, 4, 1, 0, vp(GOOD), 0, None) == 1
     d = L.moe_down_qmm
     assert d(vp(GOOD), 0, vp(GOOD), vp(GOOD), 4, 2, 8, 100, 256, vp(GOOD), vp(GOOD), vp(GOOD), 4,
-             vp(GOOD), 0, None) == 1                                    # I % 64
+             vp(GOOD), 0, 0, None) == 1                                 # I % 64
+    assert d(vp(GOOD), 0, vp(GOOD), vp(GOOD), 4, 2, 8, 128, 256, vp(GOOD), vp(GOOD), vp(GOOD), 4,
+             vp(GOOD), 5, 0, None) == 1                                 # bad y dtype
     a = moe.qdesc(512, 256, 4)
     for field, val in [("bits", 8), ("group_size", 32), ("has_bias", 1), ("rows", 256),
                        ("cols", 512), ("mode", 1), ("quantized", 0), ("scale_dtype", 1)]:
@@ -107,7 +109,10 @@ def test_qmm_and_pack_reject_before_launch(L):
     assert st == 2                                                      # bits 3 unsupported
     assert L.moe_permute(vp(GOOD), vp(GOOD), 4, 2, 0, vp(GOOD), vp(GOOD), vp(GOOD), vp(GOOD),
                          None) == 1
-    assert L.moe_combine(vp(GOOD), vp(GOOD), vp(GOOD), vp(GOOD), 4, 2, 100, vp(GOOD), None) == 1
+    assert L.moe_combine(vp(GOOD), 0, vp(GOOD), vp(GOOD), vp(GOOD), 4, 2, 100, vp(GOOD),
+                         None) == 1                                     # H % 64
+    assert L.moe_combine(vp(GOOD), 7, vp(GOOD), vp(GOOD), vp(GOOD), 4, 2, 128, vp(GOOD),
+                         None) == 1                                     # bad y dtype
     assert L.moe_swiglu(vp(GOOD), vp(GOOD), vp(GOOD), 4, 2, 256, 5, vp(GOOD), None) == 1
 
 

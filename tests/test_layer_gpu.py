@@ -409,3 +409,38 @@ def test_five_and_six_bit_layers_match_the_oracle(cuda_lib, bits, T, k, E, H, I)
         moe.moe_gate_up_qmm(x, b["sorted"], b["offsets"], b["k_dev"], cfg.slots, gu.q, gu.s, gu.b,
                             bits, moe.EPILOGUE_RAW, path=moe.PATH_TC)
     assert moe.moe_get_device_error() == 0
+
+
+@pytest.mark.parametrize("path,bits,H,I", [("gemv", 4, 512, 384), ("gemv", 8, 512, 384),
+                                           ("tc", 4, 512, 384), ("tc", 8, 512, 384),
+                                           ("gemv", 5, 512, 384), ("gemv", 4, 320, 192)])
+def test_bf16_y_is_the_rounded_fp32_y(cuda_lib, path, bits, H, I):
+    """The down product stored as bf16 is, bit for bit, the nearest-even
+    rounding of the fp32 product (every kernel family: the streamed GEMV,
+    the 5/6-bit GEMV, the plain GEMV for rows that are not whole 128-byte
+    blocks, the tensor cores); combine reading the bf16 rows equals combine
+    reading their exact fp32 values; and a layer storing y as bf16 stays
+    within the layer tolerance of the oracle."""
+    cfg = CFG["tiny"].scaled(H=H, I=I, E=16, k=4, T=300, bits=bits)
+    layer_np = workloads.make_layer(cfg)
+    x_bits = workloads.make_tokens(cfg)
+    d = dev()
+    p = path_id(cuda_lib, path)
+    layer = cuda_lib.MoELayer.from_workload(layer_np, d, path=p, y_dtype=torch.bfloat16)
+    x = cuda_lib.bf16_from_bits(x_bits, d)
+    out = to_np(layer(x))
+    b = layer.buffers(cfg.T)
+    assert b["y"].dtype == torch.bfloat16
+    dn, T, kmax, A = layer.down, cfg.T, cfg.slots, cfg.T * cfg.k
+    y32 = cuda_lib.moe_down_qmm(b["h"], b["offsets"], b["k_dev"], T, kmax, dn.q, dn.s, dn.b, bits,
+                                path=p, y_dtype=torch.float32)
+    y16 = cuda_lib.moe_down_qmm(b["h"], b["offsets"], b["k_dev"], T, kmax, dn.q, dn.s, dn.b, bits,
+                                path=p, y_dtype=torch.bfloat16)
+    assert torch.equal(y16[:A].view(torch.int16), y32[:A].to(torch.bfloat16).view(torch.int16))
+    assert torch.equal(y16[:A].view(torch.int16), b["y"][:A].view(torch.int16))
+    o16 = cuda_lib.moe_combine(y16, b["inv_pos"], b["topk_w"], b["k_dev"], T, kmax)
+    o32 = cuda_lib.moe_combine(y16.float(), b["inv_pos"], b["topk_w"], b["k_dev"], T, kmax)
+    assert torch.equal(o16.view(torch.int16), o32.view(torch.int16))
+    ref = oracle.moe_forward(x_bits, layer_np)
+    assert_layer_close(out, ref.out, f"bf16 y, {path} {bits}-bit")
+    assert cuda_lib.moe_get_device_error() == 0

@@ -84,7 +84,11 @@ __host__ __device__ constexpr int deq_warps(int bits) { return bits == 8 ? 16 : 
 __host__ __device__ constexpr int code_warp(int bits) { return kDeqWarp0 + deq_warps(bits); }
 __host__ __device__ constexpr int tc_threads(int bits) { return (code_warp(bits) + 1) * 32; }
 constexpr int kATileBytes = BM * BK * 2;                  // 16 KB bf16 weight tile
-constexpr int kKbPerA = 2;                                // k-blocks per A stage
+// k-blocks per A stage: each stage ends with a proxy fence and an arrival
+// by every dequant thread, so two k-blocks per stage (measured on the
+// prefill gate_up product: 308 us with two slots of two k-blocks, 392 us
+// with three slots of one)
+constexpr int kKbPerA = 2;
 constexpr int kAStageBytes = kKbPerA * kATileBytes;       // 32 KB
 constexpr int kBRowBytes = BK * 2;                         // one token row of a k-block
 constexpr int kCodeRowBytes = 128;                         // code bytes of a row per code slot
@@ -163,20 +167,28 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulation.
+// tcgen05.mma and tcgen05.commit are issued by one thread.  The MMA warp
+// runs its loop converged (all lanes wait, walk the tiles and form the
+// descriptors, which stay warp-uniform) and the lane that elect.sync picks,
+// the lowest one every time, issues.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// Arrive on `bar` once all tcgen05 operations issued so far by this thread complete.
+// Arrive on `bar` once all tcgen05 operations issued so far by the elected
+// lane complete (the whole warp executes it, converged).
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
           smem_u32(bar))
       : "memory");
 }
@@ -313,10 +325,10 @@ __global__ void __launch_bounds__(tc_threads(BITS), 1)
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
   // A ring (dequantized weights, kKbPerA k-blocks per stage): a_full arrived
-  // by the dequant warps once the stage's token tiles have landed too, so
-  // the MMA thread waits once per A stage; a_empty committed by the MMAs.
-  // B ring (token tiles, one k-block per slot): b_full counts the TMA bytes,
-  // b_empty is committed by the MMAs.
+  // by the dequant warps, a_empty committed by the MMAs.  B ring (token
+  // tiles, one k-block per slot): b_full counts the TMA bytes, b_empty is
+  // committed by the MMAs.  The MMA thread waits on both, so the dequant
+  // warps run ahead of the token tiles and neither ring waits on the other.
   __shared__ uint64_t a_full[kMaxStages], a_empty[kMaxStages];
   __shared__ uint64_t b_full[kMaxStages], b_empty[kMaxStages];
   __shared__ uint64_t c_full[kMaxCodeSlots], c_empty[kMaxCodeSlots];
@@ -365,19 +377,41 @@ __global__ void __launch_bounds__(tc_threads(BITS), 1)
   // the set-up above overlaps the end of the previous kernel of the stream
   pdl_wait();
   pdl_trigger();
-  if (tid == 0) {
+  // tiles of each expert, all threads at once (tile_start[e] holds expert
+  // e's count), then one warp compacts the active experts in id order with
+  // their first tiles (an active entry a <= e is written only after the
+  // warp has read the counts of its 32 experts)
+  for (int e = tid; e < p.E; e += blockDim.x) {
+    const int m = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
+    tile_start[e] = m > 0 ? p.n_mt * ntiles_of(m, p.bn_cap) : 0;
+  }
+  __syncthreads();
+  if (warp == 0) {
     int n = 0, t = 0;
-    for (int e = 0; e < p.E; ++e) {
-      const int m = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
-      if (m > 0) {
-        act_e[n] = e;
-        tile_start[n] = t;
-        t += p.n_mt * ntiles_of(m, p.bn_cap);
-        ++n;
+    for (int base = 0; base < p.E; base += 32) {
+      const int e = base + lane;
+      const int c = e < p.E ? tile_start[e] : 0;
+      __syncwarp();
+      const unsigned act = __ballot_sync(0xFFFFFFFFu, c > 0);
+      int incl = c;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += y;
       }
+      if (c > 0) {
+        const int a = n + __popc(act & lanemask_lt());
+        act_e[a] = e;
+        tile_start[a] = t + incl - c;
+      }
+      n += __popc(act);
+      t += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      __syncwarp();
     }
-    tile_start[n] = t;
-    n_act_sh = n;
+    if (lane == 0) {
+      tile_start[n] = t;
+      n_act_sh = n;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -579,7 +613,7 @@ __global__ void __launch_bounds__(tc_threads(BITS), 1)
     };
 
     long long w_dq_aempty = 0;
-    Ring ra, rb, rc;  // A ring, B ring, code ring
+    Ring ra, rc;  // A ring, code ring
     int akb = 0;      // k-block (within the tile) of the next A stage
     bool ok = true;
     for (int st0 = 0; st0 < nst && ok; st0 += PD) {
@@ -683,15 +717,6 @@ __global__ void __launch_bounds__(tc_threads(BITS), 1)
               rc.next(SC);
             }
             if (tile_end) akb = 0;
-            // the A stage is complete once its token tiles have landed too
-#pragma unroll
-            for (int h = 0; h < kKbPerA; ++h) {
-              if (h < cur.nkb && ok) {
-                if (!warp_wait(&b_full[rb.idx], rb.phase, &abort_flag)) ok = false;
-                rb.next(SB);
-              }
-            }
-            if (!ok) break;
             if (lane == 0) mbar_arrive(&a_full[sa]);
             ra.next(SA);
           }
@@ -705,76 +730,87 @@ __global__ void __launch_bounds__(tc_threads(BITS), 1)
     }
   } else if (warp == kMmaWarp) {
     // ================================= MMA =================================
-    if (lane == 0) {
-      long long w_mma_tmem = 0, w_mma_afull = 0;
-      const long long t_mma0 = clock64();
-      int64_t it = 0;
-      Ring ra, rb;  // A ring, B ring
-      int j = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++j) {
-        const TileInfo ti = tile_info(p, act_e, tile_start, n_act, t);
-        const uint32_t idesc = idesc_bf16(BM, ti.nmma);
-        const int buf = j & 1;
+    // the whole warp, converged; every wait's outcome is agreed by the warp
+    long long w_mma_tmem = 0, w_mma_afull = 0, w_mma_bfull = 0;
+    const long long t_mma0 = clock64();
+    int64_t it = 0;
+    Ring ra, rb;  // A ring, B ring
+    int j = 0;
+    bool ok = true;
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      const bool got = mbar_wait_sleep(bar, parity, kWaitBudgetCycles);
+      return __all_sync(0xFFFFFFFFu, got);
+    };
+    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++j) {
+      const TileInfo ti = tile_info(p, act_e, tile_start, n_act, t);
+      const uint32_t idesc = idesc_bf16(BM, ti.nmma);
+      const int buf = j & 1;
+      {
+        TC_T0();
+        if (!wait_all(&tmem_empty[buf], (uint32_t)(((j >> 1) & 1) ^ 1))) ok = false;
+        TC_ACC(w_mma_tmem);
+      }
+      if (__any_sync(0xFFFFFFFFu, !ok || abort_flag != 0)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d0 = tmem_base + (uint32_t)(buf * BN);
+      for (int as = 0, kb = 0; as < nas; ++as, ra.next(SA)) {
+        const int sa = ra.idx;
         {
           TC_T0();
-          if (!mbar_wait_sleep(&tmem_empty[buf], (uint32_t)(((j >> 1) & 1) ^ 1), kWaitBudgetCycles))
-            ok = false;
-          TC_ACC(w_mma_tmem);
-        }
-        if (!ok || abort_flag) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d0 = tmem_base + (uint32_t)(buf * BN);
-        // one wait per A stage keeps the MMA queue fed
-        for (int as = 0, kb = 0; as < nas; ++as, ra.next(SA)) {
-          const int sa = ra.idx;
-          {
-            TC_T0();
-            if (!mbar_wait_sleep(&a_full[sa], ra.phase, kWaitBudgetCycles)) ok = false;
-            TC_ACC(w_mma_afull);
-          }
-          if (!ok) break;
-          // operand visibility: the dequant writers' proxy fence, the token
-          // tiles' transaction counts observed by them, and their release
-          // arrivals acquired by this wait
-#pragma unroll
-          for (int h = 0; h < kKbPerA; ++h) {
-            if (kb < nkb && (h == 0 || as * kKbPerA + h < nkb)) {
-              const uint64_t adesc = smem_desc_sw128(stage_a(sa, h));
-              const uint64_t bdesc = smem_desc_sw128(stage_b(rb.idx));
-#pragma unroll
-              for (int kk = 0; kk < BK / 16; ++kk)  // K advance in the swizzle atom: 32 bytes
-                umma_bf16(d0, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
-              umma_commit(&b_empty[rb.idx]);
-              rb.next(SB);
-              ++kb;
-              ++it;
-            }
-          }
-          umma_commit(&a_empty[sa]);
+          if (!wait_all(&a_full[sa], ra.phase)) ok = false;
+          TC_ACC(w_mma_afull);
         }
         if (!ok) break;
-        umma_commit(&tmem_full[buf]);
+        // operand visibility: the dequant writers' proxy fence and release
+        // arrivals acquired by the wait above; the token tile's TMA
+        // transaction count by the wait below
+#pragma unroll
+        for (int h = 0; h < kKbPerA; ++h) {
+          if (kb < nkb && (h == 0 || as * kKbPerA + h < nkb)) {
+            {
+              TC_T0();
+              if (!wait_all(&b_full[rb.idx], rb.phase)) ok = false;
+              TC_ACC(w_mma_bfull);
+            }
+            if (!ok) break;
+            const uint64_t adesc = smem_desc_sw128(stage_a(sa, h));
+            const uint64_t bdesc = smem_desc_sw128(stage_b(rb.idx));
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)  // K advance in the swizzle atom: 32 bytes
+              umma_bf16(d0, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_commit(&b_empty[rb.idx]);
+            rb.next(SB);
+            ++kb;
+            ++it;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&a_empty[sa]);
       }
-      if (!ok) {
-        raise_device_error(p.err, MOE_DEVERR_TIMEOUT);
-        abort_flag = 1;
-      }
-      // wait for this thread's last MMAs before TMEM is released (a commit
-      // with no MMA issued before it is not relied on to arrive)
-      if (it > 0) {
-        umma_commit(&drain_bar);
-        mbar_wait(&drain_bar, 0, kWaitBudgetCycles);
-      }
+      if (!ok) break;
+      umma_commit(&tmem_full[buf]);
+    }
+    if (!ok && lane == 0) {
+      raise_device_error(p.err, MOE_DEVERR_TIMEOUT);
+      abort_flag = 1;
+    }
+    // wait for the warp's last MMAs before TMEM is released (a commit with
+    // no MMA issued before it is not relied on to arrive)
+    if (it > 0) {
+      umma_commit(&drain_bar);
+      mbar_wait(&drain_bar, 0, kWaitBudgetCycles);
+    }
+    __syncwarp();
+    if (lane == 0) {
       TC_FLUSH(4, w_mma_tmem);
       TC_FLUSH(5, w_mma_afull);
+      TC_FLUSH(12, w_mma_bfull);
       TC_FLUSH(7, clock64() - t_mma0);
       TC_FLUSH(8, it);
     }
-    __syncwarp();
   } else {
     // =============================== epilogue ===============================
     long long w_epi = 0;
@@ -954,24 +990,27 @@ moe_status_t launch_tc(const CUtensorMap& tma, const CUtensorMap& tmc, TcParams 
       return 0L;
     return (long)optin - (long)fa.sharedSizeBytes - 1024;
   }();
-  // ring depths: two A stages, code slots for about 8 k-blocks (at least
-  // 2), and as many token-tile slots as fit (at least 3, else fewer code
-  // slots)
+  // ring depths: two A stages, code slots for about 8 k-blocks, and as many
+  // token-tile slots as fit (fewer code slots, down to 2, while fewer than 4
+  // token tiles fit: each token tile is in flight from its TMA issue to the
+  // end of its MMAs, so their count sets how many k-blocks overlap)
   const long b_tile = (long)p.bn_cap * kBRowBytes;
   const long kpc = kCodeRowBytes / (BK * BITS / 8);
+  const long a_stages = 2;
   long c_stages = (8 + kpc - 1) / kpc;
   if (c_stages < 2) c_stages = 2;
-  long b_stages = 0;
-  for (; c_stages >= 2; --c_stages) {
-    b_stages = (avail - 2L * kAStageBytes - c_stages * kCodeSlotBytes) / b_tile;
-    if (b_stages >= 3) break;
+  auto fit_b = [&] { return (avail - a_stages * kAStageBytes - c_stages * kCodeSlotBytes) / b_tile; };
+  long b_stages = fit_b();
+  while (b_stages < 4 && c_stages > 2) {
+    --c_stages;
+    b_stages = fit_b();
   }
   if (b_stages > kMaxStages) b_stages = kMaxStages;
-  if (c_stages < 2 || b_stages < 2) return MOE_ERR_UNSUPPORTED;
-  p.a_stages = 2;
+  if (b_stages < 2) return MOE_ERR_UNSUPPORTED;
+  p.a_stages = (int)a_stages;
   p.b_stages = (int)b_stages;
   p.c_stages = (int)c_stages;
-  const size_t smem = 2 * (size_t)kAStageBytes + (size_t)c_stages * kCodeSlotBytes +
+  const size_t smem = (size_t)a_stages * kAStageBytes + (size_t)c_stages * kCodeSlotBytes +
                       (size_t)b_stages * b_tile + 1024;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)

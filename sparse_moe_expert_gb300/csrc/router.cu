@@ -1019,13 +1019,49 @@ int router_tokens_per_group(int T, int E) {
   return tpc;
 }
 
+// Large batches (at least 8 tokens per SM): one CTA per token group with
+// every expert, so a warp walks several tiles of the same token rows and
+// the group's logits, softmax and top-k stay in its own shared memory.  The
+// group size (32, 16 or 8 tokens) minimises waves x tokens per group.
+int router_single_cta_tokens(int T, int E) {
+  const int sms = moe_host::sm_count();
+  if ((int64_t)T < 8LL * sms) return 0;
+  int best = 0;
+  int64_t best_cost = 0;
+  for (int tpc = router_group_tokens(E); tpc >= 8; tpc >>= 1) {
+    const int64_t groups = (T + tpc - 1) / tpc;
+    const int64_t cost = (groups + sms - 1) / sms * tpc;
+    if (best == 0 || cost < best_cost) {
+      best = tpc;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
 moe_status_t launch_router(const RouterParams& p, cudaStream_t st) {
   using namespace moe_host;
   moe_status_t small_status = MOE_OK;
   if (launch_router_small(p, st, &small_status)) return small_status;
-  const int tpc = router_tokens_per_group(p.T, p.E);
+  const int single_tpc = router_single_cta_tokens(p.T, p.E);
+  const int tpc = single_tpc ? single_tpc : router_tokens_per_group(p.T, p.E);
   const int ngroups = (p.T + tpc - 1) / tpc;
-  if (ngroups > 0) {
+  if (ngroups > 0 && single_tpc) {
+    const size_t smem = (size_t)tpc * p.E * sizeof(float);
+    RouterParams q = p;
+    q.tpc = tpc;
+    q.smem_stage = 0;
+    auto kern = router_topk_kernel<1>;
+    static size_t set_max1[kMaxCachedDevices] = {};
+    const int dev = device_index();
+    if (smem > 48 * 1024 && smem > set_max1[dev]) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess)
+        return MOE_ERR_CUDA;
+      set_max1[dev] = smem;
+    }
+    if (launch(kern, ngroups, kRouterThreads, smem, st, q) != MOE_OK) return MOE_ERR_CUDA;
+  } else if (ngroups > 0) {
     size_t smem = (size_t)tpc * p.E * sizeof(float);
     // more token groups than a wave of 8-CTA clusters fills: clusters of 4
     const bool wide = (int64_t)ngroups * kRouterCluster > sm_count();

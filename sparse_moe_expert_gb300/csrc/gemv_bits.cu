@@ -11,16 +11,22 @@
 // whole words (10 for 5 bits, 12 for 6), so groups start on word
 // boundaries and a row's scales and biases index groups as for 4 and 8 bits.
 //
-// Work.  An item is (active expert, chunk of up to kBtTokens of its tokens,
-// block of 8 weight features); the persistent CTAs (two per SM) take equal
-// contiguous ranges of the item list.  Warp w of an item computes feature
-// f = 8 block + w: for SwiGLU its gate row f and up row n_out + f, else row f.
-// Lane l takes codes 2l and 2l + 1 of every group (one funnel shift over the
-// group's words brings both), dequantizes them in fp32 (s q + b, s and b
-// exact from fp16) and accumulates them against each token's two values;
-// the 32 lane partials are added by a fixed xor butterfly.  A row's value
-// depends only on its own codes, scales, biases and the tokens, so the fused
-// gate_up product equals the separate gate and up products bit for bit.
+// Work.  An item is (active expert, chunk of up to MT of its tokens, block
+// of 12 weight features); the persistent CTAs take equal contiguous ranges
+// of the item list, so a CTA walks the feature blocks of one chunk after the
+// other.  The chunk's token values are staged once in shared memory as fp32
+// ([token][K]; bf16 rounding for fp32 rows, as the other GEMV paths apply)
+// and stay there while the CTA's items keep to that chunk.  While a CTA
+// computes an item it asks L2 for the code, scale and bias lines of its next
+// item, so the weight loads of that item find their lines in L2.
+// Warp w of an item computes feature f = 12 block + w: for SwiGLU its gate
+// row f and up row n_out + f, else row f.  Lane l takes codes 2l and 2l + 1
+// of every group (one funnel shift over the group's words brings both),
+// dequantizes them in fp32 (s q + b, s and b exact from fp16) and
+// accumulates them against each token's two values; the 32 lane partials are
+// added by a fixed xor butterfly.  A row's value depends only on its own
+// codes, scales, biases and the tokens, so the fused gate_up product equals
+// the separate gate and up products bit for bit.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -28,10 +34,11 @@
 namespace moe {
 namespace {
 
-constexpr int kBtThreads = 256;
-constexpr int kBtWarps = kBtThreads / 32;
-constexpr int kBtTokens = 8;  // tokens per item
+constexpr int kBtThreads = 384;
+constexpr int kBtWarps = kBtThreads / 32;  // features per item
+constexpr int kBtMaxTokens = 8;            // tokens per chunk (at most)
 constexpr int kBtMaxE = 1024;
+constexpr size_t kBtMaxStage = 200 * 1024;  // staged token bytes (at most)
 
 enum BtMode { kBtSwiglu = 0, kBtRaw = 1 };
 enum BtAct { kBtActX = 0, kBtActF32 = 1, kBtActBf16 = 2 };
@@ -44,7 +51,8 @@ struct BtParams {
   int T, kmax, E, K;
   int n_rows;  // weight rows per expert
   int n_out;   // output columns: n_rows / 2 (SWIGLU) or n_rows
-  int blocks;  // feature blocks of 8 per (expert, chunk)
+  int blocks;  // feature blocks of kBtWarps per (expert, chunk)
+  int mt;      // tokens per chunk
   const uint32_t* wq;
   const uint16_t* ws;
   const uint16_t* wb;
@@ -61,14 +69,21 @@ __device__ __forceinline__ float bt_act(const BtParams& p, int64_t row, int64_t 
   return bf16_bits_to_f32(__ldg(static_cast<const uint16_t*>(p.act) + row * p.K + k));
 }
 
-template <int BITS, int MODE>
-__global__ void __launch_bounds__(kBtThreads) gemv_bits_kernel(BtParams p) {
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
+template <int BITS, int MODE, int MT>
+__global__ void __launch_bounds__(kBtThreads, 1) gemv_bits_kernel(BtParams p) {
   constexpr int kGroupWords = 2 * BITS;  // 64 codes of a group
   constexpr uint32_t kMask = (1u << BITS) - 1u;
+  constexpr int kRows = MODE == kBtSwiglu ? 2 : 1;
+  extern __shared__ float bt_x[];  // staged tokens [mt][K]
   __shared__ int act_e[kBtMaxE + 1], act_lo[kBtMaxE + 1], act_m[kBtMaxE + 1], act_base[kBtMaxE + 1];
   __shared__ int n_act_sh;
   __shared__ int wtot[kBtWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int mt = MT;  // tokens per chunk (p.mt)
   pdl_wait();
   pdl_trigger();
 
@@ -103,12 +118,12 @@ __global__ void __launch_bounds__(kBtThreads) gemv_bits_kernel(BtParams p) {
     __syncthreads();
   }
   const int n_act = n_act_sh;
-  // items before each active expert: chunks of kBtTokens tokens x feature blocks
+  // items before each active expert: chunks of mt tokens x feature blocks
   if (warp == 0) {
     int carry = 0;
     for (int a0 = 0; a0 < n_act; a0 += 32) {
       const int a = a0 + lane;
-      int v = a < n_act ? ((act_m[a] + kBtTokens - 1) / kBtTokens) * p.blocks : 0;
+      int v = a < n_act ? ((act_m[a] + mt - 1) / mt) * p.blocks : 0;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const int y = __shfl_up_sync(0xFFFFFFFFu, v, off);
@@ -129,71 +144,152 @@ __global__ void __launch_bounds__(kBtThreads) gemv_bits_kernel(BtParams p) {
   const int bit0 = 2 * lane * BITS;
   const int w0 = bit0 >> 5, sh = bit0 & 31;
 
-  for (int64_t it = it0; it < it1; ++it) {
+  struct Item {
+    int a, c, blk;
+  };
+  auto item_at = [&](int64_t it) {
     int lo = 0, hi = n_act - 1;  // last a with act_base[a] <= it
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (act_base[mid] <= it) lo = mid;
       else hi = mid - 1;
     }
-    const int a = lo;
-    const int local = (int)(it - act_base[a]);
-    const int c = local / p.blocks, blk = local - c * p.blocks;
-    const int r0 = act_lo[a] + c * kBtTokens;  // first sorted row of the chunk
-    const int nt = min(kBtTokens, act_m[a] - c * kBtTokens);
-    const int f = blk * 8 + warp;              // this warp's feature
-    if (f >= p.n_out) continue;
-    // activation rows of the chunk's tokens
-    int64_t arow[kBtTokens];
-#pragma unroll
-    for (int n = 0; n < kBtTokens; ++n) {
-      const int r = r0 + min(n, nt - 1);
-      arow[n] = p.act_kind == kBtActX ? (int64_t)(__ldg(p.sorted + r) / p.kmax) : (int64_t)r;
+    Item r;
+    r.a = lo;
+    const int local = (int)(it - act_base[lo]);
+    r.c = local / p.blocks;
+    r.blk = local - r.c * p.blocks;
+    return r;
+  };
+  // L2 lines of an item's code rows, scales and biases (every thread a share)
+  auto prefetch_item = [&](const Item& q) {
+    const int64_t ebase = (int64_t)act_e[q.a] * p.n_rows;
+    const int f0 = q.blk * kBtWarps;
+    const int nf = min(kBtWarps, p.n_out - f0);
+    for (int r = 0; r < kRows; ++r) {
+      const int64_t row0 = ebase + (r == 0 ? f0 : p.n_out + f0);
+      const char* cb = reinterpret_cast<const char*>(p.wq + row0 * row_words);
+      const int64_t cbytes = (int64_t)nf * row_words * 4;
+      for (int64_t o = (int64_t)tid * 128; o < cbytes; o += (int64_t)kBtThreads * 128)
+        prefetch_l2(cb + o);
+      const int64_t sbytes = (int64_t)nf * ngroups * 2;
+      const char* sb = reinterpret_cast<const char*>(p.ws + row0 * ngroups);
+      const char* bb = reinterpret_cast<const char*>(p.wb + row0 * ngroups);
+      for (int64_t o = (int64_t)tid * 128; o < sbytes; o += (int64_t)kBtThreads * 128) {
+        prefetch_l2(sb + o);
+        prefetch_l2(bb + o);
+      }
     }
-    const int64_t ebase = (int64_t)act_e[a] * p.n_rows;
-    constexpr int kRows = MODE == kBtSwiglu ? 2 : 1;
+  };
+
+  int st_a = -1, st_c = -1;
+  for (int64_t it = it0; it < it1; ++it) {
+    const Item cur = item_at(it);
+    const int lo_tok = act_lo[cur.a] + cur.c * mt;  // first sorted row of the chunk
+    const int nt = min(mt, act_m[cur.a] - cur.c * mt);
+    if (cur.a != st_a || cur.c != st_c) {
+      // stage the chunk's token values (every warp is past the previous item)
+      __syncthreads();
+#pragma unroll 1
+      for (int n = 0; n < MT; ++n) {
+        float* dst = bt_x + (size_t)n * p.K;
+        if (n < nt) {
+          const int r = lo_tok + n;
+          const int64_t row =
+              p.act_kind == kBtActX ? (int64_t)(__ldg(p.sorted + r) / p.kmax) : (int64_t)r;
+          for (int k = tid; k < p.K; k += kBtThreads) dst[k] = bt_act(p, row, k);
+        } else {
+          for (int k = tid; k < p.K; k += kBtThreads) dst[k] = 0.0f;
+        }
+      }
+      __syncthreads();
+      st_a = cur.a;
+      st_c = cur.c;
+    }
+    if (it + 1 < it1) prefetch_item(item_at(it + 1));
+    const int f = cur.blk * kBtWarps + warp;  // this warp's feature
+    if (f >= p.n_out) continue;
+    const int64_t ebase = (int64_t)act_e[cur.a] * p.n_rows;
     int64_t wrow[kRows];
     wrow[0] = ebase + f;
     if (MODE == kBtSwiglu) wrow[kRows - 1] = ebase + p.n_out + f;
-    float acc[kRows][kBtTokens];
+    float acc[kRows][MT];
 #pragma unroll
     for (int q = 0; q < kRows; ++q)
 #pragma unroll
-      for (int n = 0; n < kBtTokens; ++n) acc[q][n] = 0.0f;
-    for (int g = 0; g < ngroups; ++g) {
-      // this lane's two token values of group g, per token
-      float x0[kBtTokens], x1[kBtTokens];
+      for (int n = 0; n < MT; ++n) acc[q][n] = 0.0f;
+    // this lane's pair of staged values: token n, group g at xs[n K / 2 + 32 g]
+    const float2* xs = reinterpret_cast<const float2*>(bt_x) + lane;
+    const int kh = p.K >> 1;
+    // scales and biases of 32 groups per load (lane l holds group g32 + l);
+    // code words in batches of kGb groups, the next batch loaded while the
+    // current one is computed
+    constexpr int kGb = 4;
+    uint32_t sv[kRows] = {}, bv[kRows] = {};
+    uint32_t wlo[kGb][kRows], whi[kGb][kRows], nlo[kGb][kRows], nhi[kGb][kRows];
+    auto load_batch = [&](int g0, uint32_t (&lo)[kGb][kRows], uint32_t (&hi)[kGb][kRows]) {
 #pragma unroll
-      for (int n = 0; n < kBtTokens; ++n) {
-        x0[n] = n < nt ? bt_act(p, arow[n], (int64_t)g * 64 + 2 * lane) : 0.0f;
-        x1[n] = n < nt ? bt_act(p, arow[n], (int64_t)g * 64 + 2 * lane + 1) : 0.0f;
+      for (int j = 0; j < kGb; ++j)
+#pragma unroll
+        for (int q = 0; q < kRows; ++q) {
+          lo[j][q] = hi[j][q] = 0u;
+          if (g0 + j < ngroups) {
+            const uint32_t* gw = p.wq + wrow[q] * row_words + (int64_t)(g0 + j) * kGroupWords;
+            lo[j][q] = __ldg(gw + w0);
+            if (w0 + 1 < kGroupWords) hi[j][q] = __ldg(gw + w0 + 1);
+          }
+        }
+    };
+    load_batch(0, wlo, whi);
+    for (int g0 = 0; g0 < ngroups; g0 += kGb) {
+      if ((g0 & 31) == 0) {
+#pragma unroll
+        for (int q = 0; q < kRows; ++q) {
+          const int gl = g0 + lane;
+          sv[q] = gl < ngroups ? __ldg(p.ws + wrow[q] * ngroups + gl) : 0u;
+          bv[q] = gl < ngroups ? __ldg(p.wb + wrow[q] * ngroups + gl) : 0u;
+        }
+      }
+      if (g0 + kGb < ngroups) load_batch(g0 + kGb, nlo, nhi);
+#pragma unroll
+      for (int j = 0; j < kGb; ++j) {
+        const int g = g0 + j;
+        if (g >= ngroups) break;
+        float2 xv[MT];
+        const float2* xg = xs + g * 32;
+#pragma unroll
+        for (int n = 0; n < MT; ++n) xv[n] = xg[n * kh];
+#pragma unroll
+        for (int q = 0; q < kRows; ++q) {
+          const uint32_t v = __funnelshift_r(wlo[j][q], whi[j][q], sh);
+          const float q0 = (float)(v & kMask), q1 = (float)((v >> BITS) & kMask);
+          const float s = f16_bits_to_f32((uint16_t)__shfl_sync(0xFFFFFFFFu, sv[q], g & 31));
+          const float b = f16_bits_to_f32((uint16_t)__shfl_sync(0xFFFFFFFFu, bv[q], g & 31));
+          const float d0 = fmaf(s, q0, b), d1 = fmaf(s, q1, b);
+#pragma unroll
+          for (int n = 0; n < MT; ++n) acc[q][n] = fmaf(d1, xv[n].y, fmaf(d0, xv[n].x, acc[q][n]));
+        }
       }
 #pragma unroll
-      for (int q = 0; q < kRows; ++q) {
-        const uint32_t* gw = p.wq + wrow[q] * row_words + (int64_t)g * kGroupWords;
-        const uint32_t lo_w = __ldg(gw + w0);
-        const uint32_t hi_w = w0 + 1 < kGroupWords ? __ldg(gw + w0 + 1) : 0u;
-        const uint32_t v = __funnelshift_r(lo_w, hi_w, sh);
-        const float q0 = (float)(v & kMask), q1 = (float)((v >> BITS) & kMask);
-        const float s = f16_bits_to_f32(__ldg(p.ws + wrow[q] * ngroups + g));
-        const float b = f16_bits_to_f32(__ldg(p.wb + wrow[q] * ngroups + g));
-        const float d0 = fmaf(s, q0, b), d1 = fmaf(s, q1, b);
+      for (int j = 0; j < kGb; ++j)
 #pragma unroll
-        for (int n = 0; n < kBtTokens; ++n) acc[q][n] = fmaf(d1, x1[n], fmaf(d0, x0[n], acc[q][n]));
-      }
+        for (int q = 0; q < kRows; ++q) {
+          wlo[j][q] = nlo[j][q];
+          whi[j][q] = nhi[j][q];
+        }
     }
     // the 32 lane partials of every row and token, by a fixed xor butterfly
 #pragma unroll
     for (int q = 0; q < kRows; ++q)
 #pragma unroll
-      for (int n = 0; n < kBtTokens; ++n)
+      for (int n = 0; n < MT; ++n)
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1)
           acc[q][n] = __fadd_rn(acc[q][n], __shfl_xor_sync(0xFFFFFFFFu, acc[q][n], off));
 #pragma unroll
-    for (int n = 0; n < kBtTokens; ++n) {
+    for (int n = 0; n < MT; ++n) {
       if (lane != n || n >= nt) continue;
-      const int64_t orow = (int64_t)r0 + n;
+      const int64_t orow = (int64_t)lo_tok + n;
       if (MODE == kBtSwiglu) {
         const float hv = swiglu_f32(acc[0][n], acc[kRows - 1][n]);
         if (p.out_dtype == MOE_DTYPE_BF16)
@@ -209,10 +305,34 @@ __global__ void __launch_bounds__(kBtThreads) gemv_bits_kernel(BtParams p) {
   }
 }
 
+template <int BITS, int MODE, int MT>
+moe_status_t launch_bits_mt(const BtParams& p, cudaStream_t st) {
+  auto kern = gemv_bits_kernel<BITS, MODE, MT>;
+  const size_t smem = (size_t)p.mt * p.K * sizeof(float);
+  // the static arrays count against the same limit: raise it for any size
+  static size_t set_max[moe_host::kMaxCachedDevices] = {};  // per device
+  const int dev = moe_host::device_index();
+  if (smem > set_max[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    set_max[dev] = smem;
+  }
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kBtThreads, smem) != cudaSuccess ||
+      occ < 1)
+    return MOE_ERR_CUDA;
+  return moe_host::launch(kern, occ * moe_host::sm_count(), kBtThreads, smem, st, p);
+}
+
 template <int BITS, int MODE>
 moe_status_t launch_bits(const BtParams& p, cudaStream_t st) {
-  return moe_host::launch(gemv_bits_kernel<BITS, MODE>, 2 * moe_host::sm_count(), kBtThreads, 0,
-                          st, p);
+  switch (p.mt) {
+    case 8: return launch_bits_mt<BITS, MODE, 8>(p, st);
+    case 4: return launch_bits_mt<BITS, MODE, 4>(p, st);
+    case 2: return launch_bits_mt<BITS, MODE, 2>(p, st);
+    default: return launch_bits_mt<BITS, MODE, 1>(p, st);
+  }
 }
 
 }  // namespace
@@ -234,7 +354,14 @@ moe_status_t gemv_bits_qmm(const void* act, int act_kind, const int32_t* sorted,
   p.K = K;
   p.n_rows = n_rows;
   p.n_out = swiglu ? n_rows / 2 : n_rows;
-  p.blocks = (p.n_out + 7) / 8;
+  p.blocks = (p.n_out + kBtWarps - 1) / kBtWarps;
+  // tokens per chunk: an expert holds at most T rows, and the staged values
+  // must fit in shared memory
+  int mt = 1;
+  while (mt < kBtMaxTokens && mt < T && (size_t)(2 * mt) * K * sizeof(float) <= kBtMaxStage)
+    mt <<= 1;
+  if ((size_t)mt * K * sizeof(float) > kBtMaxStage) return MOE_ERR_UNSUPPORTED;
+  p.mt = mt;
   p.wq = wq;
   p.ws = ws;
   p.wb = wb;

@@ -64,6 +64,8 @@ def parse_args(argv=None):
                         "the next one's input; value counts layer-calls)")
     p.add_argument("--groups", type=int, default=0,
                    help="group-limited routing: best expert of each of G groups (k = G)")
+    p.add_argument("--bits", type=int, default=0, choices=[0, 4, 5, 6, 8],
+                   help="code width other than the workload's (5 or 6: the 5/6-bit GEMV)")
     p.add_argument("--experts", type=int, default=0,
                    help="smaller expert pool (same per-call work; for profiling captures)")
     p.add_argument("--y-dtype", default="auto", choices=["auto", "f32", "bf16"],
@@ -370,7 +372,22 @@ def workload_measure(moe, cfg, dev, rank, world, steps, warmup, layer_kw, nl=1, 
     return layer, layer_np, x_bits, temps, res
 
 
-def workload_summary(moe, cfg, layer, res, peaks, peak_src):
+def recorded_traffic(name, kernel_src):
+    """DRAM bytes (read + write) of one gate_up launch of workload `name`, from
+    the ncu record in profiles/traffic.json taken with the kernel source as it
+    is now (matched by its hash); None without such a record."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            for rec in json.load(f).get("records", []):
+                if rec.get("config") == name and rec.get("src") == os.path.basename(kernel_src) \
+                        and rec.get("src_sha") == file_sha(kernel_src):
+                    return rec.get("gate_up_dram_bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+def workload_summary(moe, cfg, layer, res, peaks, peak_src, name=None):
     """The measured numbers of one workload as the JSON fields of its line."""
     calls, T, nl, ms = res["calls"], res["T"], res["nl"], res["ms"]
     kt = res.get("ktot", {})
@@ -407,6 +424,8 @@ def workload_summary(moe, cfg, layer, res, peaks, peak_src):
                 "layer_frac": layer_gbs / peaks["hbm_gbs"],
                 "kernel": kernel_label, "algorithmic_bytes_per_launch": gu_b / calls,
                 "peak_source": peak_src}
+    src = os.path.join(CSRC, "gemv_bits.cu") if cfg.bits not in (4, 8) else KERNEL_SRC[path_used]
+    roof["traffic"] = recorded_traffic(name or cfg.name, src)
     kern = {"gate_up_us": gu_ms * 1e3 / calls if gu_ms else None,
             "down_us": dn_ms * 1e3 / calls if dn_ms else None,
             "gate_up_gbs": gu_gbs, "down_gbs": dn_gbs,
@@ -448,6 +467,8 @@ def run_ours(args):
     cfg = workloads.CONFIGS[args.config]
     if args.experts:
         cfg = cfg.scaled(E=args.experts)
+    if args.bits:
+        cfg = cfg.scaled(bits=args.bits)
     path = {"auto": moe.PATH_AUTO, "gemv": moe.PATH_GEMV, "tc": moe.PATH_TC}[args.path]
     y_dtype = {"auto": None, "f32": torch.float32, "bf16": torch.bfloat16}[args.y_dtype]
     gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
@@ -466,17 +487,6 @@ def run_ours(args):
     value = tokens_per_step * nl * world / (ms / 1000.0)  # layer-calls: tokens x layers
     clocks = res["clocks"]
     roof, kern = workload_summary(moe, cfg, layer, res, peaks, peak_src)
-    kernel_src = KERNEL_SRC[layer.resolved_path(T)]
-    traffic = None
-    try:
-        with open(TRAFFIC_FILE) as f:
-            for rec in json.load(f).get("records", []):
-                if rec.get("config") == cfg.name and rec.get("src") == os.path.basename(kernel_src) \
-                        and rec.get("src_sha") == file_sha(kernel_src):
-                    traffic = rec.get("gate_up_dram_bytes_per_launch")
-    except (OSError, ValueError):
-        pass
-    roof["traffic"] = traffic
 
     # end to end through the public API with pinned host buffers
     x_host = torch.from_numpy(x_bits).view(torch.bfloat16).pin_memory()
@@ -519,6 +529,7 @@ def run_ours(args):
     torch.cuda.empty_cache()
 
     if world == 1 and not args.no_configs and args.config == "decode" and not args.experts \
+            and not args.bits \
             and nl == 1 and args.groups == 0 and path == moe.PATH_AUTO and y_dtype is None:
         # the other workloads of the layer, measured the same way in this run
         cfgs = {}
@@ -535,7 +546,7 @@ def run_ours(args):
                       y_dtype=torch.float32 if name == "prefill_y_f32" else None)
             lay, _, _, _, r = workload_measure(moe, c, dev, rank, world, csteps, args.warmup, kw,
                                                clocks_gpu=gpu_id)
-            rf, kn = workload_summary(moe, c, lay, r, peaks, peak_src)
+            rf, kn = workload_summary(moe, c, lay, r, peaks, peak_src, name=name)
             cfgs[name] = {"config": dict(workload_config(c),
                                          y_storage=str(lay.y_storage(r["T"])).replace("torch.", "")),
                           "value": r["calls"] * r["T"] / (r["ms"] / 1e3),

@@ -822,7 +822,7 @@ __device__ void router_tail_warp(const RouterParams& p, const float* logits_s, i
   }
 }
 
-__global__ void __launch_bounds__(512) router_small_kernel(RouterParams p, int lg_floats) {
+__global__ void __launch_bounds__(512, 1) router_small_kernel(RouterParams p, int lg_floats) {
   extern __shared__ __align__(16) float rs_smem[];
   float* logits_s = rs_smem;                 // leader: [T][E]; then the grouping's scratch
   float* ws_s = rs_smem + lg_floats;         // this CTA's weight rows [ne][H]

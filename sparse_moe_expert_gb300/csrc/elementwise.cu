@@ -34,33 +34,51 @@ __global__ void __launch_bounds__(kEwThreads) combine_kernel(const void* __restr
     float acc[V];
 #pragma unroll
     for (int e = 0; e < V; ++e) acc[e] = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      const int r = __ldg(inv_pos + (int64_t)t * kmax + j);
-      if (r < 0) {  // dropped by its expert's capacity: no contribution
-        if (r != MOE_DROPPED) raise_device_error(err, MOE_DEVERR_BAD_INDEX);
-        continue;
-      }
-      const float w = __ldg(topk_w + (int64_t)t * kmax + j);
-      float yv[V];
-      if constexpr (BF16_Y) {
-        const uint4 q = __ldg(reinterpret_cast<const uint4*>(
-                                  static_cast<const uint16_t*>(y) + (int64_t)r * H) + v);
-        const uint32_t q4[4] = {q.x, q.y, q.z, q.w};
+    // four slots at a time: their indices, weights and rows are all loaded
+    // before the sums, which still run in ascending j
+    constexpr int kJ = 4;
+    for (int j0 = 0; j0 < k; j0 += kJ) {
+      int r[kJ];
+      float w[kJ];
+      uint4 q[kJ];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          yv[2 * e] = __uint_as_float(q4[e] << 16);
-          yv[2 * e + 1] = __uint_as_float(q4[e] & 0xFFFF0000u);
+      for (int jj = 0; jj < kJ; ++jj) {
+        const int j = j0 + jj;
+        r[jj] = j < k ? __ldg(inv_pos + (int64_t)t * kmax + j) : MOE_DROPPED;
+        w[jj] = j < k ? __ldg(topk_w + (int64_t)t * kmax + j) : 0.0f;
+      }
+#pragma unroll
+      for (int jj = 0; jj < kJ; ++jj) {
+        q[jj] = make_uint4(0u, 0u, 0u, 0u);
+        if (r[jj] >= 0) {
+          if constexpr (BF16_Y)
+            q[jj] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(y) +
+                                                         (int64_t)r[jj] * H) + v);
+          else
+            q[jj] = __ldg(reinterpret_cast<const uint4*>(static_cast<const float*>(y) +
+                                                         (int64_t)r[jj] * H) + v);
+        } else if (r[jj] != MOE_DROPPED) {
+          raise_device_error(err, MOE_DEVERR_BAD_INDEX);
         }
-      } else {
-        const float4 q = __ldg(reinterpret_cast<const float4*>(
-                                   static_cast<const float*>(y) + (int64_t)r * H) + v);
-        yv[0] = q.x;
-        yv[1] = q.y;
-        yv[2] = q.z;
-        yv[3] = q.w;
       }
 #pragma unroll
-      for (int e = 0; e < V; ++e) acc[e] = fmaf(w, yv[e], acc[e]);
+      for (int jj = 0; jj < kJ; ++jj) {
+        if (r[jj] < 0) continue;  // dropped by its expert's capacity, or past k
+        float yv[V];
+        const uint32_t q4[4] = {q[jj].x, q[jj].y, q[jj].z, q[jj].w};
+        if constexpr (BF16_Y) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            yv[2 * e] = __uint_as_float(q4[e] << 16);
+            yv[2 * e + 1] = __uint_as_float(q4[e] & 0xFFFF0000u);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) yv[e] = __uint_as_float(q4[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] = fmaf(w[jj], yv[e], acc[e]);
+      }
     }
     uint32_t o[V / 2];
 #pragma unroll

@@ -972,12 +972,14 @@ moe_status_t launch_stream(const CUtensorMap& tm, SvParams p, cudaStream_t st) {
     optin = v;
   }
   const long budget = (long)optin - static_smem - 1024;
-  // tokens per pass: as many as fit beside at least 4 ring slots
+  // tokens per pass: as many as fit beside at least 3 ring slots (a pass of
+  // 8 tokens with 3 slots beats two passes of 4 with 4 slots: each pass
+  // streams the expert's rows again)
   int stages = 0;
   for (;;) {
     stages = kSvMaxStages;
     while (stages >= 2 && (long)sv_layout(BITS, p.K, p.mts, stages, p.E).total > budget) --stages;
-    if (stages >= 4 || p.mts == 1) break;
+    if (stages >= 3 || p.mts == 1) break;
     p.mts >>= 1;
   }
   if (stages < 2) return MOE_ERR_UNSUPPORTED;

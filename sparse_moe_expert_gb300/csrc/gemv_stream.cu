@@ -135,10 +135,11 @@ struct SvLayout {
 };
 
 // Shared-memory carve-up, from a 1024-byte aligned base.
-__host__ __device__ inline SvLayout sv_layout(int bits, int K, int mts, int stages, int E) {
+__host__ __device__ inline SvLayout sv_layout(int bits, int K, int mts, int stages, int E,
+                                              bool dual) {
   const int ngroups = K / 64;
   const int gpc = kSvRowChunk / (8 * bits);
-  const int scale_bytes = 2 * 16 * (gpc * 2 + 16);
+  const int scale_bytes = (dual ? 2 : 1) * 2 * 16 * (gpc * 2 + 16);
   const int mts2 = mts < 2 ? 2 : mts;
   SvLayout L;
   uint32_t o = 0;
@@ -251,16 +252,26 @@ struct SvCursor {
 
 // GATED: a k-gated launch (p.gate); a separate instantiation, since even an
 // untaken gate check at the top cost the single-token kernels 3 %.
-template <int BITS, int MODE, bool ONE, bool GATED>
+// DUAL: rows of at most 8 blocks (1024 bytes): a tile is 32 rows (SWIGLU:
+// 16 gate rows and the 16 up rows of the same features), held as two
+// 16-row halves of a stage (four boxes of 8 rows x 8 blocks); consumer
+// warps 0-7 take the group slots of half 0 and warps 8-15 those of half 1,
+// so a short row keeps twice as many warps busy and a stage carries twice
+// the rows.
+template <int BITS, int MODE, bool ONE, bool GATED, bool DUAL>
 __global__ void __launch_bounds__(kSvThreads, 1)
     gemv_stream_kernel(const __grid_constant__ CUtensorMap tm_codes, SvParams p) {
   using S = SvShape<BITS>;
+  // bytes between the two 8-row boxes of a 16-row half, and scale bytes per stage
+  constexpr int kHalfOff = DUAL ? 8 * 1024 : kSvHalfBytes;
+  constexpr int kScaleStage = (DUAL ? 2 : 1) * S::kScaleBytes;
+  constexpr int kRowsPerTile = DUAL ? 32 : 16;
   if constexpr (GATED) {
     if (k_gate_closed(p.gate.k, p.gate.lo, p.gate.hi, p.early != 0)) return;
   }
   extern __shared__ __align__(16) unsigned char sv_raw[];
   unsigned char* sm = sv_raw + ((1024u - (smem_u32(sv_raw) & 1023u)) & 1023u);
-  const SvLayout L = sv_layout(BITS, p.K, p.mts, p.stages, p.E);
+  const SvLayout L = sv_layout(BITS, p.K, p.mts, p.stages, p.E, DUAL);
   unsigned char* codes = sm + L.codes;
   unsigned char* scales = sm + L.scales;
   uint4* xs = reinterpret_cast<uint4*>(sm + L.x);      // [G][half][n][t] B fragments
@@ -411,16 +422,19 @@ __global__ void __launch_bounds__(kSvThreads, 1)
     const long long tr_start = SV_CLK();
     for (int u = u0; u < u1 && ok; ++u, cursor_next(cu)) {
       const int64_t ebase = (int64_t)act_e[cu.a] * p.n_rows;
-      int64_t r0, r1;
+      // first rows of the tile's 8-row boxes: half h takes boxes 2h, 2h + 1
+      int64_t rb[4];
       if (MODE == kSvSwiglu) {
-        r0 = ebase + (int64_t)cu.rt * 8;
-        r1 = r0 + p.n_out;
+        rb[0] = ebase + (int64_t)cu.rt * (kRowsPerTile / 2);
+        rb[1] = rb[0] + p.n_out;
+        rb[2] = rb[0] + 8;
+        rb[3] = rb[1] + 8;
       } else {
-        r0 = ebase + (int64_t)cu.rt * 16;
-        r1 = r0 + 8;
+        rb[0] = ebase + (int64_t)cu.rt * kRowsPerTile;
+        rb[1] = rb[0] + 8;
+        rb[2] = rb[0] + 16;
+        rb[3] = rb[0] + 24;
       }
-      const int64_t grow = srow < 8 ? r0 + srow : r1 + (srow - 8);
-      const uint16_t* srcrow = (arr ? p.wb : p.ws) + grow * ngroups;
       for (int ch = 0; ch < nck; ++ch) {
         const long long tr0 = SV_CLK();
         if (abort_flag || !sv_wait(&empty[ring.idx], ring.phase ^ 1u)) {
@@ -434,20 +448,31 @@ __global__ void __launch_bounds__(kSvThreads, 1)
           if (lane == 0) {
             // blocks past the row end are zero-filled and still counted
             mbar_arrive_expect_tx(&full[ring.idx], (uint32_t)kSvCodeBytes);
-            tma_load_3d_sv(cdst, &tm_codes, (int)r0, ch * kSvBoxes, &full[ring.idx]);
-            tma_load_3d_sv(cdst + kSvHalfBytes, &tm_codes, (int)r1, ch * kSvBoxes,
-                           &full[ring.idx]);
+            if (DUAL) {
+#pragma unroll
+              for (int b = 0; b < 4; ++b)
+                tma_load_3d_sv(cdst + b * 8192, &tm_codes, (int)rb[b], 0, &full[ring.idx]);
+            } else {
+              tma_load_3d_sv(cdst, &tm_codes, (int)rb[0], ch * kSvBoxes, &full[ring.idx]);
+              tma_load_3d_sv(cdst + kSvHalfBytes, &tm_codes, (int)rb[1], ch * kSvBoxes,
+                             &full[ring.idx]);
+            }
           }
           __syncwarp();
         } else {
           const int g0 = ch * S::kGpc;
           const int gbytes = 2 * min(S::kGpc, ngroups - g0);
-          if (grow < tot_rows) {
-            unsigned char* sdst =
-                scales + (size_t)ring.idx * S::kScaleBytes + (arr * 16 + srow) * S::kScaleRow;
-            const unsigned char* src = reinterpret_cast<const unsigned char*>(srcrow + g0);
-            for (int o = 0; o < gbytes; o += p.scale_cw)
-              cp_async_sv(sdst + o, src + o, p.scale_cw);
+#pragma unroll
+          for (int h = 0; h < (DUAL ? 2 : 1); ++h) {
+            const int64_t grow = srow < 8 ? rb[2 * h] + srow : rb[2 * h + 1] + (srow - 8);
+            if (grow < tot_rows) {
+              const uint16_t* srcrow = (arr ? p.wb : p.ws) + grow * ngroups;
+              unsigned char* sdst = scales + (size_t)ring.idx * kScaleStage + h * S::kScaleBytes +
+                                    (arr * 16 + srow) * S::kScaleRow;
+              const unsigned char* src = reinterpret_cast<const unsigned char*>(srcrow + g0);
+              for (int o = 0; o < gbytes; o += p.scale_cw)
+                cp_async_sv(sdst + o, src + o, p.scale_cw);
+            }
           }
           cp_async_arrive_sv(&full[ring.idx]);
         }
@@ -629,6 +654,9 @@ __global__ void __launch_bounds__(kSvThreads, 1)
     static_assert(S::kGpw * S::kGroupBytes == 128, "a slot's groups span one 128-byte block");
     const int last_groups = ngroups - (nck - 1) * S::kGpc;
     const int rot_step = (last_groups + S::kGpw - 1) / S::kGpw;  // busy slots of the last stage
+    // DUAL: warps 0-7 hold the slots of half 0, warps 8-15 those of half 1,
+    // rotating within their eight
+    const int half = DUAL ? warp >> 3 : 0;
     // B column g of a lane: token g, or a copy of a staged token for the
     // columns past the chunk (their results are never read)
     const int bn = ONE ? 0 : min(g, mts - 1);
@@ -658,7 +686,7 @@ __global__ void __launch_bounds__(kSvThreads, 1)
         st_c = cu.c;
       }
       tr_stage += SV_CLK() - trs;
-      const int wl = (warp + u * rot_step) & (kSvConsumers - 1);
+      const int wl = DUAL ? ((warp & 7) + u * rot_step) & 7 : (warp + u * rot_step) & (kSvConsumers - 1);
       const int jb = S::kGpw * wl;
       const int soff = rr * S::kScaleRow + jb * 2;
       // sums of s * P (P = 2^(e-24) sum q x) and of b * X, rows g and g + 8;
@@ -672,12 +700,14 @@ __global__ void __launch_bounds__(kSvThreads, 1)
         }
         const long long tr1 = SV_CLK();
         tr_full += tr1 - tr0;
-        const unsigned char* cst = codes + (size_t)ring.idx * kSvCodeBytes + wl * 1024;
+        const unsigned char* cst =
+            codes + (size_t)ring.idx * kSvCodeBytes + half * 16384 + wl * 1024;
         const int g0 = ch * S::kGpc;
         const int nv = min(S::kGpw, ngroups - g0 - jb);  // this warp's groups in the stage
         if (nv > 0) {
           // scales and biases of rows g and g + 8 of the warp's groups, one load each
-          const unsigned char* sp = scales + (size_t)ring.idx * S::kScaleBytes + soff;
+          const unsigned char* sp =
+              scales + (size_t)ring.idx * kScaleStage + half * S::kScaleBytes + soff;
           typename S::ScaleVec sv[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q)
@@ -690,14 +720,14 @@ __global__ void __launch_bounds__(kSvThreads, 1)
             uint32_t a0[S::kLaneWords], a1[S::kLaneWords];
             if constexpr (BITS == 4) {
               const uint2 v0 = *reinterpret_cast<const uint2*>(cst + coff[i]);
-              const uint2 v1 = *reinterpret_cast<const uint2*>(cst + kSvHalfBytes + coff[i]);
+              const uint2 v1 = *reinterpret_cast<const uint2*>(cst + kHalfOff + coff[i]);
               a0[0] = v0.x;
               a0[1] = v0.y;
               a1[0] = v1.x;
               a1[1] = v1.y;
             } else {
               const uint4 v0 = *reinterpret_cast<const uint4*>(cst + coff[i]);
-              const uint4 v1 = *reinterpret_cast<const uint4*>(cst + kSvHalfBytes + coff[i]);
+              const uint4 v1 = *reinterpret_cast<const uint4*>(cst + kHalfOff + coff[i]);
               a0[0] = v0.x;
               a0[1] = v0.y;
               a0[2] = v0.z;
@@ -787,7 +817,7 @@ __global__ void __launch_bounds__(kSvThreads, 1)
         break;
       }
       tr_red += SV_CLK() - tr2;
-      float* rd = red + ((size_t)rs.idx * kSvConsumers + wl) * mts * 16;
+      float* rd = red + ((size_t)rs.idx * kSvConsumers + half * 8 + wl) * mts * 16;
       const int n0 = 2 * t, n1 = 2 * t + 1;
       if (n0 < mts) {
         rd[n0 * 16 + rr] = as[0] + ab[0];
@@ -838,8 +868,87 @@ __global__ void __launch_bounds__(kSvThreads, 1)
       const int64_t row0 = (int64_t)act_lo[cu.a] + (int64_t)cu.c * mts;
       const float* rd = red + (size_t)rs.idx * kSvConsumers * mts * 16;
       // A row's value is (slot partials 0..7, added in order) + (slots
-      // 8..15, in order), whatever rows and tokens share its tile.
-      if (ONE) {
+      // 8..15, in order), whatever rows and tokens share its tile.  DUAL:
+      // half h's rows take slots 8h .. 8h + 7 in order (its rows are at most
+      // 8 blocks, so the other slots of a 16-slot tile would hold zeros).
+      if constexpr (DUAL) {
+        if (ONE) {
+          // lane l: half l >> 4, its row l & 15
+          const int ri = lane & 15, hh = lane >> 4;
+          float v = 0.0f;
+#pragma unroll
+          for (int w = 0; w < 8; ++w) v += rd[(hh * 8 + w) * 16 + ri];
+          if (MODE == kSvSwiglu) {
+            const float up = __shfl_sync(0xFFFFFFFFu, v, (lane & 16) | 8 | (lane & 7));
+            const int col = cu.rt * 16 + hh * 8 + ri;
+            if (ri < 8 && col < p.n_out) {
+              const float hv = swiglu_f32(v, up);
+              const int64_t oi = row0 * p.n_out + col;
+              if (p.out_dtype == MOE_DTYPE_BF16)
+                static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16_rne(hv);
+              else
+                static_cast<float*>(p.out)[oi] = hv;
+            }
+          } else {
+            const int col = cu.rt * 32 + hh * 16 + ri;
+            if (col < p.n_rows) {
+              const int64_t oi = row0 * p.n_out + col;
+              if (p.out_dtype == MOE_DTYPE_BF16)
+                static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16_rne(v);
+              else
+                static_cast<float*>(p.out)[oi] = v;
+            }
+          }
+        } else {
+          // lane l: token l / 4, rows 4 (l & 3) .. + 3 of each half
+          const int n = lane >> 2, q = lane & 3;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (n < nt) {
+              const float4* r4 = reinterpret_cast<const float4*>(rd) + n * 4 + q;
+#pragma unroll
+              for (int w = 0; w < 8; ++w) {
+                const float4 pl = r4[(size_t)(hh * 8 + w) * mts * 4];
+                v.x += pl.x;
+                v.y += pl.y;
+                v.z += pl.z;
+                v.w += pl.w;
+              }
+            }
+            if (MODE == kSvSwiglu) {
+              float4 up;
+              up.x = __shfl_xor_sync(0xFFFFFFFFu, v.x, 2);
+              up.y = __shfl_xor_sync(0xFFFFFFFFu, v.y, 2);
+              up.z = __shfl_xor_sync(0xFFFFFFFFu, v.z, 2);
+              up.w = __shfl_xor_sync(0xFFFFFFFFu, v.w, 2);
+              const int col0 = cu.rt * 16 + hh * 8 + q * 4;
+              if (n < nt && q < 2 && col0 < p.n_out) {
+                const float4 hv = make_float4(swiglu_f32(v.x, up.x), swiglu_f32(v.y, up.y),
+                                              swiglu_f32(v.z, up.z), swiglu_f32(v.w, up.w));
+                const int64_t oi = (row0 + n) * p.n_out + col0;
+                if (p.out_dtype == MOE_DTYPE_BF16)
+                  *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + oi) = make_uint2(
+                      (uint32_t)f32_to_bf16_rne(hv.x) | ((uint32_t)f32_to_bf16_rne(hv.y) << 16),
+                      (uint32_t)f32_to_bf16_rne(hv.z) | ((uint32_t)f32_to_bf16_rne(hv.w) << 16));
+                else
+                  *reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi) = hv;
+              }
+            } else {
+              const int col0 = cu.rt * 32 + hh * 16 + q * 4;
+              if (n < nt && col0 < p.n_rows) {
+                const int64_t oi = (row0 + n) * p.n_out + col0;
+                if (p.out_dtype == MOE_DTYPE_BF16)
+                  *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + oi) = make_uint2(
+                      (uint32_t)f32_to_bf16_rne(v.x) | ((uint32_t)f32_to_bf16_rne(v.y) << 16),
+                      (uint32_t)f32_to_bf16_rne(v.z) | ((uint32_t)f32_to_bf16_rne(v.w) << 16));
+                else
+                  *reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi) = v;
+              }
+            }
+          }
+        }
+      } else if (ONE) {
         // lane l: tile row l & 15, slots 8 (l >> 4) .. + 7
         const int ri = lane & 15, wh = (lane >> 4) * 8;
         float v = 0.0f;
@@ -943,10 +1052,10 @@ __global__ void __launch_bounds__(kSvThreads, 1)
   }
 }
 
-template <int BITS, int MODE, bool ONE, bool GATED>
+template <int BITS, int MODE, bool ONE, bool GATED, bool DUAL>
 moe_status_t launch_stream_kernel(const CUtensorMap& tm, const SvParams& p, int smem,
                                   cudaStream_t st) {
-  auto kern = gemv_stream_kernel<BITS, MODE, ONE, GATED>;
+  auto kern = gemv_stream_kernel<BITS, MODE, ONE, GATED, DUAL>;
   static int set_max[moe_host::kMaxCachedDevices] = {};  // per device
   const int dev = moe_host::device_index();
   if (smem > set_max[dev]) {
@@ -959,14 +1068,15 @@ moe_status_t launch_stream_kernel(const CUtensorMap& tm, const SvParams& p, int 
 }
 
 template <int BITS, int MODE>
-moe_status_t launch_stream(const CUtensorMap& tm, SvParams p, cudaStream_t st) {
+moe_status_t launch_stream(const CUtensorMap& tm, SvParams p, bool dual, cudaStream_t st) {
   static int optin = -1, static_smem = 0;
   if (optin < 0) {
     int dev = 0, v = 0;
     cudaFuncAttributes fa;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-        cudaFuncGetAttributes(&fa, gemv_stream_kernel<BITS, MODE, false, false>) != cudaSuccess)
+        cudaFuncGetAttributes(&fa, gemv_stream_kernel<BITS, MODE, false, false, false>) !=
+            cudaSuccess)
       return MOE_ERR_CUDA;
     static_smem = (int)fa.sharedSizeBytes;
     optin = v;
@@ -978,16 +1088,21 @@ moe_status_t launch_stream(const CUtensorMap& tm, SvParams p, cudaStream_t st) {
   int stages = 0;
   for (;;) {
     stages = kSvMaxStages;
-    while (stages >= 2 && (long)sv_layout(BITS, p.K, p.mts, stages, p.E).total > budget) --stages;
+    while (stages >= 2 && (long)sv_layout(BITS, p.K, p.mts, stages, p.E, dual).total > budget)
+      --stages;
     if (stages >= 3 || p.mts == 1) break;
     p.mts >>= 1;
   }
   if (stages < 2) return MOE_ERR_UNSUPPORTED;
   p.stages = stages;
-  const int smem = (int)sv_layout(BITS, p.K, p.mts, stages, p.E).total + 1024;
-  if (p.gate.k != nullptr) return launch_stream_kernel<BITS, MODE, false, true>(tm, p, smem, st);
-  return p.mts == 1 ? launch_stream_kernel<BITS, MODE, true, false>(tm, p, smem, st)
-                    : launch_stream_kernel<BITS, MODE, false, false>(tm, p, smem, st);
+  const int smem = (int)sv_layout(BITS, p.K, p.mts, stages, p.E, dual).total + 1024;
+  if (p.gate.k != nullptr)
+    return launch_stream_kernel<BITS, MODE, false, true, false>(tm, p, smem, st);
+  if (dual)
+    return p.mts == 1 ? launch_stream_kernel<BITS, MODE, true, false, true>(tm, p, smem, st)
+                      : launch_stream_kernel<BITS, MODE, false, false, true>(tm, p, smem, st);
+  return p.mts == 1 ? launch_stream_kernel<BITS, MODE, true, false, false>(tm, p, smem, st)
+                    : launch_stream_kernel<BITS, MODE, false, false, false>(tm, p, smem, st);
 }
 
 }  // namespace
@@ -1023,7 +1138,11 @@ moe_status_t gemv_stream_qmm(const void* act, int act_kind, const int32_t* sorte
   p.K = K;
   p.n_rows = n_rows;
   p.n_out = swiglu ? n_rows / 2 : n_rows;
-  p.rt = swiglu ? (p.n_out + 7) / 8 : (n_rows + 15) / 16;
+  // rows of at most 8 blocks (ungated launches): 32-row tiles of two halves
+  const uint64_t row_words = (uint64_t)K * bits / 32;
+  const bool dual = row_words <= 8 * 32 && gate.k == nullptr;
+  p.rt = swiglu ? (p.n_out + (dual ? 15 : 7)) / (dual ? 16 : 8)
+                : (n_rows + (dual ? 31 : 15)) / (dual ? 32 : 16);
   // an expert's segment holds at most one row per token
   int mts = 1;
   while (mts < kSvMaxTokens && mts < T) mts <<= 1;
@@ -1041,18 +1160,20 @@ moe_status_t gemv_stream_qmm(const void* act, int act_kind, const int32_t* sorte
   // tile count bound (int32 positions)
   const int64_t max_tiles = (int64_t)p.rt * (A + E);
   if (max_tiles >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
-  // codes as [128-byte block][row][32 words]: boxes of 8 rows x 8 blocks
-  const uint64_t row_words = (uint64_t)K * bits / 32;
+  // codes as [128-byte block][row][32 words]: boxes of 8 rows x 16 blocks
+  // (a row's share of a stage), or 8 rows x 8 blocks for the DUAL tiles
   const uint64_t dims[3] = {32, (uint64_t)E * n_rows, row_words / 32};
   const uint64_t strides[2] = {row_words * 4, 128};
-  const uint32_t box[3] = {32, 8, (uint32_t)kSvBoxes};
+  const uint32_t box[3] = {32, 8, (uint32_t)(dual ? 8 : kSvBoxes)};
   CUtensorMap tm;
   if (!make_tensor_map_3d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, wq, dims, strides, box,
                           CU_TENSOR_MAP_SWIZZLE_128B))
     return MOE_ERR_CUDA;
   if (bits == 4)
-    return swiglu ? launch_stream<4, kSvSwiglu>(tm, p, st) : launch_stream<4, kSvRaw>(tm, p, st);
-  return swiglu ? launch_stream<8, kSvSwiglu>(tm, p, st) : launch_stream<8, kSvRaw>(tm, p, st);
+    return swiglu ? launch_stream<4, kSvSwiglu>(tm, p, dual, st)
+                  : launch_stream<4, kSvRaw>(tm, p, dual, st);
+  return swiglu ? launch_stream<8, kSvSwiglu>(tm, p, dual, st)
+                : launch_stream<8, kSvRaw>(tm, p, dual, st);
 }
 
 }  // namespace moe

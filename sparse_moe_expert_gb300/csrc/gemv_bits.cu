@@ -11,22 +11,28 @@
 // whole words (10 for 5 bits, 12 for 6), so groups start on word
 // boundaries and a row's scales and biases index groups as for 4 and 8 bits.
 //
+// Arithmetic.  Per group of 64 elements of a row (scale s, bias b):
+//   sum_i x_i (s q_i + b) = s * sum_i q_i x_i + b * X,   X = sum_i x_i.
+// sum q x runs on the tensor cores (mma.sync.m16n8k16, fp16 x fp16 -> fp32):
+// two codes OR-ed into the two halves of a 32-bit word are the fp16
+// subnormals (q0, q1) * 2^-24, exact, and the token values are staged as
+// fp16 x * 2^e with one power of two per token and group chosen so that the
+// group's max |x| 2^e lies in [2^14, 2^15) (exact for bf16 values in range).
+// One MMA step takes, in lane (g, t), codes 16t + 4s .. 16t + 4s + 3 of the
+// group (s = 0..3) for A and the same elements of token g for B, so each
+// lane reads one contiguous run of 16 codes (16b bits of the group's words,
+// brought to bit 0 by funnel shifts) and 16 contiguous token values.  The
+// four steps give P = 2^(e-24) sum q x for 16 rows x 8 tokens; CUDA cores
+// add s 2^(24-e) P and b X per group.
+//
 // Work.  An item is (active expert, chunk of up to MT of its tokens, block
-// of 12 weight features); the persistent CTAs take equal contiguous ranges
-// of the item list, so a CTA walks the feature blocks of one chunk after the
-// other.  The chunk's token values are staged once in shared memory as fp32
-// ([token][K]; bf16 rounding for fp32 rows, as the other GEMV paths apply)
-// and stay there while the CTA's items keep to that chunk.  While a CTA
-// computes an item it asks L2 for the code, scale and bias lines of its next
-// item, so the weight loads of that item find their lines in L2.
-// Warp w of an item computes feature f = 12 block + w: for SwiGLU its gate
-// row f and up row n_out + f, else row f.  Lane l takes codes 2l and 2l + 1
-// of every group (one funnel shift over the group's words brings both),
-// dequantizes them in fp32 (s q + b, s and b exact from fp16) and
-// accumulates them against each token's two values; the 32 lane partials are
-// added by a fixed xor butterfly.  A row's value depends only on its own
-// codes, scales, biases and the tokens, so the fused gate_up product equals
-// the separate gate and up products bit for bit.
+// of 16 row tiles); each of the 16 warps takes one tile of 16 rows (SwiGLU:
+// 8 gate rows and the 8 up rows of the same features) over the whole row,
+// so a row's value is reduced in one fixed order whatever rows share its
+// tile, and the fused gate_up product equals the separate gate and up
+// products bit for bit.  The chunk's token fragments are staged once in
+// shared memory and stay while the CTA's items keep to that chunk; while a
+// CTA computes an item it asks L2 for the lines of its next item.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -34,9 +40,9 @@
 namespace moe {
 namespace {
 
-constexpr int kBtThreads = 384;
-constexpr int kBtWarps = kBtThreads / 32;  // features per item
-constexpr int kBtMaxTokens = 8;            // tokens per chunk (at most)
+constexpr int kBtThreads = 512;
+constexpr int kBtWarps = kBtThreads / 32;  // row tiles per item
+constexpr int kBtMaxTokens = 8;            // tokens per chunk (the MMA's n)
 constexpr int kBtMaxE = 1024;
 constexpr size_t kBtMaxStage = 200 * 1024;  // staged token bytes (at most)
 
@@ -51,7 +57,7 @@ struct BtParams {
   int T, kmax, E, K;
   int n_rows;  // weight rows per expert
   int n_out;   // output columns: n_rows / 2 (SWIGLU) or n_rows
-  int blocks;  // feature blocks of kBtWarps per (expert, chunk)
+  int blocks;  // item blocks of kBtWarps row tiles per (expert, chunk)
   int mt;      // tokens per chunk
   const uint32_t* wq;
   const uint16_t* ws;
@@ -61,29 +67,63 @@ struct BtParams {
   unsigned int* err;
 };
 
-// Activation value k of row `row` as fp32 (bf16 rounding for fp32 rows, as
-// the other GEMV paths apply).
-__device__ __forceinline__ float bt_act(const BtParams& p, int64_t row, int64_t k) {
-  if (p.act_kind == kBtActF32)
-    return bf16_bits_to_f32(f32_to_bf16_rne(__ldg(static_cast<const float*>(p.act) + row * p.K + k)));
-  return bf16_bits_to_f32(__ldg(static_cast<const uint16_t*>(p.act) + row * p.K + k));
+// Staged tokens: fp16 values [mt][K + 8] (16 bytes of padding per token row
+// keep the fragment loads free of bank conflicts), then (X, 2^(24-e)) per
+// group and token [K / 64][mt2].
+__host__ __device__ inline int bt_xs_stride(int K) { return K + 8; }
+__host__ __device__ inline size_t bt_stage_bytes(int K, int mt) {
+  const int mt2 = mt < 2 ? 2 : mt;
+  return (size_t)mt * bt_xs_stride(K) * 2 + (size_t)(K / 64) * mt2 * 8;
 }
 
 __device__ __forceinline__ void prefetch_l2(const void* ptr) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }
 
+// d = A B (+ d when acc)
+__device__ __forceinline__ void mma_bt(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                       uint32_t a3, uint32_t b0, uint32_t b1, bool acc) {
+  if (acc)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// Codes 2j and 2j + 1 of a lane's run (its bits from bit 0 of n[0..2]) as
+// the fp16 subnormal pair (q_2j, q_2j+1) 2^-24.
+template <int BITS>
+__device__ __forceinline__ uint32_t bt_pair(const uint32_t (&n)[3], int j) {
+  constexpr uint32_t kMask = (1u << BITS) - 1u;
+  const int pos = 2 * j * BITS;  // compile-time after unrolling
+  const int wi = pos >> 5, sh = pos & 31;
+  const uint32_t lo = n[wi], hi = wi + 1 < 3 ? n[wi + 1] : 0u;
+  const uint32_t v = __funnelshift_r(lo, hi, sh);
+  return (v & kMask) | (((v >> BITS) & kMask) << 16);
+}
+
 template <int BITS, int MODE, int MT>
 __global__ void __launch_bounds__(kBtThreads, 1) gemv_bits_kernel(BtParams p) {
   constexpr int kGroupWords = 2 * BITS;  // 64 codes of a group
-  constexpr uint32_t kMask = (1u << BITS) - 1u;
-  constexpr int kRows = MODE == kBtSwiglu ? 2 : 1;
-  extern __shared__ float bt_x[];  // staged tokens [mt][K]
+  constexpr int mt = MT;
+  constexpr int mt2 = MT < 2 ? 2 : MT;
+  constexpr int kTileRows = 16;  // SWIGLU: 8 features (gate rows, then up rows)
+  extern __shared__ __align__(16) unsigned char bt_smem[];
   __shared__ int act_e[kBtMaxE + 1], act_lo[kBtMaxE + 1], act_m[kBtMaxE + 1], act_base[kBtMaxE + 1];
   __shared__ int n_act_sh;
   __shared__ int wtot[kBtWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int mt = MT;  // tokens per chunk (p.mt)
+  const int ngroups = p.K / 64;
+  const int xs_stride = bt_xs_stride(p.K);
+  uint16_t* xh = reinterpret_cast<uint16_t*>(bt_smem);  // [mt][xs_stride] fp16
+  float2* xsum = reinterpret_cast<float2*>(bt_smem + (size_t)mt * xs_stride * 2);  // [G][mt2]
   pdl_wait();
   pdl_trigger();
 
@@ -118,7 +158,7 @@ __global__ void __launch_bounds__(kBtThreads, 1) gemv_bits_kernel(BtParams p) {
     __syncthreads();
   }
   const int n_act = n_act_sh;
-  // items before each active expert: chunks of mt tokens x feature blocks
+  // items before each active expert: chunks of mt tokens x item blocks
   if (warp == 0) {
     int carry = 0;
     for (int a0 = 0; a0 < n_act; a0 += 32) {
@@ -138,11 +178,10 @@ __global__ void __launch_bounds__(kBtThreads, 1) gemv_bits_kernel(BtParams p) {
   const int64_t n_items = act_base[n_act];
   const int64_t it0 = n_items * blockIdx.x / gridDim.x;
   const int64_t it1 = n_items * (blockIdx.x + 1) / gridDim.x;
-  const int ngroups = p.K / 64;
   const int64_t row_words = (int64_t)p.K * BITS / 32;
-  // this lane's codes 2 lane, 2 lane + 1 of a group: bits [2 lane b, 2 lane b + 2b)
-  const int bit0 = 2 * lane * BITS;
-  const int w0 = bit0 >> 5, sh = bit0 & 31;
+  const int g = lane >> 2, t = lane & 3;
+  // this lane's run of 16 codes of a group: bits [16 t b, 16 t b + 16 b)
+  const int run_w0 = (16 * t * BITS) >> 5, run_sh = (16 * t * BITS) & 31;
 
   struct Item {
     int a, c, blk;
@@ -164,15 +203,16 @@ __global__ void __launch_bounds__(kBtThreads, 1) gemv_bits_kernel(BtParams p) {
   // L2 lines of an item's code rows, scales and biases (every thread a share)
   auto prefetch_item = [&](const Item& q) {
     const int64_t ebase = (int64_t)act_e[q.a] * p.n_rows;
-    const int f0 = q.blk * kBtWarps;
-    const int nf = min(kBtWarps, p.n_out - f0);
-    for (int r = 0; r < kRows; ++r) {
-      const int64_t row0 = ebase + (r == 0 ? f0 : p.n_out + f0);
+    const int span = MODE == kBtSwiglu ? kBtWarps * 8 : kBtWarps * kTileRows;
+    const int lim = MODE == kBtSwiglu ? p.n_out : p.n_rows;
+    const int nr = min(span, lim - q.blk * span);
+    for (int part = 0; part < (MODE == kBtSwiglu ? 2 : 1); ++part) {
+      const int64_t row0 = ebase + (part ? p.n_out : 0) + (int64_t)q.blk * span;
       const char* cb = reinterpret_cast<const char*>(p.wq + row0 * row_words);
-      const int64_t cbytes = (int64_t)nf * row_words * 4;
+      const int64_t cbytes = (int64_t)nr * row_words * 4;
       for (int64_t o = (int64_t)tid * 128; o < cbytes; o += (int64_t)kBtThreads * 128)
         prefetch_l2(cb + o);
-      const int64_t sbytes = (int64_t)nf * ngroups * 2;
+      const int64_t sbytes = (int64_t)nr * ngroups * 2;
       const char* sb = reinterpret_cast<const char*>(p.ws + row0 * ngroups);
       const char* bb = reinterpret_cast<const char*>(p.wb + row0 * ngroups);
       for (int64_t o = (int64_t)tid * 128; o < sbytes; o += (int64_t)kBtThreads * 128) {
@@ -188,118 +228,171 @@ __global__ void __launch_bounds__(kBtThreads, 1) gemv_bits_kernel(BtParams p) {
     const int lo_tok = act_lo[cur.a] + cur.c * mt;  // first sorted row of the chunk
     const int nt = min(mt, act_m[cur.a] - cur.c * mt);
     if (cur.a != st_a || cur.c != st_c) {
-      // stage the chunk's token values (every warp is past the previous item)
+      // stage the chunk's tokens (every warp is past the previous item): per
+      // (token, group) one thread loads the 64 values, finds the power of
+      // two, the sum (in element order) and the scaled fp16 values
       __syncthreads();
-#pragma unroll 1
-      for (int n = 0; n < MT; ++n) {
-        float* dst = bt_x + (size_t)n * p.K;
+      for (int i = tid; i < mt2 * ngroups; i += kBtThreads) {
+        const int n = i / ngroups, G = i - n * ngroups;
+        uint32_t v[32];  // 64 bf16 values, two per word
+#pragma unroll
+        for (int w = 0; w < 32; ++w) v[w] = 0u;
         if (n < nt) {
           const int r = lo_tok + n;
           const int64_t row =
               p.act_kind == kBtActX ? (int64_t)(__ldg(p.sorted + r) / p.kmax) : (int64_t)r;
-          for (int k = tid; k < p.K; k += kBtThreads) dst[k] = bt_act(p, row, k);
-        } else {
-          for (int k = tid; k < p.K; k += kBtThreads) dst[k] = 0.0f;
+          if (p.act_kind == kBtActF32) {
+            const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.act) +
+                                                                row * p.K + (int64_t)G * 64);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              const float4 f = __ldg(src + q);
+              v[2 * q] = (uint32_t)f32_to_bf16_rne(f.x) | ((uint32_t)f32_to_bf16_rne(f.y) << 16);
+              v[2 * q + 1] = (uint32_t)f32_to_bf16_rne(f.z) | ((uint32_t)f32_to_bf16_rne(f.w) << 16);
+            }
+          } else {
+            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.act) +
+                                                              row * p.K + (int64_t)G * 64);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const uint4 u = __ldg(src + q);
+              v[4 * q] = u.x;
+              v[4 * q + 1] = u.y;
+              v[4 * q + 2] = u.z;
+              v[4 * q + 3] = u.w;
+            }
+          }
         }
+        float mx = 0.0f, xsm = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 32; ++w) {
+          const float f0 = __uint_as_float(v[w] << 16), f1 = __uint_as_float(v[w] & 0xFFFF0000u);
+          mx = fmaxf(mx, fmaxf(fabsf(f0), fabsf(f1)));
+          xsm += f0;
+          xsm += f1;
+        }
+        const int E8 = (int)((__float_as_uint(mx) >> 23) & 0xFFu);
+        int e = mx == 0.0f ? 0 : (E8 == 0 ? 100 : 141 - E8);
+        e = e < -100 ? -100 : (e > 100 ? 100 : e);
+        const float sc = __uint_as_float((uint32_t)(127 + e) << 23);
+        if (n < mt) {
+          uint4* dst = reinterpret_cast<uint4*>(xh + (size_t)n * xs_stride + G * 64);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            uint32_t hw[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t w = v[4 * q + j];
+              const __half2 h2 = __floats2half2_rn(__uint_as_float(w << 16) * sc,
+                                                   __uint_as_float(w & 0xFFFF0000u) * sc);
+              hw[j] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            dst[q] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          }
+        }
+        xsum[(size_t)G * mt2 + n] = make_float2(xsm, __uint_as_float((uint32_t)(151 - e) << 23));
       }
       __syncthreads();
       st_a = cur.a;
       st_c = cur.c;
     }
     if (it + 1 < it1) prefetch_item(item_at(it + 1));
-    const int f = cur.blk * kBtWarps + warp;  // this warp's feature
-    if (f >= p.n_out) continue;
+    const int tile = cur.blk * kBtWarps + warp;
+    const int first = MODE == kBtSwiglu ? tile * 8 : tile * kTileRows;  // feature | row
+    const int limit = MODE == kBtSwiglu ? p.n_out : p.n_rows;
+    if (first >= limit) continue;  // past the matrix (warp-uniform)
     const int64_t ebase = (int64_t)act_e[cur.a] * p.n_rows;
-    int64_t wrow[kRows];
-    wrow[0] = ebase + f;
-    if (MODE == kBtSwiglu) wrow[kRows - 1] = ebase + p.n_out + f;
-    float acc[kRows][MT];
+    // MMA rows g and g + 8: gate and up rows of feature first + g (SWIGLU),
+    // else rows first + g and first + g + 8; rows past the matrix read a
+    // valid row and their results are dropped
+    const int64_t last = ebase + p.n_rows - 1;
+    const int64_t row_lo = min(ebase + first + g, last);
+    const int64_t row_hi =
+        min(MODE == kBtSwiglu ? ebase + p.n_out + first + g : ebase + first + g + 8, last);
+    const uint32_t* wlo = p.wq + row_lo * row_words + run_w0;
+    const uint32_t* whi = p.wq + row_hi * row_words + run_w0;
+    const uint16_t* slo = p.ws + row_lo * ngroups;
+    const uint16_t* shi = p.ws + row_hi * ngroups;
+    const uint16_t* blo = p.wb + row_lo * ngroups;
+    const uint16_t* bhi = p.wb + row_hi * ngroups;
+    // B columns past the chunk repeat one of its tokens (never read back)
+    const int bn = min(g, mt - 1);
+    const uint4* xq = reinterpret_cast<const uint4*>(xh + (size_t)bn * xs_stride + 16 * t);
+    const float2* xsp = xsum + (t < (mt2 >> 1) ? 2 * t : mt2 - 2);
+    float as[4] = {0.f, 0.f, 0.f, 0.f}, ab[4] = {0.f, 0.f, 0.f, 0.f};
+    // the words of group G for both rows, loaded one group ahead
+    uint32_t wl[3], wh[3], nl[3] = {0u, 0u, 0u}, nh[3] = {0u, 0u, 0u};
+    auto load_words = [&](int G, uint32_t (&a)[3], uint32_t (&b)[3]) {
+      const int64_t o = (int64_t)G * kGroupWords;
 #pragma unroll
-    for (int q = 0; q < kRows; ++q)
-#pragma unroll
-      for (int n = 0; n < MT; ++n) acc[q][n] = 0.0f;
-    // this lane's pair of staged values: token n, group g at xs[n K / 2 + 32 g]
-    const float2* xs = reinterpret_cast<const float2*>(bt_x) + lane;
-    const int kh = p.K >> 1;
-    // scales and biases of 32 groups per load (lane l holds group g32 + l);
-    // code words in batches of kGb groups, the next batch loaded while the
-    // current one is computed
-    constexpr int kGb = 4;
-    uint32_t sv[kRows] = {}, bv[kRows] = {};
-    uint32_t wlo[kGb][kRows], whi[kGb][kRows], nlo[kGb][kRows], nhi[kGb][kRows];
-    auto load_batch = [&](int g0, uint32_t (&lo)[kGb][kRows], uint32_t (&hi)[kGb][kRows]) {
-#pragma unroll
-      for (int j = 0; j < kGb; ++j)
-#pragma unroll
-        for (int q = 0; q < kRows; ++q) {
-          lo[j][q] = hi[j][q] = 0u;
-          if (g0 + j < ngroups) {
-            const uint32_t* gw = p.wq + wrow[q] * row_words + (int64_t)(g0 + j) * kGroupWords;
-            lo[j][q] = __ldg(gw + w0);
-            if (w0 + 1 < kGroupWords) hi[j][q] = __ldg(gw + w0 + 1);
-          }
-        }
+      for (int i = 0; i < 3; ++i) {
+        a[i] = __ldg(wlo + o + i);
+        b[i] = __ldg(whi + o + i);
+      }
     };
-    load_batch(0, wlo, whi);
-    for (int g0 = 0; g0 < ngroups; g0 += kGb) {
-      if ((g0 & 31) == 0) {
+    load_words(0, wl, wh);
+    for (int G = 0; G < ngroups; ++G) {
+      if (G + 1 < ngroups) load_words(G + 1, nl, nh);
+      const float s0 = f16_bits_to_f32(__ldg(slo + G)), s1 = f16_bits_to_f32(__ldg(shi + G));
+      const float b0 = f16_bits_to_f32(__ldg(blo + G)), b1 = f16_bits_to_f32(__ldg(bhi + G));
+      // this lane's run of 16 codes, from bit 0
+      uint32_t rl[3], rh[3];
+      rl[0] = __funnelshift_r(wl[0], wl[1], run_sh);
+      rl[1] = __funnelshift_r(wl[1], wl[2], run_sh);
+      rl[2] = wl[2] >> run_sh;
+      rh[0] = __funnelshift_r(wh[0], wh[1], run_sh);
+      rh[1] = __funnelshift_r(wh[1], wh[2], run_sh);
+      rh[2] = wh[2] >> run_sh;
+      const uint4 xa = xq[(size_t)G * 8], xb = xq[(size_t)G * 8 + 1];  // 16 fp16 values
+      const uint32_t xf[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+      float d[4];
 #pragma unroll
-        for (int q = 0; q < kRows; ++q) {
-          const int gl = g0 + lane;
-          sv[q] = gl < ngroups ? __ldg(p.ws + wrow[q] * ngroups + gl) : 0u;
-          bv[q] = gl < ngroups ? __ldg(p.wb + wrow[q] * ngroups + gl) : 0u;
-        }
+      for (int s = 0; s < 4; ++s)
+        mma_bt(d, bt_pair<BITS>(rl, 2 * s), bt_pair<BITS>(rh, 2 * s), bt_pair<BITS>(rl, 2 * s + 1),
+               bt_pair<BITS>(rh, 2 * s + 1), xf[2 * s], xf[2 * s + 1], s > 0);
+      const float4 X = *reinterpret_cast<const float4*>(xsp + (size_t)G * mt2);  // tokens 2t, 2t+1
+      as[0] = fmaf(s0 * X.y, d[0], as[0]);
+      as[1] = fmaf(s0 * X.w, d[1], as[1]);
+      as[2] = fmaf(s1 * X.y, d[2], as[2]);
+      as[3] = fmaf(s1 * X.w, d[3], as[3]);
+      ab[0] = fmaf(b0, X.x, ab[0]);
+      ab[1] = fmaf(b0, X.z, ab[1]);
+      ab[2] = fmaf(b1, X.x, ab[2]);
+      ab[3] = fmaf(b1, X.z, ab[3]);
+#pragma unroll
+      for (int i = 0; i < 3; ++i) {
+        wl[i] = nl[i];
+        wh[i] = nh[i];
       }
-      if (g0 + kGb < ngroups) load_batch(g0 + kGb, nlo, nhi);
-#pragma unroll
-      for (int j = 0; j < kGb; ++j) {
-        const int g = g0 + j;
-        if (g >= ngroups) break;
-        float2 xv[MT];
-        const float2* xg = xs + g * 32;
-#pragma unroll
-        for (int n = 0; n < MT; ++n) xv[n] = xg[n * kh];
-#pragma unroll
-        for (int q = 0; q < kRows; ++q) {
-          const uint32_t v = __funnelshift_r(wlo[j][q], whi[j][q], sh);
-          const float q0 = (float)(v & kMask), q1 = (float)((v >> BITS) & kMask);
-          const float s = f16_bits_to_f32((uint16_t)__shfl_sync(0xFFFFFFFFu, sv[q], g & 31));
-          const float b = f16_bits_to_f32((uint16_t)__shfl_sync(0xFFFFFFFFu, bv[q], g & 31));
-          const float d0 = fmaf(s, q0, b), d1 = fmaf(s, q1, b);
-#pragma unroll
-          for (int n = 0; n < MT; ++n) acc[q][n] = fmaf(d1, xv[n].y, fmaf(d0, xv[n].x, acc[q][n]));
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < kGb; ++j)
-#pragma unroll
-        for (int q = 0; q < kRows; ++q) {
-          wlo[j][q] = nlo[j][q];
-          whi[j][q] = nhi[j][q];
-        }
     }
-    // the 32 lane partials of every row and token, by a fixed xor butterfly
+    // lane (g, t): MMA rows g and g + 8, tokens 2t and 2t + 1
+    const float v0 = as[0] + ab[0], v1 = as[1] + ab[1], v2 = as[2] + ab[2], v3 = as[3] + ab[3];
+    const int n0 = 2 * t, n1 = 2 * t + 1;
+    if (MODE == kBtSwiglu) {
+      const int f = first + g;
+      if (f < p.n_out) {
+        const float h0 = swiglu_f32(v0, v2), h1 = swiglu_f32(v1, v3);
+        if (n0 < nt) {
+          const int64_t oi = (int64_t)(lo_tok + n0) * p.n_out + f;
+          if (p.out_dtype == MOE_DTYPE_BF16) static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16_rne(h0);
+          else static_cast<float*>(p.out)[oi] = h0;
+        }
+        if (n1 < nt) {
+          const int64_t oi = (int64_t)(lo_tok + n1) * p.n_out + f;
+          if (p.out_dtype == MOE_DTYPE_BF16) static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16_rne(h1);
+          else static_cast<float*>(p.out)[oi] = h1;
+        }
+      }
+    } else {
+      const float vv[4] = {v0, v1, v2, v3};
 #pragma unroll
-    for (int q = 0; q < kRows; ++q)
-#pragma unroll
-      for (int n = 0; n < MT; ++n)
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1)
-          acc[q][n] = __fadd_rn(acc[q][n], __shfl_xor_sync(0xFFFFFFFFu, acc[q][n], off));
-#pragma unroll
-    for (int n = 0; n < MT; ++n) {
-      if (lane != n || n >= nt) continue;
-      const int64_t orow = (int64_t)lo_tok + n;
-      if (MODE == kBtSwiglu) {
-        const float hv = swiglu_f32(acc[0][n], acc[kRows - 1][n]);
-        if (p.out_dtype == MOE_DTYPE_BF16)
-          static_cast<uint16_t*>(p.out)[orow * p.n_out + f] = f32_to_bf16_rne(hv);
-        else
-          static_cast<float*>(p.out)[orow * p.n_out + f] = hv;
-      } else if (p.out_dtype == MOE_DTYPE_BF16) {
-        static_cast<uint16_t*>(p.out)[orow * p.n_out + f] = f32_to_bf16_rne(acc[0][n]);
-      } else {
-        static_cast<float*>(p.out)[orow * p.n_out + f] = acc[0][n];
+      for (int i = 0; i < 4; ++i) {
+        const int r = first + g + (i >> 1) * 8, n = 2 * t + (i & 1);
+        if (r < p.n_rows && n < nt) {
+          const int64_t oi = (int64_t)(lo_tok + n) * p.n_out + r;
+          if (p.out_dtype == MOE_DTYPE_BF16) static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16_rne(vv[i]);
+          else static_cast<float*>(p.out)[oi] = vv[i];
+        }
       }
     }
   }
@@ -308,7 +401,7 @@ __global__ void __launch_bounds__(kBtThreads, 1) gemv_bits_kernel(BtParams p) {
 template <int BITS, int MODE, int MT>
 moe_status_t launch_bits_mt(const BtParams& p, cudaStream_t st) {
   auto kern = gemv_bits_kernel<BITS, MODE, MT>;
-  const size_t smem = (size_t)p.mt * p.K * sizeof(float);
+  const size_t smem = bt_stage_bytes(p.K, MT);
   // the static arrays count against the same limit: raise it for any size
   static size_t set_max[moe_host::kMaxCachedDevices] = {};  // per device
   const int dev = moe_host::device_index();
@@ -354,13 +447,14 @@ moe_status_t gemv_bits_qmm(const void* act, int act_kind, const int32_t* sorted,
   p.K = K;
   p.n_rows = n_rows;
   p.n_out = swiglu ? n_rows / 2 : n_rows;
-  p.blocks = (p.n_out + kBtWarps - 1) / kBtWarps;
+  // item blocks: 16 row tiles of 16 rows (SWIGLU: 8 features each)
+  p.blocks = swiglu ? (p.n_out + kBtWarps * 8 - 1) / (kBtWarps * 8)
+                    : (n_rows + kBtWarps * 16 - 1) / (kBtWarps * 16);
   // tokens per chunk: an expert holds at most T rows, and the staged values
   // must fit in shared memory
   int mt = 1;
-  while (mt < kBtMaxTokens && mt < T && (size_t)(2 * mt) * K * sizeof(float) <= kBtMaxStage)
-    mt <<= 1;
-  if ((size_t)mt * K * sizeof(float) > kBtMaxStage) return MOE_ERR_UNSUPPORTED;
+  while (mt < kBtMaxTokens && mt < T && bt_stage_bytes(K, 2 * mt) <= kBtMaxStage) mt <<= 1;
+  if (bt_stage_bytes(K, mt) > kBtMaxStage) return MOE_ERR_UNSUPPORTED;
   p.mt = mt;
   p.wq = wq;
   p.ws = ws;

@@ -26,13 +26,14 @@
 // add s 2^(24-e) P and b X per group.
 //
 // Work.  An item is (active expert, chunk of up to MT of its tokens, block
-// of 16 row tiles); each of the 16 warps takes one tile of 16 rows (SwiGLU:
+// of 12 row tiles); each of the 12 warps takes one tile of 16 rows (SwiGLU:
 // 8 gate rows and the 8 up rows of the same features) over the whole row,
 // so a row's value is reduced in one fixed order whatever rows share its
 // tile, and the fused gate_up product equals the separate gate and up
 // products bit for bit.  The chunk's token fragments are staged once in
-// shared memory and stay while the CTA's items keep to that chunk; while a
-// CTA computes an item it asks L2 for the lines of its next item.
+// shared memory and stay while the CTA's items keep to that chunk.  A warp
+// keeps the code words, scales and biases of the next three groups of its
+// rows in flight in registers.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -40,7 +41,7 @@
 namespace moe {
 namespace {
 
-constexpr int kBtThreads = 512;
+constexpr int kBtThreads = 384;
 constexpr int kBtWarps = kBtThreads / 32;  // row tiles per item
 constexpr int kBtMaxTokens = 8;            // tokens per chunk (the MMA's n)
 constexpr int kBtMaxE = 1024;
@@ -76,10 +77,6 @@ __host__ __device__ inline size_t bt_stage_bytes(int K, int mt) {
   return (size_t)mt * bt_xs_stride(K) * 2 + (size_t)(K / 64) * mt2 * 8;
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* ptr) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
-}
-
 // d = A B (+ d when acc)
 __device__ __forceinline__ void mma_bt(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                        uint32_t a3, uint32_t b0, uint32_t b1, bool acc) {
@@ -105,8 +102,9 @@ __device__ __forceinline__ uint32_t bt_pair(const uint32_t (&n)[3], int j) {
   const int pos = 2 * j * BITS;  // compile-time after unrolling
   const int wi = pos >> 5, sh = pos & 31;
   const uint32_t lo = n[wi], hi = wi + 1 < 3 ? n[wi + 1] : 0u;
-  const uint32_t v = __funnelshift_r(lo, hi, sh);
-  return (v & kMask) | (((v >> BITS) & kMask) << 16);
+  const uint32_t v = sh == 0 ? lo : __funnelshift_r(lo, hi, sh);
+  // q0 from bits 0.., q1 moved from bit BITS to bit 16
+  return (v & kMask) | ((v << (16 - BITS)) & (kMask << 16));
 }
 
 template <int BITS, int MODE, int MT>
@@ -200,28 +198,6 @@ __global__ void __launch_bounds__(kBtThreads, 1) gemv_bits_kernel(BtParams p) {
     r.blk = local - r.c * p.blocks;
     return r;
   };
-  // L2 lines of an item's code rows, scales and biases (every thread a share)
-  auto prefetch_item = [&](const Item& q) {
-    const int64_t ebase = (int64_t)act_e[q.a] * p.n_rows;
-    const int span = MODE == kBtSwiglu ? kBtWarps * 8 : kBtWarps * kTileRows;
-    const int lim = MODE == kBtSwiglu ? p.n_out : p.n_rows;
-    const int nr = min(span, lim - q.blk * span);
-    for (int part = 0; part < (MODE == kBtSwiglu ? 2 : 1); ++part) {
-      const int64_t row0 = ebase + (part ? p.n_out : 0) + (int64_t)q.blk * span;
-      const char* cb = reinterpret_cast<const char*>(p.wq + row0 * row_words);
-      const int64_t cbytes = (int64_t)nr * row_words * 4;
-      for (int64_t o = (int64_t)tid * 128; o < cbytes; o += (int64_t)kBtThreads * 128)
-        prefetch_l2(cb + o);
-      const int64_t sbytes = (int64_t)nr * ngroups * 2;
-      const char* sb = reinterpret_cast<const char*>(p.ws + row0 * ngroups);
-      const char* bb = reinterpret_cast<const char*>(p.wb + row0 * ngroups);
-      for (int64_t o = (int64_t)tid * 128; o < sbytes; o += (int64_t)kBtThreads * 128) {
-        prefetch_l2(sb + o);
-        prefetch_l2(bb + o);
-      }
-    }
-  };
-
   int st_a = -1, st_c = -1;
   for (int64_t it = it0; it < it1; ++it) {
     const Item cur = item_at(it);
@@ -296,7 +272,6 @@ __global__ void __launch_bounds__(kBtThreads, 1) gemv_bits_kernel(BtParams p) {
       st_a = cur.a;
       st_c = cur.c;
     }
-    if (it + 1 < it1) prefetch_item(item_at(it + 1));
     const int tile = cur.blk * kBtWarps + warp;
     const int first = MODE == kBtSwiglu ? tile * 8 : tile * kTileRows;  // feature | row
     const int limit = MODE == kBtSwiglu ? p.n_out : p.n_rows;
@@ -320,29 +295,36 @@ __global__ void __launch_bounds__(kBtThreads, 1) gemv_bits_kernel(BtParams p) {
     const uint4* xq = reinterpret_cast<const uint4*>(xh + (size_t)bn * xs_stride + 16 * t);
     const float2* xsp = xsum + (t < (mt2 >> 1) ? 2 * t : mt2 - 2);
     float as[4] = {0.f, 0.f, 0.f, 0.f}, ab[4] = {0.f, 0.f, 0.f, 0.f};
-    // the words of group G for both rows, loaded one group ahead
-    uint32_t wl[3], wh[3], nl[3] = {0u, 0u, 0u}, nh[3] = {0u, 0u, 0u};
-    auto load_words = [&](int G, uint32_t (&a)[3], uint32_t (&b)[3]) {
+    // the words, scales and biases of a group for both rows, in a ring of
+    // kLook register slots: group G + kLook is loaded right after group G
+    // is used (the slot indices are compile-time in the unrolled loop)
+    constexpr int kLook = 3;
+    uint32_t wv[kLook][6];
+    uint16_t sb[kLook][4];
+    auto load_group = [&](int G, uint32_t (&w)[6], uint16_t (&c)[4]) {
+      if (G >= ngroups) return;
       const int64_t o = (int64_t)G * kGroupWords;
 #pragma unroll
       for (int i = 0; i < 3; ++i) {
-        a[i] = __ldg(wlo + o + i);
-        b[i] = __ldg(whi + o + i);
+        w[i] = __ldg(wlo + o + i);
+        w[3 + i] = __ldg(whi + o + i);
       }
+      c[0] = __ldg(slo + G);
+      c[1] = __ldg(shi + G);
+      c[2] = __ldg(blo + G);
+      c[3] = __ldg(bhi + G);
     };
-    load_words(0, wl, wh);
-    for (int G = 0; G < ngroups; ++G) {
-      if (G + 1 < ngroups) load_words(G + 1, nl, nh);
-      const float s0 = f16_bits_to_f32(__ldg(slo + G)), s1 = f16_bits_to_f32(__ldg(shi + G));
-      const float b0 = f16_bits_to_f32(__ldg(blo + G)), b1 = f16_bits_to_f32(__ldg(bhi + G));
+    auto use_group = [&](int G, const uint32_t (&w)[6], const uint16_t (&c)[4]) {
+      const float s0 = f16_bits_to_f32(c[0]), s1 = f16_bits_to_f32(c[1]);
+      const float b0 = f16_bits_to_f32(c[2]), b1 = f16_bits_to_f32(c[3]);
       // this lane's run of 16 codes, from bit 0
       uint32_t rl[3], rh[3];
-      rl[0] = __funnelshift_r(wl[0], wl[1], run_sh);
-      rl[1] = __funnelshift_r(wl[1], wl[2], run_sh);
-      rl[2] = wl[2] >> run_sh;
-      rh[0] = __funnelshift_r(wh[0], wh[1], run_sh);
-      rh[1] = __funnelshift_r(wh[1], wh[2], run_sh);
-      rh[2] = wh[2] >> run_sh;
+      rl[0] = __funnelshift_r(w[0], w[1], run_sh);
+      rl[1] = __funnelshift_r(w[1], w[2], run_sh);
+      rl[2] = w[2] >> run_sh;
+      rh[0] = __funnelshift_r(w[3], w[4], run_sh);
+      rh[1] = __funnelshift_r(w[4], w[5], run_sh);
+      rh[2] = w[5] >> run_sh;
       const uint4 xa = xq[(size_t)G * 8], xb = xq[(size_t)G * 8 + 1];  // 16 fp16 values
       const uint32_t xf[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
       float d[4];
@@ -359,10 +341,17 @@ __global__ void __launch_bounds__(kBtThreads, 1) gemv_bits_kernel(BtParams p) {
       ab[1] = fmaf(b0, X.z, ab[1]);
       ab[2] = fmaf(b1, X.x, ab[2]);
       ab[3] = fmaf(b1, X.z, ab[3]);
+    };
 #pragma unroll
-      for (int i = 0; i < 3; ++i) {
-        wl[i] = nl[i];
-        wh[i] = nh[i];
+    for (int j = 0; j < kLook; ++j) load_group(j, wv[j], sb[j]);
+    for (int G0 = 0; G0 < ngroups; G0 += kLook) {
+#pragma unroll
+      for (int j = 0; j < kLook; ++j) {
+        const int G = G0 + j;
+        if (G < ngroups) {
+          use_group(G, wv[j], sb[j]);
+          load_group(G + kLook, wv[j], sb[j]);
+        }
       }
     }
     // lane (g, t): MMA rows g and g + 8, tokens 2t and 2t + 1
@@ -447,7 +436,7 @@ moe_status_t gemv_bits_qmm(const void* act, int act_kind, const int32_t* sorted,
   p.K = K;
   p.n_rows = n_rows;
   p.n_out = swiglu ? n_rows / 2 : n_rows;
-  // item blocks: 16 row tiles of 16 rows (SWIGLU: 8 features each)
+  // item blocks: 12 row tiles of 16 rows (SWIGLU: 8 features each)
   p.blocks = swiglu ? (p.n_out + kBtWarps * 8 - 1) / (kBtWarps * 8)
                     : (n_rows + kBtWarps * 16 - 1) / (kBtWarps * 16);
   // tokens per chunk: an expert holds at most T rows, and the staged values

@@ -56,18 +56,6 @@
 #include "async.cuh"
 #include "common.cuh"
 
-// Optional per-role wait accounting (compiled in only with -DMOE_TC_TRACE).
-#ifdef MOE_TC_TRACE
-__device__ unsigned long long g_tc_trace[16];
-#define TC_T0() const long long tc_t0_ = clock64()
-#define TC_ACC(var) var += clock64() - tc_t0_
-#define TC_FLUSH(slot, var) atomicAdd(&g_tc_trace[slot], (unsigned long long)(var))
-#else
-#define TC_T0()
-#define TC_ACC(var)
-#define TC_FLUSH(slot, var) ((void)(var))
-#endif
-
 namespace moe {
 namespace {
 
@@ -431,7 +419,6 @@ __global__ void __launch_bounds__(tc_threads(BITS), 1)
 
   if (warp == kLoadWarp) {
     // =============================== loader ===============================
-    long long w_load_empty = 0;
     int64_t issued = 0;
     Ring ring;  // B ring
     bool ok = true;
@@ -456,12 +443,10 @@ __global__ void __launch_bounds__(tc_threads(BITS), 1)
                                                : (uint32_t)nbox * (kBoxRows * BK * 2);
       for (int kb = 0; kb < nkb; ++kb) {
         const int s = ring.idx;
-        TC_T0();
         if (!warp_wait(&b_empty[s], ring.phase ^ 1u, &abort_flag)) {
           ok = false;
           break;
         }
-        TC_ACC(w_load_empty);
         if (lane == 0) mbar_arrive_expect_tx(&b_full[s], bytes);
         __syncwarp();
         if (ACT == kTcGatherX) {
@@ -480,10 +465,6 @@ __global__ void __launch_bounds__(tc_threads(BITS), 1)
         ++issued;
         ring.next(SB);
       }
-    }
-    if (lane == 0) {
-      TC_FLUSH(0, w_load_empty);
-      TC_FLUSH(1, issued);
     }
     if (!ok && lane == 0) {
       raise_device_error(p.err, MOE_DEVERR_TIMEOUT);
@@ -612,7 +593,6 @@ __global__ void __launch_bounds__(tc_threads(BITS), 1)
       }
     };
 
-    long long w_dq_aempty = 0;
     Ring ra, rc;  // A ring, code ring
     int akb = 0;      // k-block (within the tile) of the next A stage
     bool ok = true;
@@ -646,9 +626,7 @@ __global__ void __launch_bounds__(tc_threads(BITS), 1)
           cur.nkb = sbc.nkb;
           const int sa = ra.idx;
           {
-            TC_T0();
             if (!warp_wait(&a_empty[sa], ra.phase ^ 1u, &abort_flag)) ok = false;
-            TC_ACC(w_dq_aempty);
           }
           if (ok) {
 #pragma unroll
@@ -723,7 +701,6 @@ __global__ void __launch_bounds__(tc_threads(BITS), 1)
         }
       }
     }
-    if (lane == 0) TC_FLUSH(3, w_dq_aempty);
     if (!ok && lane == 0) {
       raise_device_error(p.err, MOE_DEVERR_TIMEOUT);
       abort_flag = 1;
@@ -731,8 +708,6 @@ __global__ void __launch_bounds__(tc_threads(BITS), 1)
   } else if (warp == kMmaWarp) {
     // ================================= MMA =================================
     // the whole warp, converged; every wait's outcome is agreed by the warp
-    long long w_mma_tmem = 0, w_mma_afull = 0, w_mma_bfull = 0;
-    const long long t_mma0 = clock64();
     int64_t it = 0;
     Ring ra, rb;  // A ring, B ring
     int j = 0;
@@ -746,9 +721,7 @@ __global__ void __launch_bounds__(tc_threads(BITS), 1)
       const uint32_t idesc = idesc_bf16(BM, ti.nmma);
       const int buf = j & 1;
       {
-        TC_T0();
         if (!wait_all(&tmem_empty[buf], (uint32_t)(((j >> 1) & 1) ^ 1))) ok = false;
-        TC_ACC(w_mma_tmem);
       }
       if (__any_sync(0xFFFFFFFFu, !ok || abort_flag != 0)) {
         ok = false;
@@ -759,9 +732,7 @@ __global__ void __launch_bounds__(tc_threads(BITS), 1)
       for (int as = 0, kb = 0; as < nas; ++as, ra.next(SA)) {
         const int sa = ra.idx;
         {
-          TC_T0();
           if (!wait_all(&a_full[sa], ra.phase)) ok = false;
-          TC_ACC(w_mma_afull);
         }
         if (!ok) break;
         // operand visibility: the dequant writers' proxy fence and release
@@ -771,9 +742,7 @@ __global__ void __launch_bounds__(tc_threads(BITS), 1)
         for (int h = 0; h < kKbPerA; ++h) {
           if (kb < nkb && (h == 0 || as * kKbPerA + h < nkb)) {
             {
-              TC_T0();
               if (!wait_all(&b_full[rb.idx], rb.phase)) ok = false;
-              TC_ACC(w_mma_bfull);
             }
             if (!ok) break;
             const uint64_t adesc = smem_desc_sw128(stage_a(sa, h));
@@ -804,17 +773,8 @@ __global__ void __launch_bounds__(tc_threads(BITS), 1)
       mbar_wait(&drain_bar, 0, kWaitBudgetCycles);
     }
     __syncwarp();
-    if (lane == 0) {
-      TC_FLUSH(4, w_mma_tmem);
-      TC_FLUSH(5, w_mma_afull);
-      TC_FLUSH(12, w_mma_bfull);
-      TC_FLUSH(7, clock64() - t_mma0);
-      TC_FLUSH(8, it);
-    }
   } else {
     // =============================== epilogue ===============================
-    long long w_epi = 0;
-    const long long t_epi0 = clock64();
     int j = 0;
     uint32_t xs = 0;  // SWIGLU exchange steps so far
     bool ok = true;
@@ -823,9 +783,7 @@ __global__ void __launch_bounds__(tc_threads(BITS), 1)
       const TileInfo ti = tile_info(p, act_e, tile_start, n_act, t);
       const int buf = j & 1;
       {
-        TC_T0();
         if (!warp_wait(&tmem_full[buf], (uint32_t)((j >> 1) & 1), &abort_flag)) ok = false;
-        TC_ACC(w_epi);
       }
       if (!ok) break;
       tc_fence_after();
@@ -923,11 +881,6 @@ __global__ void __launch_bounds__(tc_threads(BITS), 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tmem_empty[buf]);
-    }
-    if (lane == 0 && warp == 0) {
-      TC_FLUSH(9, w_epi);
-      TC_FLUSH(10, clock64() - t_epi0);
-      TC_FLUSH(11, j);
     }
     if (!ok && lane == 0) {
       raise_device_error(p.err, MOE_DEVERR_TIMEOUT);

@@ -54,22 +54,6 @@
 #include "async.cuh"
 #include "common.cuh"
 
-// Optional per-role cycle accounting (compiled in only with -DMOE_SV_TRACE).
-#ifdef MOE_SV_TRACE
-__device__ unsigned long long g_sv_trace[20];
-__device__ unsigned long long g_sv_span[2];  // min entry, max exit (globaltimer ns)
-__device__ __forceinline__ unsigned long long sv_gtime() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-#define SV_CLK() clock64()
-#define SV_ADD(slot, v) atomicAdd(&g_sv_trace[slot], (unsigned long long)(v))
-#else
-#define SV_CLK() 0LL
-#define SV_ADD(slot, v) ((void)(v))
-#endif
-
 namespace moe {
 
 bool make_tensor_map_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base,
@@ -294,10 +278,6 @@ __global__ void __launch_bounds__(kSvThreads, 1)
   __shared__ int st_nt;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-#ifdef MOE_SV_TRACE
-  const long long tr_entry = clock64();
-  if (tid == 0) atomicMin(&g_sv_span[0], sv_gtime());
-#endif
   const int stages = p.stages;
   const int mts = ONE ? 1 : p.mts;
   const int mts2 = mts < 2 ? 2 : mts;
@@ -418,8 +398,6 @@ __global__ void __launch_bounds__(kSvThreads, 1)
     int64_t issued = 0;
     SvCursor cu = cursor_at(u0);
     const int arr = lane >> 4, srow = lane & 15;  // this lane's scale row
-    long long tr_wait = 0, tr_issue = 0;
-    const long long tr_start = SV_CLK();
     for (int u = u0; u < u1 && ok; ++u, cursor_next(cu)) {
       const int64_t ebase = (int64_t)act_e[cu.a] * p.n_rows;
       // first rows of the tile's 8-row boxes: half h takes boxes 2h, 2h + 1
@@ -436,13 +414,10 @@ __global__ void __launch_bounds__(kSvThreads, 1)
         rb[3] = rb[0] + 24;
       }
       for (int ch = 0; ch < nck; ++ch) {
-        const long long tr0 = SV_CLK();
         if (abort_flag || !sv_wait(&empty[ring.idx], ring.phase ^ 1u)) {
           ok = false;
           break;
         }
-        const long long tr1 = SV_CLK();
-        tr_wait += tr1 - tr0;
         if (codes_warp) {
           unsigned char* cdst = codes + (size_t)ring.idx * kSvCodeBytes;
           if (lane == 0) {
@@ -476,19 +451,12 @@ __global__ void __launch_bounds__(kSvThreads, 1)
           }
           cp_async_arrive_sv(&full[ring.idx]);
         }
-        tr_issue += SV_CLK() - tr1;
         ++issued;
         ring.next(stages);
       }
     }
     if (!codes_warp) cp_async_wait_all_sv();
     pdl_wait();
-    if (lane == 0) {
-      SV_ADD(codes_warp ? 0 : 13, tr_wait);
-      SV_ADD(codes_warp ? 1 : 14, issued);
-      SV_ADD(codes_warp ? 2 : 15, SV_CLK() - tr_start);
-      SV_ADD(codes_warp ? 11 : 12, tr_issue);
-    }
     if (!ok && lane == 0) {
       raise_device_error(p.err, MOE_DEVERR_TIMEOUT);
       abort_flag = 1;
@@ -661,13 +629,7 @@ __global__ void __launch_bounds__(kSvThreads, 1)
     // columns past the chunk (their results are never read)
     const int bn = ONE ? 0 : min(g, mts - 1);
     SvCursor cu = cursor_at(u0);
-    long long tr_full = 0, tr_red = 0, tr_stage = 0, tr_work = 0, tr_n = 0;
-    const long long tr_start = SV_CLK();
-#ifdef MOE_SV_TRACE
-    if (tid == 0) SV_ADD(16, tr_start - tr_entry);
-#endif
     for (int u = u0; u < u1 && ok; ++u, cursor_next(cu)) {
-      const long long trs = SV_CLK();
       if (cu.a != st_a || cu.c != st_c) {
         bool need = true;
         if (p.act_kind == kSvActX && st_a >= 0) {
@@ -685,7 +647,6 @@ __global__ void __launch_bounds__(kSvThreads, 1)
         st_a = cu.a;
         st_c = cu.c;
       }
-      tr_stage += SV_CLK() - trs;
       const int wl = DUAL ? ((warp & 7) + u * rot_step) & 7 : (warp + u * rot_step) & (kSvConsumers - 1);
       const int jb = S::kGpw * wl;
       const int soff = rr * S::kScaleRow + jb * 2;
@@ -693,13 +654,10 @@ __global__ void __launch_bounds__(kSvThreads, 1)
       // ONE: token 0 only, else tokens 2t and 2t + 1
       float as[4] = {0.0f, 0.0f, 0.0f, 0.0f}, ab[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       for (int ch = 0; ch < nck; ++ch) {
-        const long long tr0 = SV_CLK();
         if (abort_flag || !sv_wait(&full[ring.idx], ring.phase)) {
           ok = false;
           break;
         }
-        const long long tr1 = SV_CLK();
-        tr_full += tr1 - tr0;
         const unsigned char* cst =
             codes + (size_t)ring.idx * kSvCodeBytes + half * 16384 + wl * 1024;
         const int g0 = ch * S::kGpc;
@@ -806,17 +764,13 @@ __global__ void __launch_bounds__(kSvThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[ring.idx]);
         ring.next(stages);
-        tr_work += SV_CLK() - tr1;
-        ++tr_n;
       }
       if (!ok) break;
       // this warp's partial sums of the tile to the epilogue
-      const long long tr2 = SV_CLK();
       if (abort_flag || !sv_wait(&red_empty[rs.idx], rs.phase ^ 1u)) {
         ok = false;
         break;
       }
-      tr_red += SV_CLK() - tr2;
       float* rd = red + ((size_t)rs.idx * kSvConsumers + half * 8 + wl) * mts * 16;
       const int n0 = 2 * t, n1 = 2 * t + 1;
       if (n0 < mts) {
@@ -831,14 +785,6 @@ __global__ void __launch_bounds__(kSvThreads, 1)
       if (lane == 0) mbar_arrive(&red_full[rs.idx]);
       rs.next(rslots);
     }
-    if (lane == 0) {
-      SV_ADD(3, tr_full);
-      SV_ADD(4, tr_red);
-      SV_ADD(5, SV_CLK() - tr_start);
-      SV_ADD(6, tr_n);
-      SV_ADD(9, tr_stage);
-      SV_ADD(10, tr_work);
-    }
     if (!ok && lane == 0) {
       raise_device_error(p.err, MOE_DEVERR_TIMEOUT);
       abort_flag = 1;
@@ -849,20 +795,16 @@ __global__ void __launch_bounds__(kSvThreads, 1)
     SvRing rs{0, 0u};
     bool ok = true;
     SvCursor cu = cursor_at(u0);
-    long long tr_wait = 0;
-    const long long tr_start = SV_CLK();
     for (int u = u0; u < u1; ++u, cursor_next(cu)) {
       if (abort_flag) {
         ok = false;
         break;
       }
-      const long long tr0 = SV_CLK();
       const bool got = mbar_wait(&red_full[rs.idx], rs.phase, kWaitBudgetCycles);
       if (!__all_sync(0xFFFFFFFFu, got)) {
         ok = false;
         break;
       }
-      tr_wait += SV_CLK() - tr0;
       const int m = act_m[cu.a];
       const int nt = min(mts, m - cu.c * mts);
       const int64_t row0 = (int64_t)act_lo[cu.a] + (int64_t)cu.c * mts;
@@ -1036,14 +978,6 @@ __global__ void __launch_bounds__(kSvThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&red_empty[rs.idx]);
       rs.next(rslots);
-    }
-    if (lane == 0) {
-      SV_ADD(7, tr_wait);
-      SV_ADD(8, SV_CLK() - tr_start);
-#ifdef MOE_SV_TRACE
-      SV_ADD(17, SV_CLK() - tr_entry);
-      atomicMax(&g_sv_span[1], sv_gtime());
-#endif
     }
     if (!ok && lane == 0) {
       raise_device_error(p.err, MOE_DEVERR_TIMEOUT);

@@ -31,11 +31,12 @@
 // so a row's value is reduced in one fixed order whatever rows share its
 // tile, and the fused gate_up product equals the separate gate and up
 // products bit for bit.  The chunk's token fragments are staged once in
-// shared memory and stay while the CTA's items keep to that chunk.  A warp
-// keeps the code words, scales and biases of the next three groups of its
-// rows in flight in registers.
+// shared memory and stay while the CTA's items keep to that chunk.  Each
+// warp streams its rows' codes through a ring of shared-memory stages filled
+// by cp.async three stages (twelve groups) ahead.
 #include <cuda_fp16.h>
 
+#include "async.cuh"
 #include "common.cuh"
 
 namespace moe {
@@ -45,7 +46,7 @@ constexpr int kBtThreads = 384;
 constexpr int kBtWarps = kBtThreads / 32;  // row tiles per item
 constexpr int kBtMaxTokens = 8;            // tokens per chunk (the MMA's n)
 constexpr int kBtMaxE = 1024;
-constexpr size_t kBtMaxStage = 200 * 1024;  // staged token bytes (at most)
+constexpr size_t kBtMaxSmem = 225 * 1024;  // dynamic shared memory (at most)
 
 enum BtMode { kBtSwiglu = 0, kBtRaw = 1 };
 enum BtAct { kBtActX = 0, kBtActF32 = 1, kBtActBf16 = 2 };
@@ -68,13 +69,48 @@ struct BtParams {
   unsigned int* err;
 };
 
-// Staged tokens: fp16 values [mt][K + 8] (16 bytes of padding per token row
-// keep the fragment loads free of bank conflicts), then (X, 2^(24-e)) per
-// group and token [K / 64][mt2].
+// Ring of a warp: bt_ring_depth slots (4 for 5 bits; 3 for 6, so that 8
+// staged tokens of 4096 values still fit beside it), each holding
+// kRingGroups groups of its 16 rows: the codes, one row after another at a
+// stride of 8b + 4 words (44 for 5 bits, 52 for 6: 16-byte aligned, and the
+// words that the 8 rows x 4 run offsets of one read touch fall in 32
+// distinct banks), then per row the 4 scales and the 4 biases (16 bytes).
+constexpr int kRingGroups = 4;
+__host__ __device__ constexpr int bt_ring_depth(int bits) { return bits == 6 ? 3 : 4; }
+__host__ __device__ constexpr int bt_ring_row_words(int bits) { return kRingGroups * 2 * bits + 4; }
+__host__ __device__ constexpr int bt_ring_codes_bytes(int bits) { return 16 * bt_ring_row_words(bits) * 4; }
+__host__ __device__ constexpr int bt_ring_slot_bytes(int bits) { return bt_ring_codes_bytes(bits) + 16 * 16; }
+
+// Shared memory: the active-expert lists [4][E + 1] ints; staged tokens, fp16
+// values [mt][K + 8] (16 bytes of padding per token row keep the fragment
+// loads free of bank conflicts), then (X, 2^(24-e)) per group and token
+// [K / 64][mt2]; then the warps' code rings.
 __host__ __device__ inline int bt_xs_stride(int K) { return K + 8; }
+__host__ __device__ inline size_t bt_act_bytes(int E) { return ((size_t)4 * (E + 1) * 4 + 15) & ~(size_t)15; }
 __host__ __device__ inline size_t bt_stage_bytes(int K, int mt) {
   const int mt2 = mt < 2 ? 2 : mt;
   return (size_t)mt * bt_xs_stride(K) * 2 + (size_t)(K / 64) * mt2 * 8;
+}
+__host__ __device__ inline size_t bt_smem_bytes(int bits, int K, int mt, int E) {
+  return bt_act_bytes(E) + bt_stage_bytes(K, mt) + (size_t)kBtWarps * bt_ring_depth(bits) * bt_ring_slot_bytes(bits);
+}
+
+// 8 or 16 bytes global -> shared, asynchronous (completion by cp.async groups).
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+// fp16 number i (0..7) of a 16-byte word
+__device__ __forceinline__ uint16_t u16_of(const uint4& v, int i) {
+  const uint32_t w = i < 2 ? v.x : (i < 4 ? v.y : (i < 6 ? v.z : v.w));
+  return (uint16_t)((i & 1) ? w >> 16 : w & 0xFFFFu);
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // d = A B (+ d when acc)
@@ -113,15 +149,22 @@ __global__ void __launch_bounds__(kBtThreads, 1) gemv_bits_kernel(BtParams p) {
   constexpr int mt = MT;
   constexpr int mt2 = MT < 2 ? 2 : MT;
   constexpr int kTileRows = 16;  // SWIGLU: 8 features (gate rows, then up rows)
+  constexpr int kRing = bt_ring_depth(BITS);
   extern __shared__ __align__(16) unsigned char bt_smem[];
-  __shared__ int act_e[kBtMaxE + 1], act_lo[kBtMaxE + 1], act_m[kBtMaxE + 1], act_base[kBtMaxE + 1];
   __shared__ int n_act_sh;
   __shared__ int wtot[kBtWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ngroups = p.K / 64;
   const int xs_stride = bt_xs_stride(p.K);
-  uint16_t* xh = reinterpret_cast<uint16_t*>(bt_smem);  // [mt][xs_stride] fp16
-  float2* xsum = reinterpret_cast<float2*>(bt_smem + (size_t)mt * xs_stride * 2);  // [G][mt2]
+  int* act_e = reinterpret_cast<int*>(bt_smem);
+  int* act_lo = act_e + (p.E + 1);
+  int* act_m = act_lo + (p.E + 1);
+  int* act_base = act_m + (p.E + 1);
+  unsigned char* stage_base = bt_smem + bt_act_bytes(p.E);
+  uint16_t* xh = reinterpret_cast<uint16_t*>(stage_base);  // [mt][xs_stride] fp16
+  float2* xsum = reinterpret_cast<float2*>(stage_base + (size_t)mt * xs_stride * 2);  // [G][mt2]
+  unsigned char* ring = stage_base + bt_stage_bytes(p.K, mt) +
+                        (size_t)warp * bt_ring_depth(BITS) * bt_ring_slot_bytes(BITS);  // this warp's ring
   pdl_wait();
   pdl_trigger();
 
@@ -281,78 +324,119 @@ __global__ void __launch_bounds__(kBtThreads, 1) gemv_bits_kernel(BtParams p) {
     // else rows first + g and first + g + 8; rows past the matrix read a
     // valid row and their results are dropped
     const int64_t last = ebase + p.n_rows - 1;
-    const int64_t row_lo = min(ebase + first + g, last);
-    const int64_t row_hi =
-        min(MODE == kBtSwiglu ? ebase + p.n_out + first + g : ebase + first + g + 8, last);
-    const uint32_t* wlo = p.wq + row_lo * row_words + run_w0;
-    const uint32_t* whi = p.wq + row_hi * row_words + run_w0;
-    const uint16_t* slo = p.ws + row_lo * ngroups;
-    const uint16_t* shi = p.ws + row_hi * ngroups;
-    const uint16_t* blo = p.wb + row_lo * ngroups;
-    const uint16_t* bhi = p.wb + row_hi * ngroups;
     // B columns past the chunk repeat one of its tokens (never read back)
     const int bn = min(g, mt - 1);
     const uint4* xq = reinterpret_cast<const uint4*>(xh + (size_t)bn * xs_stride + 16 * t);
     const float2* xsp = xsum + (t < (mt2 >> 1) ? 2 * t : mt2 - 2);
     float as[4] = {0.f, 0.f, 0.f, 0.f}, ab[4] = {0.f, 0.f, 0.f, 0.f};
-    // the words, scales and biases of a group for both rows, in a ring of
-    // kLook register slots: group G + kLook is loaded right after group G
-    // is used (the slot indices are compile-time in the unrolled loop)
-    constexpr int kLook = 3;
-    uint32_t wv[kLook][6];
-    uint16_t sb[kLook][4];
-    auto load_group = [&](int G, uint32_t (&w)[6], uint16_t (&c)[4]) {
-      if (G >= ngroups) return;
-      const int64_t o = (int64_t)G * kGroupWords;
-#pragma unroll
-      for (int i = 0; i < 3; ++i) {
-        w[i] = __ldg(wlo + o + i);
-        w[3 + i] = __ldg(whi + o + i);
-      }
-      c[0] = __ldg(slo + G);
-      c[1] = __ldg(shi + G);
-      c[2] = __ldg(blo + G);
-      c[3] = __ldg(bhi + G);
+    // The tile streams through the warp's ring: stage q holds groups
+    // 4q .. 4q + 3 of the 16 rows (ring row r is MMA row r: rows 0-7 the
+    // rows g of the lanes, 8-15 their rows g + 8), copied with cp.async
+    // kRing - 1 stages ahead of its use.  When the groups of a row are a
+    // multiple of 4 (every row and stage start is then 16-byte aligned for
+    // the codes and 8-byte aligned for the scales) a stage is 16-byte code
+    // copies and one 8-byte scale or bias copy per lane; otherwise 8-byte
+    // code copies with the words past the row end taken from its start
+    // (unused), and the scales loaded and stored in order, the group index
+    // clamped to the row.
+    constexpr int kRowWords = bt_ring_row_words(BITS);
+    constexpr int kSegWords = kRingGroups * kGroupWords;  // a row's code words of one stage
+    constexpr int kRow16 = kSegWords / 4;                 // its 16-byte copies
+    constexpr int kLane16 = 16 * kRow16 / 32;             // a lane's per stage
+    static_assert(16 * kRow16 % 32 == 0, "copies split evenly over the lanes");
+    const int nst = (ngroups + kRingGroups - 1) / kRingGroups;
+    const bool whole = (ngroups & (kRingGroups - 1)) == 0;
+    auto ring_row = [&](int r) -> int64_t {  // weight row of ring row r
+      return r < 8 ? min(ebase + first + r, last)
+                   : min(MODE == kBtSwiglu ? ebase + p.n_out + first + (r - 8) : ebase + first + r, last);
     };
-    auto use_group = [&](int G, const uint32_t (&w)[6], const uint16_t (&c)[4]) {
-      const float s0 = f16_bits_to_f32(c[0]), s1 = f16_bits_to_f32(c[1]);
-      const float b0 = f16_bits_to_f32(c[2]), b1 = f16_bits_to_f32(c[3]);
-      // this lane's run of 16 codes, from bit 0
-      uint32_t rl[3], rh[3];
-      rl[0] = __funnelshift_r(w[0], w[1], run_sh);
-      rl[1] = __funnelshift_r(w[1], w[2], run_sh);
-      rl[2] = w[2] >> run_sh;
-      rh[0] = __funnelshift_r(w[3], w[4], run_sh);
-      rh[1] = __funnelshift_r(w[4], w[5], run_sh);
-      rh[2] = w[5] >> run_sh;
-      const uint4 xa = xq[(size_t)G * 8], xb = xq[(size_t)G * 8 + 1];  // 16 fp16 values
-      const uint32_t xf[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-      float d[4];
+    const uint32_t* csrc[kLane16];  // copy i of the lane: words cw .. cw + 3 of ring row r
+    int cdst[kLane16];
 #pragma unroll
-      for (int s = 0; s < 4; ++s)
-        mma_bt(d, bt_pair<BITS>(rl, 2 * s), bt_pair<BITS>(rh, 2 * s), bt_pair<BITS>(rl, 2 * s + 1),
-               bt_pair<BITS>(rh, 2 * s + 1), xf[2 * s], xf[2 * s + 1], s > 0);
-      const float4 X = *reinterpret_cast<const float4*>(xsp + (size_t)G * mt2);  // tokens 2t, 2t+1
-      as[0] = fmaf(s0 * X.y, d[0], as[0]);
-      as[1] = fmaf(s0 * X.w, d[1], as[1]);
-      as[2] = fmaf(s1 * X.y, d[2], as[2]);
-      as[3] = fmaf(s1 * X.w, d[3], as[3]);
-      ab[0] = fmaf(b0, X.x, ab[0]);
-      ab[1] = fmaf(b0, X.z, ab[1]);
-      ab[2] = fmaf(b1, X.x, ab[2]);
-      ab[3] = fmaf(b1, X.z, ab[3]);
-    };
+    for (int i = 0; i < kLane16; ++i) {
+      const int c = lane + 32 * i;
+      const int r = c / kRow16, cw = (c - r * kRow16) * 4;
+      csrc[i] = p.wq + ring_row(r) * row_words + cw;
+      cdst[i] = (r * kRowWords + cw) * 4;
+    }
+    // scale copy of the lane: ring row lane / 2, scales (even lane) or biases
+    const int sr = lane >> 1;
+    const uint16_t* ssrc = ((lane & 1) ? p.wb : p.ws) + ring_row(sr) * ngroups;
+    const int sdst = bt_ring_codes_bytes(BITS) + sr * 16 + (lane & 1) * 8;
+    auto issue = [&](int q) {
+      if (q < nst) {
+        unsigned char* slot = ring + (size_t)(q % kRing) * bt_ring_slot_bytes(BITS);
+        const int G0 = q * kRingGroups;
+        if (whole) {
 #pragma unroll
-    for (int j = 0; j < kLook; ++j) load_group(j, wv[j], sb[j]);
-    for (int G0 = 0; G0 < ngroups; G0 += kLook) {
+          for (int i = 0; i < kLane16; ++i) cp_async16(slot + cdst[i], csrc[i] + (int64_t)G0 * kGroupWords);
+          cp_async8(slot + sdst, ssrc + G0);
+        } else {
+          for (int c = lane; c < 16 * (kSegWords / 2); c += 32) {
+            const int r = c / (kSegWords / 2), cw = (c - r * (kSegWords / 2)) * 2;
+            const int64_t w = (int64_t)G0 * kGroupWords + cw;
+            cp_async8(slot + (r * kRowWords + cw) * 4, p.wq + ring_row(r) * row_words + (w < row_words ? w : 0));
+          }
+          uint16_t v[kRingGroups];
 #pragma unroll
-      for (int j = 0; j < kLook; ++j) {
-        const int G = G0 + j;
-        if (G < ngroups) {
-          use_group(G, wv[j], sb[j]);
-          load_group(G + kLook, wv[j], sb[j]);
+          for (int j = 0; j < kRingGroups; ++j) v[j] = __ldg(ssrc + min(G0 + j, ngroups - 1));
+          *reinterpret_cast<uint2*>(slot + sdst) =
+              make_uint2((uint32_t)v[0] | ((uint32_t)v[1] << 16), (uint32_t)v[2] | ((uint32_t)v[3] << 16));
         }
       }
+      cp_async_commit();  // one group per stage, empty or not
+    };
+#pragma unroll
+    for (int q = 0; q < kRing - 1; ++q) issue(q);
+    for (int q = 0; q < nst; ++q) {
+      issue(q + kRing - 1);
+      cp_async_wait<kRing - 1>();  // stage q has landed (this lane's copies) ...
+      __syncwarp();                // ... and every lane's
+      const unsigned char* slot = ring + (size_t)(q % kRing) * bt_ring_slot_bytes(BITS);
+      const uint32_t* rlo = reinterpret_cast<const uint32_t*>(slot) + g * kRowWords + run_w0;
+      const uint32_t* rhi = reinterpret_cast<const uint32_t*>(slot) + (8 + g) * kRowWords + run_w0;
+      const uint4 sbl = *reinterpret_cast<const uint4*>(slot + bt_ring_codes_bytes(BITS) + g * 16);
+      const uint4 sbh = *reinterpret_cast<const uint4*>(slot + bt_ring_codes_bytes(BITS) + (8 + g) * 16);
+#pragma unroll
+      for (int j = 0; j < kRingGroups; ++j) {
+        const int G = q * kRingGroups + j;
+        if (G < ngroups) {
+          const float s0 = f16_bits_to_f32(u16_of(sbl, j)), s1 = f16_bits_to_f32(u16_of(sbh, j));
+          const float b0 = f16_bits_to_f32(u16_of(sbl, 4 + j)), b1 = f16_bits_to_f32(u16_of(sbh, 4 + j));
+          uint32_t w[6];
+#pragma unroll
+          for (int i = 0; i < 3; ++i) {
+            w[i] = rlo[j * kGroupWords + i];
+            w[3 + i] = rhi[j * kGroupWords + i];
+          }
+          // this lane's run of 16 codes, from bit 0
+          uint32_t rl[3], rh[3];
+          rl[0] = __funnelshift_r(w[0], w[1], run_sh);
+          rl[1] = __funnelshift_r(w[1], w[2], run_sh);
+          rl[2] = w[2] >> run_sh;
+          rh[0] = __funnelshift_r(w[3], w[4], run_sh);
+          rh[1] = __funnelshift_r(w[4], w[5], run_sh);
+          rh[2] = w[5] >> run_sh;
+          const uint4 xa = xq[(size_t)G * 8], xb = xq[(size_t)G * 8 + 1];  // 16 fp16 values
+          const uint32_t xf[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+          float d[4];
+#pragma unroll
+          for (int s = 0; s < 4; ++s)
+            mma_bt(d, bt_pair<BITS>(rl, 2 * s), bt_pair<BITS>(rh, 2 * s),
+                   bt_pair<BITS>(rl, 2 * s + 1), bt_pair<BITS>(rh, 2 * s + 1), xf[2 * s],
+                   xf[2 * s + 1], s > 0);
+          const float4 X = *reinterpret_cast<const float4*>(xsp + (size_t)G * mt2);  // tokens 2t, 2t+1
+          as[0] = fmaf(s0 * X.y, d[0], as[0]);
+          as[1] = fmaf(s0 * X.w, d[1], as[1]);
+          as[2] = fmaf(s1 * X.y, d[2], as[2]);
+          as[3] = fmaf(s1 * X.w, d[3], as[3]);
+          ab[0] = fmaf(b0, X.x, ab[0]);
+          ab[1] = fmaf(b0, X.z, ab[1]);
+          ab[2] = fmaf(b1, X.x, ab[2]);
+          ab[3] = fmaf(b1, X.z, ab[3]);
+        }
+      }
+      __syncwarp();  // the slot is rewritten by the next iteration's copies
     }
     // lane (g, t): MMA rows g and g + 8, tokens 2t and 2t + 1
     const float v0 = as[0] + ab[0], v1 = as[1] + ab[1], v2 = as[2] + ab[2], v3 = as[3] + ab[3];
@@ -390,7 +474,7 @@ __global__ void __launch_bounds__(kBtThreads, 1) gemv_bits_kernel(BtParams p) {
 template <int BITS, int MODE, int MT>
 moe_status_t launch_bits_mt(const BtParams& p, cudaStream_t st) {
   auto kern = gemv_bits_kernel<BITS, MODE, MT>;
-  const size_t smem = bt_stage_bytes(p.K, MT);
+  const size_t smem = bt_smem_bytes(BITS, p.K, MT, p.E);
   // the static arrays count against the same limit: raise it for any size
   static size_t set_max[moe_host::kMaxCachedDevices] = {};  // per device
   const int dev = moe_host::device_index();
@@ -442,8 +526,8 @@ moe_status_t gemv_bits_qmm(const void* act, int act_kind, const int32_t* sorted,
   // tokens per chunk: an expert holds at most T rows, and the staged values
   // must fit in shared memory
   int mt = 1;
-  while (mt < kBtMaxTokens && mt < T && bt_stage_bytes(K, 2 * mt) <= kBtMaxStage) mt <<= 1;
-  if (bt_stage_bytes(K, mt) > kBtMaxStage) return MOE_ERR_UNSUPPORTED;
+  while (mt < kBtMaxTokens && mt < T && bt_smem_bytes(bits, K, 2 * mt, E) <= kBtMaxSmem) mt <<= 1;
+  if (bt_smem_bytes(bits, K, mt, E) > kBtMaxSmem) return MOE_ERR_UNSUPPORTED;
   p.mt = mt;
   p.wq = wq;
   p.ws = ws;

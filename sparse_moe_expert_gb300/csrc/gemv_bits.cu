@@ -102,10 +102,11 @@ __device__ __forceinline__ void cp_async8(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
-// fp16 number i (0..7) of a 16-byte word
-__device__ __forceinline__ uint16_t u16_of(const uint4& v, int i) {
-  const uint32_t w = i < 2 ? v.x : (i < 4 ? v.y : (i < 6 ? v.z : v.w));
-  return (uint16_t)((i & 1) ? w >> 16 : w & 0xFFFFu);
+// the two fp16 numbers of a word (low half first) as floats
+__device__ __forceinline__ void half2_bits_to_f32(uint32_t w, float& lo, float& hi) {
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+  lo = f.x;
+  hi = f.y;
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -397,12 +398,21 @@ __global__ void __launch_bounds__(kBtThreads, 1) gemv_bits_kernel(BtParams p) {
       const uint32_t* rhi = reinterpret_cast<const uint32_t*>(slot) + (8 + g) * kRowWords + run_w0;
       const uint4 sbl = *reinterpret_cast<const uint4*>(slot + bt_ring_codes_bytes(BITS) + g * 16);
       const uint4 sbh = *reinterpret_cast<const uint4*>(slot + bt_ring_codes_bytes(BITS) + (8 + g) * 16);
+      // scales (s) and biases (b) of the stage's 4 groups, rows g and g + 8
+      float sl[4], sh[4], bl[4], bh[4];
+      half2_bits_to_f32(sbl.x, sl[0], sl[1]);
+      half2_bits_to_f32(sbl.y, sl[2], sl[3]);
+      half2_bits_to_f32(sbl.z, bl[0], bl[1]);
+      half2_bits_to_f32(sbl.w, bl[2], bl[3]);
+      half2_bits_to_f32(sbh.x, sh[0], sh[1]);
+      half2_bits_to_f32(sbh.y, sh[2], sh[3]);
+      half2_bits_to_f32(sbh.z, bh[0], bh[1]);
+      half2_bits_to_f32(sbh.w, bh[2], bh[3]);
 #pragma unroll
       for (int j = 0; j < kRingGroups; ++j) {
         const int G = q * kRingGroups + j;
         if (G < ngroups) {
-          const float s0 = f16_bits_to_f32(u16_of(sbl, j)), s1 = f16_bits_to_f32(u16_of(sbh, j));
-          const float b0 = f16_bits_to_f32(u16_of(sbl, 4 + j)), b1 = f16_bits_to_f32(u16_of(sbh, 4 + j));
+          const float s0 = sl[j], s1 = sh[j], b0 = bl[j], b1 = bh[j];
           uint32_t w[6];
 #pragma unroll
           for (int i = 0; i < 3; ++i) {

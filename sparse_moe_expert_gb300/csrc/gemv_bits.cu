@@ -26,14 +26,14 @@
 // add s 2^(24-e) P and b X per group.
 //
 // Work.  An item is (active expert, chunk of up to MT of its tokens, block
-// of 12 row tiles); each of the 12 warps takes one tile of 16 rows (SwiGLU:
+// of 16 row tiles); each of the 16 warps takes one tile of 16 rows (SwiGLU:
 // 8 gate rows and the 8 up rows of the same features) over the whole row,
 // so a row's value is reduced in one fixed order whatever rows share its
 // tile, and the fused gate_up product equals the separate gate and up
 // products bit for bit.  The chunk's token fragments are staged once in
 // shared memory and stay while the CTA's items keep to that chunk.  Each
-// warp streams its rows' codes through a ring of shared-memory stages filled
-// by cp.async three stages (twelve groups) ahead.
+// warp streams its rows' codes, scales and biases through a ring of
+// shared-memory stages filled by cp.async one stage (four groups) ahead.
 #include <cuda_fp16.h>
 
 #include "async.cuh"
@@ -42,7 +42,7 @@
 namespace moe {
 namespace {
 
-constexpr int kBtThreads = 384;
+constexpr int kBtThreads = 512;
 constexpr int kBtWarps = kBtThreads / 32;  // row tiles per item
 constexpr int kBtMaxTokens = 8;            // tokens per chunk (the MMA's n)
 constexpr int kBtMaxE = 1024;
@@ -69,14 +69,14 @@ struct BtParams {
   unsigned int* err;
 };
 
-// Ring of a warp: bt_ring_depth slots (4 for 5 bits; 3 for 6, so that 8
-// staged tokens of 4096 values still fit beside it), each holding
-// kRingGroups groups of its 16 rows: the codes, one row after another at a
+// Ring of a warp: two slots (with 16 warps deeper rings measured slower:
+// the cp.async copies in flight compete with the shared memory for the
+// SM's L1 storage), each holding kRingGroups groups of its 16 rows: the codes, one row after another at a
 // stride of 8b + 4 words (44 for 5 bits, 52 for 6: 16-byte aligned, and the
 // words that the 8 rows x 4 run offsets of one read touch fall in 32
 // distinct banks), then per row the 4 scales and the 4 biases (16 bytes).
 constexpr int kRingGroups = 4;
-__host__ __device__ constexpr int bt_ring_depth(int bits) { return bits == 6 ? 3 : 4; }
+__host__ __device__ constexpr int bt_ring_depth(int) { return 2; }
 __host__ __device__ constexpr int bt_ring_row_words(int bits) { return kRingGroups * 2 * bits + 4; }
 __host__ __device__ constexpr int bt_ring_codes_bytes(int bits) { return 16 * bt_ring_row_words(bits) * 4; }
 __host__ __device__ constexpr int bt_ring_slot_bytes(int bits) { return bt_ring_codes_bytes(bits) + 16 * 16; }
@@ -530,7 +530,7 @@ moe_status_t gemv_bits_qmm(const void* act, int act_kind, const int32_t* sorted,
   p.K = K;
   p.n_rows = n_rows;
   p.n_out = swiglu ? n_rows / 2 : n_rows;
-  // item blocks: 12 row tiles of 16 rows (SWIGLU: 8 features each)
+  // item blocks: 16 row tiles of 16 rows (SWIGLU: 8 features each)
   p.blocks = swiglu ? (p.n_out + kBtWarps * 8 - 1) / (kBtWarps * 8)
                     : (n_rows + kBtWarps * 16 - 1) / (kBtWarps * 16);
   // tokens per chunk: an expert holds at most T rows, and the staged values

@@ -72,6 +72,11 @@ def test_router_single_token_calls(cuda_lib):
     (8, 0, 5, 21, True, False, 3.0),    # adaptive with kmax > 3
     (8, 0, 3, 21, False, True, 0.2),
     (37, 3, 3, 700, True, True, 0.9),   # 22 token groups: the 4-CTA cluster router
+    # 8+ tokens per SM: one CTA per token group with every expert
+    (37, 3, 3, 1300, True, True, 0.9),     # ragged experts and a 20-token last group
+    (300, 2, 4, 1219, False, False, 1.1),  # 16-token groups, a last group of 3 tokens
+    (5, 2, 2, 1240, True, False, 1.0),     # fewer experts than a warp tile
+    (8, 0, 3, 1500, True, True, 1.4),      # adaptive k
 ])
 def test_router_edge_shapes(cuda_lib, E, k, kmax, T, renorm, bias, it):
     rng = np.random.default_rng(E * 100 + T)
@@ -142,7 +147,11 @@ def test_route_is_router_then_permute(cuda_lib, E, k, kmax, T, H):
 @pytest.mark.parametrize("T,kmax,k,E,skew", [(1, 4, 4, 64, False), (64, 4, 4, 64, True),
                                              (4096, 8, 8, 128, False), (512, 3, 2, 32, False),
                                              (300, 16, 16, 1024, False), (100, 3, 3, 4, True),
-                                             (0, 2, 2, 8, False)])
+                                             (0, 2, 2, 8, False),
+                                             # 32768 slots over 1024 experts; ranges of
+                                             # several chunks per CTA (past 64 chunks)
+                                             (2048, 16, 16, 1024, True),
+                                             (9000, 8, 8, 128, False), (6000, 12, 11, 512, True)])
 def test_permute_bit_exact(cuda_lib, T, kmax, k, E, skew):
     rng = np.random.default_rng(T + E)
     ids = np.full((T, kmax), -1, np.int32)
@@ -253,6 +262,7 @@ def test_group_limited_layer_matches_oracle(cuda_lib):
 @pytest.mark.parametrize("T,k,kmax,E,C", [
     (64, 4, 4, 64, 3),     # batched-decode-like: popular experts overflow
     (700, 2, 3, 16, 40),   # several CTAs of the grouping kernel
+    (25000, 2, 3, 16, 3500),  # several chunks per CTA
     (33, 3, 3, 8, 0),      # capacity 0: everything dropped
     (20, 2, 2, 8, 1000),   # capacity above every count: plain grouping
 ])

@@ -244,6 +244,26 @@ def test_full_size_sampled(cuda_lib, full_layers, name):
         torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("bits", [5, 6])
+def test_full_size_batched_five_and_six_bits_sampled(cuda_lib, bits):
+    """The batched-decode workload at full size with 5- and 6-bit codes (the
+    shared-memory ring GEMV over 8-token chunks, the busiest experts in
+    several chunks): the routing, and output, h and y of 8 sampled tokens
+    against the oracle."""
+    cfg = CFG["batched"].scaled(bits=bits)
+    layer_np = workloads.make_layer(cfg)
+    d = dev()
+    x_all = workloads.make_tokens(cfg)
+    layer = cuda_lib.MoELayer.from_workload(layer_np, d)
+    out = to_np(layer(cuda_lib.bf16_from_bits(x_all, d)))
+    toks = np.sort(np.random.default_rng(bits).choice(cfg.T, 8, replace=False))
+    ref = oracle.moe_forward(x_all, layer_np, inv_temperature=cfg.inv_temperature(0), tokens=toks)
+    assert np.array_equal(to_np(layer.buffers(cfg.T)["topk_ids"]), ref.routing.ids)
+    assert_layer_close(out[toks], ref.out[toks], f"batched {bits}-bit")
+    check_rows(layer, cfg.T, ref, f"batched {bits}-bit")
+    assert cuda_lib.moe_get_device_error() == 0
+
+
 def test_adaptive_k_queues_both_families_and_runs_the_one_for_k(cuda_lib):
     """Adaptive k with the automatic path: below ks tokens per expert the
     streamed GEMV, from ks the tensor cores, decided on the device.  Each

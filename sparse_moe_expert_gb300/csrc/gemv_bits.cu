@@ -69,12 +69,13 @@ struct BtParams {
   unsigned int* err;
 };
 
-// Ring of a warp: two slots (with 16 warps deeper rings measured slower:
+// Ring of a warp: two slots (with 16 warps, deeper rings measured slower:
 // the cp.async copies in flight compete with the shared memory for the
-// SM's L1 storage), each holding kRingGroups groups of its 16 rows: the codes, one row after another at a
-// stride of 8b + 4 words (44 for 5 bits, 52 for 6: 16-byte aligned, and the
-// words that the 8 rows x 4 run offsets of one read touch fall in 32
-// distinct banks), then per row the 4 scales and the 4 biases (16 bytes).
+// SM's L1 storage), each holding kRingGroups groups of its 16 rows: the
+// codes, one row after another at a stride of 8b + 4 words (44 for 5 bits,
+// 52 for 6: 16-byte aligned, and the words that the 8 rows x 4 run offsets
+// of one read touch fall in 32 distinct banks), then per row the 4 scales
+// and the 4 biases (16 bytes).
 constexpr int kRingGroups = 4;
 __host__ __device__ constexpr int bt_ring_depth(int) { return 2; }
 __host__ __device__ constexpr int bt_ring_row_words(int bits) { return kRingGroups * 2 * bits + 4; }
